@@ -1,0 +1,186 @@
+/*
+ * egopq.h -- C ABI of the GB300 (sm_103a) W4A8 packed-linear GEMM library.
+ *
+ * The operation (y = a_s * sum_g s * (sum_k a_q*w_q - z * sum_k a_q), bf16 out)
+ * is the linear that the quantized serving stacks on these pages turn on:
+ *  - "The 4-bit CPU path" (vllm-omni docs/edge/cpu-4bit.md), section
+ *    "W4A8 - _C::int4_scaled_mm_cpu": GPTQ-packed int4 weights, activations
+ *    quantized to int8 at run time, zero points from the checkpoint or the
+ *    constant 8 for a symmetric export.
+ *  - "EgoPQ Real-Serving Handoff", section 2 "External Artifacts": native
+ *    W4A8 serving needs exact per-group _gptq_scale / _gptq_zero metadata.
+ *  - "The 4-bit CPU path", sections "W4A16 - PyTorch tinygemm" and "Building a
+ *    checkpoint": weight-only int4, group size 128.
+ *  - "Serve a pre-quantized int8 weight-only DiT via compressed-tensors ..."
+ *    (vllm-omni issue 5), sections "Context" and "Plan": int8 weight-only
+ *    (W8A16) linears.
+ *
+ * Conventions for every call:
+ *  - Pointers are caller-owned DEVICE memory unless stated otherwise, 16-byte
+ *    aligned. The library allocates nothing per call (one static 4-byte device
+ *    error word is its only device state).
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream). They validate arguments on the host first and return a negative
+ *    egopq_status without launching anything when a check fails; a failed
+ *    launch returns EGOPQ_ERR_CUDA. egopq_last_error_string() describes the
+ *    last failure of the calling thread.
+ *  - Matrices are row-major. bf16 and fp16 values travel as their 16-bit
+ *    patterns (uint16_t).
+ *  - Shape gate: group == 128, K % 128 == 0, N % 128 == 0, M >= 0 (M == 0 is a
+ *    no-op). Shapes that do not tile the 128-row weight block are refused
+ *    rather than computed wrong ("The 4-bit CPU path", section "The weight
+ *    layout, measured": a reshape gate keeps an untiled N from being
+ *    mis-read).
+ */
+#ifndef EGOPQ_H
+#define EGOPQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  EGOPQ_OK = 0,
+  EGOPQ_ERR_INVALID_ARG = -1,       /* null pointer, bad enum, negative size */
+  EGOPQ_ERR_UNSUPPORTED_SHAPE = -2, /* group != 128, K % 128, N % 128 */
+  EGOPQ_ERR_MISALIGNED = -3,        /* an operand pointer is not 16-byte aligned */
+  EGOPQ_ERR_ARCH = -4,              /* current device is not sm_103 */
+  EGOPQ_ERR_CUDA = -5,              /* a CUDA runtime call or launch failed */
+  EGOPQ_ERR_TIMEOUT = -6            /* a kernel's bounded wait expired */
+} egopq_status;
+
+/* Kernel path. AUTO picks by M (CUDA-core GEMV for small M, the tcgen05
+ * tensor-core GEMM otherwise); the others force one path for tests and
+ * benchmarks. The choice is always this explicit argument, never global or
+ * environment state ("The 4-bit CPU path", section "Why the path choice is a
+ * config field"). */
+typedef enum { EGOPQ_PATH_AUTO = 0, EGOPQ_PATH_GEMV = 1, EGOPQ_PATH_TC = 2 } egopq_path;
+
+typedef enum {
+  EGOPQ_VARIANT_W4A8 = 0,
+  EGOPQ_VARIANT_W4A16 = 1,
+  EGOPQ_VARIANT_W8A16 = 2
+} egopq_variant;
+
+typedef void* egopq_stream_t; /* cudaStream_t */
+
+/* Library version, major*10000 + minor*100 + patch. */
+int egopq_version(void);
+
+/* ---- weight packing --------------------------------------------------------
+ * Size in bytes of the packed form of an N x K int4 weight with group 128, or
+ * 0 if the shape is refused. The packed buffer holds three regions:
+ *   codes   N*K/2 bytes in 8 KiB tiles, one per (128-row block t, group g),
+ *           at ((t*G + g) * 8192); inside a tile the 16-byte unit of chunk c
+ *           (32 codes, k = 128g + 32c ..) of row r is at (c*128 + r) * 16;
+ *           little-endian word j of a unit holds k0 = 128g+32c+8j .. k0+7 with
+ *           nibble p carrying k0 + 2p (p < 4) or k0 + 2(p-4) + 1 (p >= 4);
+ *   scales  fp16 [G][N] at offset N*K/2;
+ *   zeros   [G][N/2] bytes after the scales, z[n,g] in the low nibble for
+ *           even n, the high nibble for odd n. */
+size_t egopq_packed_w4_bytes(int64_t N, int64_t K, int group);
+
+/* Pack logical GPTQ-style int4 weights into `packed` (device,
+ * egopq_packed_w4_bytes(N,K,group) bytes). Inputs (device):
+ *   w_q        uint8 [N][K], codes 0..15 (bits above the low nibble ignored)
+ *   scale_f16  fp16  [N][G], per-group scale s[n,g]      (_gptq_scale)
+ *   zero       uint8 [N][G], per-group zero point 0..15  (_gptq_zero)
+ * Dequantized weight: s[n,g] * (w_q[n,k] - z[n,g]); zero = 8 everywhere is the
+ * symmetric grid ("The 4-bit CPU path", section "W4A8"). */
+int egopq_pack_w4(const uint8_t* w_q, const uint16_t* scale_f16, const uint8_t* zero,
+                  int64_t N, int64_t K, int group, void* packed, egopq_stream_t stream);
+
+/* Inverse of egopq_pack_w4 (test and inspection aid). */
+int egopq_unpack_w4(const void* packed, int64_t N, int64_t K, int group, uint8_t* w_q,
+                    uint16_t* scale_f16, uint8_t* zero, egopq_stream_t stream);
+
+/* ---- activation quantization -------------------------------------------------
+ * Per-token symmetric int8 quantization of x (bf16 [M][K]), fused with the
+ * per-group sums that fold the zero points into the epilogue:
+ *   a_s[m]      = max_k |x[m,k]| / 127                 (fp32 quotient)
+ *   a_q[m,k]    = clamp(round_half_even(x / a_s), -127, 127)  (fp32 quotient)
+ *   a_gsum[m,g] = sum_{k in g} a_q[m,k]
+ * A row of zeros gives a_s = 0 and a_q = 0. Outputs (device): a_q int8
+ * [M][K], a_s fp32 [M], a_gsum int32 [M][G]; a_q16 (optional, may be NULL)
+ * receives the same codes as fp16 [M][K] -- exact integers, the operand form
+ * the tensor-core path loads with TMA. ("The 4-bit CPU path", section "W4A8":
+ * the kernel quantizes activations to int8.) */
+int egopq_quant_act_i8(const uint16_t* x_bf16, int64_t M, int64_t K, int group, int8_t* a_q,
+                       float* a_s, int32_t* a_gsum, uint16_t* a_q16, egopq_stream_t stream);
+
+/* ---- W4A8 GEMM -----------------------------------------------------------------
+ * y[m,n] = bf16( a_s[m] * sum_g s[n,g] * (sum_{k in g} a_q[m,k] w_q[n,k]
+ *                                         - z[n,g] * a_gsum[m,g]) )
+ * Inputs from egopq_quant_act_i8 and egopq_pack_w4; y is bf16 [M][N]. The
+ * GEMV path reads a_q and a_gsum; the tensor-core path reads a_q16 (required
+ * when it runs) and folds z into its weight operand. Both form each group's
+ * integer partial exactly before scaling. */
+int egopq_w4a8_gemm(const int8_t* a_q, const uint16_t* a_q16, const float* a_s,
+                    const int32_t* a_gsum, const void* packed, int64_t M, int64_t N, int64_t K,
+                    int group, uint16_t* y_bf16, egopq_stream_t stream);
+int egopq_w4a8_gemm_ex(const int8_t* a_q, const uint16_t* a_q16, const float* a_s,
+                       const int32_t* a_gsum, const void* packed, int64_t M, int64_t N,
+                       int64_t K, int group, uint16_t* y_bf16, int path, egopq_stream_t stream);
+
+/* Test readout: the integer group partials Q[m][n][g] (int32 [M][N][G]) the
+ * chosen path forms before scaling, from the same main loop:
+ *   Q[m,n,g] = sum_{k in g} a_q[m,k] w_q[n,k] - z[n,g] * sum_{k in g} a_q[m,k]. */
+int egopq_w4a8_group_partials(const int8_t* a_q, const uint16_t* a_q16, const int32_t* a_gsum,
+                              const void* packed, int64_t M, int64_t N, int64_t K, int group,
+                              int32_t* Q, int path, egopq_stream_t stream);
+
+/* ---- W4A16 GEMM ------------------------------------------------------------------
+ * y[m,n] = bf16( sum_g s[n,g] * sum_{k in g} x[m,k] * (w_q[n,k] - z[n,g]) )
+ * x bf16 [M][K]; packed as for W4A8; y bf16 [M][N]. ("The 4-bit CPU path",
+ * section "W4A16 - PyTorch tinygemm".) */
+int egopq_w4a16_gemm(const uint16_t* x_bf16, const void* packed, int64_t M, int64_t N,
+                     int64_t K, int group, uint16_t* y_bf16, egopq_stream_t stream);
+int egopq_w4a16_gemm_ex(const uint16_t* x_bf16, const void* packed, int64_t M, int64_t N,
+                        int64_t K, int group, uint16_t* y_bf16, int path,
+                        egopq_stream_t stream);
+
+/* ---- W8A16 GEMM ------------------------------------------------------------------
+ * y[m,n] = bf16( s[n] * sum_k x[m,k] * w_q[n,k] )
+ * x bf16 [M][K]; w_q int8 [N][K] row-major in [-127, 127] (symmetric,
+ * per-output-channel; no pack step); scale_f16 fp16 [N]; y bf16 [M][N].
+ * ("Serve a pre-quantized int8 weight-only DiT ...", sections "Context" and
+ * "Plan".) */
+int egopq_w8a16_gemm(const uint16_t* x_bf16, const int8_t* w_q, const uint16_t* scale_f16,
+                     int64_t M, int64_t N, int64_t K, uint16_t* y_bf16, egopq_stream_t stream);
+int egopq_w8a16_gemm_ex(const uint16_t* x_bf16, const int8_t* w_q, const uint16_t* scale_f16,
+                        int64_t M, int64_t N, int64_t K, uint16_t* y_bf16, int path,
+                        egopq_stream_t stream);
+
+/* ---- support, status --------------------------------------------------------------
+ * 1 if (M, N, K, group, variant) is accepted by the parity-tested kernels on
+ * the current device, 0 if not. It claims nothing the kernels do not run (a
+ * capability query that accepted a format its kernel then broke on is the
+ * failure recorded in "Serve a pre-quantized int8 weight-only DiT ...",
+ * amendment comment). */
+int egopq_supported(int64_t M, int64_t N, int64_t K, int group, int variant);
+
+/* Synchronize `stream`, then read and clear the device error word: EGOPQ_OK,
+ * EGOPQ_ERR_TIMEOUT if a kernel's bounded wait expired since the last call, or
+ * EGOPQ_ERR_CUDA if the synchronization itself failed. Every wait inside the
+ * kernels is bounded (2 s); once one expires its kernel's results are invalid,
+ * and kernels launched before this call reads the word may give up early. */
+int egopq_device_status(egopq_stream_t stream);
+
+/* Human-readable text for the calling thread's most recent failure. */
+const char* egopq_last_error_string(void);
+
+/* Self-test of the bounded-wait machinery: launches one CTA that waits on an
+ * mbarrier nothing will complete, with a deadline of `timeout_us`
+ * microseconds (1..1000000). The kernel gives up, records the timeout in the
+ * device error word and returns; egopq_device_status then reports
+ * EGOPQ_ERR_TIMEOUT. No fault, trap or hang is involved. */
+int egopq_selftest_timeout(int timeout_us, egopq_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EGOPQ_H */

@@ -1,0 +1,69 @@
+"""Host-side checks of the C ABI (no GPU needed, no compute calls).
+
+The library must build for sm_103a, load, and export every function the header
+declares; host validation must reject bad arguments before touching the device.
+"""
+import ctypes
+import os
+
+import pytest
+
+import w4a8_quantized_gemm_gb300 as eg
+from w4a8_quantized_gemm_gb300 import builder
+
+
+@pytest.fixture(scope="module")
+def lib():
+    builder.build()
+    return eg.load()
+
+
+def test_library_exports_every_header_function(lib):
+    names = eg.header_functions()
+    assert len(names) >= 16
+    raw = ctypes.CDLL(eg.LIB_PATH)
+    missing = [n for n in names if not hasattr(raw, n)]
+    assert not missing, missing
+    assert lib.egopq_version() >= 10000
+
+
+def test_packed_size_and_shape_gate(lib):
+    assert lib.egopq_packed_w4_bytes(3584, 3584, 128) == 3584 * 3584 // 2 + 28 * 3584 * 5 // 2
+    assert lib.egopq_packed_w4_bytes(152064, 3584, 128) == 152064 * 3584 // 2 + 28 * 152064 * 5 // 2
+    assert lib.egopq_packed_w4_bytes(80, 3584, 128) == 0       # N does not tile 128 rows
+    assert lib.egopq_packed_w4_bytes(128, 200, 128) == 0
+    assert lib.egopq_packed_w4_bytes(128, 256, 64) == 0
+
+
+def test_host_validation_rejects_before_launch(lib):
+    A = 0x10000  # aligned fake device address: never dereferenced on these paths
+    s = None
+    # NULL and misaligned pointers
+    assert lib.egopq_pack_w4(None, A, A, 128, 128, 128, A, s) == -1
+    assert lib.egopq_pack_w4(A + 4, A, A, 128, 128, 128, A, s) == -3
+    # shape gate
+    assert lib.egopq_pack_w4(A, A, A, 100, 128, 128, A, s) == -2
+    assert lib.egopq_quant_act_i8(A, 4, 200, 128, A, A, A, None, s) == -2
+    assert lib.egopq_w4a8_gemm_ex(A, A, A, A, A, 4, 256, 512, 32, A, 0, s) == -2
+    assert lib.egopq_w4a8_gemm_ex(A, A, A, A, A, -1, 256, 512, 128, A, 0, s) == -1
+    # unknown path is refused on the host
+    assert lib.egopq_w4a8_gemm_ex(A, A, A, A, A, 4, 256, 512, 128, A, 7, s) == -1
+    assert b"path" in lib.egopq_last_error_string()
+    # empty batch: accepted as a no-op without touching any pointer
+    assert lib.egopq_w4a8_gemm_ex(None, None, None, None, None, 0, 256, 512, 128, None, 0, s) == 0
+    assert lib.egopq_quant_act_i8(None, 0, 512, 128, None, None, None, None, s) == 0
+    assert lib.egopq_selftest_timeout(0, s) == -1
+
+
+def test_binding_fails_loudly_without_library(monkeypatch):
+    monkeypatch.setattr(eg, "LIB_PATH", os.path.join(os.path.dirname(eg.LIB_PATH), "nope.so"))
+    monkeypatch.setattr(eg, "_lib", None)
+    with pytest.raises(RuntimeError, match="missing"):
+        eg.load()
+
+
+def test_header_names_follow_the_pages_operations():
+    names = set(eg.header_functions())
+    for required in ["egopq_pack_w4", "egopq_quant_act_i8", "egopq_w4a8_gemm",
+                     "egopq_w4a16_gemm", "egopq_w8a16_gemm"]:
+        assert required in names

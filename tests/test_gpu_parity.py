@@ -1,0 +1,317 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Integer stages (activation codes, scales, group sums, packing, group partials)
+are compared bit for bit; bf16 outputs against the bar in tests/helpers.py.
+Sizes span several 128-row tiles and ragged token tails; the full Qwen2.5-7B and
+DiT shapes are checked on sampled rows/columns the oracle computes directly.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from helpers import check_bf16_output, to_dev, to_host_bits, w4_case
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover - collected on CPU, skipped there
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+import w4a8_quantized_gemm_gb300 as eg  # noqa: E402
+
+PATHS = [eg.PATH_GEMV, eg.PATH_TC]
+SHAPES_7B = {"q": (3584, 3584), "k": (3584, 512), "gate": (3584, 18944), "down": (18944, 3584)}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    eg.load()
+    torch.cuda.set_device(0)
+    yield
+    assert eg.device_status() == 0
+
+
+def dev_weights(w):
+    return (to_dev(w.w_q), to_dev(w.scale_f16, torch.float16), to_dev(w.zero))
+
+
+def run_w4a8(x, w, path, M, N, K):
+    packed = eg.pack_w4(*dev_weights(w))
+    a = eg.quant_act(to_dev(x, torch.bfloat16))
+    y = eg.w4a8_gemm(a, packed, N, K, path=path)
+    return a, packed, y
+
+
+# ------------------------------------------------------------ activation quant
+
+@pytest.mark.parametrize("M,K", [(16, 512), (1, 3584), (5, 18944), (129, 1024), (300, 384)])
+def test_quant_act_bit_exact(M, K):
+    x = synth.activations(0, 1, 0, M, K)
+    if M > 3:
+        x[2] = 0                                     # an all-zero token
+        x[3] = 0
+        x[3, K // 3] = 0xC47A                        # a single outlier (-1000)
+    a = eg.quant_act(to_dev(x, torch.bfloat16))
+    a_q, a_s, asum = oracle.quant_act(x)
+    assert np.array_equal(a.a_q.cpu().numpy(), a_q)
+    assert np.array_equal(a.a_s.cpu().numpy().view(np.uint32), a_s.view(np.uint32))
+    assert np.array_equal(a.a_gsum.cpu().numpy(), asum)
+    assert np.array_equal(a.a_q16.float().cpu().numpy(), a_q.astype(np.float32))
+
+
+def test_quant_act_ties_from_golden_rows():
+    # rows whose quotients x / a_s sit exactly on .5 (round-half-even decides)
+    rows = [[254, 1, 3, -5, 0, 7, -1, 100], [-254, 3, 5, -3, -1, 1, 9, 11]]
+    x = np.zeros((2, 128), np.float32)
+    x[:, :8] = rows
+    xb = (x.view(np.uint32) >> 16).astype(np.uint16)
+    a = eg.quant_act(to_dev(xb, torch.bfloat16))
+    got = a.a_q.cpu().numpy()[:, :8]
+    assert got.tolist() == [[127, 0, 2, -2, 0, 4, 0, 50], [-127, 2, 2, -2, 0, 0, 4, 6]]
+
+
+# -------------------------------------------------------------------- packing
+
+@pytest.mark.parametrize("N,K", [(128, 128), (256, 512), (512, 3584)])
+def test_pack_bit_exact_and_roundtrip(N, K):
+    w = synth.w4_weights(0, 2, 0, N, K)
+    packed = eg.pack_w4(*dev_weights(w))
+    ref = oracle.pack_w4(w.w_q, w.scale_f16, w.zero)
+    assert np.array_equal(packed.cpu().numpy(), ref)
+    w2, s2, z2 = eg.unpack_w4(packed, N, K)
+    assert np.array_equal(w2.cpu().numpy(), w.w_q)
+    assert np.array_equal(to_host_bits(s2), w.scale_f16)
+    assert np.array_equal(z2.cpu().numpy(), w.zero)
+
+
+# ------------------------------------------------------------- group partials
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("M", [1, 3, 4, 5, 16, 17, 64, 129])
+def test_w4a8_group_partials_bit_exact(path, M):
+    N, K = 256, 512
+    x, w = w4_case(0, M, N, K)
+    a, packed, _ = run_w4a8(x, w, path, M, N, K)
+    Q = eg.w4a8_group_partials(a, packed, N, K, path=path).cpu().numpy()
+    a_q, _, _ = oracle.quant_act(x)
+    assert np.array_equal(Q, oracle.group_partials(a_q, w.w_q, w.zero))
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("case", ["max_pos", "max_neg", "alternating"])
+def test_w4a8_group_partials_worst_case_magnitudes(path, case):
+    """|Q| up to 128*127*15 = 243840: the tensor-core path must stay exact
+    (fp16 integer products accumulated in fp32 within one group)."""
+    M, N, K = 16, 128, 512
+    G = K // 128
+    x = np.full((M, K), 0x3F80, np.uint16)                     # 1.0 -> a_q = 127
+    w_q = np.full((N, K), 15, np.uint8)
+    z = np.zeros((N, G), np.uint8)
+    if case == "max_neg":
+        w_q[:] = 0
+        z[:] = 15
+    elif case == "alternating":
+        x[:, 1::2] = 0xBF80                                    # -1.0 -> a_q = -127
+        w_q[:, 1::2] = 0
+        w_q[::2, :] = 15 - w_q[::2, :]                         # half the rows flipped
+        z[:, :] = np.arange(N)[:, None] % 16
+    s = np.full((N, G), 0x3C00, np.uint16)                     # 1.0
+    w = synth.W4Weights(w_q, s, z, 128)
+    a, packed, _ = run_w4a8(x, w, path, M, N, K)
+    Q = eg.w4a8_group_partials(a, packed, N, K, path=path).cpu().numpy()
+    a_q, _, _ = oracle.quant_act(x)
+    ref = oracle.group_partials(a_q, w_q, z)
+    if case == "max_pos":
+        assert ref.max() == 243840
+    if case == "max_neg":
+        assert ref.min() == -243840
+    assert np.array_equal(Q, ref)
+
+
+# ------------------------------------------------------------------ W4A8 output
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 8, 15, 16, 17, 31, 64, 100, 127, 128, 129, 256])
+def test_w4a8_output_sweep_small(path, M):
+    N, K = 256, 512
+    x, w = w4_case(0, M, N, K)
+    a, packed, y = run_w4a8(x, w, path, M, N, K)
+    a_q, a_s, _ = oracle.quant_act(x)
+    _, y_ref = oracle.w4a8(a_q, a_s, w.w_q, w.scale_f16, w.zero)
+    check_bf16_output(to_host_bits(y), y_ref, f"W4A8 path={path} M={M}")
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_w4a8_output_many_tiles(path):
+    # several 128-row weight tiles, 28 groups, ragged token tail, split-K clusters
+    M, N, K = 37, 1024, 3584
+    x, w = w4_case(0, M, N, K, layer=3)
+    a, packed, y = run_w4a8(x, w, path, M, N, K)
+    a_q, a_s, _ = oracle.quant_act(x)
+    _, y_ref = oracle.w4a8(a_q, a_s, w.w_q, w.scale_f16, w.zero)
+    check_bf16_output(to_host_bits(y), y_ref, f"W4A8 path={path}")
+
+
+def test_w4a8_paths_agree_and_deterministic():
+    M, N, K = 4, 512, 3584
+    x, w = w4_case(1, M, N, K)
+    _, _, y1 = run_w4a8(x, w, eg.PATH_GEMV, M, N, K)
+    _, _, y2 = run_w4a8(x, w, eg.PATH_GEMV, M, N, K)
+    _, _, y3 = run_w4a8(x, w, eg.PATH_TC, M, N, K)
+    _, _, y4 = run_w4a8(x, w, eg.PATH_TC, M, N, K)
+    assert torch.equal(y1, y2) and torch.equal(y3, y4)
+    a_q, a_s, _ = oracle.quant_act(x)
+    _, y_ref = oracle.w4a8(a_q, a_s, w.w_q, w.scale_f16, w.zero)
+    check_bf16_output(to_host_bits(y1), y_ref, "gemv")
+    check_bf16_output(to_host_bits(y3), y_ref, "tc")
+
+
+def _sampled_check(x, w, y_bits, rows, cols, what):
+    a_q, a_s, _ = oracle.quant_act(x[rows])
+    _, y_ref = oracle.w4a8(a_q, a_s, w.w_q[cols], w.scale_f16[cols], w.zero[cols])
+    check_bf16_output(y_bits[np.ix_(rows, cols)], y_ref, what)
+
+
+@pytest.mark.parametrize("name", list(SHAPES_7B))
+@pytest.mark.parametrize("M", [1, 4, 16])
+def test_w4a8_decode_7b_shapes(name, M):
+    K, N = SHAPES_7B[name]
+    x, w = w4_case(1, M, N, K, linear=synth.LINEARS[name])
+    a, packed, y = run_w4a8(x, w, eg.PATH_AUTO, M, N, K)
+    a_q, a_s, asum = oracle.quant_act(x)
+    assert np.array_equal(a.a_q.cpu().numpy(), a_q)
+    cols = np.unique(np.concatenate([np.arange(128), np.arange(N - 128, N),
+                                     np.random.default_rng(M).choice(N, 256, replace=False)]))
+    _sampled_check(x, w, to_host_bits(y), np.arange(M), cols, f"decode {name} M={M}")
+
+
+@pytest.mark.parametrize("name,M", [("q", 512), ("gate", 2048), ("down", 4096), ("k", 4096)])
+def test_w4a8_prefill_7b_shapes_sampled(name, M):
+    K, N = SHAPES_7B[name]
+    x, w = w4_case(2, M, N, K, linear=synth.LINEARS[name])
+    a, packed, y = run_w4a8(x, w, eg.PATH_AUTO, M, N, K)
+    a_q, a_s, asum = oracle.quant_act(x)
+    assert np.array_equal(a.a_q.cpu().numpy(), a_q)
+    assert np.array_equal(a.a_gsum.cpu().numpy(), asum)
+    rng = np.random.default_rng(M + N)
+    rows = np.unique(np.concatenate([np.arange(4), np.arange(M - 4, M), rng.choice(M, 8, replace=False)]))
+    cols = np.unique(np.concatenate([np.arange(64), np.arange(N - 64, N), rng.choice(N, 128, replace=False)]))
+    _sampled_check(x, w, to_host_bits(y), rows, cols, f"prefill {name} M={M}")
+
+
+def test_w4a8_head_prefill_sampled():
+    """Untied quantized output head, K=3584, N=152064, at M=512."""
+    M, K, N = 512, 3584, 152064
+    x, w = w4_case(2, M, N, K, linear=synth.LINEARS["head"])
+    a, packed, y = run_w4a8(x, w, eg.PATH_AUTO, M, N, K)
+    rng = np.random.default_rng(7)
+    rows = np.array([0, 1, 255, 256, 510, 511])
+    cols = np.unique(np.concatenate([np.arange(32), np.arange(N - 32, N), rng.choice(N, 192, replace=False)]))
+    _sampled_check(x, w, to_host_bits(y), rows, cols, "head M=512")
+
+
+# ------------------------------------------------------- W4A16 and W8A16 output
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("M", [1, 3, 16, 17, 130])
+def test_w4a16_output(path, M):
+    N, K = 384, 1024
+    x, w = w4_case(4, M, N, K, outliers=False)
+    packed = eg.pack_w4(*dev_weights(w))
+    y = eg.w4a16_gemm(to_dev(x, torch.bfloat16), packed, N, K, path=path)
+    _, y_ref = oracle.w4a16(x, w.w_q, w.scale_f16, w.zero)
+    check_bf16_output(to_host_bits(y), y_ref, f"W4A16 path={path} M={M}")
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("M", [1, 3, 16, 17, 130])
+def test_w8a16_output(path, M):
+    N, K = 384, 1024
+    w8, s8 = synth.w8_weights(4, 0, 0, N, K)
+    x = synth.activations(4, 0, 0, M, K, outliers=False)
+    y = eg.w8a16_gemm(to_dev(x, torch.bfloat16), to_dev(w8), to_dev(s8, torch.float16), path=path)
+    _, y_ref = oracle.w8a16(x, w8, s8)
+    check_bf16_output(to_host_bits(y), y_ref, f"W8A16 path={path} M={M}")
+
+
+@pytest.mark.parametrize("K,N", [(3072, 3072), (3072, 12288), (12288, 3072)])
+@pytest.mark.parametrize("M", [1, 16, 4096])
+def test_weight_only_dit_shapes_sampled(K, N, M):
+    x = synth.activations(4, 1, 0, M, K, outliers=False)
+    w = synth.w4_weights(4, 1, 0, N, K)
+    w8, s8 = synth.w8_weights(4, 1, 0, N, K)
+    xd = to_dev(x, torch.bfloat16)
+    y4 = to_host_bits(eg.w4a16_gemm(xd, eg.pack_w4(*dev_weights(w)), N, K))
+    y8 = to_host_bits(eg.w8a16_gemm(xd, to_dev(w8), to_dev(s8, torch.float16)))
+    rng = np.random.default_rng(K + N + M)
+    rows = np.unique(np.concatenate([[0, M - 1], rng.choice(M, min(M, 6), replace=False)]))
+    cols = np.unique(np.concatenate([[0, N - 1], rng.choice(N, 160, replace=False)]))
+    _, r4 = oracle.w4a16(x[rows], w.w_q[cols], w.scale_f16[cols], w.zero[cols])
+    _, r8 = oracle.w8a16(x[rows], w8[cols], s8[cols])
+    check_bf16_output(y4[np.ix_(rows, cols)], r4, f"W4A16 DiT K={K} N={N} M={M}")
+    check_bf16_output(y8[np.ix_(rows, cols)], r8, f"W8A16 DiT K={K} N={N} M={M}")
+
+
+# ----------------------------------------------------------------- edge cases
+
+def test_empty_batch_is_a_noop():
+    K, N = 512, 256
+    w = synth.w4_weights(0, 0, 0, N, K)
+    packed = eg.pack_w4(*dev_weights(w))
+    x = torch.empty((0, K), dtype=torch.bfloat16, device="cuda")
+    a = eg.quant_act(x)
+    y = eg.w4a8_gemm(a, packed, N, K)
+    assert y.shape == (0, N)
+
+
+def test_output_guard_bands_untouched():
+    M, N, K = 17, 256, 512
+    x, w = w4_case(0, M, N, K)
+    packed = eg.pack_w4(*dev_weights(w))
+    a = eg.quant_act(to_dev(x, torch.bfloat16))
+    for path in PATHS:
+        pad = 4096
+        buf = torch.full((M * N + 2 * pad,), 12345, dtype=torch.int16, device="cuda")
+        out = buf[pad:pad + M * N].view(torch.bfloat16).view(M, N)
+        eg.w4a8_gemm(a, packed, N, K, path=path, out=out)
+        torch.cuda.synchronize()
+        assert torch.all(buf[:pad] == 12345) and torch.all(buf[pad + M * N:] == 12345)
+
+
+def test_rejections():
+    K, N = 512, 256
+    w = synth.w4_weights(0, 0, 0, N, K)
+    packed = eg.pack_w4(*dev_weights(w))
+    a = eg.quant_act(to_dev(synth.activations(0, 0, 0, 4, K), torch.bfloat16))
+    lib = eg.load()
+    s = torch.cuda.current_stream().cuda_stream
+    y = torch.empty((4, N), dtype=torch.bfloat16, device="cuda")
+    # N not a multiple of 128, misaligned output, missing fp16 codes on the TC path
+    assert lib.egopq_w4a8_gemm_ex(a.a_q.data_ptr(), a.a_q16.data_ptr(), a.a_s.data_ptr(),
+                                  a.a_gsum.data_ptr(), packed.data_ptr(), 4, 192, K, 128,
+                                  y.data_ptr(), 0, s) == -2
+    assert lib.egopq_w4a8_gemm_ex(a.a_q.data_ptr(), a.a_q16.data_ptr(), a.a_s.data_ptr(),
+                                  a.a_gsum.data_ptr(), packed.data_ptr(), 4, N, K, 128,
+                                  y.data_ptr() + 2, 0, s) == -3
+    assert lib.egopq_w4a8_gemm_ex(a.a_q.data_ptr(), None, a.a_s.data_ptr(),
+                                  a.a_gsum.data_ptr(), packed.data_ptr(), 4, N, K, 128,
+                                  y.data_ptr(), eg.PATH_TC, s) == -1
+    assert lib.egopq_w4a8_gemm_ex(a.a_q.data_ptr(), a.a_q16.data_ptr(), a.a_s.data_ptr(),
+                                  a.a_gsum.data_ptr(), packed.data_ptr(), 4, N, K, 64,
+                                  y.data_ptr(), 0, s) == -2
+    assert eg.supported(4, N, K) and not eg.supported(4, 80, K)
+    assert eg.device_status() == 0
+
+
+def test_bounded_wait_reports_timeout_without_fault():
+    eg.selftest_timeout(2000)          # 2 ms deadline, nothing ever arrives
+    assert eg.device_status() == -6    # reported, then cleared
+    assert eg.device_status() == 0
+    # the context is still usable
+    M, N, K = 4, 256, 512
+    x, w = w4_case(0, M, N, K)
+    a, packed, y = run_w4a8(x, w, eg.PATH_TC, M, N, K)
+    a_q, a_s, _ = oracle.quant_act(x)
+    _, y_ref = oracle.w4a8(a_q, a_s, w.w_q, w.scale_f16, w.zero)
+    check_bf16_output(to_host_bits(y), y_ref, "after timeout self-test")

@@ -1,0 +1,244 @@
+"""GB300 (sm_103a) W4A8 packed-linear GEMM: thin Python binding of libegopq.
+
+Argument marshalling only: every step of the path runs in the CUDA kernels of
+`libegopq.so` (built in-tree by `w4a8_quantized_gemm_gb300.builder`). PyTorch
+provides device memory and the current stream. There is no CPU fallback: if the
+library is missing or the device is not sm_103, calls raise.
+
+Typical use (one linear, W4A8):
+
+    packed = pack_w4(w_q, scale_f16, zero)            # once per weight
+    a = quant_act(x)                                  # per token batch
+    y = w4a8_gemm(a, packed, N, K)                    # bf16 [M, N]
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+from typing import NamedTuple, Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libegopq.so")
+HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "egopq.h")
+
+PATH_AUTO, PATH_GEMV, PATH_TC = 0, 1, 2
+VARIANT_W4A8, VARIANT_W4A16, VARIANT_W8A16 = 0, 1, 2
+STATUS = {0: "OK", -1: "INVALID_ARG", -2: "UNSUPPORTED_SHAPE", -3: "MISALIGNED",
+          -4: "ARCH", -5: "CUDA", -6: "TIMEOUT"}
+GROUP = 128
+
+_lock = threading.Lock()
+_lib = None
+
+
+class EgopqError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"egopq error {code} ({STATUS.get(code, '?')}): {msg}")
+        self.code = code
+
+
+def build(force: bool = False) -> str:
+    from . import builder
+    return builder.build(force=force)
+
+
+def load() -> ctypes.CDLL:
+    """Load libegopq.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m w4a8_quantized_gemm_gb300.builder`")
+        lib = ctypes.CDLL(LIB_PATH)
+        i64, i32, vp, sz = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
+        sig = {
+            "egopq_version": (i32, []),
+            "egopq_last_error_string": (ctypes.c_char_p, []),
+            "egopq_packed_w4_bytes": (sz, [i64, i64, i32]),
+            "egopq_pack_w4": (i32, [vp, vp, vp, i64, i64, i32, vp, vp]),
+            "egopq_unpack_w4": (i32, [vp, i64, i64, i32, vp, vp, vp, vp]),
+            "egopq_quant_act_i8": (i32, [vp, i64, i64, i32, vp, vp, vp, vp, vp]),
+            "egopq_w4a8_gemm": (i32, [vp, vp, vp, vp, vp, i64, i64, i64, i32, vp, vp]),
+            "egopq_w4a8_gemm_ex": (i32, [vp, vp, vp, vp, vp, i64, i64, i64, i32, vp, i32, vp]),
+            "egopq_w4a8_group_partials": (i32, [vp, vp, vp, vp, i64, i64, i64, i32, vp, i32, vp]),
+            "egopq_w4a16_gemm": (i32, [vp, vp, i64, i64, i64, i32, vp, vp]),
+            "egopq_w4a16_gemm_ex": (i32, [vp, vp, i64, i64, i64, i32, vp, i32, vp]),
+            "egopq_w8a16_gemm": (i32, [vp, vp, vp, i64, i64, i64, vp, vp]),
+            "egopq_w8a16_gemm_ex": (i32, [vp, vp, vp, i64, i64, i64, vp, i32, vp]),
+            "egopq_supported": (i32, [i64, i64, i64, i32, i32]),
+            "egopq_device_status": (i32, [vp]),
+            "egopq_selftest_timeout": (i32, [i32, vp]),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+def header_functions() -> list:
+    """Names of the functions include/egopq.h declares."""
+    with open(HEADER_PATH) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"\b(egopq_[a-z0-9_]+)\s*\(", text)))
+
+
+# ------------------------------------------------------------------ helpers --
+
+def _check(rc: int):
+    if rc != 0:
+        raise EgopqError(rc, load().egopq_last_error_string().decode(errors="replace"))
+
+
+def _stream(stream: Optional[torch.cuda.Stream] = None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensor must be on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return t.data_ptr()
+
+
+def _dtype(t: torch.Tensor, *dtypes):
+    if t.dtype not in dtypes:
+        raise TypeError(f"expected dtype in {dtypes}, got {t.dtype}")
+
+
+# --------------------------------------------------------------------- API ---
+
+def packed_w4_bytes(N: int, K: int, group: int = GROUP) -> int:
+    return int(load().egopq_packed_w4_bytes(N, K, group))
+
+
+def pack_w4(w_q: torch.Tensor, scale_f16: torch.Tensor, zero: torch.Tensor,
+            out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """w_q uint8 [N,K] codes 0..15, scale fp16 [N,G], zero uint8 [N,G] -> packed uint8."""
+    _dtype(w_q, torch.uint8)
+    _dtype(scale_f16, torch.float16, torch.int16, torch.uint16)
+    _dtype(zero, torch.uint8)
+    N, K = w_q.shape
+    nbytes = packed_w4_bytes(N, K)
+    if nbytes == 0:
+        raise EgopqError(-2, f"shape N={N} K={K} is not packable (K, N multiples of 128)")
+    if out is None:
+        out = torch.empty(nbytes, dtype=torch.uint8, device=w_q.device)
+    _check(load().egopq_pack_w4(_ptr(w_q), _ptr(scale_f16), _ptr(zero), N, K, GROUP,
+                                _ptr(out), _stream(stream)))
+    return out
+
+
+def unpack_w4(packed: torch.Tensor, N: int, K: int, stream=None):
+    G = K // GROUP
+    dev = packed.device
+    w = torch.empty((N, K), dtype=torch.uint8, device=dev)
+    s = torch.empty((N, G), dtype=torch.float16, device=dev)
+    z = torch.empty((N, G), dtype=torch.uint8, device=dev)
+    _check(load().egopq_unpack_w4(_ptr(packed), N, K, GROUP, _ptr(w), _ptr(s), _ptr(z),
+                                  _stream(stream)))
+    return w, s, z
+
+
+class QuantAct(NamedTuple):
+    a_q: torch.Tensor      # int8 [M, K]
+    a_s: torch.Tensor      # fp32 [M]
+    a_gsum: torch.Tensor   # int32 [M, G]
+    a_q16: Optional[torch.Tensor]  # fp16 [M, K] (exact integer codes) or None
+
+
+def quant_act(x: torch.Tensor, with_f16: bool = True, out: Optional[QuantAct] = None,
+              stream=None) -> QuantAct:
+    """Per-token symmetric int8 quantization of bf16 x [M, K]."""
+    _dtype(x, torch.bfloat16, torch.int16, torch.uint16)
+    M, K = x.shape
+    if out is None:
+        dev = x.device
+        out = QuantAct(torch.empty((M, K), dtype=torch.int8, device=dev),
+                       torch.empty((M,), dtype=torch.float32, device=dev),
+                       torch.empty((M, max(K // GROUP, 1)), dtype=torch.int32, device=dev),
+                       torch.empty((M, K), dtype=torch.float16, device=dev) if with_f16 else None)
+    _check(load().egopq_quant_act_i8(_ptr(x), M, K, GROUP, _ptr(out.a_q), _ptr(out.a_s),
+                                     _ptr(out.a_gsum), _ptr(out.a_q16), _stream(stream)))
+    return out
+
+
+def w4a8_gemm(a: QuantAct, packed: torch.Tensor, N: int, K: int, path: int = PATH_AUTO,
+              out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    M = a.a_q.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=a.a_q.device)
+    _check(load().egopq_w4a8_gemm_ex(_ptr(a.a_q), _ptr(a.a_q16), _ptr(a.a_s), _ptr(a.a_gsum),
+                                     _ptr(packed), M, N, K, GROUP, _ptr(out), path,
+                                     _stream(stream)))
+    return out
+
+
+def w4a8_group_partials(a: QuantAct, packed: torch.Tensor, N: int, K: int,
+                        path: int = PATH_TC, stream=None) -> torch.Tensor:
+    M = a.a_q.shape[0]
+    Q = torch.empty((M, N, K // GROUP), dtype=torch.int32, device=a.a_q.device)
+    _check(load().egopq_w4a8_group_partials(_ptr(a.a_q), _ptr(a.a_q16), _ptr(a.a_gsum),
+                                            _ptr(packed), M, N, K, GROUP, _ptr(Q), path,
+                                            _stream(stream)))
+    return Q
+
+
+def w4a16_gemm(x: torch.Tensor, packed: torch.Tensor, N: int, K: int, path: int = PATH_AUTO,
+               out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    _dtype(x, torch.bfloat16)
+    M = x.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _check(load().egopq_w4a16_gemm_ex(_ptr(x), _ptr(packed), M, N, K, GROUP, _ptr(out), path,
+                                      _stream(stream)))
+    return out
+
+
+def w8a16_gemm(x: torch.Tensor, w_q: torch.Tensor, scale_f16: torch.Tensor,
+               path: int = PATH_AUTO, out: Optional[torch.Tensor] = None,
+               stream=None) -> torch.Tensor:
+    _dtype(x, torch.bfloat16)
+    _dtype(w_q, torch.int8)
+    M, K = x.shape
+    N = w_q.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _check(load().egopq_w8a16_gemm_ex(_ptr(x), _ptr(w_q), _ptr(scale_f16), M, N, K, _ptr(out),
+                                      path, _stream(stream)))
+    return out
+
+
+def w4a8_linear(x: torch.Tensor, packed: torch.Tensor, N: int, path: int = PATH_AUTO,
+                stream=None) -> torch.Tensor:
+    """Quantize x per token, then the W4A8 GEMM: y = x W^T with W4A8 arithmetic."""
+    a = quant_act(x, stream=stream)
+    return w4a8_gemm(a, packed, N, x.shape[1], path=path, stream=stream)
+
+
+def supported(M: int, N: int, K: int, variant: int = VARIANT_W4A8, group: int = GROUP) -> bool:
+    return bool(load().egopq_supported(M, N, K, group, variant))
+
+
+def device_status(stream=None) -> int:
+    """Synchronize and return (and clear) the device error status code."""
+    return int(load().egopq_device_status(_stream(stream)))
+
+
+def selftest_timeout(timeout_us: int, stream=None) -> None:
+    _check(load().egopq_selftest_timeout(timeout_us, _stream(stream)))
+
+
+def version() -> int:
+    return int(load().egopq_version())

@@ -1,0 +1,293 @@
+// egopq_api.cu -- the C ABI declared in include/egopq.h: argument validation,
+// path dispatch, the device error word and error strings. No allocation
+// happens here; every buffer belongs to the caller.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "../../include/egopq.h"
+#include "egopq_internal.h"
+
+namespace egopq {
+__device__ unsigned int g_error_word = 0;
+}
+
+using namespace egopq;
+
+namespace {
+
+thread_local char g_msg[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(EGOPQ_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s per bounded wait
+constexpr int64_t kMaxDim = (int64_t)1 << 31;
+
+// sm_103 check, cached per device
+int check_arch() {
+  static int cached[64];  // 0 unknown, 1 ok, 2 bad
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev >= 0 && dev < 64 && cached[dev]) return cached[dev] == 1 ? EGOPQ_OK : EGOPQ_ERR_ARCH;
+  int major = 0, minor = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  const bool ok = (major == 10 && minor == 3);
+  if (dev >= 0 && dev < 64) cached[dev] = ok ? 1 : 2;
+  if (!ok) return fail(EGOPQ_ERR_ARCH, "device %d is sm_%d%d; this library is built for sm_103a", dev,
+                       major, minor);
+  return EGOPQ_OK;
+}
+
+int check_w4_shape(int64_t M, int64_t N, int64_t K, int group) {
+  if (M < 0 || N <= 0 || K <= 0 || M >= kMaxDim || N >= kMaxDim || K >= kMaxDim)
+    return fail(EGOPQ_ERR_INVALID_ARG, "bad sizes M=%lld N=%lld K=%lld", (long long)M,
+                (long long)N, (long long)K);
+  if (group != 128) return fail(EGOPQ_ERR_UNSUPPORTED_SHAPE, "group must be 128 (got %d)", group);
+  if (K % 128 || N % 128)
+    return fail(EGOPQ_ERR_UNSUPPORTED_SHAPE,
+                "K (%lld) and N (%lld) must be multiples of 128", (long long)K, (long long)N);
+  return EGOPQ_OK;
+}
+
+int check_ptrs(int n, ...) {
+  va_list ap;
+  va_start(ap, n);
+  for (int i = 0; i < n; ++i) {
+    const char* name = va_arg(ap, const char*);
+    const void* p = va_arg(ap, const void*);
+    if (!p) {
+      va_end(ap);
+      return fail(EGOPQ_ERR_INVALID_ARG, "%s is NULL", name);
+    }
+    if (!aligned16(p)) {
+      va_end(ap);
+      return fail(EGOPQ_ERR_MISALIGNED, "%s is not 16-byte aligned", name);
+    }
+  }
+  va_end(ap);
+  return EGOPQ_OK;
+}
+
+int run_gemm(const GemmArgs& a, int path, cudaStream_t st) {
+  if (path != EGOPQ_PATH_AUTO && path != EGOPQ_PATH_GEMV && path != EGOPQ_PATH_TC)
+    return fail(EGOPQ_ERR_INVALID_ARG, "unknown path %d", path);
+  int rc = check_arch();
+  if (rc) return rc;
+  if (a.M == 0) return EGOPQ_OK;
+  int use = path;
+  if (use == EGOPQ_PATH_AUTO) use = (a.M <= kGemvMaxRows && a.variant == kW4A8) ? EGOPQ_PATH_GEMV
+                                                                               : EGOPQ_PATH_TC;
+  if (use == EGOPQ_PATH_TC && a.variant == kW4A8 && !a.a_q16)
+    return fail(EGOPQ_ERR_INVALID_ARG, "a_q16 is required by the tensor-core path");
+  cudaError_t e = (use == EGOPQ_PATH_GEMV) ? launch_gemv(a, st) : launch_tc_gemm(a, st);
+  if (e == cudaErrorNotSupported)
+    return fail(EGOPQ_ERR_UNSUPPORTED_SHAPE, "shape not supported by the requested path");
+  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  return EGOPQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int egopq_version(void) { return 1 * 10000 + 0 * 100 + 0; }
+
+const char* egopq_last_error_string(void) { return g_msg; }
+
+size_t egopq_packed_w4_bytes(int64_t N, int64_t K, int group) {
+  if (group != 128 || N <= 0 || K <= 0 || N % 128 || K % 128 || N >= kMaxDim || K >= kMaxDim)
+    return 0;
+  const int64_t G = K / 128;
+  return (size_t)(N * K / 2 + 2 * G * N + G * N / 2);
+}
+
+int egopq_pack_w4(const uint8_t* w_q, const uint16_t* scale_f16, const uint8_t* zero, int64_t N,
+                  int64_t K, int group, void* packed, egopq_stream_t stream) {
+  int rc = check_w4_shape(0, N, K, group);
+  if (rc) return rc;
+  rc = check_ptrs(4, "w_q", w_q, "scale_f16", scale_f16, "zero", zero, "packed", packed);
+  if (rc) return rc;
+  if ((rc = check_arch())) return rc;
+  cudaError_t e = launch_pack_w4(w_q, scale_f16, zero, N, K, packed, (cudaStream_t)stream);
+  return e == cudaSuccess ? EGOPQ_OK : cuda_fail(e, "pack_w4 launch");
+}
+
+int egopq_unpack_w4(const void* packed, int64_t N, int64_t K, int group, uint8_t* w_q,
+                    uint16_t* scale_f16, uint8_t* zero, egopq_stream_t stream) {
+  int rc = check_w4_shape(0, N, K, group);
+  if (rc) return rc;
+  rc = check_ptrs(4, "packed", packed, "w_q", w_q, "scale_f16", scale_f16, "zero", zero);
+  if (rc) return rc;
+  if ((rc = check_arch())) return rc;
+  cudaError_t e = launch_unpack_w4(packed, N, K, w_q, scale_f16, zero, (cudaStream_t)stream);
+  return e == cudaSuccess ? EGOPQ_OK : cuda_fail(e, "unpack_w4 launch");
+}
+
+int egopq_quant_act_i8(const uint16_t* x_bf16, int64_t M, int64_t K, int group, int8_t* a_q,
+                       float* a_s, int32_t* a_gsum, uint16_t* a_q16, egopq_stream_t stream) {
+  if (M < 0 || K <= 0 || M >= kMaxDim || K >= kMaxDim)
+    return fail(EGOPQ_ERR_INVALID_ARG, "bad sizes M=%lld K=%lld", (long long)M, (long long)K);
+  if (group != 128) return fail(EGOPQ_ERR_UNSUPPORTED_SHAPE, "group must be 128 (got %d)", group);
+  if (K % 128) return fail(EGOPQ_ERR_UNSUPPORTED_SHAPE, "K must be a multiple of 128");
+  if (M == 0) return EGOPQ_OK;
+  int rc = check_ptrs(4, "x_bf16", x_bf16, "a_q", a_q, "a_s", a_s, "a_gsum", a_gsum);
+  if (rc) return rc;
+  if (a_q16 && !aligned16(a_q16)) return fail(EGOPQ_ERR_MISALIGNED, "a_q16 is not 16-byte aligned");
+  if ((rc = check_arch())) return rc;
+  cudaError_t e = launch_quant_act(x_bf16, M, K, a_q, a_s, a_gsum, a_q16, (cudaStream_t)stream);
+  return e == cudaSuccess ? EGOPQ_OK : cuda_fail(e, "quant_act launch");
+}
+
+int egopq_w4a8_gemm_ex(const int8_t* a_q, const uint16_t* a_q16, const float* a_s,
+                       const int32_t* a_gsum, const void* packed, int64_t M, int64_t N,
+                       int64_t K, int group, uint16_t* y_bf16, int path, egopq_stream_t stream) {
+  int rc = check_w4_shape(M, N, K, group);
+  if (rc) return rc;
+  if (M == 0) return EGOPQ_OK;
+  rc = check_ptrs(5, "a_q", a_q, "a_s", a_s, "a_gsum", a_gsum, "packed", packed, "y_bf16", y_bf16);
+  if (rc) return rc;
+  if (a_q16 && !aligned16(a_q16)) return fail(EGOPQ_ERR_MISALIGNED, "a_q16 is not 16-byte aligned");
+  GemmArgs a{};
+  a.variant = kW4A8;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.a_q = a_q;
+  a.a_q16 = a_q16;
+  a.a_s = a_s;
+  a.a_gsum = a_gsum;
+  a.packed = static_cast<const uint8_t*>(packed);
+  a.y = y_bf16;
+  a.timeout_ns = kDefaultTimeoutNs;
+  return run_gemm(a, path, (cudaStream_t)stream);
+}
+
+int egopq_w4a8_gemm(const int8_t* a_q, const uint16_t* a_q16, const float* a_s,
+                    const int32_t* a_gsum, const void* packed, int64_t M, int64_t N, int64_t K,
+                    int group, uint16_t* y_bf16, egopq_stream_t stream) {
+  return egopq_w4a8_gemm_ex(a_q, a_q16, a_s, a_gsum, packed, M, N, K, group, y_bf16,
+                            EGOPQ_PATH_AUTO, stream);
+}
+
+int egopq_w4a8_group_partials(const int8_t* a_q, const uint16_t* a_q16, const int32_t* a_gsum,
+                              const void* packed, int64_t M, int64_t N, int64_t K, int group,
+                              int32_t* Q, int path, egopq_stream_t stream) {
+  int rc = check_w4_shape(M, N, K, group);
+  if (rc) return rc;
+  if (M == 0) return EGOPQ_OK;
+  rc = check_ptrs(4, "a_q", a_q, "a_gsum", a_gsum, "packed", packed, "Q", Q);
+  if (rc) return rc;
+  if (a_q16 && !aligned16(a_q16)) return fail(EGOPQ_ERR_MISALIGNED, "a_q16 is not 16-byte aligned");
+  GemmArgs a{};
+  a.variant = kW4A8;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.a_q = a_q;
+  a.a_q16 = a_q16;
+  a.a_gsum = a_gsum;
+  a.packed = static_cast<const uint8_t*>(packed);
+  a.partials = Q;
+  a.timeout_ns = kDefaultTimeoutNs;
+  return run_gemm(a, path, (cudaStream_t)stream);
+}
+
+int egopq_w4a16_gemm_ex(const uint16_t* x_bf16, const void* packed, int64_t M, int64_t N,
+                        int64_t K, int group, uint16_t* y_bf16, int path,
+                        egopq_stream_t stream) {
+  int rc = check_w4_shape(M, N, K, group);
+  if (rc) return rc;
+  if (M == 0) return EGOPQ_OK;
+  rc = check_ptrs(3, "x_bf16", x_bf16, "packed", packed, "y_bf16", y_bf16);
+  if (rc) return rc;
+  GemmArgs a{};
+  a.variant = kW4A16;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.x = x_bf16;
+  a.packed = static_cast<const uint8_t*>(packed);
+  a.y = y_bf16;
+  a.timeout_ns = kDefaultTimeoutNs;
+  return run_gemm(a, path, (cudaStream_t)stream);
+}
+
+int egopq_w4a16_gemm(const uint16_t* x_bf16, const void* packed, int64_t M, int64_t N,
+                     int64_t K, int group, uint16_t* y_bf16, egopq_stream_t stream) {
+  return egopq_w4a16_gemm_ex(x_bf16, packed, M, N, K, group, y_bf16, EGOPQ_PATH_AUTO, stream);
+}
+
+int egopq_w8a16_gemm_ex(const uint16_t* x_bf16, const int8_t* w_q, const uint16_t* scale_f16,
+                        int64_t M, int64_t N, int64_t K, uint16_t* y_bf16, int path,
+                        egopq_stream_t stream) {
+  int rc = check_w4_shape(M, N, K, 128);
+  if (rc) return rc;
+  if (M == 0) return EGOPQ_OK;
+  rc = check_ptrs(4, "x_bf16", x_bf16, "w_q", w_q, "scale_f16", scale_f16, "y_bf16", y_bf16);
+  if (rc) return rc;
+  GemmArgs a{};
+  a.variant = kW8A16;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.x = x_bf16;
+  a.w8 = w_q;
+  a.s8 = scale_f16;
+  a.y = y_bf16;
+  a.timeout_ns = kDefaultTimeoutNs;
+  return run_gemm(a, path, (cudaStream_t)stream);
+}
+
+int egopq_w8a16_gemm(const uint16_t* x_bf16, const int8_t* w_q, const uint16_t* scale_f16,
+                     int64_t M, int64_t N, int64_t K, uint16_t* y_bf16, egopq_stream_t stream) {
+  return egopq_w8a16_gemm_ex(x_bf16, w_q, scale_f16, M, N, K, y_bf16, EGOPQ_PATH_AUTO, stream);
+}
+
+int egopq_supported(int64_t M, int64_t N, int64_t K, int group, int variant) {
+  if (variant < EGOPQ_VARIANT_W4A8 || variant > EGOPQ_VARIANT_W8A16) return 0;
+  if (variant == EGOPQ_VARIANT_W8A16) group = 128;
+  if (M < 0 || N <= 0 || K <= 0 || M >= kMaxDim || N >= kMaxDim || K >= kMaxDim) return 0;
+  if (group != 128 || K % 128 || N % 128) return 0;
+  if (check_arch() != EGOPQ_OK) return 0;
+  return 1;
+}
+
+int egopq_device_status(egopq_stream_t stream) {
+  cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  unsigned int word = 0;
+  e = cudaMemcpyFromSymbol(&word, g_error_word, sizeof(word));
+  if (e != cudaSuccess) return cuda_fail(e, "read error word");
+  if (word) {
+    const unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero));
+    if (e != cudaSuccess) return cuda_fail(e, "clear error word");
+    if (word & kErrTimeout) return fail(EGOPQ_ERR_TIMEOUT, "a kernel's bounded wait expired");
+  }
+  return EGOPQ_OK;
+}
+
+int egopq_selftest_timeout(int timeout_us, egopq_stream_t stream) {
+  if (timeout_us < 1 || timeout_us > 1000000)
+    return fail(EGOPQ_ERR_INVALID_ARG, "timeout_us must be in [1, 1000000]");
+  int rc = check_arch();
+  if (rc) return rc;
+  cudaError_t e = launch_selftest_timeout((uint64_t)timeout_us * 1000ull, (cudaStream_t)stream);
+  return e == cudaSuccess ? EGOPQ_OK : cuda_fail(e, "selftest launch");
+}
+
+}  // extern "C"

@@ -1,0 +1,54 @@
+// egopq_internal.h -- launchers shared between the kernel files and the C ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "egopq_common.cuh"
+
+namespace egopq {
+
+enum Variant { kW4A8 = 0, kW4A16 = 1, kW8A16 = 2 };
+
+// Operands of one GEMM call, already validated by the ABI layer.
+struct GemmArgs {
+  int variant;
+  int64_t M, N, K;
+  // W4A8
+  const int8_t* a_q;
+  const uint16_t* a_q16;
+  const float* a_s;
+  const int32_t* a_gsum;
+  // W4A16 / W8A16
+  const uint16_t* x;
+  // packed int4 weight (W4A8, W4A16)
+  const uint8_t* packed;
+  // int8 weight and per-channel scale (W8A16)
+  const int8_t* w8;
+  const uint16_t* s8;
+  // outputs
+  uint16_t* y;
+  int32_t* partials;  // non-null: write group partials instead of y (W4A8 only)
+  uint64_t timeout_ns;
+};
+
+cudaError_t launch_quant_act(const uint16_t* x, int64_t M, int64_t K, int8_t* a_q, float* a_s,
+                             int32_t* a_gsum, uint16_t* a_q16, cudaStream_t st);
+cudaError_t launch_pack_w4(const uint8_t* w_q, const uint16_t* s, const uint8_t* z, int64_t N,
+                           int64_t K, void* packed, cudaStream_t st);
+cudaError_t launch_unpack_w4(const void* packed, int64_t N, int64_t K, uint8_t* w_q, uint16_t* s,
+                             uint8_t* z, cudaStream_t st);
+
+// CUDA-core GEMV (small M). Returns cudaErrorNotSupported for shapes it does
+// not take.
+cudaError_t launch_gemv(const GemmArgs& a, cudaStream_t st);
+// tcgen05 tensor-core GEMM (any M).
+cudaError_t launch_tc_gemm(const GemmArgs& a, cudaStream_t st);
+// Bounded-wait self test.
+cudaError_t launch_selftest_timeout(uint64_t timeout_ns, cudaStream_t st);
+
+// Largest M per GEMV launch slice.
+constexpr int kGemvMaxRows = 4;
+
+}  // namespace egopq

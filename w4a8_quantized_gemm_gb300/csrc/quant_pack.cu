@@ -1,0 +1,201 @@
+// quant_pack.cu -- per-token int8 activation quantization and int4 weight
+// packing kernels.
+//
+// Activation quantization follows "The 4-bit CPU path", section "W4A8 -
+// _C::int4_scaled_mm_cpu" (activations are quantized to int8 at run time):
+// symmetric per token, a_s = absmax / 127, a_q = round_half_even(x / a_s)
+// clamped to +-127, both quotients IEEE fp32 (so the integer codes match any
+// correctly rounded implementation bit for bit). The same pass emits the
+// per-group sums of a_q that fold the zero points into the GEMM epilogue, and
+// optionally the codes as exact fp16 integers for the tensor-core path.
+//
+// Weight packing lays GPTQ-style int4 codes (per-group _gptq_scale /
+// _gptq_zero, "EgoPQ Real-Serving Handoff", section 2) out in 8 KiB tiles of
+// 128 rows x 128 K so that one 1-D bulk copy stages a whole (row block, group)
+// tile, and so that one AND/OR per 32-bit word yields two consecutive K
+// values as an fp16 pair. The layout is documented in include/egopq.h.
+#include "egopq_internal.h"
+
+namespace egopq {
+
+constexpr int kQuantThreads = 256;
+
+__global__ void __launch_bounds__(kQuantThreads)
+quant_act_kernel(const uint16_t* __restrict__ x, int64_t K, int8_t* __restrict__ a_q,
+                 float* __restrict__ a_s, int32_t* __restrict__ a_gsum,
+                 uint16_t* __restrict__ a_q16) {
+  const int64_t m = blockIdx.x;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + m * K);
+  const int64_t nvec = K / 8;  // 8 bf16 per 16-byte vector; K % 128 == 0
+  __shared__ float warp_max[kQuantThreads / 32];
+
+  float amax = 0.f;
+  for (int64_t v = threadIdx.x; v < nvec; v += kQuantThreads) {
+    uint4 p = __ldg(xr + v);
+    uint32_t w[4] = {p.x, p.y, p.z, p.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      amax = fmaxf(amax, fabsf(__uint_as_float(w[i] << 16)));
+      amax = fmaxf(amax, fabsf(__uint_as_float(w[i] & 0xFFFF0000u)));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  amax = warp_max[0];
+#pragma unroll
+  for (int i = 1; i < kQuantThreads / 32; ++i) amax = fmaxf(amax, warp_max[i]);
+
+  const float s = __fdiv_rn(amax, 127.0f);
+  if (threadIdx.x == 0) a_s[m] = s;
+  const bool zero_row = (amax == 0.f);
+
+  for (int64_t v = threadIdx.x; v < nvec; v += kQuantThreads) {
+    uint4 p = __ldg(xr + v);
+    uint32_t w[4] = {p.x, p.y, p.z, p.w};
+    int q[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float lo = __uint_as_float(w[i] << 16);
+      float hi = __uint_as_float(w[i] & 0xFFFF0000u);
+      int ql = zero_row ? 0 : __float2int_rn(__fdiv_rn(lo, s));
+      int qh = zero_row ? 0 : __float2int_rn(__fdiv_rn(hi, s));
+      q[2 * i] = max(-127, min(127, ql));
+      q[2 * i + 1] = max(-127, min(127, qh));
+    }
+    uint2 packed;
+    packed.x = (uint32_t)(q[0] & 0xFF) | ((uint32_t)(q[1] & 0xFF) << 8) |
+               ((uint32_t)(q[2] & 0xFF) << 16) | ((uint32_t)(q[3] & 0xFF) << 24);
+    packed.y = (uint32_t)(q[4] & 0xFF) | ((uint32_t)(q[5] & 0xFF) << 8) |
+               ((uint32_t)(q[6] & 0xFF) << 16) | ((uint32_t)(q[7] & 0xFF) << 24);
+    reinterpret_cast<uint2*>(a_q + m * K)[v] = packed;
+    if (a_q16) {
+      uint32_t h[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        __half2 hv = __halves2half2(__int2half_rn(q[2 * i]), __int2half_rn(q[2 * i + 1]));
+        h[i] = *reinterpret_cast<uint32_t*>(&hv);
+      }
+      reinterpret_cast<uint4*>(a_q16 + m * K)[v] = make_uint4(h[0], h[1], h[2], h[3]);
+    }
+    // 16 consecutive vectors make one 128-wide group; kQuantThreads % 16 == 0
+    // K % 128 == 0, so the 16 lanes of a half-warp are all inside the loop or
+    // all outside it; reduce within the half-warp only.
+    int sum = q[0] + q[1] + q[2] + q[3] + q[4] + q[5] + q[6] + q[7];
+    const unsigned half_mask = 0xFFFFu << (threadIdx.x & 16);
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) sum += __shfl_xor_sync(half_mask, sum, o);
+    if ((threadIdx.x & 15) == 0) a_gsum[m * (K / 128) + v / 16] = sum;
+  }
+}
+
+// nibble p of a packed word carries K offset kNibbleK[p] inside its 8-wide run
+__device__ __constant__ int kNibbleK[8] = {0, 2, 4, 6, 1, 3, 5, 7};
+
+__global__ void pack_codes_kernel(const uint8_t* __restrict__ w_q, int64_t N, int64_t K,
+                                  uint32_t* __restrict__ out) {
+  const int64_t G = K / 128;
+  const int64_t nwords = N * K / 8;
+  for (int64_t w = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; w < nwords;
+       w += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t tile = w / 2048, u = w % 2048;
+    const int64_t t = tile / G, g = tile % G;
+    const int64_t unit = u / 4, j = u % 4;
+    const int64_t c = unit / 128, r = unit % 128;
+    const int64_t n = t * 128 + r, k0 = g * 128 + c * 32 + j * 8;
+    const uint2 src = *reinterpret_cast<const uint2*>(w_q + n * K + k0);
+    const uint8_t* b = reinterpret_cast<const uint8_t*>(&src);
+    uint32_t word = 0;
+#pragma unroll
+    for (int p = 0; p < 8; ++p) word |= (uint32_t)(b[kNibbleK[p]] & 0xF) << (4 * p);
+    out[w] = word;
+  }
+}
+
+__global__ void unpack_codes_kernel(const uint32_t* __restrict__ in, int64_t N, int64_t K,
+                                    uint8_t* __restrict__ w_q) {
+  const int64_t G = K / 128;
+  const int64_t nwords = N * K / 8;
+  for (int64_t w = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; w < nwords;
+       w += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t tile = w / 2048, u = w % 2048;
+    const int64_t t = tile / G, g = tile % G;
+    const int64_t unit = u / 4, j = u % 4;
+    const int64_t c = unit / 128, r = unit % 128;
+    const int64_t n = t * 128 + r, k0 = g * 128 + c * 32 + j * 8;
+    const uint32_t word = in[w];
+    uint2 dst;
+    uint8_t* b = reinterpret_cast<uint8_t*>(&dst);
+#pragma unroll
+    for (int p = 0; p < 8; ++p) b[kNibbleK[p]] = (word >> (4 * p)) & 0xF;
+    *reinterpret_cast<uint2*>(w_q + n * K + k0) = dst;
+  }
+}
+
+// scales: [N][G] -> [G][N] (and back); zeros: [N][G] bytes -> [G][N/2] nibble pairs
+__global__ void pack_meta_kernel(const uint16_t* __restrict__ s, const uint8_t* __restrict__ z,
+                                 int64_t N, int64_t G, uint16_t* __restrict__ s_out,
+                                 uint8_t* __restrict__ z_out) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < G * N;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t g = i / N, n = i % N;
+    s_out[i] = s[n * G + g];
+    if ((n & 1) == 0)
+      z_out[g * (N / 2) + n / 2] =
+          (uint8_t)((z[n * G + g] & 0xF) | ((z[(n + 1) * G + g] & 0xF) << 4));
+  }
+}
+
+__global__ void unpack_meta_kernel(const uint16_t* __restrict__ s_in,
+                                   const uint8_t* __restrict__ z_in, int64_t N, int64_t G,
+                                   uint16_t* __restrict__ s, uint8_t* __restrict__ z) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < G * N;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t g = i / N, n = i % N;
+    s[n * G + g] = s_in[i];
+    const uint8_t b = z_in[g * (N / 2) + n / 2];
+    z[n * G + g] = (n & 1) ? (b >> 4) : (b & 0xF);
+  }
+}
+
+static unsigned grid_for(int64_t work, int threads) {
+  int64_t b = (work + threads - 1) / threads;
+  return (unsigned)(b < 1 ? 1 : (b > 65535 * 8 ? 65535 * 8 : b));
+}
+
+cudaError_t launch_quant_act(const uint16_t* x, int64_t M, int64_t K, int8_t* a_q, float* a_s,
+                             int32_t* a_gsum, uint16_t* a_q16, cudaStream_t st) {
+  quant_act_kernel<<<(unsigned)M, kQuantThreads, 0, st>>>(x, K, a_q, a_s, a_gsum, a_q16);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack_w4(const uint8_t* w_q, const uint16_t* s, const uint8_t* z, int64_t N,
+                           int64_t K, void* packed, cudaStream_t st) {
+  const int64_t G = K / 128;
+  uint8_t* base = static_cast<uint8_t*>(packed);
+  pack_codes_kernel<<<grid_for(N * K / 8, 256), 256, 0, st>>>(w_q, N, K,
+                                                               reinterpret_cast<uint32_t*>(base));
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  uint16_t* s_out = reinterpret_cast<uint16_t*>(base + N * K / 2);
+  uint8_t* z_out = base + N * K / 2 + 2 * G * N;
+  pack_meta_kernel<<<grid_for(G * N, 256), 256, 0, st>>>(s, z, N, G, s_out, z_out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_unpack_w4(const void* packed, int64_t N, int64_t K, uint8_t* w_q, uint16_t* s,
+                             uint8_t* z, cudaStream_t st) {
+  const int64_t G = K / 128;
+  const uint8_t* base = static_cast<const uint8_t*>(packed);
+  unpack_codes_kernel<<<grid_for(N * K / 8, 256), 256, 0, st>>>(
+      reinterpret_cast<const uint32_t*>(base), N, K, w_q);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const uint16_t* s_in = reinterpret_cast<const uint16_t*>(base + N * K / 2);
+  const uint8_t* z_in = base + N * K / 2 + 2 * G * N;
+  unpack_meta_kernel<<<grid_for(G * N, 256), 256, 0, st>>>(s_in, z_in, N, G, s, z);
+  return cudaGetLastError();
+}
+
+}  // namespace egopq

@@ -1,0 +1,570 @@
+// tc_gemm.cu -- tcgen05 tensor-core GEMM for the W4A8, W4A16 and W8A16 linears.
+//
+// The pages describe the W4A8 linear only as prior art for other hardware (an
+// AMX CPU kernel, "The 4-bit CPU path", section "W4A8 - _C::int4_scaled_mm_cpu";
+// an optional CUTLASS large-prefill dispatch, "EgoPQ Real-Serving Handoff",
+// section 1). This kernel is designed for sm_103a from the method itself:
+//
+//   y[m,n] = a_s[m] * sum_g s[n,g] * Q[m,n,g],
+//   Q[m,n,g] = sum_{k in g} a_q[m,k] * (w_q[n,k] - z[n,g])
+//
+// sm_103a has no integer tcgen05.mma, so each group partial is formed EXACTLY
+// on the kind::f16 path: a_q (|a_q| <= 127) and w_q - z (in [-15, 15]) are
+// exact fp16 integers, every product is exact, and a 128-wide group sums to at
+// most 128*127*15 = 243840 < 2^24 in magnitude, so fp32 accumulation of one
+// group in Tensor Memory is exact. The accumulator is drained after every
+// group, scaled by s[n,g] and accumulated in fp32 registers.
+//
+// Operand roles ("swap AB"): the 128 weight rows of a tile are the MMA's M
+// dimension and live in TENSOR MEMORY as the A operand; the token tile (BT
+// tokens, 16..128) is the MMA's N dimension and comes from shared memory as
+// the B operand, staged by TMA with 128-byte swizzle. The dequantized weights
+// therefore never touch shared memory: converter warps read the packed int4
+// tile (one 8 KiB bulk copy per 128 rows x 128 K), turn codes into
+// (w_q - z) fp16 pairs with one AND/OR and one HSUB2/HFMA2 per pair, and
+// store them straight into TMEM with tcgen05.st.
+//
+// Warp roles (448 threads, one CTA per SM):
+//   warps 0-7   drain: TMEM accumulator -> registers, *s, accumulate, epilogue;
+//               warps 0-3 own token columns [0, BT/2), warps 4-7 [BT/2, BT)
+//   warps 8-11  convert: packed int4 (or int8) smem tile -> fp16/bf16 in TMEM
+//   warp  12    TMA producer (activations tile + weight tile per group)
+//   warp  13    TMEM allocator and single-thread MMA issuer
+// (a warp reaches TMEM lanes 32*(warp % 4) .. +31, so each role that touches
+// TMEM is a whole warpgroup)
+// Pipelines: S shared-memory stages, 2 TMEM A buffers, 2 TMEM accumulators,
+// all handed over with mbarriers; every wait is bounded.
+//
+// Split-K for small grids: a cluster of up to 8 CTAs shares one output tile,
+// each taking a contiguous range of groups; partial sums are reduced through
+// distributed shared memory in rank order (deterministic, no global scratch).
+//
+// Variants: W4A16 uses bf16 operands (activations as given, w_q - z exact in
+// bf16) and no a_s; W8A16 converts int8 weights to bf16 and accumulates all
+// of K in TMEM, applying the per-channel scale once at the end.
+#include "egopq_internal.h"
+
+namespace egopq {
+
+constexpr int kTcThreads = 448;
+constexpr int kProducerWarp = 12, kMmaWarp = 13, kConvWarp0 = 8;
+constexpr int kNumA = 2;   // TMEM A-operand buffers (64 columns each)
+constexpr int kNumD = 2;   // TMEM accumulators (BT columns each)
+constexpr int kMaxSmem = 232448;
+
+struct TcParams {
+  int64_t M, N, K;
+  int G, ks;
+  const float* a_s;
+  const uint8_t* packed;
+  const uint16_t* s8;
+  uint16_t* y;
+  int32_t* partials;
+  uint64_t timeout_ns;
+};
+
+template <int VARIANT, int BT>
+struct TcCfg {
+  static constexpr int kActBox = BT * 128;                        // one 64-wide K box, bytes
+  static constexpr int kActBytes = 2 * kActBox;                   // a 128-wide group
+  static constexpr int kWBytes = (VARIANT == kW8A16) ? 16384 : 8192;
+  static constexpr int kStageBytes = kActBytes + kWBytes;
+  static constexpr int kStagesRaw = (kMaxSmem - 2048) / kStageBytes;
+  static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
+  static constexpr int kBarOffset = kStages * kStageBytes;
+  static constexpr int kSmemBytes = kBarOffset + 256 + 1024;     // + barriers + alignment slack
+  static constexpr int kTmemColsRaw = kNumD * BT + kNumA * 64;
+  static constexpr int kTmemCols = kTmemColsRaw <= 32    ? 32
+                                   : kTmemColsRaw <= 64  ? 64
+                                   : kTmemColsRaw <= 128 ? 128
+                                   : kTmemColsRaw <= 256 ? 256
+                                                         : 512;
+  static constexpr bool kDrainPerGroup = (VARIANT != kW8A16);
+  static constexpr int kBf16 = (VARIANT == kW4A8) ? 0 : 1;
+  static_assert(kStages >= 2, "shared memory too small for two stages");
+  static_assert(kTmemColsRaw <= 512, "TMEM budget");
+  static_assert(BT % 16 == 0 && BT >= 16 && BT <= 128, "token tile");
+};
+
+template <int VARIANT, int BT, bool PARTIALS>
+__global__ void __launch_bounds__(kTcThreads, 1)
+tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
+               const __grid_constant__ CUtensorMap w8_map, const TcParams p) {
+  using C = TcCfg<VARIANT, BT>;
+  constexpr int S = C::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  // 1024-byte alignment for the 128-byte-swizzle atoms
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t base = (raw_addr + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw_addr);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ks = blockIdx.x;
+  const int64_t m0 = (int64_t)blockIdx.y * BT;
+  const int64_t n0 = (int64_t)blockIdx.z * 128;
+  const int64_t N = p.N, K = p.K;
+  const int G = p.G;
+  const int g0 = (int)((int64_t)ks * G / p.ks), g1 = (int)((int64_t)(ks + 1) * G / p.ks);
+  const int ng = g1 - g0;
+
+  // barriers and flags
+  const uint32_t bar0 = base + C::kBarOffset;
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
+  auto afull_bar = [&](int i) { return bar0 + 8u * (2 * S + i); };
+  auto aempty_bar = [&](int i) { return bar0 + 8u * (2 * S + kNumA + i); };
+  auto dfull_bar = [&](int i) { return bar0 + 8u * (2 * S + 2 * kNumA + i); };
+  auto dempty_bar = [&](int i) { return bar0 + 8u * (2 * S + 2 * kNumA + kNumD + i); };
+  uint8_t* misc = smem + C::kBarOffset + 8 * (2 * S + 2 * kNumA + 2 * kNumD);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
+  auto stage_act = [&](int s) { return base + (uint32_t)(s * C::kStageBytes); };
+  auto stage_w_ptr = [&](int s) { return smem + s * C::kStageBytes + C::kActBytes; };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1 + 4);
+    }
+    for (int i = 0; i < kNumA; ++i) {
+      mbar_init(afull_bar(i), 4);
+      mbar_init(aempty_bar(i), 1);
+    }
+    for (int i = 0; i < kNumD; ++i) {
+      mbar_init(dfull_bar(i), 1);
+      mbar_init(dempty_bar(i), 8);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kProducerWarp && lane == 0) {
+    prefetch_tensormap(&act_map);
+    if constexpr (VARIANT == kW8A16) prefetch_tensormap(&w8_map);
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t d_tmem = tmem;                  // accumulators: columns [0, 2*BT)
+  const uint32_t a_tmem = tmem + kNumD * BT;     // A operand:    columns [2*BT, 2*BT+128)
+  const uint64_t tmo = p.timeout_ns;
+
+  constexpr int HB = BT / 2;  // token columns per drain warpgroup
+  // Each role ends with the same named CTA barrier (all 448 threads) and, for
+  // split-K clusters, the same two cluster barriers, so the drain warps can
+  // keep their accumulators in registers through the epilogue.
+  auto teardown_sync = [&]() {
+    tc_fence_before();
+    asm volatile("bar.sync 1, %0;" ::"n"(kTcThreads) : "memory");
+  };
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int issued = 0;
+      for (int i = 0; i < ng; ++i) {
+        const int s = i % S;
+        if (!mbar_wait(empty_bar(s), ((i / S) & 1) ^ 1, abort_flag, tmo)) break;
+        mbar_arrive_expect_tx(full_bar(s), C::kStageBytes);
+        const int g = g0 + i;
+        tma_load_2d(stage_act(s), &act_map, full_bar(s), g * 128, (int)m0);
+        tma_load_2d(stage_act(s) + C::kActBox, &act_map, full_bar(s), g * 128 + 64, (int)m0);
+        if constexpr (VARIANT == kW8A16) {
+          tma_load_2d(stage_act(s) + C::kActBytes, &w8_map, full_bar(s), g * 128, (int)n0);
+        } else {
+          const uint8_t* src = p.packed + ((int64_t)blockIdx.z * G + g) * 8192;
+          bulk_load(stage_act(s) + C::kActBytes, src, 8192, full_bar(s));
+        }
+        ++issued;
+      }
+      // wait (bounded) for every copy this thread issued to land before exit
+      for (int i = (issued > S ? issued - S : 0); i < issued; ++i) {
+        volatile int no_abort = 0;
+        mbar_wait(full_bar(i % S), (i / S) & 1, &no_abort, tmo);
+      }
+    }
+    __syncwarp();
+    teardown_sync();
+    if (!PARTIALS && p.ks > 1) {
+      cluster_sync_all();
+      cluster_sync_all();
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_f16(128, BT, C::kBf16);
+      int last_empty = -1;
+      for (int i = 0; i < ng; ++i) {
+        const int s = i % S, ab = i % kNumA;
+        const int di = C::kDrainPerGroup ? i : 0;
+        const int db = di % kNumD;
+        if (!mbar_wait(full_bar(s), (i / S) & 1, abort_flag, tmo)) break;
+        if (!mbar_wait(afull_bar(ab), (i / kNumA) & 1, abort_flag, tmo)) break;
+        if (C::kDrainPerGroup || i == 0)
+          if (!mbar_wait(dempty_bar(db), ((di / kNumD) & 1) ^ 1, abort_flag, tmo)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t b_addr = stage_act(s) + (j >> 2) * C::kActBox + (j & 3) * 32;
+          const uint32_t acc = C::kDrainPerGroup ? (j > 0) : (i > 0 || j > 0);
+          tc_mma_f16_ts(d_tmem + db * BT, a_tmem + ab * 64 + j * 8, sdesc_kmajor_sw128(b_addr),
+                        idesc, acc);
+        }
+        tc_commit(empty_bar(s));
+        tc_commit(aempty_bar(ab));
+        if (C::kDrainPerGroup || i == ng - 1) tc_commit(dfull_bar(db));
+        last_empty = i;
+      }
+      if (last_empty >= 0) {  // let the last MMAs finish before teardown
+        volatile int no_abort = 0;
+        mbar_wait(empty_bar(last_empty % S), (last_empty / S) & 1, &no_abort, tmo);
+      }
+    }
+    __syncwarp();
+    teardown_sync();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+    if (!PARTIALS && p.ks > 1) {
+      cluster_sync_all();
+      cluster_sync_all();
+    }
+  } else if (warp >= kConvWarp0) {
+    // ------------------------------------------------------------ converters
+    const int r = (warp - kConvWarp0) * 32 + lane;  // weight row in the tile == TMEM lane
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint8_t* zeros = p.packed + N * K / 2 + 2 * (int64_t)G * N;
+    for (int i = 0; i < ng; ++i) {
+      const int s = i % S, ab = i % kNumA;
+      const int g = g0 + i;
+      if (!mbar_wait(full_bar(s), (i / S) & 1, abort_flag, tmo)) break;
+      uint32_t out[64];
+      if constexpr (VARIANT == kW8A16) {
+        const uint8_t* wt = stage_w_ptr(s) + r * 128;
+        uint4 v[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          v[c] = *reinterpret_cast<const uint4*>(wt + ((c ^ (r & 7)) * 16));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty_bar(s));
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint32_t wv[4] = {v[c].x ^ 0x80808080u, v[c].y ^ 0x80808080u,
+                                  v[c].z ^ 0x80808080u, v[c].w ^ 0x80808080u};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              // 2^23 + (w + 128) as fp32 bits, minus 2^23 + 128: exactly w
+              const float lo =
+                  __uint_as_float(prmt(wv[q], 0x4B000000u, 0x7650u | (2 * h))) - 8388736.0f;
+              const float hi =
+                  __uint_as_float(prmt(wv[q], 0x4B000000u, 0x7650u | (2 * h + 1))) - 8388736.0f;
+              __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
+              out[c * 8 + q * 2 + h] = *reinterpret_cast<uint32_t*>(&b2);
+            }
+          }
+        }
+      } else {
+        const uint8_t* wt = stage_w_ptr(s) + r * 16;
+        uint4 v[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) v[c] = *reinterpret_cast<const uint4*>(wt + c * 2048);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty_bar(s));
+        const int64_t n = n0 + r;
+        const uint8_t zb = __ldg(zeros + (int64_t)g * (N / 2) + (n >> 1));
+        const uint32_t z = (n & 1) ? (zb >> 4) : (zb & 0xF);
+        if constexpr (VARIANT == kW4A8) {
+          // fp16: 0x6400|e = 1024+e, 0x6400|(e<<4) = 1024+16e (exact)
+          const __half2 zlo = __half2half2(__ushort_as_half((uint16_t)(0x6400u | z)));
+          const __half2 zhi = __half2half2(__float2half_rn(64.0f + (float)z));
+          const __half2 sixteenth = __float2half2_rn(0.0625f);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const uint32_t wv[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint32_t w = wv[j], w2 = wv[j] >> 8;
+              uint32_t h0 = lop3_and_or(w, 0x000F000Fu, 0x64006400u);
+              uint32_t h1 = lop3_and_or(w, 0x00F000F0u, 0x64006400u);
+              uint32_t h2 = lop3_and_or(w2, 0x000F000Fu, 0x64006400u);
+              uint32_t h3 = lop3_and_or(w2, 0x00F000F0u, 0x64006400u);
+              __half2 r0 = __hsub2(*reinterpret_cast<__half2*>(&h0), zlo);
+              __half2 r1 = __hfma2(*reinterpret_cast<__half2*>(&h1), sixteenth, __hneg2(zhi));
+              __half2 r2 = __hsub2(*reinterpret_cast<__half2*>(&h2), zlo);
+              __half2 r3 = __hfma2(*reinterpret_cast<__half2*>(&h3), sixteenth, __hneg2(zhi));
+              out[c * 16 + j * 4 + 0] = *reinterpret_cast<uint32_t*>(&r0);
+              out[c * 16 + j * 4 + 1] = *reinterpret_cast<uint32_t*>(&r1);
+              out[c * 16 + j * 4 + 2] = *reinterpret_cast<uint32_t*>(&r2);
+              out[c * 16 + j * 4 + 3] = *reinterpret_cast<uint32_t*>(&r3);
+            }
+          }
+        } else {
+          // bf16: 0x4300|e = 128+e (exact for e < 128)
+          const __nv_bfloat162 zz =
+              __bfloat162bfloat162(__ushort_as_bfloat16((uint16_t)(0x4300u | z)));
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const uint32_t wv[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                uint32_t h = lop3_and_or(wv[j] >> (4 * q), 0x000F000Fu, 0x43004300u);
+                __nv_bfloat162 rr = __hsub2(*reinterpret_cast<__nv_bfloat162*>(&h), zz);
+                out[c * 16 + j * 4 + q] = *reinterpret_cast<uint32_t*>(&rr);
+              }
+            }
+          }
+        }
+      }
+      if (!mbar_wait(aempty_bar(ab), ((i / kNumA) & 1) ^ 1, abort_flag, tmo)) break;
+      const uint32_t dst = a_tmem + lane_base + ab * 64;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t chunk[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) chunk[q] = out[c * 16 + q];
+        tmem_st16(dst + c * 16, chunk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(afull_bar(ab));
+    }
+    __syncwarp();
+    teardown_sync();
+    if (!PARTIALS && p.ks > 1) {
+      cluster_sync_all();
+      cluster_sync_all();
+    }
+  } else {
+    // ------------------------------------------------------------ drain (warps 0-7)
+    const int r = (warp & 3) * 32 + lane;
+    const int col0 = (warp >> 2) * HB;
+    const int64_t n = n0 + r;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint16_t* scales = reinterpret_cast<const uint16_t*>(p.packed + N * K / 2);
+    const int nd = C::kDrainPerGroup ? ng : (ng > 0 ? 1 : 0);
+    float R[HB];  // fp32 running sums for this thread's weight row
+#pragma unroll
+    for (int t = 0; t < HB; ++t) R[t] = 0.f;
+    for (int i = 0; i < nd; ++i) {
+      const int db = i % kNumD;
+      const int g = g0 + i;
+      float s = 1.f;
+      if constexpr (C::kDrainPerGroup) s = f16_bits_to_f32(__ldg(scales + (int64_t)g * N + n));
+      if (!mbar_wait(dfull_bar(db), (i / kNumD) & 1, abort_flag, tmo)) break;
+      tc_fence_after();
+      constexpr int CW = HB < 16 ? HB : 16;  // columns per tcgen05.ld
+#pragma unroll
+      for (int cb = 0; cb < HB / CW; ++cb) {
+        uint32_t v[16];
+        const uint32_t src = d_tmem + lane_base + db * BT + col0 + cb * CW;
+        if constexpr (CW == 16) tmem_ld16(src, v);
+        else tmem_ld8(src, v);
+        tmem_wait_ld();
+        if constexpr (PARTIALS) {
+#pragma unroll
+          for (int q = 0; q < CW; ++q) {
+            const int64_t m = m0 + col0 + cb * CW + q;
+            if (m < p.M) p.partials[(m * N + n) * G + g] = __float2int_rn(__uint_as_float(v[q]));
+          }
+        } else {
+#pragma unroll
+          for (int q = 0; q < CW; ++q) R[cb * CW + q] = fmaf(s, __uint_as_float(v[q]), R[cb * CW + q]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(dempty_bar(db));
+    }
+    if constexpr (VARIANT == kW8A16) {
+      const float sc = f16_bits_to_f32(__ldg(p.s8 + n));
+#pragma unroll
+      for (int t = 0; t < HB; ++t) R[t] *= sc;
+    }
+    __syncwarp();
+    teardown_sync();
+    if constexpr (!PARTIALS) {
+      // every copy and MMA of this CTA has completed: the stages are free
+      float* red = reinterpret_cast<float*>(smem);  // [BT][128]
+      if (p.ks > 1) {
+#pragma unroll
+        for (int t = 0; t < HB; ++t) red[(col0 + t) * 128 + r] = R[t];
+        cluster_sync_all();
+        if (cluster_ctarank() == 0) {
+          const uint32_t local = smem_u32(red);
+          for (int rk = 1; rk < p.ks; ++rk) {
+            const uint32_t remote = map_to_rank(local, rk);
+#pragma unroll
+            for (int t = 0; t < HB; ++t) R[t] += ld_dsmem_f32(remote + ((col0 + t) * 128 + r) * 4);
+          }
+        }
+        cluster_sync_all();
+      }
+      if (p.ks == 1 || cluster_ctarank() == 0) {
+#pragma unroll
+        for (int t = 0; t < HB; ++t) {
+          const int64_t m = m0 + col0 + t;
+          if (m < p.M) {
+            float v = R[t];
+            if constexpr (VARIANT == kW4A8) v = __ldg(p.a_s + m) * v;
+            p.y[m * N + n] = f32_to_bf16_bits(v);
+          }
+        }
+      }
+    }
+  }
+}
+
+// ---- bounded-wait self test -----------------------------------------------------
+__global__ void selftest_timeout_kernel(uint64_t timeout_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  // nothing ever arrives on `bar`: the wait must give up and flag a timeout
+  if (threadIdx.x == 0) mbar_wait(smem_u32(&bar), 0, &abort_flag, timeout_ns);
+  __syncthreads();
+}
+
+cudaError_t launch_selftest_timeout(uint64_t timeout_ns, cudaStream_t st) {
+  selftest_timeout_kernel<<<1, 32, 0, st>>>(timeout_ns);
+  return cudaGetLastError();
+}
+
+// ---- host side ----------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+// 2-D row-major [rows][cols] tensor, box {box_cols, box_rows}, 128-byte swizzle.
+static bool make_map(CUtensorMap* map, CUtensorMapDataType dt, int elem_bytes, const void* ptr,
+                     int64_t rows, int64_t cols, int box_cols, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(cols * elem_bytes)};
+  cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+static int tc_sm_count() {
+  static int count = 0;
+  if (!count) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&count, cudaDevAttrMultiProcessorCount, dev);
+    if (count <= 0) count = 148;
+  }
+  return count;
+}
+
+template <int VARIANT, int BT, bool PARTIALS>
+static cudaError_t launch_tc(const GemmArgs& a, cudaStream_t st) {
+  using C = TcCfg<VARIANT, BT>;
+  CUtensorMap act_map, w8_map;
+  memset(&w8_map, 0, sizeof(w8_map));
+  const void* act_ptr = (VARIANT == kW4A8) ? (const void*)a.a_q16 : (const void*)a.x;
+  const CUtensorMapDataType adt =
+      (VARIANT == kW4A8) ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if (!make_map(&act_map, adt, 2, act_ptr, a.M, a.K, 64, BT)) return cudaErrorInvalidValue;
+  if (VARIANT == kW8A16) {
+    if (!make_map(&w8_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.w8, a.N, a.K, 128, 128))
+      return cudaErrorInvalidValue;
+  }
+  const int G = (int)(a.K / 128);
+  const int64_t m_tiles = (a.M + BT - 1) / BT;
+  const int64_t n_tiles = a.N / 128;
+  const int64_t tiles = m_tiles * n_tiles;
+  int ks = 1;
+  if (tiles < tc_sm_count()) {
+    ks = (int)((tc_sm_count() + tiles - 1) / tiles);
+    if (ks > 8) ks = 8;
+    if (ks > G) ks = G;
+  }
+  if (m_tiles > 65535 || n_tiles > 65535) return cudaErrorInvalidValue;
+  TcParams p{};
+  p.M = a.M;
+  p.N = a.N;
+  p.K = a.K;
+  p.G = G;
+  p.ks = ks;
+  p.a_s = a.a_s;
+  p.packed = a.packed;
+  p.s8 = a.s8;
+  p.y = a.y;
+  p.partials = a.partials;
+  p.timeout_ns = a.timeout_ns;
+  auto kern = tc_gemm_kernel<VARIANT, BT, PARTIALS>;
+  static bool attr_set = false;  // one-time opt-in to the large shared-memory carve-out
+  if (!attr_set) {
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)ks, (unsigned)m_tiles, (unsigned)n_tiles);
+  cfg.blockDim = dim3(kTcThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)ks;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, act_map, w8_map, p);
+}
+
+template <int VARIANT, bool PARTIALS>
+static cudaError_t launch_tc_bt(const GemmArgs& a, cudaStream_t st) {
+  if (a.M <= 16) return launch_tc<VARIANT, 16, PARTIALS>(a, st);
+  if (a.M <= 32) return launch_tc<VARIANT, 32, PARTIALS>(a, st);
+  if (a.M <= 64) return launch_tc<VARIANT, 64, PARTIALS>(a, st);
+  return launch_tc<VARIANT, 128, PARTIALS>(a, st);
+}
+
+cudaError_t launch_tc_gemm(const GemmArgs& a, cudaStream_t st) {
+  if (a.M == 0) return cudaSuccess;
+  switch (a.variant) {
+    case kW4A8:
+      return a.partials ? launch_tc_bt<kW4A8, true>(a, st) : launch_tc_bt<kW4A8, false>(a, st);
+    case kW4A16:
+      return launch_tc_bt<kW4A16, false>(a, st);
+    case kW8A16:
+      return launch_tc_bt<kW8A16, false>(a, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace egopq
