@@ -11,6 +11,7 @@ Workloads (synthetic, seeded; shapes of Qwen2.5-7B linears and DiT blocks):
   dit      one step = W4A16 and W8A16 on K=3072,N in {3072,12288} and
            K=12288,N=3072 at M in {1, 16, 4096}.
   tiny     M=16, K=512, N=256 (the oracle-sized case).
+  linear   one W4A8 linear of --k/--n at --m tokens (used for profiling captures).
 
 value = algorithmic bytes (decode, dit-weight-only at M<=16) or algorithmic
 integer ops (prefill) per second over K timed steps, inputs resident in HBM.
@@ -137,7 +138,7 @@ class ClockSampler:
 class Workload:
     """A list of launches per step ("ops"), built once; inputs resident on device."""
 
-    def __init__(self, name, dev, copies=None, m=1):
+    def __init__(self, name, dev, copies=None, m=1, lin=(3584, 3584)):
         import torch
 
         import synth
@@ -148,11 +149,13 @@ class Workload:
         self.inputs = []      # per copy: list of device tensors fed from host in e2e
         self.outputs = []
         t = lambda a, dt=None: _to_dev(torch, a, dev, dt)
-        if name in ("decode", "prefill", "tiny"):
+        if name in ("decode", "prefill", "tiny", "linear"):
             if name == "decode":
                 ms, shapes, n_copies = [1, 4, 16], SHAPES_7B, copies or 4
             elif name == "prefill":
                 ms, shapes, n_copies = [512, 2048, 4096], SHAPES_7B + [HEAD], copies or 1
+            elif name == "linear":
+                ms, shapes, n_copies = [m], [("q", lin[0], lin[1])], copies or 1
             else:
                 ms, shapes, n_copies = [16], [("q", 512, 256)], copies or 1
             self.layers = []
@@ -168,7 +171,7 @@ class Workload:
             self.acts = {}
             for M in ms:
                 for inp in sorted(set(INPUT_OF.get(nm, "head") for nm, _, _ in shapes)):
-                    K = 512 if name == "tiny" else INPUT_K[inp]
+                    K = {"tiny": 512, "linear": shapes[0][1]}.get(name, INPUT_K.get(inp))
                     x = synth.activations(1, 0, {"attn": 0, "o": 3, "mlp": 4, "down": 6,
                                                  "head": 7}[inp], M, K)
                     xd = t(x, torch.bfloat16)
@@ -228,13 +231,14 @@ class Workload:
     # one step's launches, as (label, kind, M, N, K, bytes, ops, fn)
     def step_ops(self, copy: int):
         eg, ops = self.eg, []
-        if self.name in ("decode", "prefill", "tiny", "model"):
+        if self.name in ("decode", "prefill", "tiny", "linear", "model"):
             layers = [self.layers[copy]] if self.name != "model" else self.layers
             for M in self.ms:
                 for li, packs in enumerate(layers):
                     done = set()
                     for (nm, K, N) in self.shapes:
-                        inp = INPUT_OF.get(nm, "head") if self.name != "tiny" else "attn"
+                        inp = INPUT_OF.get(nm, "head") if self.name not in ("tiny", "linear") \
+                            else "attn"
                         x, xd, a = self.acts[(M, inp)]
                         if inp not in done:
                             done.add(inp)
@@ -309,7 +313,7 @@ def run_ours(args, rank, world):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", rank)) if world > 1 else 0)
     torch.cuda.set_device(dev)
     eg.load()
-    wl = Workload(args.workload, dev, m=args.m)
+    wl = Workload(args.workload, dev, m=args.m, lin=(args.k, args.n))
     peaks = load_peaks()
     copies = wl.n_copies
     step_ops = [wl.step_ops(c) for c in range(copies)]
@@ -362,7 +366,7 @@ def run_ours(args, rank, world):
     ms_step = ms_total / args.steps
     per_step_bytes = sum(op[5] for op in step_ops[0])
     per_step_ops = sum(op[6] for op in step_ops[0])
-    unit_is_ops = args.workload == "prefill"
+    unit_is_ops = args.workload == "prefill" or (args.workload == "linear" and args.m > 64)
     per_step_units = per_step_ops if unit_is_ops else per_step_bytes
     value = per_step_units * args.steps * world / (ms_total * 1e-3) / (1e12 if unit_is_ops else 1e9)
 
@@ -386,8 +390,7 @@ def run_ours(args, rank, world):
         d["ops"] += op[6]
         d["launches"] += 1
     dom_name, dom = max(per_kernel.items(), key=lambda kv: kv[1]["ms"])
-    if dom_name.startswith("tc_gemm") and (args.workload == "prefill" or
-                                           (args.workload == "dit" and False)):
+    if dom_name.startswith("tc_gemm") and unit_is_ops:
         achieved = dom["ops"] / (dom["ms"] * 1e-3) / 1e12
         # fp16 kind::f16 MMA: same nominal rate as bf16
         roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops_sustained"],
@@ -474,6 +477,7 @@ def workload_config(args, wl, per_step_bytes, per_step_ops):
         "model": f"full 7B linear pass: 28 layers x 7 linears + head at M={args.m}",
         "dit": "weight-only W4A16 and W8A16 on DiT blocks K=3072/12288, M in {1,16,4096}",
         "tiny": "tiny W4A8: M=16, K=512, N=256",
+        "linear": f"one W4A8 linear K={args.k} N={args.n} at M={args.m}",
     }[args.workload]}
     cfg.update({"layer_copies": wl.n_copies, "bytes_per_step": per_step_bytes,
                 "int_ops_per_step": per_step_ops,
@@ -542,13 +546,14 @@ def run_reference(args, rank, world):
         pass
     wl = _WL()
     wl.n_copies = 1
-    unit_is_ops = args.workload == "prefill"
+    unit_is_ops = args.workload == "prefill" or (args.workload == "linear" and args.m > 64)
     shapes = {"decode": [(M, K, N) for M in (1, 4, 16) for (_, K, N) in SHAPES_7B],
               "prefill": [(M, K, N) for M in (512, 2048, 4096) for (_, K, N) in SHAPES_7B + [HEAD]],
               "model": [(args.m, K, N) for (_, K, N) in SHAPES_7B] + [(args.m, HEAD[1], HEAD[2])],
               "dit": [(M, K, N) for M in (1, 16, 4096) for (K, N) in
                       [(3072, 3072), (3072, 12288), (12288, 3072)]],
-              "tiny": [(16, 512, 256)]}[args.workload]
+              "tiny": [(16, 512, 256)],
+              "linear": [(args.m, args.k, args.n)]}[args.workload]
     kind = "w4a16" if args.workload == "dit" else "w4a8"
     wl.step_ops = lambda c: [(f"M={M} K={K} N={N}", kind, M, N, K, 0, 0, None)
                              for (M, K, N) in shapes]
@@ -583,9 +588,11 @@ def main():
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["decode", "prefill", "model", "dit", "tiny"],
+    ap.add_argument("--workload", choices=["decode", "prefill", "model", "dit", "tiny", "linear"],
                     default="decode")
-    ap.add_argument("--m", type=int, default=1, help="tokens for --workload model")
+    ap.add_argument("--m", type=int, default=1, help="tokens for --workload model / linear")
+    ap.add_argument("--k", type=int, default=3584, help="K for --workload linear")
+    ap.add_argument("--n", type=int, default=3584, help="N for --workload linear")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
