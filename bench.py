@@ -91,7 +91,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -138,12 +138,12 @@ class ClockSampler:
 class Workload:
     """A list of launches per step ("ops"), built once; inputs resident on device."""
 
-    def __init__(self, name, dev, copies=None, m=1, lin=(3584, 3584)):
+    def __init__(self, name, dev, copies=None, m=1, lin=(3584, 3584), path=0):
         import torch
 
         import synth
         import w4a8_quantized_gemm_gb300 as eg
-        self.torch, self.eg, self.dev, self.name = torch, eg, dev, name
+        self.torch, self.eg, self.dev, self.name, self.path = torch, eg, dev, name, path
         self.steps_ops = []   # per layer copy: list of (kind, callable-args)
         self.ops_meta = []    # (kind, M, N, K, bytes, ops)
         self.inputs = []      # per copy: list of device tensors fed from host in e2e
@@ -226,7 +226,7 @@ class Workload:
             self.layers = [None]
         else:
             raise ValueError(name)
-        self.n_copies = len(self.layers)
+        self.n_copies = 1 if name == "model" else len(self.layers)
 
     # one step's launches, as (label, kind, M, N, K, bytes, ops, fn)
     def step_ops(self, copy: int):
@@ -249,7 +249,7 @@ class Workload:
                         ops.append((f"{nm} M={M}", "w4a8", M, N, K, w4a8_bytes(M, N, K),
                                     2 * M * N * K,
                                     (lambda a=a, p=packs[nm], N=N, K=K, y=y:
-                                     eg.w4a8_gemm(a, p, N, K, out=y))))
+                                     eg.w4a8_gemm(a, p, N, K, out=y, path=self.path))))
                 if self.name == "model":
                     x, xd, a = self.acts[(M, "head")]
                     K, N = HEAD[1], HEAD[2]
@@ -259,7 +259,7 @@ class Workload:
                     ops.append((f"head M={M}", "w4a8", M, N, K, w4a8_bytes(M, N, K),
                                 2 * M * N * K,
                                 (lambda a=a, p=self.head, N=N, K=K, y=y:
-                                 eg.w4a8_gemm(a, p, N, K, out=y))))
+                                 eg.w4a8_gemm(a, p, N, K, out=y, path=self.path))))
         else:
             for M in self.ms:
                 for (K, N) in self.dit_shapes:
@@ -269,11 +269,11 @@ class Workload:
                     ops.append((f"w4a16 K={K} N={N} M={M}", "w4a16", M, N, K,
                                 w4a16_bytes(M, N, K), 2 * M * N * K,
                                 (lambda xd=xd, p=p4, N=N, K=K, y=y4:
-                                 eg.w4a16_gemm(xd, p, N, K, out=y))))
+                                 eg.w4a16_gemm(xd, p, N, K, out=y, path=self.path))))
                     ops.append((f"w8a16 K={K} N={N} M={M}", "w8a16", M, N, K,
                                 w8a16_bytes(M, N, K), 2 * M * N * K,
                                 (lambda xd=xd, w8=w8, s8=s8, y=y8:
-                                 eg.w8a16_gemm(xd, w8, s8, out=y))))
+                                 eg.w8a16_gemm(xd, w8, s8, out=y, path=self.path))))
         return ops
 
     def host_io(self):
@@ -296,11 +296,12 @@ def _to_dev(torch, a, dev, dt=None):
     return t.view(dt) if dt is not None else t
 
 
-def kernel_label(eg, kind, M):
+def kernel_label(eg, kind, M, path):
     if kind == "quant":
         return "quant_act_kernel"
     if kind == "w4a8":
-        return "gemv_w4_kernel (W4A8)" if M <= 4 else "tc_gemm_kernel (W4A8)"
+        gemv = path == eg.PATH_GEMV or (path == eg.PATH_AUTO and M <= 4)
+        return "gemv_w4_kernel (W4A8)" if gemv else "tc_gemm_kernel (W4A8)"
     return f"tc_gemm_kernel ({kind.upper()})"
 
 
@@ -313,7 +314,8 @@ def run_ours(args, rank, world):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", rank)) if world > 1 else 0)
     torch.cuda.set_device(dev)
     eg.load()
-    wl = Workload(args.workload, dev, m=args.m, lin=(args.k, args.n))
+    path = {"auto": eg.PATH_AUTO, "gemv": eg.PATH_GEMV, "tc": eg.PATH_TC}[args.path]
+    wl = Workload(args.workload, dev, m=args.m, lin=(args.k, args.n), path=path)
     peaks = load_peaks()
     copies = wl.n_copies
     step_ops = [wl.step_ops(c) for c in range(copies)]
@@ -370,25 +372,33 @@ def run_ours(args, rank, world):
     per_step_units = per_step_ops if unit_is_ops else per_step_bytes
     value = per_step_units * args.steps * world / (ms_total * 1e-3) / (1e12 if unit_is_ops else 1e9)
 
-    # ---- per-kernel durations (events around each launch, same stream) -------
+    # ---- per-kernel durations: for each kernel, a CUDA graph of just its
+    # launches in the step (per layer copy), replayed over K steps and timed
+    # with events on the launching stream -------------------------------------
     per_kernel = {}
-    with torch.cuda.stream(stream):
-        evs = []
-        for i in range(args.steps):
-            for op in step_ops[i % copies]:
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record(stream)
-                op[7]()
-                b.record(stream)
-                evs.append((op, a, b))
-    stream.synchronize()
-    for op, a, b in evs:
-        lab = kernel_label(eg, op[1], op[2])
-        d = per_kernel.setdefault(lab, {"ms": 0.0, "bytes": 0, "ops": 0, "launches": 0})
-        d["ms"] += a.elapsed_time(b)
-        d["bytes"] += op[5]
-        d["ops"] += op[6]
-        d["launches"] += 1
+    labels = sorted(set(kernel_label(eg, op[1], op[2], path) for op in step_ops[0]))
+    for lab in labels:
+        sub_graphs, nbytes, nops, nl = [], 0, 0, 0
+        for c in range(copies):
+            sel = [op for op in step_ops[c] if kernel_label(eg, op[1], op[2], path) == lab]
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for op in sel:
+                    op[7]()
+            sub_graphs.append(g)
+            if c == 0:
+                nbytes, nops, nl = (sum(op[5] for op in sel), sum(op[6] for op in sel), len(sel))
+        with torch.cuda.stream(stream):
+            for i in range(3):
+                sub_graphs[i % copies].replay()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for i in range(args.steps):
+                sub_graphs[i % copies].replay()
+            b.record(stream)
+        stream.synchronize()
+        per_kernel[lab] = {"ms": a.elapsed_time(b), "bytes": nbytes * args.steps,
+                           "ops": nops * args.steps, "launches": nl * args.steps}
     dom_name, dom = max(per_kernel.items(), key=lambda kv: kv[1]["ms"])
     if dom_name.startswith("tc_gemm") and unit_is_ops:
         achieved = dom["ops"] / (dom["ms"] * 1e-3) / 1e12
@@ -402,18 +412,24 @@ def run_ours(args, rank, world):
     roof.update({"kernel": dom_name, "traffic": None, "peak_source": peaks["source"],
                  "avg_launch_us": dom["ms"] * 1e3 / dom["launches"]})
 
-    # ---- end to end through the API: H2D inputs, step, D2H outputs ------------
+    # ---- end to end through the API: each step copies its activations from
+    # pinned host memory, replays the captured step (the same API calls) and
+    # copies its outputs back to pinned host memory ----------------------------
     ins, outs = wl.host_io()
     h2d = sum(h.numel() * h.element_size() for h, _ in ins)
     d2h = sum(h.numel() * h.element_size() for _, h in outs)
     torch.cuda.synchronize()
+
+    def e2e_step(i):
+        for h, d in ins:
+            d.copy_(h, non_blocking=True)
+        graphs[i % copies].replay()
+        for d, h in outs:
+            h.copy_(d, non_blocking=True)
+
     with torch.cuda.stream(stream):
         for i in range(2):
-            for h, d in ins:
-                d.copy_(h, non_blocking=True)
-            step(i % copies)
-            for d, h in outs:
-                h.copy_(d, non_blocking=True)
+            e2e_step(i)
     stream.synchronize()
     t0 = time.perf_counter()
     e2 = torch.cuda.Event(enable_timing=True)
@@ -421,11 +437,7 @@ def run_ours(args, rank, world):
     with torch.cuda.stream(stream):
         e2.record(stream)
         for i in range(args.steps):
-            for h, d in ins:
-                d.copy_(h, non_blocking=True)
-            step(i % copies)
-            for d, h in outs:
-                h.copy_(d, non_blocking=True)
+            e2e_step(i)
         e3.record(stream)
     stream.synchronize()
     e2e_ms = e2.elapsed_time(e3)
@@ -461,6 +473,7 @@ def run_ours(args, rank, world):
                 "ms_per_step": round(max(e2e_ms, wall_ms) / args.steps, 5)},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
+        "path": args.path,
         "device_status": status,
     }
     if rank == 0 and not args.no_cpu_baseline:
@@ -585,7 +598,8 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: about half a second of work)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=["decode", "prefill", "model", "dit", "tiny", "linear"],
@@ -595,7 +609,11 @@ def main():
     ap.add_argument("--n", type=int, default=3584, help="N for --workload linear")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--path", choices=["auto", "gemv", "tc"], default="auto")
     args = ap.parse_args()
+    if args.steps is None:
+        args.steps = {"decode": 1500, "model": 200, "tiny": 2000, "linear": 200}.get(
+            args.workload, 40) if args.impl == "ours" else 3
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -204,6 +204,17 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int ab_bf16) {
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// ---- programmatic dependent launch ---------------------------------------------
+// Wait until the preceding grid in the stream has completed and its writes are
+// visible (a no-op when the launch carried no programmatic dependency).
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Allow the next grid in the stream to begin launching.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- cluster helpers -----------------------------------------------------------
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;

@@ -28,7 +28,10 @@
 
 namespace egopq {
 
-constexpr int kGemvThreads = 128;
+constexpr int kGemvConsumers = 128;                 // one thread per weight row of a tile
+constexpr int kGemvThreads = kGemvConsumers + 32;   // + one producer warp
+constexpr int kGemvStages = 8;
+constexpr int kGemvStageBytes = 8192 + 256 + 64;    // codes, scales, zero nibbles
 constexpr int kGemvMaxGroupsPerCta = 64;
 
 struct GemvParams {
@@ -41,7 +44,242 @@ struct GemvParams {
   const uint8_t* packed;
   uint16_t* y;
   int32_t* partials;
+  uint64_t timeout_ns;
 };
+
+// Decode kernel for the packed int4 weight (W4A8 and W4A16). CTA = one
+// 128-row tile x a contiguous range of groups; a producer lane streams each
+// group's 8 KiB code tile, its 128 scales and 64 bytes of zero nibbles into an
+// 8-stage shared-memory ring with 1-D bulk copies (weights first, before the
+// preceding kernel has finished); each consumer thread owns one weight row.
+template <int VARIANT, int MT, bool PARTIALS>
+__global__ void __launch_bounds__(kGemvThreads)
+gemv_w4_kernel(const GemvParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ks = blockIdx.x, t = blockIdx.y;
+  const int G = p.G;
+  const int g0 = (int)((int64_t)ks * G / p.ks), g1 = (int)((int64_t)(ks + 1) * G / p.ks);
+  const int ng = g1 - g0;
+  const int64_t N = p.N, K = p.K;
+  const uint16_t* scales = reinterpret_cast<const uint16_t*>(p.packed + N * K / 2);
+  const uint8_t* zeros = p.packed + N * K / 2 + 2 * (int64_t)G * N;
+
+  // smem: ring | barriers | abort flag | reduction buffer | staged activations
+  uint8_t* ring = smem;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kGemvStages * kGemvStageBytes);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kGemvStages);
+  float* red = reinterpret_cast<float*>(smem + kGemvStages * kGemvStageBytes + 256);
+  uint8_t* act = reinterpret_cast<uint8_t*>(red + MT * 128);
+  auto full_bar = [&](int s) { return smem_u32(bars + s); };
+  auto empty_bar = [&](int s) { return smem_u32(bars + kGemvStages + s); };
+  const uint64_t tmo = p.timeout_ns;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kGemvStages; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 4);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == 4) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      auto issue = [&](int i) {
+        const int s = i % kGemvStages, g = g0 + i;
+        const uint32_t dst = smem_u32(ring + s * kGemvStageBytes);
+        mbar_arrive_expect_tx(full_bar(s), kGemvStageBytes);
+        bulk_load(dst, p.packed + ((int64_t)t * G + g) * 8192, 8192, full_bar(s));
+        bulk_load(dst + 8192, scales + (int64_t)g * N + (int64_t)t * 128, 256, full_bar(s));
+        bulk_load(dst + 8192 + 256, zeros + (int64_t)g * (N / 2) + (int64_t)t * 64, 64,
+                  full_bar(s));
+      };
+      int issued = 0;
+      for (int i = 0; i < ng; ++i) {
+        if (i >= kGemvStages &&
+            !mbar_wait(empty_bar(i % kGemvStages), ((i / kGemvStages) & 1) ^ 1, abort_flag, tmo))
+          break;
+        issue(i);
+        ++issued;
+      }
+      for (int i = (issued > kGemvStages ? issued - kGemvStages : 0); i < issued; ++i) {
+        volatile int no_abort = 0;
+        mbar_wait(full_bar(i % kGemvStages), (i / kGemvStages) & 1, &no_abort, tmo);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ---------------------------------------------------------------- consumers
+    const int r = threadIdx.x;  // row in the tile
+    const int64_t n = (int64_t)t * 128 + r;
+    griddep_wait();             // activations come from the preceding kernel
+    if (threadIdx.x == 0) griddep_launch_dependents();
+    // stage this CTA's activations, permuted to the nibble order
+    if constexpr (VARIANT == kW4A8) {
+      uint2* aw = reinterpret_cast<uint2*>(act);
+      int32_t* as = reinterpret_cast<int32_t*>(act + (size_t)ng * MT * 16 * sizeof(uint2));
+      for (int i = threadIdx.x; i < ng * MT * 16; i += kGemvConsumers) {
+        const int gl = i / (MT * 16), m = (i / 16) % MT, cj = i % 16;
+        uint2 v = make_uint2(0, 0);
+        if (m < p.rows) {
+          const int64_t k0 = (int64_t)(g0 + gl) * 128 + cj * 8;
+          const uint2 X = *reinterpret_cast<const uint2*>(p.a_q + m * K + k0);
+          v.x = prmt(X.x, X.y, 0x5140);  // K offsets {0,4,1,5}
+          v.y = prmt(X.x, X.y, 0x7362);  // K offsets {2,6,3,7}
+        }
+        aw[i] = v;
+      }
+      for (int i = threadIdx.x; i < ng * MT; i += kGemvConsumers) {
+        const int gl = i / MT, m = i % MT;
+        as[i] = (m < p.rows) ? p.a_gsum[m * G + g0 + gl] : 0;
+      }
+    } else {
+      float* xs = reinterpret_cast<float*>(act);
+      for (int i = threadIdx.x; i < ng * MT * 128; i += kGemvConsumers) {
+        const int gl = i / (MT * 128), m = (i / 128) % MT, kk = i % 128;
+        // position kk = 32c + 8j + nib holds K offset 32c + 8j + e(nib)
+        const int nib = kk & 7;
+        const int e = (nib < 4) ? 2 * nib : 2 * (nib - 4) + 1;
+        float v = 0.f;
+        if (m < p.rows)
+          v = bf16_bits_to_f32(p.x[m * K + (int64_t)(g0 + gl) * 128 + (kk & ~7) + e]);
+        xs[i] = v;
+      }
+    }
+    asm volatile("bar.sync 2, %0;" ::"n"(kGemvConsumers) : "memory");
+
+    float acc[MT];
+#pragma unroll
+    for (int m = 0; m < MT; ++m) acc[m] = 0.f;
+    for (int i = 0; i < ng; ++i) {
+      const int s = i % kGemvStages, g = g0 + i;
+      if (!mbar_wait(full_bar(s), (i / kGemvStages) & 1, abort_flag, tmo)) break;
+      const uint8_t* st = ring + s * kGemvStageBytes;
+      uint4 cur[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) cur[c] = *reinterpret_cast<const uint4*>(st + (c * 128 + r) * 16);
+      const float sc = f16_bits_to_f32(reinterpret_cast<const uint16_t*>(st + 8192)[r]);
+      const uint8_t zb = st[8192 + 256 + (r >> 1)];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty_bar(s));
+      const int z = (r & 1) ? (zb >> 4) : (zb & 0xF);
+      if constexpr (VARIANT == kW4A8) {
+        const uint4* aw = reinterpret_cast<const uint4*>(act) + (size_t)i * MT * 8;
+        const int32_t* as =
+            reinterpret_cast<const int32_t*>(act + (size_t)ng * MT * 16 * sizeof(uint2));
+        int dot[MT];
+#pragma unroll
+        for (int m = 0; m < MT; ++m) dot[m] = 0;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint32_t wv[4] = {cur[c].x, cur[c].y, cur[c].z, cur[c].w};
+#pragma unroll
+          for (int jj = 0; jj < 2; ++jj) {
+            const uint32_t lo0 = wv[2 * jj] & 0x0F0F0F0Fu, hi0 = (wv[2 * jj] >> 4) & 0x0F0F0F0Fu;
+            const uint32_t lo1 = wv[2 * jj + 1] & 0x0F0F0F0Fu,
+                           hi1 = (wv[2 * jj + 1] >> 4) & 0x0F0F0F0Fu;
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+              const uint4 a = aw[m * 8 + c * 2 + jj];
+              dot[m] = __dp4a((int)lo0, (int)a.x, dot[m]);
+              dot[m] = __dp4a((int)hi0, (int)a.y, dot[m]);
+              dot[m] = __dp4a((int)lo1, (int)a.z, dot[m]);
+              dot[m] = __dp4a((int)hi1, (int)a.w, dot[m]);
+            }
+          }
+        }
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+          const int q = dot[m] - z * as[i * MT + m];
+          if constexpr (PARTIALS) {
+            if (m < p.rows) p.partials[((int64_t)m * N + n) * G + g] = q;
+          } else {
+            acc[m] = fmaf(sc, (float)q, acc[m]);
+          }
+        }
+      } else {
+        const float* xs = reinterpret_cast<const float*>(act) + (size_t)i * MT * 128;
+        const float zf = 8388608.0f + (float)z;
+        float part[MT];
+#pragma unroll
+        for (int m = 0; m < MT; ++m) part[m] = 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint32_t wv[4] = {cur[c].x, cur[c].y, cur[c].z, cur[c].w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            float v[8];
+#pragma unroll
+            for (int nib = 0; nib < 8; ++nib)
+              v[nib] = __uint_as_float(0x4B000000u | ((wv[j] >> (4 * nib)) & 0xFu)) - zf;
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+              const float4 xa = *reinterpret_cast<const float4*>(xs + m * 128 + c * 32 + j * 8);
+              const float4 xb =
+                  *reinterpret_cast<const float4*>(xs + m * 128 + c * 32 + j * 8 + 4);
+              part[m] = fmaf(xa.x, v[0], part[m]);
+              part[m] = fmaf(xa.y, v[1], part[m]);
+              part[m] = fmaf(xa.z, v[2], part[m]);
+              part[m] = fmaf(xa.w, v[3], part[m]);
+              part[m] = fmaf(xb.x, v[4], part[m]);
+              part[m] = fmaf(xb.y, v[5], part[m]);
+              part[m] = fmaf(xb.z, v[6], part[m]);
+              part[m] = fmaf(xb.w, v[7], part[m]);
+            }
+          }
+        }
+#pragma unroll
+        for (int m = 0; m < MT; ++m) acc[m] = fmaf(sc, part[m], acc[m]);
+      }
+    }
+    if constexpr (!PARTIALS) {
+      if (p.ks > 1) {
+#pragma unroll
+        for (int m = 0; m < MT; ++m) red[m * 128 + r] = acc[m];
+      } else {
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+          if (m < p.rows) {
+            float v = acc[m];
+            if constexpr (VARIANT == kW4A8) v = p.a_s[m] * v;
+            p.y[m * N + n] = f32_to_bf16_bits(v);
+          }
+        }
+      }
+    }
+  }
+  // ---- split-K: reduce the cluster's partial sums through DSMEM (all threads)
+  if constexpr (!PARTIALS) {
+    if (p.ks > 1) {
+      cluster_sync_all();
+      if (cluster_ctarank() == 0 && warp < 4) {
+        const int r = threadIdx.x;
+        const int64_t n = (int64_t)t * 128 + r;
+        float acc[MT];
+#pragma unroll
+        for (int m = 0; m < MT; ++m) acc[m] = red[m * 128 + r];
+        const uint32_t local = smem_u32(red);
+        for (int rk = 1; rk < p.ks; ++rk) {
+          const uint32_t remote = map_to_rank(local, rk);
+#pragma unroll
+          for (int m = 0; m < MT; ++m) acc[m] += ld_dsmem_f32(remote + (m * 128 + r) * 4);
+        }
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+          if (m < p.rows) {
+            float v = acc[m];
+            if constexpr (VARIANT == kW4A8) v = p.a_s[m] * v;
+            p.y[m * N + n] = f32_to_bf16_bits(v);
+          }
+        }
+      }
+      cluster_sync_all();
+    }
+  }
+}
 
 __device__ __forceinline__ uint4 ldg_stream(const void* p) {
   uint4 v;
@@ -49,201 +287,6 @@ __device__ __forceinline__ uint4 ldg_stream(const void* p) {
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "l"(p));
   return v;
-}
-
-template <int VARIANT, int MT, bool PARTIALS>
-__global__ void __launch_bounds__(kGemvThreads)
-gemv_w4_kernel(const GemvParams p) {
-  extern __shared__ __align__(16) uint8_t smem[];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int ks = blockIdx.x, slab = blockIdx.y;
-  const int G = p.G;
-  const int g0 = (int)((int64_t)ks * G / p.ks), g1 = (int)((int64_t)(ks + 1) * G / p.ks);
-  const int ng = g1 - g0;
-  const int64_t N = p.N, K = p.K;
-  const int64_t n = (int64_t)slab * 32 + lane;
-  const int64_t t = slab >> 2;
-  const int r = (slab & 3) * 32 + lane;
-  const uint8_t* codes = p.packed;
-  const uint16_t* scales = reinterpret_cast<const uint16_t*>(p.packed + N * K / 2);
-  const uint8_t* zeros = p.packed + N * K / 2 + 2 * (int64_t)G * N;
-
-  // ---- stage this CTA's activations (permuted to the nibble order) ----------
-  // W4A8: per (group, row m, chunk c, word j) a uint2 {lo, hi} of int8 quads;
-  // then int32 group sums. W4A16: 128 floats per (group, row), nibble order.
-  float* red = reinterpret_cast<float*>(smem);  // [4 warps][MT][32], reused below
-  uint8_t* act = smem + 4 * MT * 32 * sizeof(float);
-  if constexpr (VARIANT == kW4A8) {
-    uint2* aw = reinterpret_cast<uint2*>(act);
-    int32_t* as = reinterpret_cast<int32_t*>(act + (size_t)ng * MT * 16 * sizeof(uint2));
-    for (int i = threadIdx.x; i < ng * MT * 16; i += kGemvThreads) {
-      const int gl = i / (MT * 16), m = (i / 16) % MT, cj = i % 16;
-      uint2 v = make_uint2(0, 0);
-      if (m < p.rows) {
-        const int64_t k0 = (int64_t)(g0 + gl) * 128 + cj * 8;
-        const uint2 X = *reinterpret_cast<const uint2*>(p.a_q + m * K + k0);
-        v.x = prmt(X.x, X.y, 0x5140);  // K offsets {0,4,1,5}
-        v.y = prmt(X.x, X.y, 0x7362);  // K offsets {2,6,3,7}
-      }
-      aw[i] = v;
-    }
-    for (int i = threadIdx.x; i < ng * MT; i += kGemvThreads) {
-      const int gl = i / MT, m = i % MT;
-      as[i] = (m < p.rows) ? p.a_gsum[m * G + g0 + gl] : 0;
-    }
-  } else {
-    float* xs = reinterpret_cast<float*>(act);
-    for (int i = threadIdx.x; i < ng * MT * 128; i += kGemvThreads) {
-      const int gl = i / (MT * 128), m = (i / 128) % MT, kk = i % 128;
-      // position kk = 32c + 8j + nib holds K offset 32c + 8j + e(nib)
-      const int nib = kk & 7;
-      const int e = (nib < 4) ? 2 * nib : 2 * (nib - 4) + 1;
-      float v = 0.f;
-      if (m < p.rows)
-        v = bf16_bits_to_f32(p.x[m * K + (int64_t)(g0 + gl) * 128 + (kk & ~7) + e]);
-      xs[i] = v;
-    }
-  }
-  __syncthreads();
-
-  float acc[MT];
-#pragma unroll
-  for (int m = 0; m < MT; ++m) acc[m] = 0.f;
-
-  auto load_tile = [&](int g, uint4 (&w)[4]) {
-    const uint8_t* base = codes + ((t * G + g) * 8192) + (int64_t)r * 16;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) w[c] = ldg_stream(base + c * 2048);
-  };
-
-  int g = g0 + warp;
-  uint4 cur[4], nxt[4];
-  if (g < g1) load_tile(g, cur);
-  for (; g < g1; g += 4) {
-    const int gn = g + 4;
-    if (gn < g1) load_tile(gn, nxt);
-    const uint8_t zb = __ldg(zeros + (int64_t)g * (N / 2) + (n >> 1));
-    const int z = (n & 1) ? (zb >> 4) : (zb & 0xF);
-    const float s = f16_bits_to_f32(__ldg(scales + (int64_t)g * N + n));
-    const int gl = g - g0;
-    if constexpr (VARIANT == kW4A8) {
-      const uint4* aw = reinterpret_cast<const uint4*>(act) + (size_t)gl * MT * 8;
-      const int32_t* as =
-          reinterpret_cast<const int32_t*>(act + (size_t)ng * MT * 16 * sizeof(uint2));
-      int dot[MT];
-#pragma unroll
-      for (int m = 0; m < MT; ++m) dot[m] = 0;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const uint32_t wv[4] = {cur[c].x, cur[c].y, cur[c].z, cur[c].w};
-#pragma unroll
-        for (int jj = 0; jj < 2; ++jj) {
-          const uint32_t lo0 = wv[2 * jj] & 0x0F0F0F0Fu, hi0 = (wv[2 * jj] >> 4) & 0x0F0F0F0Fu;
-          const uint32_t lo1 = wv[2 * jj + 1] & 0x0F0F0F0Fu,
-                         hi1 = (wv[2 * jj + 1] >> 4) & 0x0F0F0F0Fu;
-#pragma unroll
-          for (int m = 0; m < MT; ++m) {
-            const uint4 a = aw[m * 8 + c * 2 + jj];
-            dot[m] = __dp4a((int)lo0, (int)a.x, dot[m]);
-            dot[m] = __dp4a((int)hi0, (int)a.y, dot[m]);
-            dot[m] = __dp4a((int)lo1, (int)a.z, dot[m]);
-            dot[m] = __dp4a((int)hi1, (int)a.w, dot[m]);
-          }
-        }
-      }
-#pragma unroll
-      for (int m = 0; m < MT; ++m) {
-        const int q = dot[m] - z * as[gl * MT + m];
-        if constexpr (PARTIALS) {
-          if (m < p.rows) p.partials[((int64_t)m * N + n) * G + g] = q;
-        } else {
-          acc[m] = fmaf(s, (float)q, acc[m]);
-        }
-      }
-    } else {
-      const float* xs = reinterpret_cast<const float*>(act) + (size_t)gl * MT * 128;
-      const float zf = 8388608.0f + (float)z;
-      float part[MT];
-#pragma unroll
-      for (int m = 0; m < MT; ++m) part[m] = 0.f;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const uint32_t wv[4] = {cur[c].x, cur[c].y, cur[c].z, cur[c].w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          float v[8];
-#pragma unroll
-          for (int nib = 0; nib < 8; ++nib)
-            v[nib] = __uint_as_float(0x4B000000u | ((wv[j] >> (4 * nib)) & 0xFu)) - zf;
-#pragma unroll
-          for (int m = 0; m < MT; ++m) {
-            const float4 xa = *reinterpret_cast<const float4*>(xs + m * 128 + c * 32 + j * 8);
-            const float4 xb = *reinterpret_cast<const float4*>(xs + m * 128 + c * 32 + j * 8 + 4);
-            part[m] = fmaf(xa.x, v[0], part[m]);
-            part[m] = fmaf(xa.y, v[1], part[m]);
-            part[m] = fmaf(xa.z, v[2], part[m]);
-            part[m] = fmaf(xa.w, v[3], part[m]);
-            part[m] = fmaf(xb.x, v[4], part[m]);
-            part[m] = fmaf(xb.y, v[5], part[m]);
-            part[m] = fmaf(xb.z, v[6], part[m]);
-            part[m] = fmaf(xb.w, v[7], part[m]);
-          }
-        }
-      }
-#pragma unroll
-      for (int m = 0; m < MT; ++m) acc[m] = fmaf(s, part[m], acc[m]);
-    }
-    if (gn < g1) {
-#pragma unroll
-      for (int c = 0; c < 4; ++c) cur[c] = nxt[c];
-    }
-  }
-  if constexpr (!PARTIALS) {
-  // ---- reduce: the 4 warps of the CTA, then the CTAs of the cluster --------
-#pragma unroll
-  for (int m = 0; m < MT; ++m) red[(warp * MT + m) * 32 + lane] = acc[m];
-  __syncthreads();
-  float* cta_sum = red + 4 * MT * 32;  // [MT][32], inside the staging area
-  if (warp == 0) {
-#pragma unroll
-    for (int m = 0; m < MT; ++m) {
-      float v = red[(0 * MT + m) * 32 + lane];
-      v += red[(1 * MT + m) * 32 + lane];
-      v += red[(2 * MT + m) * 32 + lane];
-      v += red[(3 * MT + m) * 32 + lane];
-      acc[m] = v;
-    }
-  }
-  if (p.ks > 1) {
-    if (warp == 0) {
-#pragma unroll
-      for (int m = 0; m < MT; ++m) cta_sum[m * 32 + lane] = acc[m];
-    }
-    cluster_sync_all();
-    if (cluster_ctarank() == 0 && warp == 0) {
-      const uint32_t local = smem_u32(cta_sum);
-#pragma unroll
-      for (int m = 0; m < MT; ++m) acc[m] = cta_sum[m * 32 + lane];
-      for (int rk = 1; rk < p.ks; ++rk) {
-        const uint32_t remote = map_to_rank(local, rk);
-#pragma unroll
-        for (int m = 0; m < MT; ++m) acc[m] += ld_dsmem_f32(remote + (m * 32 + lane) * 4);
-      }
-    }
-    cluster_sync_all();
-    if (cluster_ctarank() != 0) return;
-  }
-  if (warp == 0) {
-#pragma unroll
-    for (int m = 0; m < MT; ++m) {
-      if (m < p.rows) {
-        float v = acc[m];
-        if constexpr (VARIANT == kW4A8) v = p.a_s[m] * v;
-        p.y[m * N + n] = f32_to_bf16_bits(v);
-      }
-    }
-  }
-  }  // !PARTIALS
 }
 
 // ---- W8A16 ------------------------------------------------------------------
@@ -336,13 +379,9 @@ static int sm_count() {
 template <int VARIANT, int MT, bool PARTIALS>
 static cudaError_t launch_w4_slice(const GemvParams& p, cudaStream_t st) {
   const int ng_max = (p.G + p.ks - 1) / p.ks;
-  size_t act_bytes = (VARIANT == kW4A8) ? (size_t)ng_max * MT * (16 * 8 + 4)
-                                        : (size_t)ng_max * MT * 128 * 4;
-  size_t smem = 4 * MT * 32 * 4 + act_bytes;
-  // the reduction buffers (4*MT*32 + MT*32 floats) must fit in front of and
-  // inside the staging area
-  const size_t red_need = (4 * MT * 32 + MT * 32) * 4;
-  if (smem < red_need) smem = red_need;
+  const size_t act_bytes = (VARIANT == kW4A8) ? (size_t)ng_max * MT * (16 * 8 + 4)
+                                              : (size_t)ng_max * MT * 128 * 4;
+  const size_t smem = (size_t)kGemvStages * kGemvStageBytes + 256 + MT * 128 * 4 + act_bytes;
   auto kern = gemv_w4_kernel<VARIANT, MT, PARTIALS>;
   static size_t attr_smem = 0;  // largest carve-out requested so far for this instantiation
   if (smem > attr_smem) {
@@ -352,17 +391,19 @@ static cudaError_t launch_w4_slice(const GemvParams& p, cudaStream_t st) {
     attr_smem = smem;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)p.ks, (unsigned)(p.N / 32), 1);
+  cfg.gridDim = dim3((unsigned)p.ks, (unsigned)(p.N / 128), 1);
   cfg.blockDim = dim3(kGemvThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)p.ks;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
@@ -396,16 +437,21 @@ cudaError_t launch_gemv(const GemmArgs& a, cudaStream_t st) {
     return cudaSuccess;
   }
   const int G = (int)(a.K / 128);
-  const int64_t slabs = a.N / 32;
-  // split K across a cluster so the grid covers the GPU a few times over,
-  // keeping at least two groups per warp and at most kGemvMaxGroupsPerCta per CTA
-  int ks = (int)((4LL * sm_count() + slabs - 1) / slabs);
-  const int ks_cap = G / 8 > 0 ? G / 8 : 1;
-  if (ks > ks_cap) ks = ks_cap;
-  const int ks_min = (G + kGemvMaxGroupsPerCta - 1) / kGemvMaxGroupsPerCta;
-  if (ks < ks_min) ks = ks_min;
-  if (ks > 8) ks = 8;
-  if (ks < 1) ks = 1;
+  const int64_t tiles = a.N / 128;
+  // split the groups of each tile over a cluster so that about two CTAs per
+  // SM stream weights, keeping at most kGemvMaxGroupsPerCta groups per CTA
+  const int64_t slots = 2LL * sm_count();
+  int ks = 1;
+  double best = 1e30;
+  for (int c = 1; c <= 8 && c <= G; ++c) {
+    if ((G + c - 1) / c > kGemvMaxGroupsPerCta) continue;
+    const int64_t rounds = (tiles * c + slots - 1) / slots;
+    const double cost = (double)rounds * ((G + c - 1) / c) * (c > 1 ? 1.03 : 1.0);
+    if (cost < best - 1e-9) {
+      best = cost;
+      ks = c;
+    }
+  }
   if ((G + ks - 1) / ks > kGemvMaxGroupsPerCta) return cudaErrorNotSupported;
   for (int64_t m0 = 0; m0 < a.M; m0 += kGemvMaxRows) {
     GemvParams p{};
@@ -417,6 +463,7 @@ cudaError_t launch_gemv(const GemmArgs& a, cudaStream_t st) {
     p.rows = (int)((a.M - m0) < kGemvMaxRows ? (a.M - m0) : kGemvMaxRows);
     p.packed = a.packed;
     p.y = a.y + m0 * a.N;
+    p.timeout_ns = a.timeout_ns;
     cudaError_t e;
     if (a.variant == kW4A8) {
       p.a_q = a.a_q + m0 * a.K;

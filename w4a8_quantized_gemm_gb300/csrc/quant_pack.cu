@@ -24,6 +24,8 @@ __global__ void __launch_bounds__(kQuantThreads)
 quant_act_kernel(const uint16_t* __restrict__ x, int64_t K, int8_t* __restrict__ a_q,
                  float* __restrict__ a_s, int32_t* __restrict__ a_gsum,
                  uint16_t* __restrict__ a_q16) {
+  griddep_wait();
+  if (threadIdx.x == 0) griddep_launch_dependents();
   const int64_t m = blockIdx.x;
   const uint4* xr = reinterpret_cast<const uint4*>(x + m * K);
   const int64_t nvec = K / 8;  // 8 bf16 per 16-byte vector; K % 128 == 0
@@ -87,6 +89,82 @@ quant_act_kernel(const uint16_t* __restrict__ x, int64_t K, int8_t* __restrict__
 #pragma unroll
     for (int o = 8; o > 0; o >>= 1) sum += __shfl_xor_sync(half_mask, sum, o);
     if ((threadIdx.x & 15) == 0) a_gsum[m * (K / 128) + v / 16] = sum;
+  }
+}
+
+// Single-pass variant: the whole row stays in registers (up to kRegVec 16-byte
+// vectors per thread, K <= kQuantRegThreads * kRegVec * 8), so x is read from
+// memory once. It waits for the preceding kernel only when the launch carried a
+// programmatic dependency.
+constexpr int kQuantRegThreads = 512;
+constexpr int kRegVec = 8;
+
+__global__ void __launch_bounds__(kQuantRegThreads)
+quant_act_reg_kernel(const uint16_t* __restrict__ x, int64_t K, int8_t* __restrict__ a_q,
+                     float* __restrict__ a_s, int32_t* __restrict__ a_gsum,
+                     uint16_t* __restrict__ a_q16) {
+  griddep_wait();
+  if (threadIdx.x == 0) griddep_launch_dependents();
+  const int64_t m = blockIdx.x;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + m * K);
+  const int nvec = (int)(K / 8);
+  __shared__ float warp_max[kQuantRegThreads / 32];
+  uint4 v[kRegVec];
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < kRegVec; ++i) {
+    const int idx = threadIdx.x + i * kQuantRegThreads;
+    v[i] = idx < nvec ? __ldg(xr + idx) : make_uint4(0, 0, 0, 0);
+    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      amax = fmaxf(amax, fabsf(__uint_as_float(w[j] << 16)));
+      amax = fmaxf(amax, fabsf(__uint_as_float(w[j] & 0xFFFF0000u)));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  amax = warp_max[0];
+#pragma unroll
+  for (int i = 1; i < kQuantRegThreads / 32; ++i) amax = fmaxf(amax, warp_max[i]);
+  const float s = __fdiv_rn(amax, 127.0f);
+  if (threadIdx.x == 0) a_s[m] = s;
+  const bool zero_row = (amax == 0.f);
+#pragma unroll
+  for (int i = 0; i < kRegVec; ++i) {
+    const int idx = threadIdx.x + i * kQuantRegThreads;
+    if (idx >= nvec) break;  // whole half-warps leave together (nvec % 16 == 0)
+    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+    int q[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float lo = __uint_as_float(w[j] << 16);
+      const float hi = __uint_as_float(w[j] & 0xFFFF0000u);
+      q[2 * j] = zero_row ? 0 : max(-127, min(127, __float2int_rn(__fdiv_rn(lo, s))));
+      q[2 * j + 1] = zero_row ? 0 : max(-127, min(127, __float2int_rn(__fdiv_rn(hi, s))));
+    }
+    uint2 packed;
+    packed.x = (uint32_t)(q[0] & 0xFF) | ((uint32_t)(q[1] & 0xFF) << 8) |
+               ((uint32_t)(q[2] & 0xFF) << 16) | ((uint32_t)(q[3] & 0xFF) << 24);
+    packed.y = (uint32_t)(q[4] & 0xFF) | ((uint32_t)(q[5] & 0xFF) << 8) |
+               ((uint32_t)(q[6] & 0xFF) << 16) | ((uint32_t)(q[7] & 0xFF) << 24);
+    reinterpret_cast<uint2*>(a_q + m * K)[idx] = packed;
+    if (a_q16) {
+      uint32_t h[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        __half2 hv = __halves2half2(__int2half_rn(q[2 * j]), __int2half_rn(q[2 * j + 1]));
+        h[j] = *reinterpret_cast<uint32_t*>(&hv);
+      }
+      reinterpret_cast<uint4*>(a_q16 + m * K)[idx] = make_uint4(h[0], h[1], h[2], h[3]);
+    }
+    int sum = q[0] + q[1] + q[2] + q[3] + q[4] + q[5] + q[6] + q[7];
+    const unsigned half_mask = 0xFFFFu << (threadIdx.x & 16);
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) sum += __shfl_xor_sync(half_mask, sum, o);
+    if ((threadIdx.x & 15) == 0) a_gsum[m * (K / 128) + idx / 16] = sum;
   }
 }
 
@@ -166,8 +244,20 @@ static unsigned grid_for(int64_t work, int threads) {
 
 cudaError_t launch_quant_act(const uint16_t* x, int64_t M, int64_t K, int8_t* a_q, float* a_s,
                              int32_t* a_gsum, uint16_t* a_q16, cudaStream_t st) {
-  quant_act_kernel<<<(unsigned)M, kQuantThreads, 0, st>>>(x, K, a_q, a_s, a_gsum, a_q16);
-  return cudaGetLastError();
+  // few tokens: one wide CTA per row, one read of x (latency); many tokens:
+  // narrower CTAs, several resident per SM (throughput)
+  const bool reg = (M <= 64 && K <= (int64_t)kQuantRegThreads * kRegVec * 8);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)M, 1, 1);
+  cfg.blockDim = dim3(reg ? kQuantRegThreads : kQuantThreads, 1, 1);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (reg) return cudaLaunchKernelEx(&cfg, quant_act_reg_kernel, x, K, a_q, a_s, a_gsum, a_q16);
+  return cudaLaunchKernelEx(&cfg, quant_act_kernel, x, K, a_q, a_s, a_gsum, a_q16);
 }
 
 cudaError_t launch_pack_w4(const uint8_t* w_q, const uint16_t* s, const uint8_t* z, int64_t N,

@@ -55,6 +55,8 @@ constexpr int kMaxSmem = 232448;
 struct TcParams {
   int64_t M, N, K;
   int G, ks;
+  int m_tiles, n_tiles;
+  int persistent;  // 1: CTAs stride over tiles with all of K; 0: one tile per CTA, split-K cluster
   const float* a_s;
   const uint8_t* packed;
   const uint16_t* s8;
@@ -68,10 +70,13 @@ struct TcCfg {
   static constexpr int kActBox = BT * 128;                        // one 64-wide K box, bytes
   static constexpr int kActBytes = 2 * kActBox;                   // a 128-wide group
   static constexpr int kWBytes = (VARIANT == kW8A16) ? 16384 : 8192;
-  static constexpr int kStageBytes = kActBytes + kWBytes;
-  static constexpr int kStagesRaw = (kMaxSmem - 2048) / kStageBytes;
+  static constexpr int kZBytes = (VARIANT == kW8A16) ? 0 : 64;   // zero nibbles of 128 rows
+  static constexpr int kStageBytes = kActBytes + kWBytes;        // multiple of 1024
+  static constexpr int kTxBytes = kStageBytes + kZBytes;
+  static constexpr int kStagesRaw = (kMaxSmem - 2048) / (kStageBytes + 64);
   static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
-  static constexpr int kBarOffset = kStages * kStageBytes;
+  static constexpr int kZOffset = kStages * kStageBytes;
+  static constexpr int kBarOffset = kZOffset + kStages * 64;
   static constexpr int kSmemBytes = kBarOffset + 256 + 1024;     // + barriers + alignment slack
   static constexpr int kTmemColsRaw = kNumD * BT + kNumA * 64;
   static constexpr int kTmemCols = kTmemColsRaw <= 32    ? 32
@@ -84,6 +89,7 @@ struct TcCfg {
   static_assert(kStages >= 2, "shared memory too small for two stages");
   static_assert(kTmemColsRaw <= 512, "TMEM budget");
   static_assert(BT % 16 == 0 && BT >= 16 && BT <= 128, "token tile");
+  static_assert(kStageBytes % 1024 == 0, "stage alignment");
 };
 
 template <int VARIANT, int BT, bool PARTIALS>
@@ -92,6 +98,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
                const __grid_constant__ CUtensorMap w8_map, const TcParams p) {
   using C = TcCfg<VARIANT, BT>;
   constexpr int S = C::kStages;
+  constexpr int HB = BT / 2;  // token columns per drain warpgroup
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the 128-byte-swizzle atoms
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -99,15 +106,36 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
   uint8_t* smem = smem_raw + (base - raw_addr);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int ks = blockIdx.x;
-  const int64_t m0 = (int64_t)blockIdx.y * BT;
-  const int64_t n0 = (int64_t)blockIdx.z * 128;
   const int64_t N = p.N, K = p.K;
   const int G = p.G;
-  const int g0 = (int)((int64_t)ks * G / p.ks), g1 = (int)((int64_t)(ks + 1) * G / p.ks);
-  const int ng = g1 - g0;
 
-  // barriers and flags
+  // ---- this CTA's work: a flat sequence of (tile, group) items ---------------
+  // persistent: tiles blockIdx.x, +gridDim.x, ... each with all G groups;
+  // split-K:    tile (blockIdx.y, blockIdx.z), groups of cluster rank blockIdx.x.
+  int u_begin, u_step, n_units, g0, g1;
+  if (p.persistent) {
+    const int total = p.m_tiles * p.n_tiles;
+    u_begin = blockIdx.x;
+    u_step = gridDim.x;
+    n_units = u_begin < total ? (total - u_begin + u_step - 1) / u_step : 0;
+    g0 = 0;
+    g1 = G;
+  } else {
+    u_begin = blockIdx.y + blockIdx.z * p.m_tiles;
+    u_step = 1;
+    n_units = 1;
+    g0 = (int)((int64_t)blockIdx.x * G / p.ks);
+    g1 = (int)((int64_t)(blockIdx.x + 1) * G / p.ks);
+  }
+  const int ng = g1 - g0;
+  const int n_items = n_units * ng;
+  auto item_tile = [&](int i, int& mt, int& nt) {
+    const int u = u_begin + (i / ng) * u_step;
+    mt = u % p.m_tiles;
+    nt = u / p.m_tiles;
+  };
+
+  // ---- barriers and flags ------------------------------------------------------
   const uint32_t bar0 = base + C::kBarOffset;
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
@@ -120,6 +148,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
   auto stage_act = [&](int s) { return base + (uint32_t)(s * C::kStageBytes); };
   auto stage_w_ptr = [&](int s) { return smem + s * C::kStageBytes + C::kActBytes; };
+  auto stage_z_ptr = [&](int s) { return smem + C::kZOffset + s * 64; };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -152,8 +181,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
   const uint32_t d_tmem = tmem;                  // accumulators: columns [0, 2*BT)
   const uint32_t a_tmem = tmem + kNumD * BT;     // A operand:    columns [2*BT, 2*BT+128)
   const uint64_t tmo = p.timeout_ns;
+  const bool cluster_reduce = !PARTIALS && !p.persistent && p.ks > 1;
 
-  constexpr int HB = BT / 2;  // token columns per drain warpgroup
   // Each role ends with the same named CTA barrier (all 448 threads) and, for
   // split-K clusters, the same two cluster barriers, so the drain warps can
   // keep their accumulators in registers through the epilogue.
@@ -165,20 +194,44 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      int issued = 0;
-      for (int i = 0; i < ng; ++i) {
+      const uint8_t* zeros = p.packed + N * K / 2 + 2 * (int64_t)G * N;
+      auto load_weights = [&](int i, int s) {
+        int mt, nt;
+        item_tile(i, mt, nt);
+        const int g = g0 + i % ng;
+        if constexpr (VARIANT == kW8A16) {
+          tma_load_2d(stage_act(s) + C::kActBytes, &w8_map, full_bar(s), g * 128, nt * 128);
+        } else {
+          bulk_load(stage_act(s) + C::kActBytes, p.packed + ((int64_t)nt * G + g) * 8192, 8192,
+                    full_bar(s));
+          bulk_load(smem_u32(stage_z_ptr(s)), zeros + (int64_t)g * (N / 2) + (int64_t)nt * 64, 64,
+                    full_bar(s));
+        }
+      };
+      auto load_act = [&](int i, int s) {
+        int mt, nt;
+        item_tile(i, mt, nt);
+        const int g = g0 + i % ng;
+        tma_load_2d(stage_act(s), &act_map, full_bar(s), g * 128, mt * BT);
+        tma_load_2d(stage_act(s) + C::kActBox, &act_map, full_bar(s), g * 128 + 64, mt * BT);
+      };
+      // weights do not depend on the preceding grid: start streaming them
+      // before waiting for it; activations only after
+      const int n_pre = n_items < S ? n_items : S;
+      for (int i = 0; i < n_pre; ++i) {
+        mbar_arrive_expect_tx(full_bar(i), C::kTxBytes);
+        load_weights(i, i);
+      }
+      griddep_wait();
+      griddep_launch_dependents();
+      for (int i = 0; i < n_pre; ++i) load_act(i, i);
+      int issued = n_pre;
+      for (int i = n_pre; i < n_items; ++i) {
         const int s = i % S;
         if (!mbar_wait(empty_bar(s), ((i / S) & 1) ^ 1, abort_flag, tmo)) break;
-        mbar_arrive_expect_tx(full_bar(s), C::kStageBytes);
-        const int g = g0 + i;
-        tma_load_2d(stage_act(s), &act_map, full_bar(s), g * 128, (int)m0);
-        tma_load_2d(stage_act(s) + C::kActBox, &act_map, full_bar(s), g * 128 + 64, (int)m0);
-        if constexpr (VARIANT == kW8A16) {
-          tma_load_2d(stage_act(s) + C::kActBytes, &w8_map, full_bar(s), g * 128, (int)n0);
-        } else {
-          const uint8_t* src = p.packed + ((int64_t)blockIdx.z * G + g) * 8192;
-          bulk_load(stage_act(s) + C::kActBytes, src, 8192, full_bar(s));
-        }
+        mbar_arrive_expect_tx(full_bar(s), C::kTxBytes);
+        load_weights(i, s);
+        load_act(i, s);
         ++issued;
       }
       // wait (bounded) for every copy this thread issued to land before exit
@@ -189,7 +242,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
     }
     __syncwarp();
     teardown_sync();
-    if (!PARTIALS && p.ks > 1) {
+    if (cluster_reduce) {
       cluster_sync_all();
       cluster_sync_all();
     }
@@ -197,38 +250,39 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_f16(128, BT, C::kBf16);
-      int last_empty = -1;
-      for (int i = 0; i < ng; ++i) {
+      int last = -1;
+      for (int i = 0; i < n_items; ++i) {
         const int s = i % S, ab = i % kNumA;
-        const int di = C::kDrainPerGroup ? i : 0;
+        const int gi = i % ng;  // group index inside the tile
+        const int di = C::kDrainPerGroup ? i : i / ng;
         const int db = di % kNumD;
         if (!mbar_wait(full_bar(s), (i / S) & 1, abort_flag, tmo)) break;
         if (!mbar_wait(afull_bar(ab), (i / kNumA) & 1, abort_flag, tmo)) break;
-        if (C::kDrainPerGroup || i == 0)
+        if (C::kDrainPerGroup || gi == 0)
           if (!mbar_wait(dempty_bar(db), ((di / kNumD) & 1) ^ 1, abort_flag, tmo)) break;
         tc_fence_after();
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const uint32_t b_addr = stage_act(s) + (j >> 2) * C::kActBox + (j & 3) * 32;
-          const uint32_t acc = C::kDrainPerGroup ? (j > 0) : (i > 0 || j > 0);
+          const uint32_t acc = C::kDrainPerGroup ? (j > 0) : (gi > 0 || j > 0);
           tc_mma_f16_ts(d_tmem + db * BT, a_tmem + ab * 64 + j * 8, sdesc_kmajor_sw128(b_addr),
                         idesc, acc);
         }
         tc_commit(empty_bar(s));
         tc_commit(aempty_bar(ab));
-        if (C::kDrainPerGroup || i == ng - 1) tc_commit(dfull_bar(db));
-        last_empty = i;
+        if (C::kDrainPerGroup || gi == ng - 1) tc_commit(dfull_bar(db));
+        last = i;
       }
-      if (last_empty >= 0) {  // let the last MMAs finish before teardown
+      if (last >= 0) {  // let the last MMAs finish before teardown
         volatile int no_abort = 0;
-        mbar_wait(empty_bar(last_empty % S), (last_empty / S) & 1, &no_abort, tmo);
+        mbar_wait(empty_bar(last % S), (last / S) & 1, &no_abort, tmo);
       }
     }
     __syncwarp();
     teardown_sync();
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
-    if (!PARTIALS && p.ks > 1) {
+    if (cluster_reduce) {
       cluster_sync_all();
       cluster_sync_all();
     }
@@ -236,10 +290,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
     // ------------------------------------------------------------ converters
     const int r = (warp - kConvWarp0) * 32 + lane;  // weight row in the tile == TMEM lane
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const uint8_t* zeros = p.packed + N * K / 2 + 2 * (int64_t)G * N;
-    for (int i = 0; i < ng; ++i) {
+    for (int i = 0; i < n_items; ++i) {
       const int s = i % S, ab = i % kNumA;
-      const int g = g0 + i;
       if (!mbar_wait(full_bar(s), (i / S) & 1, abort_flag, tmo)) break;
       uint32_t out[64];
       if constexpr (VARIANT == kW8A16) {
@@ -273,15 +325,14 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
         uint4 v[4];
 #pragma unroll
         for (int c = 0; c < 4; ++c) v[c] = *reinterpret_cast<const uint4*>(wt + c * 2048);
+        const uint8_t zb = stage_z_ptr(s)[r >> 1];
         __syncwarp();
         if (lane == 0) mbar_arrive(empty_bar(s));
-        const int64_t n = n0 + r;
-        const uint8_t zb = __ldg(zeros + (int64_t)g * (N / 2) + (n >> 1));
-        const uint32_t z = (n & 1) ? (zb >> 4) : (zb & 0xF);
+        const uint32_t z = (r & 1) ? (zb >> 4) : (zb & 0xF);
         if constexpr (VARIANT == kW4A8) {
           // fp16: 0x6400|e = 1024+e, 0x6400|(e<<4) = 1024+16e (exact)
           const __half2 zlo = __half2half2(__ushort_as_half((uint16_t)(0x6400u | z)));
-          const __half2 zhi = __half2half2(__float2half_rn(64.0f + (float)z));
+          const __half2 nzhi = __half2half2(__float2half_rn(-64.0f - (float)z));
           const __half2 sixteenth = __float2half2_rn(0.0625f);
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
@@ -294,9 +345,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
               uint32_t h2 = lop3_and_or(w2, 0x000F000Fu, 0x64006400u);
               uint32_t h3 = lop3_and_or(w2, 0x00F000F0u, 0x64006400u);
               __half2 r0 = __hsub2(*reinterpret_cast<__half2*>(&h0), zlo);
-              __half2 r1 = __hfma2(*reinterpret_cast<__half2*>(&h1), sixteenth, __hneg2(zhi));
+              __half2 r1 = __hfma2(*reinterpret_cast<__half2*>(&h1), sixteenth, nzhi);
               __half2 r2 = __hsub2(*reinterpret_cast<__half2*>(&h2), zlo);
-              __half2 r3 = __hfma2(*reinterpret_cast<__half2*>(&h3), sixteenth, __hneg2(zhi));
+              __half2 r3 = __hfma2(*reinterpret_cast<__half2*>(&h3), sixteenth, nzhi);
               out[c * 16 + j * 4 + 0] = *reinterpret_cast<uint32_t*>(&r0);
               out[c * 16 + j * 4 + 1] = *reinterpret_cast<uint32_t*>(&r1);
               out[c * 16 + j * 4 + 2] = *reinterpret_cast<uint32_t*>(&r2);
@@ -338,7 +389,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
     }
     __syncwarp();
     teardown_sync();
-    if (!PARTIALS && p.ks > 1) {
+    if (cluster_reduce) {
       cluster_sync_all();
       cluster_sync_all();
     }
@@ -346,68 +397,114 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
     // ------------------------------------------------------------ drain (warps 0-7)
     const int r = (warp & 3) * 32 + lane;
     const int col0 = (warp >> 2) * HB;
-    const int64_t n = n0 + r;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint16_t* scales = reinterpret_cast<const uint16_t*>(p.packed + N * K / 2);
-    const int nd = C::kDrainPerGroup ? ng : (ng > 0 ? 1 : 0);
-    float R[HB];  // fp32 running sums for this thread's weight row
+    griddep_wait();  // a_s and y belong to the stream's order
+    float R[HB];     // fp32 running sums for this thread's weight row
+    auto scale_of = [&](int i) -> float {
+      if constexpr (C::kDrainPerGroup) {
+        int mt, nt;
+        item_tile(i, mt, nt);
+        return f16_bits_to_f32(__ldg(scales + (int64_t)(g0 + i % ng) * N + (int64_t)nt * 128 + r));
+      } else {
+        return 1.f;
+      }
+    };
+    float s_next = n_items > 0 ? scale_of(0) : 0.f;
+    bool ok = true;
+    int mt = 0, nt = 0;
+    for (int k = 0; k < n_units && ok; ++k) {
+      item_tile(k * ng, mt, nt);
+      const int64_t n = (int64_t)nt * 128 + r;
+      const int64_t m0 = (int64_t)mt * BT;
 #pragma unroll
-    for (int t = 0; t < HB; ++t) R[t] = 0.f;
-    for (int i = 0; i < nd; ++i) {
-      const int db = i % kNumD;
-      const int g = g0 + i;
-      float s = 1.f;
-      if constexpr (C::kDrainPerGroup) s = f16_bits_to_f32(__ldg(scales + (int64_t)g * N + n));
-      if (!mbar_wait(dfull_bar(db), (i / kNumD) & 1, abort_flag, tmo)) break;
-      tc_fence_after();
-      constexpr int CW = HB < 16 ? HB : 16;  // columns per tcgen05.ld
+      for (int t = 0; t < HB; ++t) R[t] = 0.f;
+      const int nd = C::kDrainPerGroup ? ng : 1;
+      for (int gi = 0; gi < nd; ++gi) {
+        const int i = k * ng + gi;
+        const int di = C::kDrainPerGroup ? i : k;
+        const int db = di % kNumD;
+        const float s = s_next;
+        if (C::kDrainPerGroup && i + 1 < n_items) s_next = scale_of(i + 1);
+        if (!mbar_wait(dfull_bar(db), (di / kNumD) & 1, abort_flag, tmo)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        constexpr int CW = HB < 16 ? HB : 16;       // columns per tcgen05.ld
+        constexpr int PAIR = (HB / CW) >= 2 ? 2 : 1;  // loads in flight per wait
 #pragma unroll
-      for (int cb = 0; cb < HB / CW; ++cb) {
-        uint32_t v[16];
-        const uint32_t src = d_tmem + lane_base + db * BT + col0 + cb * CW;
-        if constexpr (CW == 16) tmem_ld16(src, v);
-        else tmem_ld8(src, v);
-        tmem_wait_ld();
-        if constexpr (PARTIALS) {
+        for (int cb = 0; cb < HB / CW; cb += PAIR) {
+          uint32_t v[PAIR][16];
 #pragma unroll
-          for (int q = 0; q < CW; ++q) {
-            const int64_t m = m0 + col0 + cb * CW + q;
-            if (m < p.M) p.partials[(m * N + n) * G + g] = __float2int_rn(__uint_as_float(v[q]));
+          for (int q2 = 0; q2 < PAIR; ++q2) {
+            const uint32_t src = d_tmem + lane_base + db * BT + col0 + (cb + q2) * CW;
+            if constexpr (CW == 16) tmem_ld16(src, v[q2]);
+            else tmem_ld8(src, v[q2]);
           }
-        } else {
+          tmem_wait_ld();
 #pragma unroll
-          for (int q = 0; q < CW; ++q) R[cb * CW + q] = fmaf(s, __uint_as_float(v[q]), R[cb * CW + q]);
+          for (int q2 = 0; q2 < PAIR; ++q2) {
+            if constexpr (PARTIALS) {
+              const int g = g0 + gi;
+#pragma unroll
+              for (int q = 0; q < CW; ++q) {
+                const int64_t m = m0 + col0 + (cb + q2) * CW + q;
+                if (m < p.M)
+                  p.partials[(m * N + n) * G + g] = __float2int_rn(__uint_as_float(v[q2][q]));
+              }
+            } else {
+#pragma unroll
+              for (int q = 0; q < CW; ++q)
+                R[(cb + q2) * CW + q] = fmaf(s, __uint_as_float(v[q2][q]), R[(cb + q2) * CW + q]);
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(dempty_bar(db));
+      }
+      if (!ok) break;
+      if constexpr (VARIANT == kW8A16) {
+        const float sc = f16_bits_to_f32(__ldg(p.s8 + n));
+#pragma unroll
+        for (int t = 0; t < HB; ++t) R[t] *= sc;
+      }
+      if constexpr (!PARTIALS) {
+        if (!cluster_reduce) {
+#pragma unroll
+          for (int t = 0; t < HB; ++t) {
+            const int64_t m = m0 + col0 + t;
+            if (m < p.M) {
+              float v = R[t];
+              if constexpr (VARIANT == kW4A8) v = __ldg(p.a_s + m) * v;
+              p.y[m * N + n] = f32_to_bf16_bits(v);
+            }
+          }
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(dempty_bar(db));
-    }
-    if constexpr (VARIANT == kW8A16) {
-      const float sc = f16_bits_to_f32(__ldg(p.s8 + n));
-#pragma unroll
-      for (int t = 0; t < HB; ++t) R[t] *= sc;
     }
     __syncwarp();
     teardown_sync();
-    if constexpr (!PARTIALS) {
-      // every copy and MMA of this CTA has completed: the stages are free
+    if (cluster_reduce) {
+      // one tile per CTA; every copy and MMA of this CTA has completed, so the
+      // stages are free for the partial sums
+      const int64_t n = (int64_t)nt * 128 + r;
+      const int64_t m0 = (int64_t)mt * BT;
       float* red = reinterpret_cast<float*>(smem);  // [BT][128]
-      if (p.ks > 1) {
 #pragma unroll
-        for (int t = 0; t < HB; ++t) red[(col0 + t) * 128 + r] = R[t];
-        cluster_sync_all();
-        if (cluster_ctarank() == 0) {
-          const uint32_t local = smem_u32(red);
-          for (int rk = 1; rk < p.ks; ++rk) {
-            const uint32_t remote = map_to_rank(local, rk);
+      for (int t = 0; t < HB; ++t) red[(col0 + t) * 128 + r] = R[t];
+      cluster_sync_all();
+      if (cluster_ctarank() == 0) {
+        const uint32_t local = smem_u32(red);
+        for (int rk = 1; rk < p.ks; ++rk) {
+          const uint32_t remote = map_to_rank(local, rk);
 #pragma unroll
-            for (int t = 0; t < HB; ++t) R[t] += ld_dsmem_f32(remote + ((col0 + t) * 128 + r) * 4);
-          }
+          for (int t = 0; t < HB; ++t) R[t] += ld_dsmem_f32(remote + ((col0 + t) * 128 + r) * 4);
         }
-        cluster_sync_all();
       }
-      if (p.ks == 1 || cluster_ctarank() == 0) {
+      cluster_sync_all();
+      if (cluster_ctarank() == 0) {
 #pragma unroll
         for (int t = 0; t < HB; ++t) {
           const int64_t m = m0 + col0 + t;
@@ -487,6 +584,25 @@ static int tc_sm_count() {
   return count;
 }
 
+// Split of the work over the GPU. With enough tiles, a persistent grid (one
+// CTA per SM) strides over them with all of K; otherwise each tile's K groups
+// are split over a cluster of ks CTAs. ks minimises rounds * groups-per-unit.
+static void choose_split(int64_t tiles, int G, int sms, int* ks_out, int* persistent_out) {
+  double best = 1e30;
+  int best_ks = 1;
+  for (int ks = 1; ks <= 8 && ks <= G; ++ks) {
+    const int64_t units = tiles * ks;
+    const int64_t rounds = (units + sms - 1) / sms;
+    const double cost = (double)rounds * ((G + ks - 1) / ks) * (ks > 1 ? 1.05 : 1.0);
+    if (cost < best - 1e-9) {
+      best = cost;
+      best_ks = ks;
+    }
+  }
+  *ks_out = best_ks;
+  *persistent_out = (best_ks == 1 && tiles > sms) ? 1 : 0;
+}
+
 template <int VARIANT, int BT, bool PARTIALS>
 static cudaError_t launch_tc(const GemmArgs& a, cudaStream_t st) {
   using C = TcCfg<VARIANT, BT>;
@@ -504,19 +620,19 @@ static cudaError_t launch_tc(const GemmArgs& a, cudaStream_t st) {
   const int64_t m_tiles = (a.M + BT - 1) / BT;
   const int64_t n_tiles = a.N / 128;
   const int64_t tiles = m_tiles * n_tiles;
-  int ks = 1;
-  if (tiles < tc_sm_count()) {
-    ks = (int)((tc_sm_count() + tiles - 1) / tiles);
-    if (ks > 8) ks = 8;
-    if (ks > G) ks = G;
-  }
-  if (m_tiles > 65535 || n_tiles > 65535) return cudaErrorInvalidValue;
+  if (m_tiles > 65535 || n_tiles > 65535 || tiles >= (1LL << 31)) return cudaErrorInvalidValue;
+  const int sms = tc_sm_count();
+  int ks = 1, persistent = 0;
+  choose_split(tiles, G, sms, &ks, &persistent);
   TcParams p{};
   p.M = a.M;
   p.N = a.N;
   p.K = a.K;
   p.G = G;
   p.ks = ks;
+  p.m_tiles = (int)m_tiles;
+  p.n_tiles = (int)n_tiles;
+  p.persistent = persistent;
   p.a_s = a.a_s;
   p.packed = a.packed;
   p.s8 = a.s8;
@@ -532,17 +648,22 @@ static cudaError_t launch_tc(const GemmArgs& a, cudaStream_t st) {
     attr_set = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)ks, (unsigned)m_tiles, (unsigned)n_tiles);
+  if (persistent)
+    cfg.gridDim = dim3((unsigned)(tiles < sms ? tiles : sms), 1, 1);
+  else
+    cfg.gridDim = dim3((unsigned)ks, (unsigned)m_tiles, (unsigned)n_tiles);
   cfg.blockDim = dim3(kTcThreads, 1, 1);
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)ks;
+  attr[0].val.clusterDim.x = persistent ? 1u : (unsigned)ks;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kern, act_map, w8_map, p);
 }
 
