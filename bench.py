@@ -133,12 +133,24 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def max_over_ranks(value: float, device=None) -> float:
+    """Replicas only: the one cross-rank step is this timing reduction (MAX),
+    followed by a barrier. Works on NCCL (device tensor) and gloo (CPU)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64,
+                     device=device if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.barrier()
+    return float(t.item())
+
+
 # --------------------------------------------------------------- workloads ----
 
 class Workload:
     """A list of launches per step ("ops"), built once; inputs resident on device."""
 
-    def __init__(self, name, dev, copies=None, m=1, lin=(3584, 3584), path=0):
+    def __init__(self, name, dev, copies=None, m=1, lin=(3584, 3584), path=0, variant="w4a8"):
         import torch
 
         import synth
@@ -149,6 +161,8 @@ class Workload:
         self.inputs = []      # per copy: list of device tensors fed from host in e2e
         self.outputs = []
         t = lambda a, dt=None: _to_dev(torch, a, dev, dt)
+        if name == "linear" and variant != "w4a8":  # weight-only single linear
+            name = self.name = "dit"
         if name in ("decode", "prefill", "tiny", "linear"):
             if name == "decode":
                 ms, shapes, n_copies = [1, 4, 16], SHAPES_7B, copies or 4
@@ -207,9 +221,12 @@ class Workload:
                 self.acts[(m, inp)] = (x, t(x, torch.bfloat16), a)
             self.ys = {(m, nm): torch.empty((m, N), dtype=torch.bfloat16, device=dev)
                        for (nm, K, N) in SHAPES_7B + [HEAD]}
-        elif name == "dit":
-            self.ms = [1, 16, 4096]
-            self.dit_shapes = [(3072, 3072), (3072, 12288), (12288, 3072)]
+        if name == "dit":
+            self.ms = [1, 16, 4096] if variant == "w4a8" else [m]
+            self.dit_shapes = ([(3072, 3072), (3072, 12288), (12288, 3072)]
+                               if variant == "w4a8" else [tuple(lin)])
+            self.dit_variants = ("w4", "w8") if variant == "w4a8" else \
+                ("w4",) if variant == "w4a16" else ("w8",)
             self.dit_w = {}
             for (K, N) in self.dit_shapes:
                 w = synth.w4_weights(4, 0, 0, N, K)
@@ -218,13 +235,13 @@ class Workload:
                                                  t(w.zero)), t(w8), t(s8, torch.float16))
             self.acts = {}
             for M in self.ms:
-                for K in (3072, 12288):
+                for K in sorted(set(k for k, _ in self.dit_shapes)):
                     x = synth.activations(4, 0, 0, M, K, outliers=False)
                     self.acts[(M, K)] = (x, t(x, torch.bfloat16))
             self.ys = {(M, K, N, v): torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-                       for M in self.ms for (K, N) in self.dit_shapes for v in ("w4", "w8")}
+                       for M in self.ms for (K, N) in self.dit_shapes for v in self.dit_variants}
             self.layers = [None]
-        else:
+        elif name not in ("decode", "prefill", "tiny", "linear", "model"):
             raise ValueError(name)
         self.n_copies = 1 if name == "model" else len(self.layers)
 
@@ -265,15 +282,18 @@ class Workload:
                 for (K, N) in self.dit_shapes:
                     x, xd = self.acts[(M, K)]
                     p4, w8, s8 = self.dit_w[(K, N)]
-                    y4, y8 = self.ys[(M, K, N, "w4")], self.ys[(M, K, N, "w8")]
-                    ops.append((f"w4a16 K={K} N={N} M={M}", "w4a16", M, N, K,
-                                w4a16_bytes(M, N, K), 2 * M * N * K,
-                                (lambda xd=xd, p=p4, N=N, K=K, y=y4:
-                                 eg.w4a16_gemm(xd, p, N, K, out=y, path=self.path))))
-                    ops.append((f"w8a16 K={K} N={N} M={M}", "w8a16", M, N, K,
-                                w8a16_bytes(M, N, K), 2 * M * N * K,
-                                (lambda xd=xd, w8=w8, s8=s8, y=y8:
-                                 eg.w8a16_gemm(xd, w8, s8, out=y, path=self.path))))
+                    if "w4" in self.dit_variants:
+                        y4 = self.ys[(M, K, N, "w4")]
+                        ops.append((f"w4a16 K={K} N={N} M={M}", "w4a16", M, N, K,
+                                    w4a16_bytes(M, N, K), 2 * M * N * K,
+                                    (lambda xd=xd, p=p4, N=N, K=K, y=y4:
+                                     eg.w4a16_gemm(xd, p, N, K, out=y, path=self.path))))
+                    if "w8" in self.dit_variants:
+                        y8 = self.ys[(M, K, N, "w8")]
+                        ops.append((f"w8a16 K={K} N={N} M={M}", "w8a16", M, N, K,
+                                    w8a16_bytes(M, N, K), 2 * M * N * K,
+                                    (lambda xd=xd, w8=w8, s8=s8, y=y8:
+                                     eg.w8a16_gemm(xd, w8, s8, out=y, path=self.path))))
         return ops
 
     def host_io(self):
@@ -315,7 +335,8 @@ def run_ours(args, rank, world):
     torch.cuda.set_device(dev)
     eg.load()
     path = {"auto": eg.PATH_AUTO, "gemv": eg.PATH_GEMV, "tc": eg.PATH_TC}[args.path]
-    wl = Workload(args.workload, dev, m=args.m, lin=(args.k, args.n), path=path)
+    wl = Workload(args.workload, dev, m=args.m, lin=(args.k, args.n), path=path,
+                  variant=args.variant)
     peaks = load_peaks()
     copies = wl.n_copies
     step_ops = [wl.step_ops(c) for c in range(copies)]
@@ -361,10 +382,7 @@ def run_ours(args, rank, world):
     torch.cuda.synchronize()
     ms_total = e0.elapsed_time(e1)
     if world > 1:
-        t = torch.tensor([ms_total], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_total = float(t.item())
-        torch.distributed.barrier()
+        ms_total = max_over_ranks(ms_total, dev)
     ms_step = ms_total / args.steps
     per_step_bytes = sum(op[5] for op in step_ops[0])
     per_step_ops = sum(op[6] for op in step_ops[0])
@@ -610,6 +628,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--path", choices=["auto", "gemv", "tc"], default="auto")
+    ap.add_argument("--variant", choices=["w4a8", "w4a16", "w8a16"], default="w4a8",
+                    help="variant for --workload linear")
     args = ap.parse_args()
     if args.steps is None:
         args.steps = {"decode": 1500, "model": 200, "tiny": 2000, "linear": 200}.get(

@@ -48,8 +48,6 @@ namespace egopq {
 
 constexpr int kTcThreads = 448;
 constexpr int kProducerWarp = 12, kMmaWarp = 13, kConvWarp0 = 8;
-constexpr int kNumA = 2;   // TMEM A-operand buffers (64 columns each)
-constexpr int kNumD = 2;   // TMEM accumulators (BT columns each)
 constexpr int kMaxSmem = 232448;
 
 struct TcParams {
@@ -67,6 +65,12 @@ struct TcParams {
 
 template <int VARIANT, int BT>
 struct TcCfg {
+  // TMEM: kNumD accumulators of BT columns + kNumA A-operand buffers of 64
+  // columns. Small token tiles leave room for deeper buffering, which lets the
+  // converters run several groups ahead of the MMAs and the MMAs several
+  // groups ahead of the drain.
+  static constexpr int kNumD = BT <= 32 ? 4 : 2;
+  static constexpr int kNumA = BT <= 64 ? 6 : 4;
   static constexpr int kActBox = BT * 128;                        // one 64-wide K box, bytes
   static constexpr int kActBytes = 2 * kActBox;                   // a 128-wide group
   static constexpr int kWBytes = (VARIANT == kW8A16) ? 16384 : 8192;
@@ -77,7 +81,7 @@ struct TcCfg {
   static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
   static constexpr int kZOffset = kStages * kStageBytes;
   static constexpr int kBarOffset = kZOffset + kStages * 64;
-  static constexpr int kSmemBytes = kBarOffset + 256 + 1024;     // + barriers + alignment slack
+  static constexpr int kSmemBytes = kBarOffset + 512 + 1024;     // + barriers + alignment slack
   static constexpr int kTmemColsRaw = kNumD * BT + kNumA * 64;
   static constexpr int kTmemCols = kTmemColsRaw <= 32    ? 32
                                    : kTmemColsRaw <= 64  ? 64
@@ -88,6 +92,7 @@ struct TcCfg {
   static constexpr int kBf16 = (VARIANT == kW4A8) ? 0 : 1;
   static_assert(kStages >= 2, "shared memory too small for two stages");
   static_assert(kTmemColsRaw <= 512, "TMEM budget");
+  static_assert(8 * (2 * kStages + 2 * kNumA + 2 * kNumD) + 8 <= 512, "barrier region");
   static_assert(BT % 16 == 0 && BT >= 16 && BT <= 128, "token tile");
   static_assert(kStageBytes % 1024 == 0, "stage alignment");
 };
@@ -99,6 +104,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
   using C = TcCfg<VARIANT, BT>;
   constexpr int S = C::kStages;
   constexpr int HB = BT / 2;  // token columns per drain warpgroup
+  constexpr int kNumA = C::kNumA, kNumD = C::kNumD;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the 128-byte-swizzle atoms
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -178,8 +184,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t d_tmem = tmem;                  // accumulators: columns [0, 2*BT)
-  const uint32_t a_tmem = tmem + kNumD * BT;     // A operand:    columns [2*BT, 2*BT+128)
+  const uint32_t d_tmem = tmem;                  // accumulators: columns [0, kNumD*BT)
+  const uint32_t a_tmem = tmem + kNumD * BT;     // A operand: kNumA buffers of 64 columns
   const uint64_t tmo = p.timeout_ns;
   const bool cluster_reduce = !PARTIALS && !p.persistent && p.ks > 1;
 
