@@ -42,6 +42,36 @@ HEAD = ("head", 3584, 152064)
 INPUT_OF = {"q": "attn", "k": "attn", "v": "attn", "o": "o", "gate": "mlp", "up": "mlp",
             "down": "down"}
 INPUT_K = {"attn": 3584, "o": 3584, "mlp": 3584, "down": 18944, "head": 3584}
+FUSED = {"qkv": ["q", "k", "v"], "gate_up": ["gate", "up"]}
+INPUT_OF.update({"qkv": "attn", "gate_up": "mlp"})
+
+
+def fuse_shapes(shapes):
+    """Sibling linears sharing an input as one GEMM (weights concatenated along N)."""
+    out, seen = [], set()
+    for (nm, K, N) in shapes:
+        group = next((f for f, parts in FUSED.items() if nm in parts), None)
+        if group is None:
+            out.append((nm, K, N))
+        elif group not in seen:
+            seen.add(group)
+            out.append((group, K, sum(n for (x, _, n) in shapes if x in FUSED[group])))
+    return out
+
+
+def pack_linear(eg, synth, t, torch, config, layer, nm, N, K):
+    """Pack one linear (or a fused sibling group, each part drawn from its own
+    seed so the data equal the unfused linears')."""
+    import numpy as np
+    parts = FUSED.get(nm, [nm])
+    ws = [synth.w4_weights(config, layer, synth.LINEARS.get(p, 0),
+                           {"q": 3584, "k": 512, "v": 512, "gate": 18944, "up": 18944}.get(p, N)
+                           if len(parts) > 1 else N, K) for p in parts]
+    w_q = np.concatenate([w.w_q for w in ws])
+    s = np.concatenate([w.scale_f16 for w in ws])
+    z = np.concatenate([w.zero for w in ws])
+    assert w_q.shape == (N, K)
+    return eg.pack_w4(t(w_q), t(s, torch.float16), t(z))
 G128 = 128
 
 
@@ -150,7 +180,8 @@ def max_over_ranks(value: float, device=None) -> float:
 class Workload:
     """A list of launches per step ("ops"), built once; inputs resident on device."""
 
-    def __init__(self, name, dev, copies=None, m=1, lin=(3584, 3584), path=0, variant="w4a8"):
+    def __init__(self, name, dev, copies=None, m=1, lin=(3584, 3584), path=0, variant="w4a8",
+                 fused=False):
         import torch
 
         import synth
@@ -172,12 +203,13 @@ class Workload:
                 ms, shapes, n_copies = [m], [("q", lin[0], lin[1])], copies or 1
             else:
                 ms, shapes, n_copies = [16], [("q", 512, 256)], copies or 1
+            if fused and name in ("decode", "prefill"):
+                shapes = fuse_shapes(shapes)
             self.layers = []
             for c in range(n_copies):
                 packs = {}
                 for (nm, K, N) in shapes:
-                    w = synth.w4_weights(1, c, synth.LINEARS.get(nm, 0), N, K)
-                    packs[nm] = eg.pack_w4(t(w.w_q), t(w.scale_f16, torch.float16), t(w.zero))
+                    packs[nm] = pack_linear(eg, synth, t, torch, 1, c, nm, N, K)
                 self.layers.append(packs)
             torch.cuda.synchronize()
             self.ms = ms
@@ -198,13 +230,12 @@ class Workload:
                        for M in ms for (nm, K, N) in shapes}
         elif name == "model":
             self.ms = [m]
-            self.shapes = SHAPES_7B
+            self.shapes = fuse_shapes(SHAPES_7B) if fused else SHAPES_7B
             self.layers = []
             for layer in range(28):
                 packs = {}
-                for (nm, K, N) in SHAPES_7B:
-                    w = synth.w4_weights(3, layer, synth.LINEARS[nm], N, K)
-                    packs[nm] = eg.pack_w4(t(w.w_q), t(w.scale_f16, torch.float16), t(w.zero))
+                for (nm, K, N) in self.shapes:
+                    packs[nm] = pack_linear(eg, synth, t, torch, 3, layer, nm, N, K)
                 self.layers.append(packs)
             wh = synth.w4_weights(3, 0, synth.LINEARS["head"], HEAD[2], HEAD[1])
             self.head = eg.pack_w4(t(wh.w_q), t(wh.scale_f16, torch.float16), t(wh.zero))
@@ -220,7 +251,7 @@ class Workload:
                                 torch.empty((m, K), dtype=torch.float16, device=dev))
                 self.acts[(m, inp)] = (x, t(x, torch.bfloat16), a)
             self.ys = {(m, nm): torch.empty((m, N), dtype=torch.bfloat16, device=dev)
-                       for (nm, K, N) in SHAPES_7B + [HEAD]}
+                       for (nm, K, N) in self.shapes + [HEAD]}
         if name == "dit":
             self.ms = [1, 16, 4096] if variant == "w4a8" else [m]
             self.dit_shapes = ([(3072, 3072), (3072, 12288), (12288, 3072)]
@@ -336,7 +367,7 @@ def run_ours(args, rank, world):
     eg.load()
     path = {"auto": eg.PATH_AUTO, "gemv": eg.PATH_GEMV, "tc": eg.PATH_TC}[args.path]
     wl = Workload(args.workload, dev, m=args.m, lin=(args.k, args.n), path=path,
-                  variant=args.variant)
+                  variant=args.variant, fused=args.fused)
     peaks = load_peaks()
     copies = wl.n_copies
     step_ops = [wl.step_ops(c) for c in range(copies)]
@@ -516,7 +547,8 @@ def workload_config(args, wl, per_step_bytes, per_step_ops):
                              if wl.n_copies > 1 or args.workload == "model"
                              else "per-step weights larger than L2" if args.workload == "prefill"
                              else "small (L2 resident)",
-                "graphs": "one CUDA graph per layer copy"})
+                "graphs": "one CUDA graph per layer copy",
+                "fused_siblings": bool(args.fused)})
     return cfg
 
 
@@ -630,6 +662,8 @@ def main():
     ap.add_argument("--path", choices=["auto", "gemv", "tc"], default="auto")
     ap.add_argument("--variant", choices=["w4a8", "w4a16", "w8a16"], default="w4a8",
                     help="variant for --workload linear")
+    ap.add_argument("--fused", action="store_true",
+                    help="run q|k|v and gate|up as one GEMM each (same weights, same outputs)")
     args = ap.parse_args()
     if args.steps is None:
         args.steps = {"decode": 1500, "model": 200, "tiny": 2000, "linear": 200}.get(

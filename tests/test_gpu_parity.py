@@ -315,3 +315,31 @@ def test_bounded_wait_reports_timeout_without_fault():
     a_q, a_s, _ = oracle.quant_act(x)
     _, y_ref = oracle.w4a8(a_q, a_s, w.w_q, w.scale_f16, w.zero)
     check_bf16_output(to_host_bits(y), y_ref, "after timeout self-test")
+
+
+@pytest.mark.parametrize("M", [1, 4, 16, 200])
+def test_fused_sibling_linears_equal_separate(M):
+    """q|k|v packed as one weight (N = 3584+512+512): the fused GEMM's column
+    blocks are the separate linears' outputs."""
+    K = 3584
+    parts = [("q", 3584), ("k", 512), ("v", 512)]
+    ws = [synth.w4_weights(5, 0, synth.LINEARS[nm], n, K) for nm, n in parts]
+    fused = synth.W4Weights(np.concatenate([w.w_q for w in ws]),
+                            np.concatenate([w.scale_f16 for w in ws]),
+                            np.concatenate([w.zero for w in ws]), 128)
+    x = synth.activations(5, 0, 0, M, K)
+    a = eg.quant_act(to_dev(x, torch.bfloat16))
+    N = sum(n for _, n in parts)
+    yf = to_host_bits(eg.w4a8_gemm(a, eg.pack_w4(*dev_weights(fused)), N, K))
+    off = 0
+    a_q, a_s, _ = oracle.quant_act(x)
+    cols = np.random.default_rng(M).choice(N, 96, replace=False)
+    _, y_ref = oracle.w4a8(a_q, a_s, fused.w_q[cols], fused.scale_f16[cols], fused.zero[cols])
+    check_bf16_output(yf[:, cols], y_ref, f"fused qkv M={M}")
+    for (nm, n), w in zip(parts, ws):
+        ys = to_host_bits(eg.w4a8_gemm(a, eg.pack_w4(*dev_weights(w)), n, K))
+        if M <= 4:  # GEMV: each row's sum is formed the same way whatever N is
+            assert np.array_equal(yf[:, off:off + n], ys), nm
+        else:
+            check_bf16_output(yf[:, off:off + n], ys, f"fused vs {nm}")
+        off += n

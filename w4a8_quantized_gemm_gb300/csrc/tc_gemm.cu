@@ -42,6 +42,8 @@
 // Variants: W4A16 uses bf16 operands (activations as given, w_q - z exact in
 // bf16) and no a_s; W8A16 converts int8 weights to bf16 and accumulates all
 // of K in TMEM, applying the per-channel scale once at the end.
+#include <cmath>
+
 #include "egopq_internal.h"
 
 namespace egopq {
@@ -55,6 +57,7 @@ struct TcParams {
   int G, ks;
   int m_tiles, n_tiles;
   int persistent;  // 1: CTAs stride over tiles with all of K; 0: one tile per CTA, split-K cluster
+  int band;        // persistent tile order: bands of `band` m-tiles, m fastest inside a band
   const float* a_s;
   const uint8_t* packed;
   const uint16_t* s8;
@@ -97,6 +100,28 @@ struct TcCfg {
   static_assert(kStageBytes % 1024 == 0, "stage alignment");
 };
 
+// y[m0+t][n] = bf16(a_s[m0+t] * R[t]) (W4A8) or bf16(R[t]), t < HB, rows < M.
+// Eight rows at a time, with a compiler barrier between chunks so the a_s
+// loads are not all hoisted (they would cost a register each).
+template <int VARIANT, int HB>
+__device__ __forceinline__ void store_row(const float (&R)[HB], const TcParams& p, int64_t m0,
+                                          int64_t n) {
+  constexpr int CH = HB < 8 ? HB : 8;
+#pragma unroll
+  for (int c = 0; c < HB; c += CH) {
+    asm volatile("" ::: "memory");
+#pragma unroll
+    for (int t = c; t < c + CH; ++t) {
+      const int64_t m = m0 + t;
+      if (m < p.M) {
+        float v = R[t];
+        if constexpr (VARIANT == kW4A8) v = __ldg(p.a_s + m) * v;
+        p.y[m * p.N + n] = f32_to_bf16_bits(v);
+      }
+    }
+  }
+}
+
 template <int VARIANT, int BT, bool PARTIALS>
 __global__ void __launch_bounds__(kTcThreads, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
@@ -135,10 +160,23 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
   }
   const int ng = g1 - g0;
   const int n_items = n_units * ng;
-  auto item_tile = [&](int i, int& mt, int& nt) {
-    const int u = u_begin + (i / ng) * u_step;
-    mt = u % p.m_tiles;
-    nt = u / p.m_tiles;
+  // tile u -> (mt, nt). Persistent grids walk bands of p.band m-tiles, m
+  // fastest inside a band, so the tiles in flight at once share a few
+  // activation tiles and a few weight tiles (both stay in L2).
+  auto unit_tile = [&](int k, int& mt, int& nt) {
+    const int u = u_begin + k * u_step;
+    if (p.persistent) {
+      const int band_tiles = p.band * p.n_tiles;
+      const int b = u / band_tiles;
+      const int idx = u - b * band_tiles;
+      const int m_base = b * p.band;
+      const int bm = min(p.band, p.m_tiles - m_base);
+      nt = idx / bm;
+      mt = m_base + (idx - nt * bm);
+    } else {
+      mt = u % p.m_tiles;
+      nt = u / p.m_tiles;
+    }
   };
 
   // ---- barriers and flags ------------------------------------------------------
@@ -201,10 +239,23 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const uint8_t* zeros = p.packed + N * K / 2 + 2 * (int64_t)G * N;
-      auto load_weights = [&](int i, int s) {
-        int mt, nt;
-        item_tile(i, mt, nt);
-        const int g = g0 + i % ng;
+      // item i = (unit i / ng, group g0 + i % ng), walked with counters
+      int w_k = 0, w_gi = 0, w_mt = 0, w_nt = 0;   // weights cursor
+      int a_k = 0, a_gi = 0, a_mt = 0, a_nt = 0;   // activations cursor
+      if (n_items > 0) {
+        unit_tile(0, w_mt, w_nt);
+        a_mt = w_mt;
+        a_nt = w_nt;
+      }
+      auto advance = [&](int& k, int& gi, int& mt, int& nt) {
+        if (++gi == ng) {
+          gi = 0;
+          if (++k < n_units) unit_tile(k, mt, nt);
+        }
+      };
+      auto load_weights = [&](int s) {
+        const int nt = w_nt, g = g0 + w_gi;
+        advance(w_k, w_gi, w_mt, w_nt);
         if constexpr (VARIANT == kW8A16) {
           tma_load_2d(stage_act(s) + C::kActBytes, &w8_map, full_bar(s), g * 128, nt * 128);
         } else {
@@ -214,10 +265,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
                     full_bar(s));
         }
       };
-      auto load_act = [&](int i, int s) {
-        int mt, nt;
-        item_tile(i, mt, nt);
-        const int g = g0 + i % ng;
+      auto load_act = [&](int s) {
+        const int mt = a_mt, g = g0 + a_gi;
+        advance(a_k, a_gi, a_mt, a_nt);
         tma_load_2d(stage_act(s), &act_map, full_bar(s), g * 128, mt * BT);
         tma_load_2d(stage_act(s) + C::kActBox, &act_map, full_bar(s), g * 128 + 64, mt * BT);
       };
@@ -226,18 +276,18 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
       const int n_pre = n_items < S ? n_items : S;
       for (int i = 0; i < n_pre; ++i) {
         mbar_arrive_expect_tx(full_bar(i), C::kTxBytes);
-        load_weights(i, i);
+        load_weights(i);
       }
       griddep_wait();
       griddep_launch_dependents();
-      for (int i = 0; i < n_pre; ++i) load_act(i, i);
+      for (int i = 0; i < n_pre; ++i) load_act(i);
       int issued = n_pre;
       for (int i = n_pre; i < n_items; ++i) {
         const int s = i % S;
         if (!mbar_wait(empty_bar(s), ((i / S) & 1) ^ 1, abort_flag, tmo)) break;
         mbar_arrive_expect_tx(full_bar(s), C::kTxBytes);
-        load_weights(i, s);
-        load_act(i, s);
+        load_weights(s);
+        load_act(s);
         ++issued;
       }
       // wait (bounded) for every copy this thread issued to land before exit
@@ -257,10 +307,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_f16(128, BT, C::kBf16);
       int last = -1;
-      for (int i = 0; i < n_items; ++i) {
+      int gi = 0, ti = 0;  // group index inside the tile, tile counter
+      for (int i = 0; i < n_items; ++i, gi = (gi + 1 == ng) ? (++ti, 0) : gi + 1) {
         const int s = i % S, ab = i % kNumA;
-        const int gi = i % ng;  // group index inside the tile
-        const int di = C::kDrainPerGroup ? i : i / ng;
+        const int di = C::kDrainPerGroup ? i : ti;
         const int db = di % kNumD;
         if (!mbar_wait(full_bar(s), (i / S) & 1, abort_flag, tmo)) break;
         if (!mbar_wait(afull_bar(ab), (i / kNumA) & 1, abort_flag, tmo)) break;
@@ -407,22 +457,29 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
     const uint16_t* scales = reinterpret_cast<const uint16_t*>(p.packed + N * K / 2);
     griddep_wait();  // a_s and y belong to the stream's order
     float R[HB];     // fp32 running sums for this thread's weight row
-    auto scale_of = [&](int i) -> float {
-      if constexpr (C::kDrainPerGroup) {
-        int mt, nt;
-        item_tile(i, mt, nt);
-        return f16_bits_to_f32(__ldg(scales + (int64_t)(g0 + i % ng) * N + (int64_t)nt * 128 + r));
-      } else {
-        return 1.f;
-      }
-    };
-    float s_next = n_items > 0 ? scale_of(0) : 0.f;
-    bool ok = true;
+    // per-group scales s[g][n] of this thread's row, walked with a pointer and
+    // prefetched one group ahead (the next tile's first one at a tile's end)
+    const uint16_t* sp = nullptr;
+    float s_next = 0.f;
     int mt = 0, nt = 0;
+    if (n_items > 0) {
+      unit_tile(0, mt, nt);
+      sp = scales + (int64_t)g0 * N + (int64_t)nt * 128 + r;
+      if constexpr (C::kDrainPerGroup) s_next = f16_bits_to_f32(__ldg(sp));
+    }
+    bool ok = true;
     for (int k = 0; k < n_units && ok; ++k) {
-      item_tile(k * ng, mt, nt);
+      if (k > 0) unit_tile(k, mt, nt);
       const int64_t n = (int64_t)nt * 128 + r;
       const int64_t m0 = (int64_t)mt * BT;
+      const uint16_t* sp_tile = scales + (int64_t)g0 * N + n;
+      // the next tile's first scale, fetched now and used after this tile
+      float s_first_next = 0.f;
+      if (C::kDrainPerGroup && k + 1 < n_units) {
+        int mt2, nt2;
+        unit_tile(k + 1, mt2, nt2);
+        s_first_next = f16_bits_to_f32(__ldg(scales + (int64_t)g0 * N + (int64_t)nt2 * 128 + r));
+      }
 #pragma unroll
       for (int t = 0; t < HB; ++t) R[t] = 0.f;
       const int nd = C::kDrainPerGroup ? ng : 1;
@@ -431,14 +488,18 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
         const int di = C::kDrainPerGroup ? i : k;
         const int db = di % kNumD;
         const float s = s_next;
-        if (C::kDrainPerGroup && i + 1 < n_items) s_next = scale_of(i + 1);
+        if constexpr (C::kDrainPerGroup)
+          s_next = (gi + 1 < ng) ? f16_bits_to_f32(__ldg(sp_tile + (int64_t)(gi + 1) * N))
+                                 : s_first_next;
         if (!mbar_wait(dfull_bar(db), (di / kNumD) & 1, abort_flag, tmo)) {
           ok = false;
           break;
         }
         tc_fence_after();
         constexpr int CW = HB < 16 ? HB : 16;       // columns per tcgen05.ld
-        constexpr int PAIR = (HB / CW) >= 2 ? 2 : 1;  // loads in flight per wait
+        // loads in flight per wait (one at HB = 64, where the 64 accumulators
+        // leave no room for a second 16-column buffer)
+        constexpr int PAIR = (HB / CW) >= 2 && HB < 64 ? 2 : 1;
 #pragma unroll
         for (int cb = 0; cb < HB / CW; cb += PAIR) {
           uint32_t v[PAIR][16];
@@ -478,15 +539,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
       }
       if constexpr (!PARTIALS) {
         if (!cluster_reduce) {
-#pragma unroll
-          for (int t = 0; t < HB; ++t) {
-            const int64_t m = m0 + col0 + t;
-            if (m < p.M) {
-              float v = R[t];
-              if constexpr (VARIANT == kW4A8) v = __ldg(p.a_s + m) * v;
-              p.y[m * N + n] = f32_to_bf16_bits(v);
-            }
-          }
+          store_row<VARIANT, HB>(R, p, m0 + col0, n);
         }
       }
     }
@@ -511,15 +564,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
       }
       cluster_sync_all();
       if (cluster_ctarank() == 0) {
-#pragma unroll
-        for (int t = 0; t < HB; ++t) {
-          const int64_t m = m0 + col0 + t;
-          if (m < p.M) {
-            float v = R[t];
-            if constexpr (VARIANT == kW4A8) v = __ldg(p.a_s + m) * v;
-            p.y[m * N + n] = f32_to_bf16_bits(v);
-          }
-        }
+        store_row<VARIANT, HB>(R, p, m0 + col0, n);
       }
     }
   }
@@ -594,19 +639,37 @@ static int tc_sm_count() {
 // CTA per SM) strides over them with all of K; otherwise each tile's K groups
 // are split over a cluster of ks CTAs. ks minimises rounds * groups-per-unit.
 static void choose_split(int64_t tiles, int G, int sms, int* ks_out, int* persistent_out) {
+  // enough tiles to fill the GPU: persistent, all of K per tile
+  if (tiles >= sms) {
+    *ks_out = 1;
+    *persistent_out = 1;
+    return;
+  }
+  // otherwise split K over a cluster, one round, as many SMs busy as possible
+  // (a split costs about one group of prologue/reduction per CTA)
   double best = 1e30;
   int best_ks = 1;
   for (int ks = 1; ks <= 8 && ks <= G; ++ks) {
     const int64_t units = tiles * ks;
     const int64_t rounds = (units + sms - 1) / sms;
-    const double cost = (double)rounds * ((G + ks - 1) / ks) * (ks > 1 ? 1.05 : 1.0);
+    const double cost = (double)rounds * ((G + ks - 1) / ks + (ks > 1 ? 1.0 : 0.0));
     if (cost < best - 1e-9) {
       best = cost;
       best_ks = ks;
     }
   }
   *ks_out = best_ks;
-  *persistent_out = (best_ks == 1 && tiles > sms) ? 1 : 0;
+  *persistent_out = 0;
+}
+
+// Band height (in m-tiles) for the persistent tile order: the tiles in flight
+// (about `concurrent`) cover `band` activation tiles and concurrent/band weight
+// tiles; minimise band*act + (concurrent/band)*w.
+static int choose_band(int64_t m_tiles, int64_t concurrent, double act_tile, double w_tile) {
+  int band = (int)(std::sqrt((double)concurrent * w_tile / act_tile) + 0.5);
+  if (band < 1) band = 1;
+  if (band > m_tiles) band = (int)m_tiles;
+  return band;
 }
 
 template <int VARIANT, int BT, bool PARTIALS>
@@ -639,6 +702,10 @@ static cudaError_t launch_tc(const GemmArgs& a, cudaStream_t st) {
   p.m_tiles = (int)m_tiles;
   p.n_tiles = (int)n_tiles;
   p.persistent = persistent;
+  p.band = persistent ? choose_band(m_tiles, tiles < sms ? tiles : sms,
+                                    (double)BT * a.K * 2.0,
+                                    (double)128 * a.K / ((VARIANT == kW8A16) ? 1.0 : 2.0))
+                      : 1;
   p.a_s = a.a_s;
   p.packed = a.packed;
   p.s8 = a.s8;
