@@ -460,7 +460,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
     // per-group scales s[g][n] of this thread's row, walked with a pointer and
     // prefetched one group ahead (the next tile's first one at a tile's end)
     const uint16_t* sp = nullptr;
-    float s_next = 0.f;
+    float s_next = 1.f;  // weight-only int8: no per-group scale (per-channel scale at the end)
     int mt = 0, nt = 0;
     if (n_items > 0) {
       unit_tile(0, mt, nt);
