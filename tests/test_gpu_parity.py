@@ -343,3 +343,37 @@ def test_fused_sibling_linears_equal_separate(M):
         else:
             check_bf16_output(yf[:, off:off + n], ys, f"fused vs {nm}")
         off += n
+
+
+@pytest.mark.parametrize("n_tiles", [76, 78, 77])
+def test_w4a8_persistent_multicast_clusters_full(n_tiles):
+    """Grids with at least one tile per SM run persistently; n-tile counts
+    divisible by 4 / 2 / neither share activation tiles over clusters of
+    4 / 2 / 1 CTAs. Ragged token tail (M=200 over two 128-token tiles), full
+    oracle comparison."""
+    M, K, N = 200, 512, 128 * n_tiles
+    x, w = w4_case(6, M, N, K)
+    a, packed, y = run_w4a8(x, w, eg.PATH_TC, M, N, K)
+    a_q, a_s, _ = oracle.quant_act(x)
+    _, y_ref = oracle.w4a8(a_q, a_s, w.w_q, w.scale_f16, w.zero)
+    check_bf16_output(to_host_bits(y), y_ref, f"persistent n_tiles={n_tiles}")
+    Q = eg.w4a8_group_partials(a, packed, N, K, path=eg.PATH_TC).cpu().numpy()
+    rows = [0, 127, 128, 199]
+    assert np.array_equal(Q[rows], oracle.group_partials(a_q[rows], w.w_q, w.zero))
+
+
+@pytest.mark.parametrize("variant", ["w4a16", "w8a16"])
+def test_weight_only_persistent_multicast_full(variant):
+    M, K, N = 256, 384, 128 * 76
+    x = synth.activations(7, 0, 0, M, K, outliers=False)
+    if variant == "w4a16":
+        w = synth.w4_weights(7, 0, 0, N, K)
+        y = eg.w4a16_gemm(to_dev(x, torch.bfloat16), eg.pack_w4(*dev_weights(w)), N, K,
+                          path=eg.PATH_TC)
+        _, y_ref = oracle.w4a16(x, w.w_q, w.scale_f16, w.zero)
+    else:
+        w8, s8 = synth.w8_weights(7, 0, 0, N, K)
+        y = eg.w8a16_gemm(to_dev(x, torch.bfloat16), to_dev(w8), to_dev(s8, torch.float16),
+                          path=eg.PATH_TC)
+        _, y_ref = oracle.w8a16(x, w8, s8)
+    check_bf16_output(to_host_bits(y), y_ref, f"{variant} persistent")
