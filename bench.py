@@ -181,12 +181,13 @@ class Workload:
     """A list of launches per step ("ops"), built once; inputs resident on device."""
 
     def __init__(self, name, dev, copies=None, m=1, lin=(3584, 3584), path=0, variant="w4a8",
-                 fused=False):
+                 fused=False, api="gemm"):
         import torch
 
         import synth
         import w4a8_quantized_gemm_gb300 as eg
         self.torch, self.eg, self.dev, self.name, self.path = torch, eg, dev, name, path
+        self.api, self._ws = api, {}
         self.steps_ops = []   # per layer copy: list of (kind, callable-args)
         self.ops_meta = []    # (kind, M, N, K, bytes, ops)
         self.inputs = []      # per copy: list of device tensors fed from host in e2e
@@ -288,6 +289,19 @@ class Workload:
                         inp = INPUT_OF.get(nm, "head") if self.name not in ("tiny", "linear") \
                             else "attn"
                         x, xd, a = self.acts[(M, inp)]
+                        if self.api == "linear":
+                            # same algorithmic bytes as the two-call step: the
+                            # first linear of each input carries its quantization
+                            qb = 0 if inp in done else quant_bytes(M, K)
+                            done.add(inp)
+                            y = self.ys[(M, nm)]
+                            ws = self.workspace(M, K)
+                            ops.append((f"{nm} M={M}", "w4a8", M, N, K,
+                                        w4a8_bytes(M, N, K) + qb, 2 * M * N * K,
+                                        (lambda xd=xd, p=packs[nm], N=N, y=y, ws=ws:
+                                         eg.w4a8_linear(xd, p, N, out=y, workspace=ws,
+                                                        path=self.path))))
+                            continue
                         if inp not in done:
                             done.add(inp)
                             ops.append((f"quant {inp} M={M}", "quant", M, 0, K,
@@ -327,6 +341,17 @@ class Workload:
                                      eg.w8a16_gemm(xd, w8, s8, out=y, path=self.path))))
         return ops
 
+    def workspace(self, M, K):
+        """Device workspace of the one-call linear, shared by every call of one
+        (M, K) (calls are ordered on one stream)."""
+        need = self.eg.w4a8_linear_workspace_bytes(M, K, self.path)
+        if not need:
+            return None
+        key = (M, K)
+        if key not in self._ws:
+            self._ws[key] = self.torch.empty(need, dtype=self.torch.uint8, device=self.dev)
+        return self._ws[key]
+
     def host_io(self):
         """(host pinned inputs, device inputs, device outputs) for the e2e leg."""
         torch = self.torch
@@ -351,7 +376,7 @@ def kernel_label(eg, kind, M, path):
     if kind == "quant":
         return "quant_act_kernel"
     if kind == "w4a8":
-        gemv = path == eg.PATH_GEMV or (path == eg.PATH_AUTO and M <= 4)
+        gemv = path == eg.PATH_GEMV or (path == eg.PATH_AUTO and M <= 8)
         return "gemv_w4_kernel (W4A8)" if gemv else "tc_gemm_kernel (W4A8)"
     return f"tc_gemm_kernel ({kind.upper()})"
 
@@ -367,7 +392,7 @@ def run_ours(args, rank, world):
     eg.load()
     path = {"auto": eg.PATH_AUTO, "gemv": eg.PATH_GEMV, "tc": eg.PATH_TC}[args.path]
     wl = Workload(args.workload, dev, m=args.m, lin=(args.k, args.n), path=path,
-                  variant=args.variant, fused=args.fused)
+                  variant=args.variant, fused=args.fused, api=args.api)
     peaks = load_peaks()
     copies = wl.n_copies
     step_ops = [wl.step_ops(c) for c in range(copies)]
@@ -548,7 +573,7 @@ def workload_config(args, wl, per_step_bytes, per_step_ops):
                              else "per-step weights larger than L2" if args.workload == "prefill"
                              else "small (L2 resident)",
                 "graphs": "one CUDA graph per layer copy",
-                "fused_siblings": bool(args.fused)})
+                "fused_siblings": bool(args.fused), "api": args.api})
     return cfg
 
 
@@ -662,6 +687,9 @@ def main():
     ap.add_argument("--path", choices=["auto", "gemv", "tc"], default="auto")
     ap.add_argument("--variant", choices=["w4a8", "w4a16", "w8a16"], default="w4a8",
                     help="variant for --workload linear")
+    ap.add_argument("--api", choices=["gemm", "linear"], default="gemm",
+                    help="gemm: egopq_quant_act_i8 + egopq_w4a8_gemm per linear input; "
+                         "linear: one egopq_w4a8_linear call per linear")
     ap.add_argument("--fused", action="store_true",
                     help="run q|k|v and gate|up as one GEMM each (same weights, same outputs)")
     args = ap.parse_args()

@@ -52,8 +52,8 @@ typedef enum {
   EGOPQ_ERR_TIMEOUT = -6            /* a kernel's bounded wait expired */
 } egopq_status;
 
-/* Kernel path. AUTO picks by M (CUDA-core GEMV for small M, the tcgen05
- * tensor-core GEMM otherwise); the others force one path for tests and
+/* Kernel path. AUTO picks by M (W4A8: CUDA-core GEMV for M <= 8, the tcgen05
+ * tensor-core GEMM otherwise; W4A16 and W8A16: tensor-core GEMM); the others force one path for tests and
  * benchmarks. The choice is always this explicit argument, never global or
  * environment state ("The 4-bit CPU path", section "Why the path choice is a
  * config field"). */
@@ -124,6 +124,19 @@ int egopq_w4a8_gemm(const int8_t* a_q, const uint16_t* a_q16, const float* a_s,
 int egopq_w4a8_gemm_ex(const int8_t* a_q, const uint16_t* a_q16, const float* a_s,
                        const int32_t* a_gsum, const void* packed, int64_t M, int64_t N,
                        int64_t K, int group, uint16_t* y_bf16, int path, egopq_stream_t stream);
+
+/* One-call W4A8 linear from bf16 activations: per-token int8 quantization as
+ * in egopq_quant_act_i8 into `workspace`, then the W4A8 GEMM on `path`, y bf16
+ * [M][N]. `workspace` is caller-owned device memory of at least
+ * egopq_w4a8_linear_workspace_bytes(M, K, group, path) bytes, 16-byte
+ * aligned, holding the quantized activations between the two kernels; calls
+ * sharing one workspace must be ordered on one stream. Results are
+ * bit-identical to egopq_quant_act_i8 followed by egopq_w4a8_gemm_ex on the
+ * same path (the byte count is 0 for shapes the call refuses). */
+size_t egopq_w4a8_linear_workspace_bytes(int64_t M, int64_t K, int group, int path);
+int egopq_w4a8_linear(const uint16_t* x_bf16, const void* packed, int64_t M, int64_t N, int64_t K,
+                      int group, uint16_t* y_bf16, void* workspace, size_t workspace_bytes,
+                      int path, egopq_stream_t stream);
 
 /* Test readout: the integer group partials Q[m][n][g] (int32 [M][N][G]) the
  * chosen path forms before scaling, from the same main loop:

@@ -346,11 +346,11 @@ def test_fused_sibling_linears_equal_separate(M):
 
 
 @pytest.mark.parametrize("n_tiles", [76, 78, 77])
-def test_w4a8_persistent_multicast_clusters_full(n_tiles):
-    """Grids with at least one tile per SM run persistently; n-tile counts
-    divisible by 4 / 2 / neither share activation tiles over clusters of
-    4 / 2 / 1 CTAs. Ragged token tail (M=200 over two 128-token tiles), full
-    oracle comparison."""
+def test_w4a8_persistent_grid_full(n_tiles):
+    """Grids with at least one tile per SM run persistently, striding over the
+    tiles in bands of m-tiles; n-tile counts around one and two per SM, a
+    ragged token tail (M=200 over two 128-token tiles), full oracle
+    comparison."""
     M, K, N = 200, 512, 128 * n_tiles
     x, w = w4_case(6, M, N, K)
     a, packed, y = run_w4a8(x, w, eg.PATH_TC, M, N, K)
@@ -363,7 +363,7 @@ def test_w4a8_persistent_multicast_clusters_full(n_tiles):
 
 
 @pytest.mark.parametrize("variant", ["w4a16", "w8a16"])
-def test_weight_only_persistent_multicast_full(variant):
+def test_weight_only_persistent_grid_full(variant):
     M, K, N = 256, 384, 128 * 76
     x = synth.activations(7, 0, 0, M, K, outliers=False)
     if variant == "w4a16":
@@ -377,3 +377,44 @@ def test_weight_only_persistent_multicast_full(variant):
                           path=eg.PATH_TC)
         _, y_ref = oracle.w8a16(x, w8, s8)
     check_bf16_output(to_host_bits(y), y_ref, f"{variant} persistent")
+
+
+# ------------------------------------------------------- one-call W4A8 linear
+
+@pytest.mark.parametrize("path", [eg.PATH_AUTO, eg.PATH_GEMV, eg.PATH_TC])
+@pytest.mark.parametrize("M", [1, 3, 4, 8, 16, 17, 129])
+def test_w4a8_linear_equals_quant_then_gemm(path, M):
+    """The one-call linear (quantization staged in a caller workspace, then the
+    GEMM) is bit-identical to the two-call sequence on the same path, and meets
+    the bar against the oracle."""
+    N, K = 384, 3584
+    x, w = w4_case(8, M, N, K)
+    x[min(2, M - 1)] = 0  # an all-zero token
+    packed = eg.pack_w4(*dev_weights(w))
+    xd = to_dev(x, torch.bfloat16)
+    y1 = eg.w4a8_linear(xd, packed, N, path=path)
+    two_step_path = path if path != eg.PATH_AUTO else (eg.PATH_GEMV if M <= 8 else eg.PATH_TC)
+    y2 = eg.w4a8_gemm(eg.quant_act(xd), packed, N, K, path=two_step_path)
+    assert torch.equal(y1, y2)
+    a_q, a_s, _ = oracle.quant_act(x)
+    _, y_ref = oracle.w4a8(a_q, a_s, w.w_q, w.scale_f16, w.zero)
+    check_bf16_output(to_host_bits(y1), y_ref, f"linear path={path} M={M}")
+
+
+def test_w4a8_linear_workspace_checks():
+    M, N, K = 32, 256, 512
+    x, w = w4_case(8, M, N, K)
+    packed = eg.pack_w4(*dev_weights(w))
+    need = eg.w4a8_linear_workspace_bytes(M, K, eg.PATH_TC)
+    assert need > eg.w4a8_linear_workspace_bytes(M, K, eg.PATH_GEMV) > 0
+    lib = eg.load()
+    xd = to_dev(x, torch.bfloat16)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    args = (xd.data_ptr(), packed.data_ptr(), M, N, K, 128, y.data_ptr())
+    assert lib.egopq_w4a8_linear(*args, None, 0, eg.PATH_TC, s) == -1
+    assert lib.egopq_w4a8_linear(*args, ws.data_ptr(), need - 1, eg.PATH_TC, s) == -1
+    assert lib.egopq_w4a8_linear(*args, ws.data_ptr(), need, eg.PATH_TC, s) == 0
+    assert lib.egopq_w4a8_linear(*args, None, 0, eg.PATH_GEMV, s) == -1
+    assert eg.device_status() == 0

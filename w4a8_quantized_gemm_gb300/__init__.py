@@ -71,6 +71,8 @@ def load() -> ctypes.CDLL:
             "egopq_w4a16_gemm_ex": (i32, [vp, vp, i64, i64, i64, i32, vp, i32, vp]),
             "egopq_w8a16_gemm": (i32, [vp, vp, vp, i64, i64, i64, vp, vp]),
             "egopq_w8a16_gemm_ex": (i32, [vp, vp, vp, i64, i64, i64, vp, i32, vp]),
+            "egopq_w4a8_linear_workspace_bytes": (sz, [i64, i64, i32, i32]),
+            "egopq_w4a8_linear": (i32, [vp, vp, i64, i64, i64, i32, vp, vp, sz, i32, vp]),
             "egopq_supported": (i32, [i64, i64, i64, i32, i32]),
             "egopq_device_status": (i32, [vp]),
             "egopq_selftest_timeout": (i32, [i32, vp]),
@@ -185,6 +187,28 @@ def w4a8_gemm(a: QuantAct, packed: torch.Tensor, N: int, K: int, path: int = PAT
     return out
 
 
+def w4a8_linear_workspace_bytes(M: int, K: int, path: int = PATH_AUTO) -> int:
+    return int(load().egopq_w4a8_linear_workspace_bytes(M, K, GROUP, path))
+
+
+def w4a8_linear(x: torch.Tensor, packed: torch.Tensor, N: int, path: int = PATH_AUTO,
+                out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                stream=None) -> torch.Tensor:
+    """One-call W4A8 linear from bf16 x [M, K]: per-token int8 quantization into
+    a workspace, then the W4A8 GEMM (two kernels, one call)."""
+    _dtype(x, torch.bfloat16)
+    M, K = x.shape
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    need = w4a8_linear_workspace_bytes(M, K, path)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(load().egopq_w4a8_linear(_ptr(x), _ptr(packed), M, N, K, GROUP, _ptr(out),
+                                    _ptr(workspace), ws_bytes, path, _stream(stream)))
+    return out
+
+
 def w4a8_group_partials(a: QuantAct, packed: torch.Tensor, N: int, K: int,
                         path: int = PATH_TC, stream=None) -> torch.Tensor:
     M = a.a_q.shape[0]
@@ -218,13 +242,6 @@ def w8a16_gemm(x: torch.Tensor, w_q: torch.Tensor, scale_f16: torch.Tensor,
     _check(load().egopq_w8a16_gemm_ex(_ptr(x), _ptr(w_q), _ptr(scale_f16), M, N, K, _ptr(out),
                                       path, _stream(stream)))
     return out
-
-
-def w4a8_linear(x: torch.Tensor, packed: torch.Tensor, N: int, path: int = PATH_AUTO,
-                stream=None) -> torch.Tensor:
-    """Quantize x per token, then the W4A8 GEMM: y = x W^T with W4A8 arithmetic."""
-    a = quant_act(x, stream=stream)
-    return w4a8_gemm(a, packed, N, x.shape[1], path=path, stream=stream)
 
 
 def supported(M: int, N: int, K: int, variant: int = VARIANT_W4A8, group: int = GROUP) -> bool:

@@ -89,8 +89,8 @@ int run_gemm(const GemmArgs& a, int path, cudaStream_t st) {
   if (rc) return rc;
   if (a.M == 0) return EGOPQ_OK;
   int use = path;
-  if (use == EGOPQ_PATH_AUTO) use = (a.M <= kGemvMaxRows && a.variant == kW4A8) ? EGOPQ_PATH_GEMV
-                                                                               : EGOPQ_PATH_TC;
+  if (use == EGOPQ_PATH_AUTO)
+    use = (a.M <= kGemvAutoMaxM && a.variant == kW4A8) ? EGOPQ_PATH_GEMV : EGOPQ_PATH_TC;
   if (use == EGOPQ_PATH_TC && a.variant == kW4A8 && !a.a_q16)
     return fail(EGOPQ_ERR_INVALID_ARG, "a_q16 is required by the tensor-core path");
   cudaError_t e = (use == EGOPQ_PATH_GEMV) ? launch_gemv(a, st) : launch_tc_gemm(a, st);
@@ -181,6 +181,76 @@ int egopq_w4a8_gemm(const int8_t* a_q, const uint16_t* a_q16, const float* a_s,
                     int group, uint16_t* y_bf16, egopq_stream_t stream) {
   return egopq_w4a8_gemm_ex(a_q, a_q16, a_s, a_gsum, packed, M, N, K, group, y_bf16,
                             EGOPQ_PATH_AUTO, stream);
+}
+
+// Workspace of the one-call linear: the quantized activations it stages
+// between its two kernels, in 256-byte aligned regions -- codes int8 [M][K],
+// scales fp32 [M], group sums int32 [M][G], and on the tensor-core path the
+// fp16 codes [M][K] its TMA loads read.
+static size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+static int linear_path(int64_t M, int path) {
+  if (path == EGOPQ_PATH_AUTO) return M <= kGemvAutoMaxM ? EGOPQ_PATH_GEMV : EGOPQ_PATH_TC;
+  return path;
+}
+
+size_t egopq_w4a8_linear_workspace_bytes(int64_t M, int64_t K, int group, int path) {
+  if (M <= 0 || K <= 0 || group != 128 || K % 128 || M >= kMaxDim || K >= kMaxDim) return 0;
+  if (path != EGOPQ_PATH_AUTO && path != EGOPQ_PATH_GEMV && path != EGOPQ_PATH_TC) return 0;
+  size_t bytes = align256((size_t)(M * K)) + align256((size_t)(4 * M)) +
+                 align256((size_t)(4 * M * (K / 128)));
+  if (linear_path(M, path) == EGOPQ_PATH_TC) bytes += align256((size_t)(2 * M * K));
+  return bytes;
+}
+
+namespace egopq {
+// Quantize x into `ws` (layout above) and run the W4A8 GEMM on `use`.
+int run_linear(const uint16_t* x_bf16, const void* packed, int64_t M, int64_t N, int64_t K,
+               uint16_t* y_bf16, uint8_t* ws, int use, cudaStream_t st) {
+  int8_t* a_q = reinterpret_cast<int8_t*>(ws);
+  float* a_s = reinterpret_cast<float*>(ws + align256((size_t)(M * K)));
+  int32_t* asum = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(a_s) + align256((size_t)(4 * M)));
+  uint16_t* a_q16 = nullptr;
+  if (use == EGOPQ_PATH_TC)
+    a_q16 = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(asum) +
+                                        align256((size_t)(4 * M * (K / 128))));
+  cudaError_t e = launch_quant_act(x_bf16, M, K, a_q, a_s, asum, a_q16, st);
+  if (e != cudaSuccess) return cuda_fail(e, "quant_act launch");
+  GemmArgs a{};
+  a.variant = kW4A8;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.a_q = a_q;
+  a.a_q16 = a_q16;
+  a.a_s = a_s;
+  a.a_gsum = asum;
+  a.packed = static_cast<const uint8_t*>(packed);
+  a.y = y_bf16;
+  a.timeout_ns = kDefaultTimeoutNs;
+  e = (use == EGOPQ_PATH_GEMV) ? launch_gemv(a, st) : launch_tc_gemm(a, st);
+  if (e == cudaErrorNotSupported)
+    return fail(EGOPQ_ERR_UNSUPPORTED_SHAPE, "shape not supported by the requested path");
+  return e == cudaSuccess ? EGOPQ_OK : cuda_fail(e, "gemm launch");
+}
+}  // namespace egopq
+
+int egopq_w4a8_linear(const uint16_t* x_bf16, const void* packed, int64_t M, int64_t N, int64_t K,
+                      int group, uint16_t* y_bf16, void* workspace, size_t workspace_bytes,
+                      int path, egopq_stream_t stream) {
+  int rc = check_w4_shape(M, N, K, group);
+  if (rc) return rc;
+  if (path != EGOPQ_PATH_AUTO && path != EGOPQ_PATH_GEMV && path != EGOPQ_PATH_TC)
+    return fail(EGOPQ_ERR_INVALID_ARG, "unknown path %d", path);
+  if (M == 0) return EGOPQ_OK;
+  rc = check_ptrs(4, "x_bf16", x_bf16, "packed", packed, "y_bf16", y_bf16, "workspace", workspace);
+  if (rc) return rc;
+  const size_t need = egopq_w4a8_linear_workspace_bytes(M, K, group, path);
+  if (workspace_bytes < need)
+    return fail(EGOPQ_ERR_INVALID_ARG, "workspace of %zu bytes is smaller than %zu", workspace_bytes,
+                need);
+  if ((rc = check_arch())) return rc;
+  return run_linear(x_bf16, packed, M, N, K, y_bf16, static_cast<uint8_t*>(workspace),
+                    linear_path(M, path), (cudaStream_t)stream);
 }
 
 int egopq_w4a8_group_partials(const int8_t* a_q, const uint16_t* a_q16, const int32_t* a_gsum,

@@ -48,7 +48,9 @@ cudaError_t launch_tc_gemm(const GemmArgs& a, cudaStream_t st);
 // Bounded-wait self test.
 cudaError_t launch_selftest_timeout(uint64_t timeout_ns, cudaStream_t st);
 
-// Largest M per GEMV launch slice.
-constexpr int kGemvMaxRows = 4;
+// Largest M per W4A8 GEMV launch (larger M run as several launches).
+constexpr int kGemvMaxRows = 16;
+// AUTO path: W4A8 batches up to this many tokens take the GEMV.
+constexpr int kGemvAutoMaxM = 8;
 
 }  // namespace egopq

@@ -1,4 +1,4 @@
-// gemv.cu -- CUDA-core decode kernels for small M (M <= 4 per launch slice).
+// gemv.cu -- CUDA-core decode kernels for small M (up to 16 token rows per launch).
 //
 // Decode is a weight-streaming problem: every packed weight byte is read once
 // per token batch, so the kernels below are built to keep HBM busy. Each CTA
@@ -411,7 +411,9 @@ template <int VARIANT, bool PARTIALS>
 static cudaError_t launch_w4_rows(const GemvParams& p, cudaStream_t st) {
   if (p.rows == 1) return launch_w4_slice<VARIANT, 1, PARTIALS>(p, st);
   if (p.rows == 2) return launch_w4_slice<VARIANT, 2, PARTIALS>(p, st);
-  return launch_w4_slice<VARIANT, 4, PARTIALS>(p, st);
+  if (p.rows <= 4 || VARIANT != kW4A8) return launch_w4_slice<VARIANT, 4, PARTIALS>(p, st);
+  if (p.rows <= 8) return launch_w4_slice<kW4A8, 8, PARTIALS>(p, st);
+  return launch_w4_slice<kW4A8, 16, PARTIALS>(p, st);
 }
 
 cudaError_t launch_gemv(const GemmArgs& a, cudaStream_t st) {
@@ -421,8 +423,9 @@ cudaError_t launch_gemv(const GemmArgs& a, cudaStream_t st) {
     int64_t blocks = (warps_needed * 32 + kW8Threads - 1) / kW8Threads;
     const int64_t cap = (int64_t)sm_count() * 8;
     if (blocks > cap) blocks = cap;
-    for (int64_t m0 = 0; m0 < a.M; m0 += kGemvMaxRows) {
-      const int rows = (int)((a.M - m0) < kGemvMaxRows ? (a.M - m0) : kGemvMaxRows);
+    constexpr int kW8MaxRows = 4;  // token rows per W8A16 GEMV launch
+    for (int64_t m0 = 0; m0 < a.M; m0 += kW8MaxRows) {
+      const int rows = (int)((a.M - m0) < kW8MaxRows ? (a.M - m0) : kW8MaxRows);
       const uint16_t* x = a.x + m0 * a.K;
       uint16_t* y = a.y + m0 * a.N;
       if (rows == 1)
@@ -453,14 +456,16 @@ cudaError_t launch_gemv(const GemmArgs& a, cudaStream_t st) {
     }
   }
   if ((G + ks - 1) / ks > kGemvMaxGroupsPerCta) return cudaErrorNotSupported;
-  for (int64_t m0 = 0; m0 < a.M; m0 += kGemvMaxRows) {
+  // token rows per launch: up to 16 for W4A8 (dp4a), 4 for W4A16 (fp32 FMA)
+  const int max_rows = (a.variant == kW4A8) ? kGemvMaxRows : 4;
+  for (int64_t m0 = 0; m0 < a.M; m0 += max_rows) {
     GemvParams p{};
     p.M = a.M;
     p.N = a.N;
     p.K = a.K;
     p.G = G;
     p.ks = ks;
-    p.rows = (int)((a.M - m0) < kGemvMaxRows ? (a.M - m0) : kGemvMaxRows);
+    p.rows = (int)((a.M - m0) < max_rows ? (a.M - m0) : max_rows);
     p.packed = a.packed;
     p.y = a.y + m0 * a.N;
     p.timeout_ns = a.timeout_ns;

@@ -24,12 +24,13 @@
 // (w_q - z) fp16 pairs with one AND/OR and one HSUB2/HFMA2 per pair, and
 // store them straight into TMEM with tcgen05.st.
 //
-// Warp roles (448 threads, one CTA per SM):
+// Warp roles (448 threads, 576 for token tiles of at most 32; one CTA per SM):
 //   warps 0-7   drain: TMEM accumulator -> registers, *s, accumulate, epilogue;
 //               warps 0-3 own token columns [0, BT/2), warps 4-7 [BT/2, BT)
 //   warps 8-11  convert: packed int4 (or int8) smem tile -> fp16/bf16 in TMEM
-//   warp  12    TMA producer (activations tile + weight tile per group)
-//   warp  13    TMEM allocator and single-thread MMA issuer
+//               (small tiles: a second set, warps 12-15, takes every other group)
+//   next warp   TMA producer (activations tile + weight tile per group)
+//   last warp   TMEM allocator and single-thread MMA issuer
 // (a warp reaches TMEM lanes 32*(warp % 4) .. +31, so each role that touches
 // TMEM is a whole warpgroup)
 // Pipelines: S shared-memory stages, 2 TMEM A buffers, 2 TMEM accumulators,
@@ -48,8 +49,7 @@
 
 namespace egopq {
 
-constexpr int kTcThreads = 448;
-constexpr int kProducerWarp = 12, kMmaWarp = 13, kConvWarp0 = 8;
+constexpr int kConvWarp0 = 8;  // warps 0-7 drain, then the converter warps
 constexpr int kMaxSmem = 232448;
 
 struct TcParams {
@@ -58,8 +58,6 @@ struct TcParams {
   int m_tiles, n_tiles;
   int persistent;  // 1: CTAs stride over tiles with all of K; 0: one tile per CTA, split-K cluster
   int band;        // persistent tile order: bands of `band` m-tiles, m fastest inside a band
-  int mc;          // persistent: CTAs per cluster sharing each activation tile by TMA multicast
-                   // (cluster rank r takes n-tile mc*j + r); 1 = no multicast
   const float* a_s;
   const uint8_t* packed;
   const uint16_t* s8;
@@ -75,13 +73,14 @@ struct TcCfg {
   // converters run several groups ahead of the MMAs and the MMAs several
   // groups ahead of the drain.
   // Small token tiles split a group's 8 dependent MMAs over kChains
-  // independent accumulators (k-step j feeds chain j % kChains) so that
-  // consecutive MMAs do not wait on each other; the drain adds the chains
-  // (integers below 2^24: still exact).
+  // independent accumulators (k-step j feeds chain j % kChains): a small-N
+  // MMA is short, so a chain of dependent ones is latency-bound, while
+  // independent ones overlap. The drain adds the chains (integers below 2^24:
+  // the sum stays exact).
   static constexpr int kChains = BT == 16 ? 4 : (BT == 32 ? 2 : 1);
   static constexpr int kDCols = kChains * BT;  // TMEM columns of one accumulator buffer
-  static constexpr int kNumD = 2;
-  static constexpr int kNumA = BT <= 64 ? 6 : 4;
+  static constexpr int kNumD = BT <= 64 ? 4 : 2;
+  static constexpr int kNumA = 4;
   static constexpr int kActBox = BT * 128;                        // one 64-wide K box, bytes
   static constexpr int kActBytes = 2 * kActBox;                   // a 128-wide group
   static constexpr int kWBytes = (VARIANT == kW8A16) ? 16384 : 8192;
@@ -89,7 +88,10 @@ struct TcCfg {
   static constexpr int kStageBytes = kActBytes + kWBytes;        // multiple of 1024
   static constexpr int kTxBytes = kStageBytes + kZBytes;
   static constexpr int kStagesRaw = (kMaxSmem - 2048) / (kStageBytes + 64);
-  static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
+  // deep rings for small token tiles (decode streams weights: bytes in flight
+  // hide HBM latency); larger tiles are bounded by shared memory
+  static constexpr int kStageCap = BT <= 32 ? 16 : 8;
+  static constexpr int kStages = kStagesRaw > kStageCap ? kStageCap : kStagesRaw;
   static constexpr int kZOffset = kStages * kStageBytes;
   static constexpr int kBarOffset = kZOffset + kStages * 64;
   static constexpr int kSmemBytes = kBarOffset + 512 + 1024;     // + barriers + alignment slack
@@ -99,6 +101,13 @@ struct TcCfg {
                                    : kTmemColsRaw <= 128 ? 128
                                    : kTmemColsRaw <= 256 ? 256
                                                          : 512;
+  // Converter warp sets: with small token tiles the MMA and drain per group are
+  // short, so a second set of four converter warps takes every other group
+  // (each set's store-to-arrive latency overlaps the other's conversion).
+  static constexpr int kConvSets = BT <= 32 ? 2 : 1;
+  static constexpr int kProducerWarp = kConvWarp0 + 4 * kConvSets;
+  static constexpr int kMmaWarp = kProducerWarp + 1;
+  static constexpr int kThreads = 32 * (kMmaWarp + 1);
   static constexpr bool kDrainPerGroup = (VARIANT != kW8A16);
   static constexpr int kBf16 = (VARIANT == kW4A8) ? 0 : 1;
   static_assert(kStages >= 2, "shared memory too small for two stages");
@@ -131,7 +140,7 @@ __device__ __forceinline__ void store_row(const float (&R)[HB], const TcParams& 
 }
 
 template <int VARIANT, int BT, bool PARTIALS>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(TcCfg<VARIANT, BT>::kThreads, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
                const __grid_constant__ CUtensorMap w8_map, const TcParams p) {
   using C = TcCfg<VARIANT, BT>;
@@ -152,14 +161,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
   // persistent: tiles blockIdx.x, +gridDim.x, ... each with all G groups;
   // split-K:    tile (blockIdx.y, blockIdx.z), groups of cluster rank blockIdx.x.
   int u_begin, u_step, n_units, g0, g1;
-  const int mc = p.persistent ? p.mc : 1;
-  const uint32_t mc_rank = mc > 1 ? cluster_ctarank() : 0;
-  const uint16_t mc_mask = (uint16_t)((1u << mc) - 1u);
   if (p.persistent) {
-    // units are groups of mc n-tiles sharing one m-tile, one unit per cluster
-    const int total = p.m_tiles * (p.n_tiles / mc);
-    u_begin = blockIdx.x / mc;
-    u_step = gridDim.x / mc;
+    const int total = p.m_tiles * p.n_tiles;
+    u_begin = blockIdx.x;
+    u_step = gridDim.x;
     n_units = u_begin < total ? (total - u_begin + u_step - 1) / u_step : 0;
     g0 = 0;
     g1 = G;
@@ -178,15 +183,13 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
   auto unit_tile = [&](int k, int& mt, int& nt) {
     const int u = u_begin + k * u_step;
     if (p.persistent) {
-      const int n_units_n = p.n_tiles / mc;
-      const int band_tiles = p.band * n_units_n;
+      const int band_tiles = p.band * p.n_tiles;
       const int b = u / band_tiles;
       const int idx = u - b * band_tiles;
       const int m_base = b * p.band;
       const int bm = min(p.band, p.m_tiles - m_base);
-      const int ntg = idx / bm;
-      mt = m_base + (idx - ntg * bm);
-      nt = ntg * mc + (int)mc_rank;
+      nt = idx / bm;
+      mt = m_base + (idx - nt * bm);
     } else {
       mt = u % p.m_tiles;
       nt = u / p.m_tiles;
@@ -211,7 +214,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), mc + 4);  // MMA commits of every CTA sharing the stage + converters
+      mbar_init(empty_bar(s), 1 + 4);
     }
     for (int i = 0; i < kNumA; ++i) {
       mbar_init(afull_bar(i), 4);
@@ -224,11 +227,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == kProducerWarp && lane == 0) {
+  if (warp == C::kProducerWarp && lane == 0) {
     prefetch_tensormap(&act_map);
     if constexpr (VARIANT == kW8A16) prefetch_tensormap(&w8_map);
   }
-  if (warp == kMmaWarp) {
+  if (warp == C::kMmaWarp) {
     tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
     tmem_relinquish();
   }
@@ -246,13 +249,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
   // keep their accumulators in registers through the epilogue.
   auto teardown_sync = [&]() {
     tc_fence_before();
-    asm volatile("bar.sync 1, %0;" ::"n"(kTcThreads) : "memory");
-    // multicast clusters: no CTA leaves while a peer may still deliver a tile
-    // or a stage-release arrival into its shared memory
-    if (mc > 1) cluster_sync_all();
+    asm volatile("bar.sync 1, %0;" ::"n"(C::kThreads) : "memory");
   };
 
-  if (warp == kProducerWarp) {
+  if (warp == C::kProducerWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const uint8_t* zeros = p.packed + N * K / 2 + 2 * (int64_t)G * N;
@@ -285,18 +285,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
       auto load_act = [&](int s) {
         const int mt = a_mt, g = g0 + a_gi;
         advance(a_k, a_gi, a_mt, a_nt);
-        if (mc > 1) {
-          // this CTA's slice of the token rows, delivered to every CTA of the cluster
-          const int rows = BT / mc;
-          const uint32_t off = mc_rank * rows * 128;
-          const int y = mt * BT + (int)mc_rank * rows;
-          tma_load_2d_multicast(stage_act(s) + off, &act_map, full_bar(s), g * 128, y, mc_mask);
-          tma_load_2d_multicast(stage_act(s) + C::kActBox + off, &act_map, full_bar(s),
-                                g * 128 + 64, y, mc_mask);
-        } else {
-          tma_load_2d(stage_act(s), &act_map, full_bar(s), g * 128, mt * BT);
-          tma_load_2d(stage_act(s) + C::kActBox, &act_map, full_bar(s), g * 128 + 64, mt * BT);
-        }
+        tma_load_2d(stage_act(s), &act_map, full_bar(s), g * 128, mt * BT);
+        tma_load_2d(stage_act(s) + C::kActBox, &act_map, full_bar(s), g * 128 + 64, mt * BT);
       };
       // weights do not depend on the preceding grid: start streaming them
       // before waiting for it; activations only after
@@ -329,7 +319,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
       cluster_sync_all();
       cluster_sync_all();
     }
-  } else if (warp == kMmaWarp) {
+  } else if (warp == C::kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_f16(128, BT, C::kBf16);
@@ -350,10 +340,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
           constexpr int CH = C::kChains;
           const uint32_t acc = C::kDrainPerGroup ? (j >= CH) : (gi > 0 || j >= CH);
           tc_mma_f16_ts(d_tmem + db * C::kDCols + (j % CH) * BT, a_tmem + ab * 64 + j * 8,
-                        sdesc_kmajor_sw128(b_addr), idesc, acc);
+                        sdesc_kmajor_sw128(b_addr),
+                        idesc, acc);
         }
-        if (mc > 1) tc_commit_multicast(empty_bar(s), mc_mask);
-        else tc_commit(empty_bar(s));
+        tc_commit(empty_bar(s));
         tc_commit(aempty_bar(ab));
         if (C::kDrainPerGroup || gi == ng - 1) tc_commit(dfull_bar(db));
         last = i;
@@ -373,9 +363,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
     }
   } else if (warp >= kConvWarp0) {
     // ------------------------------------------------------------ converters
-    const int r = (warp - kConvWarp0) * 32 + lane;  // weight row in the tile == TMEM lane
+    const int r = ((warp - kConvWarp0) & 3) * 32 + lane;  // weight row == TMEM lane
+    const int set = (warp - kConvWarp0) >> 2;             // this set converts items set, +sets..
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    for (int i = 0; i < n_items; ++i) {
+    for (int i = set; i < n_items; i += C::kConvSets) {
       const int s = i % S, ab = i % kNumA;
       if (!mbar_wait(full_bar(s), (i / S) & 1, abort_flag, tmo)) break;
       uint32_t out[64];
@@ -539,22 +530,26 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
             else tmem_ld8(src, v[q2]);
           }
           if constexpr (C::kChains > 1) {
-            // add the other accumulation chains of the same columns
+            // the other accumulation chains of the same columns
+            uint32_t w[C::kChains - 1][PAIR][16];
 #pragma unroll
-            for (int ch = 1; ch < C::kChains; ++ch) {
+            for (int ch = 1; ch < C::kChains; ++ch)
 #pragma unroll
               for (int q2 = 0; q2 < PAIR; ++q2) {
-                uint32_t w[16];
                 const uint32_t src =
                     d_tmem + lane_base + db * C::kDCols + ch * BT + col0 + (cb + q2) * CW;
-                if constexpr (CW == 16) tmem_ld16(src, w);
-                else tmem_ld8(src, w);
-                tmem_wait_ld();
+                if constexpr (CW == 16) tmem_ld16(src, w[ch - 1][q2]);
+                else tmem_ld8(src, w[ch - 1][q2]);
+              }
+            tmem_wait_ld();
+#pragma unroll
+            for (int ch = 1; ch < C::kChains; ++ch)
+#pragma unroll
+              for (int q2 = 0; q2 < PAIR; ++q2)
 #pragma unroll
                 for (int q = 0; q < CW; ++q)
-                  v[q2][q] = __float_as_uint(__uint_as_float(v[q2][q]) + __uint_as_float(w[q]));
-              }
-            }
+                  v[q2][q] = __float_as_uint(__uint_as_float(v[q2][q]) +
+                                             __uint_as_float(w[ch - 1][q2][q]));
           }
           tmem_wait_ld();
 #pragma unroll
@@ -722,6 +717,16 @@ static int choose_band(int64_t m_tiles, int64_t concurrent, double act_tile, dou
 template <int VARIANT, int BT, bool PARTIALS>
 static cudaError_t launch_tc(const GemmArgs& a, cudaStream_t st) {
   using C = TcCfg<VARIANT, BT>;
+  CUtensorMap act_map, w8_map;
+  memset(&w8_map, 0, sizeof(w8_map));
+  const void* act_ptr = (VARIANT == kW4A8) ? (const void*)a.a_q16 : (const void*)a.x;
+  const CUtensorMapDataType adt =
+      (VARIANT == kW4A8) ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if (!make_map(&act_map, adt, 2, act_ptr, a.M, a.K, 64, BT)) return cudaErrorInvalidValue;
+  if (VARIANT == kW8A16) {
+    if (!make_map(&w8_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.w8, a.N, a.K, 128, 128))
+      return cudaErrorInvalidValue;
+  }
   const int G = (int)(a.K / 128);
   const int64_t m_tiles = (a.M + BT - 1) / BT;
   const int64_t n_tiles = a.N / 128;
@@ -730,63 +735,6 @@ static cudaError_t launch_tc(const GemmArgs& a, cudaStream_t st) {
   const int sms = tc_sm_count();
   int ks = 1, persistent = 0;
   choose_split(tiles, G, sms, &ks, &persistent);
-  auto kern = tc_gemm_kernel<VARIANT, BT, PARTIALS>;
-  static bool attr_set = false;  // one-time opt-in to the large shared-memory carve-out
-  if (!attr_set) {
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
-  cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(kTcThreads, 1, 1);
-  cfg.dynamicSmemBytes = C::kSmemBytes;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 2;
-
-  // Persistent grids share each activation tile across a cluster of mc CTAs
-  // (TMA multicast), cutting the activation traffic into shared memory by mc.
-  int mc = 1, clusters = 0;
-  static int max_clusters_cache[5] = {-1, -1, -1, -1, -1};  // co-resident clusters of size 2, 4
-  if (persistent) {
-    for (int cand : {4, 2}) {
-      if (n_tiles % cand || BT % (8 * cand)) continue;
-      attr[0].val.clusterDim.x = (unsigned)cand;
-      cfg.gridDim = dim3((unsigned)(cand * sms), 1, 1);
-      int max_clusters = max_clusters_cache[cand];
-      if (max_clusters < 0) {
-        if (cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg) != cudaSuccess) {
-          cudaGetLastError();
-          max_clusters = 0;
-        }
-        max_clusters_cache[cand] = max_clusters;
-      }
-      if (max_clusters * cand >= (sms * 7) / 8) {
-        mc = cand;
-        clusters = max_clusters;
-        break;
-      }
-    }
-  }
-  CUtensorMap act_map, w8_map;
-  memset(&w8_map, 0, sizeof(w8_map));
-  const void* act_ptr = (VARIANT == kW4A8) ? (const void*)a.a_q16 : (const void*)a.x;
-  const CUtensorMapDataType adt =
-      (VARIANT == kW4A8) ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  if (!make_map(&act_map, adt, 2, act_ptr, a.M, a.K, 64, BT / mc)) return cudaErrorInvalidValue;
-  if (VARIANT == kW8A16) {
-    if (!make_map(&w8_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.w8, a.N, a.K, 128, 128))
-      return cudaErrorInvalidValue;
-  }
   TcParams p{};
   p.M = a.M;
   p.N = a.N;
@@ -796,26 +744,41 @@ static cudaError_t launch_tc(const GemmArgs& a, cudaStream_t st) {
   p.m_tiles = (int)m_tiles;
   p.n_tiles = (int)n_tiles;
   p.persistent = persistent;
-  p.mc = mc;
+  p.band = persistent ? choose_band(m_tiles, tiles < sms ? tiles : sms,
+                                    (double)BT * a.K * 2.0,
+                                    (double)128 * a.K / ((VARIANT == kW8A16) ? 1.0 : 2.0))
+                      : 1;
   p.a_s = a.a_s;
   p.packed = a.packed;
   p.s8 = a.s8;
   p.y = a.y;
   p.partials = a.partials;
   p.timeout_ns = a.timeout_ns;
-  if (persistent) {
-    const int64_t units = tiles / mc;
-    const int64_t conc_units = mc > 1 ? (clusters < units ? clusters : units)
-                                      : (tiles < sms ? tiles : sms);
-    p.band = choose_band(m_tiles, conc_units, (double)BT * a.K * 2.0,
-                         (double)mc * 128 * a.K / ((VARIANT == kW8A16) ? 1.0 : 2.0));
-    cfg.gridDim = dim3((unsigned)(conc_units * mc), 1, 1);
-    attr[0].val.clusterDim.x = (unsigned)mc;
-  } else {
-    p.band = 1;
-    cfg.gridDim = dim3((unsigned)ks, (unsigned)m_tiles, (unsigned)n_tiles);
-    attr[0].val.clusterDim.x = (unsigned)ks;
+  auto kern = tc_gemm_kernel<VARIANT, BT, PARTIALS>;
+  static bool attr_set = false;  // one-time opt-in to the large shared-memory carve-out
+  if (!attr_set) {
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
   }
+  cudaLaunchConfig_t cfg = {};
+  if (persistent)
+    cfg.gridDim = dim3((unsigned)(tiles < sms ? tiles : sms), 1, 1);
+  else
+    cfg.gridDim = dim3((unsigned)ks, (unsigned)m_tiles, (unsigned)n_tiles);
+  cfg.blockDim = dim3(C::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = persistent ? 1u : (unsigned)ks;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kern, act_map, w8_map, p);
 }
 
