@@ -138,6 +138,21 @@ int egopq_w4a8_linear(const uint16_t* x_bf16, const void* packed, int64_t M, int
                       int group, uint16_t* y_bf16, void* workspace, size_t workspace_bytes,
                       int path, egopq_stream_t stream);
 
+/* egopq_w4a8_linear for callers that cannot allocate device memory -- a
+ * plugin inside a framework that owns every device buffer, or a serving loop
+ * that must never enter cudaMalloc. The pages have no counterpart; this is a
+ * deployment convenience. Same arguments and results as egopq_w4a8_linear
+ * minus the workspace: the quantized activations are staged in a 16 MiB
+ * file-scope device array that every GPU loading the library holds until the
+ * process exits. Calls whose staging exceeds 16 MiB (about 3*M*K bytes on the
+ * tensor-core path, M*K on the GEMV path) return EGOPQ_ERR_UNSUPPORTED_SHAPE.
+ * All calls share the array: calls that overlap on the GPU race on it. The
+ * first call on each device looks the array's address up with that device
+ * current; make that first call before any stream capture. Allocates nothing. */
+int egopq_w4a8_linear_noalloc(const uint16_t* x_bf16, const void* packed, int64_t M, int64_t N,
+                              int64_t K, int group, uint16_t* y_bf16, int path,
+                              egopq_stream_t stream);
+
 /* Test readout: the integer group partials Q[m][n][g] (int32 [M][N][G]) the
  * chosen path forms before scaling, from the same main loop:
  *   Q[m,n,g] = sum_{k in g} a_q[m,k] w_q[n,k] - z[n,g] * sum_{k in g} a_q[m,k]. */

@@ -73,6 +73,7 @@ def load() -> ctypes.CDLL:
             "egopq_w8a16_gemm_ex": (i32, [vp, vp, vp, i64, i64, i64, vp, i32, vp]),
             "egopq_w4a8_linear_workspace_bytes": (sz, [i64, i64, i32, i32]),
             "egopq_w4a8_linear": (i32, [vp, vp, i64, i64, i64, i32, vp, vp, sz, i32, vp]),
+            "egopq_w4a8_linear_noalloc": (i32, [vp, vp, i64, i64, i64, i32, vp, i32, vp]),
             "egopq_supported": (i32, [i64, i64, i64, i32, i32]),
             "egopq_device_status": (i32, [vp]),
             "egopq_selftest_timeout": (i32, [i32, vp]),

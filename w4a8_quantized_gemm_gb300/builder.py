@@ -16,7 +16,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libegopq.so")
-SOURCES = ["egopq_api.cu", "quant_pack.cu", "gemv.cu", "tc_gemm.cu"]
+SOURCES = ["egopq_api.cu", "quant_pack.cu", "gemv.cu", "tc_gemm.cu", "no_alloc.cu"]
 HEADERS = ["egopq_common.cuh", "egopq_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-rdc=true", "-Xcompiler", "-fPIC",

@@ -202,7 +202,13 @@ size_t egopq_w4a8_linear_workspace_bytes(int64_t M, int64_t K, int group, int pa
   return bytes;
 }
 
+}  // extern "C"
+
 namespace egopq {
+// Record `msg` as the calling thread's last error (read back through
+// egopq_last_error_string) and return `code`.
+int set_last_error(int code, const char* msg) { return fail(code, "%s", msg); }
+
 // Quantize x into `ws` (layout above) and run the W4A8 GEMM on `use`.
 int run_linear(const uint16_t* x_bf16, const void* packed, int64_t M, int64_t N, int64_t K,
                uint16_t* y_bf16, uint8_t* ws, int use, cudaStream_t st) {
@@ -233,6 +239,8 @@ int run_linear(const uint16_t* x_bf16, const void* packed, int64_t M, int64_t N,
   return e == cudaSuccess ? EGOPQ_OK : cuda_fail(e, "gemm launch");
 }
 }  // namespace egopq
+
+extern "C" {
 
 int egopq_w4a8_linear(const uint16_t* x_bf16, const void* packed, int64_t M, int64_t N, int64_t K,
                       int group, uint16_t* y_bf16, void* workspace, size_t workspace_bytes,
