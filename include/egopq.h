@@ -72,15 +72,19 @@ int egopq_version(void);
 
 /* ---- weight packing --------------------------------------------------------
  * Size in bytes of the packed form of an N x K int4 weight with group 128, or
- * 0 if the shape is refused. The packed buffer holds three regions:
- *   codes   N*K/2 bytes in 8 KiB tiles, one per (128-row block t, group g),
- *           at ((t*G + g) * 8192); inside a tile the 16-byte unit of chunk c
- *           (32 codes, k = 128g + 32c ..) of row r is at (c*128 + r) * 16;
- *           little-endian word j of a unit holds k0 = 128g+32c+8j .. k0+7 with
- *           nibble p carrying k0 + 2p (p < 4) or k0 + 2(p-4) + 1 (p >= 4);
- *   scales  fp16 [G][N] at offset N*K/2;
- *   zeros   [G][N/2] bytes after the scales, z[n,g] in the low nibble for
- *           even n, the high nibble for odd n. */
+ * 0 if the shape is refused (N*K/2 + 5*N*G/2 bytes otherwise). The packed
+ * buffer is a sequence of 8512-byte records, one per (128-row block t,
+ * group g), record (t, g) at byte (t*G + g) * 8512, so that a kernel fetches
+ * everything one group of a row block needs with a single copy:
+ *   [0, 8192)     codes: the 16-byte unit of chunk c (32 codes, k = 128g+32c..)
+ *                 of row r = n - 128t at (c*128 + r) * 16; little-endian word
+ *                 j of a unit holds k0 = 128g+32c+8j .. k0+7, nibble p carrying
+ *                 k0 + 2p (p < 4) or k0 + 2(p-4) + 1 (p >= 4);
+ *   [8192, 8448)  fp16 scale s[n,g] of row r at 8192 + 2r;
+ *   [8448, 8512)  zero points: z[n,g] of row r in byte 8448 + r/2, low nibble
+ *                 for even r, high nibble for odd r.
+ * The layout is this library's own (the pages fix only the logical codes,
+ * scales and zero points below). */
 size_t egopq_packed_w4_bytes(int64_t N, int64_t K, int group);
 
 /* Pack logical GPTQ-style int4 weights into `packed` (device,

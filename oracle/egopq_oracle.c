@@ -211,26 +211,27 @@ void oracle_w8a16(const uint16_t* x_bf16, const int8_t* w_q, const uint16_t* s_f
 /* ---- packed int4 weight layout ------------------------------------------- */
 /*
  * The packed buffer for an N x K weight with group 128 (K % 128 == 0,
- * N % 128 == 0; G = K/128, T = N/128) is three regions, back to back:
+ * N % 128 == 0; G = K/128, T = N/128) is one 8512-byte record per (row block
+ * t, group g) -- rows n = 128t..128t+127, columns k = 128g..128g+127 -- at
+ * ((t*G + g) * 8512), records of one row block consecutive in g:
  *
- *  codes   N*K/2 bytes. Tile (t, g) -- rows n = 128t..128t+127, columns
- *          k = 128g..128g+127 -- is 8192 bytes at ((t*G + g) * 8192). Inside a
- *          tile, the 16-byte unit for chunk c (0..3) of row r (0..127) sits at
- *          (c*128 + r) * 16; chunk c holds k = 128g + 32c .. +31. Inside the
- *          unit, little-endian 32-bit word j (0..3) holds the eight codes
- *          k0 = 128g + 32c + 8j .. k0+7; nibble p (bits 4p..4p+3) carries
- *          k0 + 2p for p < 4 and k0 + 2(p-4) + 1 for p >= 4.
- *  scales  2*G*N bytes at N*K/2: s[n,g] as fp16 at 2*(g*N + n).
- *  zeros   G*N/2 bytes after the scales: z[n,g] in byte g*(N/2) + n/2, low
- *          nibble for even n, high nibble for odd n.
+ *  codes   bytes [0, 8192): the 16-byte unit for chunk c (0..3) of row r
+ *          (0..127) sits at (c*128 + r) * 16; chunk c holds k = 128g + 32c ..
+ *          +31. Inside the unit, little-endian 32-bit word j (0..3) holds the
+ *          eight codes k0 = 128g + 32c + 8j .. k0+7; nibble p (bits 4p..4p+3)
+ *          carries k0 + 2p for p < 4 and k0 + 2(p-4) + 1 for p >= 4.
+ *  scales  bytes [8192, 8448): s[n,g] as fp16 at 8192 + 2r.
+ *  zeros   bytes [8448, 8512): z[n,g] in byte 8448 + r/2, low nibble for even
+ *          r, high nibble for odd r.
+ *
+ * Total T*G*8512 = N*K/2 + 2.5*N*G bytes.
  */
 int64_t oracle_packed_w4_bytes(int64_t N, int64_t K, int64_t group) {
   if (group != 128 || K <= 0 || N <= 0 || K % 128 || N % 128) return 0;
-  int64_t G = K / 128;
-  return N * K / 2 + 2 * G * N + G * N / 2;
+  return (N / 128) * (K / 128) * 8512;
 }
 
-/* Byte offset and nibble shift of code (n, k) in the codes region. */
+/* Byte offset and nibble shift of code (n, k). */
 void oracle_code_location(int64_t N, int64_t K, int64_t n, int64_t k,
                           int64_t* byte_offset, int* shift) {
   (void)N;
@@ -238,7 +239,7 @@ void oracle_code_location(int64_t N, int64_t K, int64_t n, int64_t k,
   int64_t t = n / 128, r = n % 128, g = k / 128, kk = k % 128;
   int64_t c = kk / 32, j = (kk % 32) / 8, e = kk % 8;
   int p = (e % 2 == 0) ? (int)(e / 2) : (int)(4 + e / 2);
-  *byte_offset = (t * G + g) * 8192 + (c * 128 + r) * 16 + j * 4 + p / 2;
+  *byte_offset = (t * G + g) * 8512 + (c * 128 + r) * 16 + j * 4 + p / 2;
   *shift = (p % 2) * 4;
 }
 
@@ -255,16 +256,14 @@ int oracle_pack_w4(const uint8_t* w_q, const uint16_t* s_f16, const uint8_t* z,
       oracle_code_location(N, K, n, k, &off, &sh);
       packed[off] |= (uint8_t)((w_q[n * K + k] & 0xF) << sh);
     }
-  uint8_t* sreg = packed + N * K / 2;
-  for (int64_t g = 0; g < G; ++g)
-    for (int64_t n = 0; n < N; ++n) {
+  for (int64_t n = 0; n < N; ++n)
+    for (int64_t g = 0; g < G; ++g) {
+      uint8_t* rec = packed + ((n / 128) * G + g) * 8512;
+      int64_t r = n % 128;
       uint16_t v = s_f16[n * G + g];
-      sreg[2 * (g * N + n)] = (uint8_t)(v & 0xFF);
-      sreg[2 * (g * N + n) + 1] = (uint8_t)(v >> 8);
+      rec[8192 + 2 * r] = (uint8_t)(v & 0xFF);
+      rec[8192 + 2 * r + 1] = (uint8_t)(v >> 8);
+      rec[8448 + r / 2] |= (uint8_t)((z[n * G + g] & 0xF) << ((r % 2) * 4));
     }
-  uint8_t* zreg = sreg + 2 * G * N;
-  for (int64_t g = 0; g < G; ++g)
-    for (int64_t n = 0; n < N; ++n)
-      zreg[g * (N / 2) + n / 2] |= (uint8_t)((z[n * G + g] & 0xF) << ((n % 2) * 4));
   return 0;
 }

@@ -341,23 +341,23 @@ def unpack_reference(packed, N, K):
     """Decode the packed layout by reshaping (an independent route from the
     oracle's per-code location function)."""
     G, T = K // 128, N // 128
-    codes = packed[: N * K // 2].reshape(T, G, 4, 128, 4, 4)   # t, g, c, r, j, byte
+    rec = packed.reshape(T, G, 8512)
+    codes = rec[:, :, :8192].reshape(T, G, 4, 128, 4, 4)   # t, g, c, r, j, byte
     b = codes.astype(np.uint32)
     word = b[..., 0] | (b[..., 1] << 8) | (b[..., 2] << 16) | (b[..., 3] << 24)  # t,g,c,r,j
     nib = np.stack([(word >> (4 * p)) & 0xF for p in range(8)], axis=-1)  # ...,p
-    order = [0, 2, 4, 6, 1, 3, 5, 7]  # nibble p -> k offset e(p)
-    e = np.empty(8, np.int64)
-    e[np.arange(8)] = order
+    e = np.array([0, 2, 4, 6, 1, 3, 5, 7])  # nibble p -> k offset e(p)
     vals = np.empty_like(nib)
     vals[..., e] = nib  # vals[..., e(p)] = nib[..., p]
     # axes: t, g, c, r, j, e -> n = 128t + r, k = 128g + 32c + 8j + e
     w = vals.transpose(0, 3, 1, 2, 4, 5).reshape(N, K).astype(np.uint8)
-    sreg = packed[N * K // 2: N * K // 2 + 2 * G * N].view(np.uint16).reshape(G, N).T
-    zb = packed[N * K // 2 + 2 * G * N:].reshape(G, N // 2)
-    z = np.empty((N, G), np.uint8)
-    z[0::2] = (zb & 0xF).T
-    z[1::2] = (zb >> 4).T
-    return w, np.ascontiguousarray(sreg), z
+    s = np.ascontiguousarray(rec[:, :, 8192:8448]).view(np.uint16)  # t, g, r
+    s = s.transpose(0, 2, 1).reshape(N, G)
+    zb = rec[:, :, 8448:8512]                                        # t, g, r/2
+    z = np.empty((T, 128, G), np.uint8)
+    z[:, 0::2, :] = (zb & 0xF).transpose(0, 2, 1)
+    z[:, 1::2, :] = (zb >> 4).transpose(0, 2, 1)
+    return w, np.ascontiguousarray(s), z.reshape(N, G)
 
 
 def test_pack_roundtrip_and_index_pattern():
@@ -385,8 +385,8 @@ def test_pack_layout_spot_locations():
         (0, 8, 4, 0),                      # next word
         (0, 32, 128 * 16, 0),              # chunk 1 starts after 128 rows x 16 B
         (1, 0, 16, 0),                     # row 1
-        (0, 128, 8192, 0),                 # group 1 of tile 0
-        (128, 0, 2 * 8192, 0),             # tile 1 (G = 2 groups per tile row)
+        (0, 128, 8512, 0),                 # group 1 of row block 0 (8512-byte records)
+        (128, 0, 2 * 8512, 0),             # row block 1 (G = 2 groups per row block)
     ]:
         w = np.zeros((N, K), np.uint8)
         w[nn, kk] = 0xF
@@ -402,3 +402,4 @@ def test_pack_rejects_unsupported_shapes():
     assert oracle.packed_w4_bytes(128, 200) == 0       # K not a multiple of the group
     assert oracle.packed_w4_bytes(128, 256, 64) == 0   # only group 128 is packed
     assert oracle.packed_w4_bytes(128, 256) == 128 * 128 + 2 * 2 * 128 + 128
+    assert oracle.packed_w4_bytes(128, 256) == 2 * 8512

@@ -31,7 +31,7 @@ namespace egopq {
 constexpr int kGemvConsumers = 128;                 // one thread per weight row of a tile
 constexpr int kGemvThreads = kGemvConsumers + 32;   // + one producer warp
 constexpr int kGemvStages = 8;
-constexpr int kGemvStageBytes = 8192 + 256 + 64;    // codes, scales, zero nibbles
+constexpr int kGemvStageBytes = 8512;               // one packed record: codes, scales, zeros
 constexpr int kGemvMaxGroupsPerCta = 64;
 
 struct GemvParams {
@@ -49,9 +49,11 @@ struct GemvParams {
 
 // Decode kernel for the packed int4 weight (W4A8 and W4A16). CTA = one
 // 128-row tile x a contiguous range of groups; a producer lane streams each
-// group's 8 KiB code tile, its 128 scales and 64 bytes of zero nibbles into an
-// 8-stage shared-memory ring with 1-D bulk copies (weights first, before the
-// preceding kernel has finished); each consumer thread owns one weight row.
+// group's 8512-byte packed record (codes, 128 scales, 64 bytes of zero
+// nibbles) into an 8-stage shared-memory ring with one 1-D bulk copy per
+// group -- few, large copies keep the copy engine's per-copy cost out of the
+// way -- starting before the preceding kernel has finished; each consumer
+// thread owns one weight row.
 template <int VARIANT, int MT, bool PARTIALS>
 __global__ void __launch_bounds__(kGemvThreads)
 gemv_w4_kernel(const GemvParams p) {
@@ -62,8 +64,6 @@ gemv_w4_kernel(const GemvParams p) {
   const int g0 = (int)((int64_t)ks * G / p.ks), g1 = (int)((int64_t)(ks + 1) * G / p.ks);
   const int ng = g1 - g0;
   const int64_t N = p.N, K = p.K;
-  const uint16_t* scales = reinterpret_cast<const uint16_t*>(p.packed + N * K / 2);
-  const uint8_t* zeros = p.packed + N * K / 2 + 2 * (int64_t)G * N;
 
   // smem: ring | barriers | abort flag | reduction buffer | staged activations
   uint8_t* ring = smem;
@@ -88,14 +88,12 @@ gemv_w4_kernel(const GemvParams p) {
   if (warp == 4) {
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
+      // one copy per group: the packed record holds codes, scales and zeros
       auto issue = [&](int i) {
         const int s = i % kGemvStages, g = g0 + i;
-        const uint32_t dst = smem_u32(ring + s * kGemvStageBytes);
         mbar_arrive_expect_tx(full_bar(s), kGemvStageBytes);
-        bulk_load(dst, p.packed + ((int64_t)t * G + g) * 8192, 8192, full_bar(s));
-        bulk_load(dst + 8192, scales + (int64_t)g * N + (int64_t)t * 128, 256, full_bar(s));
-        bulk_load(dst + 8192 + 256, zeros + (int64_t)g * (N / 2) + (int64_t)t * 64, 64,
-                  full_bar(s));
+        bulk_load(smem_u32(ring + s * kGemvStageBytes),
+                  p.packed + ((int64_t)t * G + g) * kGemvStageBytes, kGemvStageBytes, full_bar(s));
       };
       int issued = 0;
       for (int i = 0; i < ng; ++i) {

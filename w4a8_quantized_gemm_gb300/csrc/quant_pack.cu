@@ -10,10 +10,11 @@
 // optionally the codes as exact fp16 integers for the tensor-core path.
 //
 // Weight packing lays GPTQ-style int4 codes (per-group _gptq_scale /
-// _gptq_zero, "EgoPQ Real-Serving Handoff", section 2) out in 8 KiB tiles of
-// 128 rows x 128 K so that one 1-D bulk copy stages a whole (row block, group)
-// tile, and so that one AND/OR per 32-bit word yields two consecutive K
-// values as an fp16 pair. The layout is documented in include/egopq.h.
+// _gptq_zero, "EgoPQ Real-Serving Handoff", section 2) out in 8512-byte
+// records of 128 rows x 128 K -- codes, scales and zero points together -- so
+// that one 1-D bulk copy stages everything a (row block, group) needs, and so
+// that one AND/OR per 32-bit word yields two consecutive K values as an fp16
+// pair. The layout is documented in include/egopq.h.
 #include "egopq_internal.h"
 
 namespace egopq {
@@ -171,14 +172,19 @@ quant_act_reg_kernel(const uint16_t* __restrict__ x, int64_t K, int8_t* __restri
 // nibble p of a packed word carries K offset kNibbleK[p] inside its 8-wide run
 __device__ __constant__ int kNibbleK[8] = {0, 2, 4, 6, 1, 3, 5, 7};
 
+// Packed records: one 8512-byte record per (row block t, group g) at
+// (t*G + g) * 8512 -- codes [0, 8192), fp16 scales [8192, 8448), zero nibbles
+// [8448, 8512) -- so one bulk copy stages everything a group of 128 rows needs.
+constexpr int64_t kRecBytes = 8512;
+
 __global__ void pack_codes_kernel(const uint8_t* __restrict__ w_q, int64_t N, int64_t K,
-                                  uint32_t* __restrict__ out) {
+                                  uint8_t* __restrict__ out) {
   const int64_t G = K / 128;
   const int64_t nwords = N * K / 8;
   for (int64_t w = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; w < nwords;
        w += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t tile = w / 2048, u = w % 2048;
-    const int64_t t = tile / G, g = tile % G;
+    const int64_t rec = w / 2048, u = w % 2048;
+    const int64_t t = rec / G, g = rec % G;
     const int64_t unit = u / 4, j = u % 4;
     const int64_t c = unit / 128, r = unit % 128;
     const int64_t n = t * 128 + r, k0 = g * 128 + c * 32 + j * 8;
@@ -187,22 +193,22 @@ __global__ void pack_codes_kernel(const uint8_t* __restrict__ w_q, int64_t N, in
     uint32_t word = 0;
 #pragma unroll
     for (int p = 0; p < 8; ++p) word |= (uint32_t)(b[kNibbleK[p]] & 0xF) << (4 * p);
-    out[w] = word;
+    *reinterpret_cast<uint32_t*>(out + rec * kRecBytes + u * 4) = word;
   }
 }
 
-__global__ void unpack_codes_kernel(const uint32_t* __restrict__ in, int64_t N, int64_t K,
+__global__ void unpack_codes_kernel(const uint8_t* __restrict__ in, int64_t N, int64_t K,
                                     uint8_t* __restrict__ w_q) {
   const int64_t G = K / 128;
   const int64_t nwords = N * K / 8;
   for (int64_t w = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; w < nwords;
        w += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t tile = w / 2048, u = w % 2048;
-    const int64_t t = tile / G, g = tile % G;
+    const int64_t rec = w / 2048, u = w % 2048;
+    const int64_t t = rec / G, g = rec % G;
     const int64_t unit = u / 4, j = u % 4;
     const int64_t c = unit / 128, r = unit % 128;
     const int64_t n = t * 128 + r, k0 = g * 128 + c * 32 + j * 8;
-    const uint32_t word = in[w];
+    const uint32_t word = *reinterpret_cast<const uint32_t*>(in + rec * kRecBytes + u * 4);
     uint2 dst;
     uint8_t* b = reinterpret_cast<uint8_t*>(&dst);
 #pragma unroll
@@ -211,29 +217,30 @@ __global__ void unpack_codes_kernel(const uint32_t* __restrict__ in, int64_t N, 
   }
 }
 
-// scales: [N][G] -> [G][N] (and back); zeros: [N][G] bytes -> [G][N/2] nibble pairs
+// scales [N][G] and zeros [N][G] into (and out of) the records
 __global__ void pack_meta_kernel(const uint16_t* __restrict__ s, const uint8_t* __restrict__ z,
-                                 int64_t N, int64_t G, uint16_t* __restrict__ s_out,
-                                 uint8_t* __restrict__ z_out) {
+                                 int64_t N, int64_t G, uint8_t* __restrict__ out) {
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < G * N;
        i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t g = i / N, n = i % N;
-    s_out[i] = s[n * G + g];
-    if ((n & 1) == 0)
-      z_out[g * (N / 2) + n / 2] =
-          (uint8_t)((z[n * G + g] & 0xF) | ((z[(n + 1) * G + g] & 0xF) << 4));
+    uint8_t* rec = out + ((n / 128) * G + g) * kRecBytes;
+    const int64_t r = n % 128;
+    *reinterpret_cast<uint16_t*>(rec + 8192 + 2 * r) = s[n * G + g];
+    if ((r & 1) == 0)
+      rec[8448 + r / 2] = (uint8_t)((z[n * G + g] & 0xF) | ((z[(n + 1) * G + g] & 0xF) << 4));
   }
 }
 
-__global__ void unpack_meta_kernel(const uint16_t* __restrict__ s_in,
-                                   const uint8_t* __restrict__ z_in, int64_t N, int64_t G,
+__global__ void unpack_meta_kernel(const uint8_t* __restrict__ in, int64_t N, int64_t G,
                                    uint16_t* __restrict__ s, uint8_t* __restrict__ z) {
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < G * N;
        i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t g = i / N, n = i % N;
-    s[n * G + g] = s_in[i];
-    const uint8_t b = z_in[g * (N / 2) + n / 2];
-    z[n * G + g] = (n & 1) ? (b >> 4) : (b & 0xF);
+    const uint8_t* rec = in + ((n / 128) * G + g) * kRecBytes;
+    const int64_t r = n % 128;
+    s[n * G + g] = *reinterpret_cast<const uint16_t*>(rec + 8192 + 2 * r);
+    const uint8_t b = rec[8448 + r / 2];
+    z[n * G + g] = (r & 1) ? (b >> 4) : (b & 0xF);
   }
 }
 
@@ -264,13 +271,10 @@ cudaError_t launch_pack_w4(const uint8_t* w_q, const uint16_t* s, const uint8_t*
                            int64_t K, void* packed, cudaStream_t st) {
   const int64_t G = K / 128;
   uint8_t* base = static_cast<uint8_t*>(packed);
-  pack_codes_kernel<<<grid_for(N * K / 8, 256), 256, 0, st>>>(w_q, N, K,
-                                                               reinterpret_cast<uint32_t*>(base));
+  pack_codes_kernel<<<grid_for(N * K / 8, 256), 256, 0, st>>>(w_q, N, K, base);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  uint16_t* s_out = reinterpret_cast<uint16_t*>(base + N * K / 2);
-  uint8_t* z_out = base + N * K / 2 + 2 * G * N;
-  pack_meta_kernel<<<grid_for(G * N, 256), 256, 0, st>>>(s, z, N, G, s_out, z_out);
+  pack_meta_kernel<<<grid_for(G * N, 256), 256, 0, st>>>(s, z, N, G, base);
   return cudaGetLastError();
 }
 
@@ -278,13 +282,10 @@ cudaError_t launch_unpack_w4(const void* packed, int64_t N, int64_t K, uint8_t* 
                              uint8_t* z, cudaStream_t st) {
   const int64_t G = K / 128;
   const uint8_t* base = static_cast<const uint8_t*>(packed);
-  unpack_codes_kernel<<<grid_for(N * K / 8, 256), 256, 0, st>>>(
-      reinterpret_cast<const uint32_t*>(base), N, K, w_q);
+  unpack_codes_kernel<<<grid_for(N * K / 8, 256), 256, 0, st>>>(base, N, K, w_q);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const uint16_t* s_in = reinterpret_cast<const uint16_t*>(base + N * K / 2);
-  const uint8_t* z_in = base + N * K / 2 + 2 * G * N;
-  unpack_meta_kernel<<<grid_for(G * N, 256), 256, 0, st>>>(s_in, z_in, N, G, s, z);
+  unpack_meta_kernel<<<grid_for(G * N, 256), 256, 0, st>>>(base, N, G, s, z);
   return cudaGetLastError();
 }
 

@@ -58,6 +58,7 @@ struct TcParams {
   int m_tiles, n_tiles;
   int persistent;  // 1: CTAs stride over tiles with all of K; 0: one tile per CTA, split-K cluster
   int band;        // persistent tile order: bands of `band` m-tiles, m fastest inside a band
+  int act3d;       // 1: activation map is 3-D, one copy per 128-wide group; 0: 2-D, two copies
   const float* a_s;
   const uint8_t* packed;
   const uint16_t* s8;
@@ -83,17 +84,19 @@ struct TcCfg {
   static constexpr int kNumA = 4;
   static constexpr int kActBox = BT * 128;                        // one 64-wide K box, bytes
   static constexpr int kActBytes = 2 * kActBox;                   // a 128-wide group
-  static constexpr int kWBytes = (VARIANT == kW8A16) ? 16384 : 8192;
-  static constexpr int kZBytes = (VARIANT == kW8A16) ? 0 : 64;   // zero nibbles of 128 rows
+  // weights of one group: the int8 tile, or one packed int4 record (8192 B of
+  // codes, 256 B of scales, 64 B of zero nibbles), padded to keep stages
+  // 1024-byte aligned
+  static constexpr int kWCopyBytes = (VARIANT == kW8A16) ? 16384 : 8512;
+  static constexpr int kWBytes = (VARIANT == kW8A16) ? 16384 : 9216;
   static constexpr int kStageBytes = kActBytes + kWBytes;        // multiple of 1024
-  static constexpr int kTxBytes = kStageBytes + kZBytes;
-  static constexpr int kStagesRaw = (kMaxSmem - 2048) / (kStageBytes + 64);
+  static constexpr int kTxBytes = kActBytes + kWCopyBytes;
+  static constexpr int kStagesRaw = (kMaxSmem - 2048) / kStageBytes;
   // deep rings for small token tiles (decode streams weights: bytes in flight
   // hide HBM latency); larger tiles are bounded by shared memory
   static constexpr int kStageCap = BT <= 32 ? 16 : 8;
   static constexpr int kStages = kStagesRaw > kStageCap ? kStageCap : kStagesRaw;
-  static constexpr int kZOffset = kStages * kStageBytes;
-  static constexpr int kBarOffset = kZOffset + kStages * 64;
+  static constexpr int kBarOffset = kStages * kStageBytes;
   static constexpr int kSmemBytes = kBarOffset + 512 + 1024;     // + barriers + alignment slack
   static constexpr int kTmemColsRaw = kNumD * kDCols + kNumA * 64;
   static constexpr int kTmemCols = kTmemColsRaw <= 32    ? 32
@@ -209,7 +212,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
   auto stage_act = [&](int s) { return base + (uint32_t)(s * C::kStageBytes); };
   auto stage_w_ptr = [&](int s) { return smem + s * C::kStageBytes + C::kActBytes; };
-  auto stage_z_ptr = [&](int s) { return smem + C::kZOffset + s * 64; };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -255,7 +257,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
   if (warp == C::kProducerWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      const uint8_t* zeros = p.packed + N * K / 2 + 2 * (int64_t)G * N;
       // item i = (unit i / ng, group g0 + i % ng), walked with counters
       int w_k = 0, w_gi = 0, w_mt = 0, w_nt = 0;   // weights cursor
       int a_k = 0, a_gi = 0, a_mt = 0, a_nt = 0;   // activations cursor
@@ -276,17 +277,19 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
         if constexpr (VARIANT == kW8A16) {
           tma_load_2d(stage_act(s) + C::kActBytes, &w8_map, full_bar(s), g * 128, nt * 128);
         } else {
-          bulk_load(stage_act(s) + C::kActBytes, p.packed + ((int64_t)nt * G + g) * 8192, 8192,
-                    full_bar(s));
-          bulk_load(smem_u32(stage_z_ptr(s)), zeros + (int64_t)g * (N / 2) + (int64_t)nt * 64, 64,
+          bulk_load(stage_act(s) + C::kActBytes, p.packed + ((int64_t)nt * G + g) * 8512, 8512,
                     full_bar(s));
         }
       };
       auto load_act = [&](int s) {
         const int mt = a_mt, g = g0 + a_gi;
         advance(a_k, a_gi, a_mt, a_nt);
-        tma_load_2d(stage_act(s), &act_map, full_bar(s), g * 128, mt * BT);
-        tma_load_2d(stage_act(s) + C::kActBox, &act_map, full_bar(s), g * 128 + 64, mt * BT);
+        if (p.act3d) {
+          tma_load_3d(stage_act(s), &act_map, full_bar(s), 0, mt * BT, g * 2);
+        } else {
+          tma_load_2d(stage_act(s), &act_map, full_bar(s), g * 128, mt * BT);
+          tma_load_2d(stage_act(s) + C::kActBox, &act_map, full_bar(s), g * 128 + 64, mt * BT);
+        }
       };
       // weights do not depend on the preceding grid: start streaming them
       // before waiting for it; activations only after
@@ -401,7 +404,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
         uint4 v[4];
 #pragma unroll
         for (int c = 0; c < 4; ++c) v[c] = *reinterpret_cast<const uint4*>(wt + c * 2048);
-        const uint8_t zb = stage_z_ptr(s)[r >> 1];
+        const uint8_t zb = stage_w_ptr(s)[8448 + (r >> 1)];
         __syncwarp();
         if (lane == 0) mbar_arrive(empty_bar(s));
         const uint32_t z = (r & 1) ? (zb >> 4) : (zb & 0xF);
@@ -474,17 +477,21 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
     const int r = (warp & 3) * 32 + lane;
     const int col0 = (warp >> 2) * HB;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const uint16_t* scales = reinterpret_cast<const uint16_t*>(p.packed + N * K / 2);
+    // scale of row r, group g: half-word 4096 + r of record (tile, g), records
+    // 4256 half-words apart
+    auto scale_ptr = [&](int tile, int g) {
+      return reinterpret_cast<const uint16_t*>(p.packed + ((int64_t)tile * G + g) * 8512 + 8192) + r;
+    };
     griddep_wait();  // a_s and y belong to the stream's order
     float R[HB];     // fp32 running sums for this thread's weight row
-    // per-group scales s[g][n] of this thread's row, walked with a pointer and
+    // per-group scales of this thread's row, walked with a pointer and
     // prefetched one group ahead (the next tile's first one at a tile's end)
     const uint16_t* sp = nullptr;
     float s_next = 1.f;  // weight-only int8: no per-group scale (per-channel scale at the end)
     int mt = 0, nt = 0;
     if (n_items > 0) {
       unit_tile(0, mt, nt);
-      sp = scales + (int64_t)g0 * N + (int64_t)nt * 128 + r;
+      sp = scale_ptr(nt, g0);
       if constexpr (C::kDrainPerGroup) s_next = f16_bits_to_f32(__ldg(sp));
     }
     bool ok = true;
@@ -492,13 +499,13 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
       if (k > 0) unit_tile(k, mt, nt);
       const int64_t n = (int64_t)nt * 128 + r;
       const int64_t m0 = (int64_t)mt * BT;
-      const uint16_t* sp_tile = scales + (int64_t)g0 * N + n;
+      const uint16_t* sp_tile = scale_ptr(nt, g0);
       // the next tile's first scale, fetched now and used after this tile
       float s_first_next = 0.f;
       if (C::kDrainPerGroup && k + 1 < n_units) {
         int mt2, nt2;
         unit_tile(k + 1, mt2, nt2);
-        s_first_next = f16_bits_to_f32(__ldg(scales + (int64_t)g0 * N + (int64_t)nt2 * 128 + r));
+        s_first_next = f16_bits_to_f32(__ldg(scale_ptr(nt2, g0)));
       }
 #pragma unroll
       for (int t = 0; t < HB; ++t) R[t] = 0.f;
@@ -509,7 +516,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
         const int db = di % kNumD;
         const float s = s_next;
         if constexpr (C::kDrainPerGroup)
-          s_next = (gi + 1 < ng) ? f16_bits_to_f32(__ldg(sp_tile + (int64_t)(gi + 1) * N))
+          s_next = (gi + 1 < ng) ? f16_bits_to_f32(__ldg(sp_tile + (int64_t)(gi + 1) * 4256))
                                  : s_first_next;
         if (!mbar_wait(dfull_bar(db), (di / kNumD) & 1, abort_flag, tmo)) {
           ok = false;
@@ -666,6 +673,23 @@ static bool make_map(CUtensorMap* map, CUtensorMapDataType dt, int elem_bytes, c
   return r == CUDA_SUCCESS;
 }
 
+// Activations [rows][cols] seen as 3-D {64, rows, cols/64}: a box {64, box_rows,
+// 2} lands as two [box_rows][64] swizzled tiles back to back, i.e. one copy per
+// 128-wide group instead of two.
+static bool make_act_map_3d(CUtensorMap* map, CUtensorMapDataType dt, const void* ptr, int64_t rows,
+                            int64_t cols, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || cols % 64) return false;
+  cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(cols / 64)};
+  cuuint64_t strides[2] = {(cuuint64_t)(cols * 2), 128};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, dt, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 static int tc_sm_count() {
   static int count = 0;
   if (!count) {
@@ -722,7 +746,9 @@ static cudaError_t launch_tc(const GemmArgs& a, cudaStream_t st) {
   const void* act_ptr = (VARIANT == kW4A8) ? (const void*)a.a_q16 : (const void*)a.x;
   const CUtensorMapDataType adt =
       (VARIANT == kW4A8) ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  if (!make_map(&act_map, adt, 2, act_ptr, a.M, a.K, 64, BT)) return cudaErrorInvalidValue;
+  int act3d = make_act_map_3d(&act_map, adt, act_ptr, a.M, a.K, BT) ? 1 : 0;
+  if (!act3d && !make_map(&act_map, adt, 2, act_ptr, a.M, a.K, 64, BT))
+    return cudaErrorInvalidValue;
   if (VARIANT == kW8A16) {
     if (!make_map(&w8_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.w8, a.N, a.K, 128, 128))
       return cudaErrorInvalidValue;
@@ -744,6 +770,7 @@ static cudaError_t launch_tc(const GemmArgs& a, cudaStream_t st) {
   p.m_tiles = (int)m_tiles;
   p.n_tiles = (int)n_tiles;
   p.persistent = persistent;
+  p.act3d = act3d;
   p.band = persistent ? choose_band(m_tiles, tiles < sms ? tiles : sms,
                                     (double)BT * a.K * 2.0,
                                     (double)128 * a.K / ((VARIANT == kW8A16) ? 1.0 : 2.0))
