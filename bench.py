@@ -225,7 +225,7 @@ class Workload:
                     a = eg.QuantAct(torch.empty((M, K), dtype=torch.int8, device=dev),
                                     torch.empty((M,), dtype=torch.float32, device=dev),
                                     torch.empty((M, K // G128), dtype=torch.int32, device=dev),
-                                    torch.empty((M, K), dtype=torch.float16, device=dev))
+                                    eg.tc_operand(M, K, dev))
                     self.acts[(M, inp)] = (x, xd, a)
             self.ys = {(M, nm): torch.empty((M, N), dtype=torch.bfloat16, device=dev)
                        for M in ms for (nm, K, N) in shapes}
@@ -249,7 +249,7 @@ class Workload:
                 a = eg.QuantAct(torch.empty((m, K), dtype=torch.int8, device=dev),
                                 torch.empty((m,), dtype=torch.float32, device=dev),
                                 torch.empty((m, K // G128), dtype=torch.int32, device=dev),
-                                torch.empty((m, K), dtype=torch.float16, device=dev))
+                                eg.tc_operand(m, K, dev))
                 self.acts[(m, inp)] = (x, t(x, torch.bfloat16), a)
             self.ys = {(m, nm): torch.empty((m, N), dtype=torch.bfloat16, device=dev)
                        for (nm, K, N) in self.shapes + [HEAD]}

@@ -108,24 +108,32 @@ int egopq_unpack_w4(const void* packed, int64_t N, int64_t K, int group, uint8_t
  *   a_q[m,k]    = clamp(round_half_even(x / a_s), -127, 127)  (fp32 quotient)
  *   a_gsum[m,g] = sum_{k in g} a_q[m,k]
  * A row of zeros gives a_s = 0 and a_q = 0. Outputs (device): a_q int8
- * [M][K], a_s fp32 [M], a_gsum int32 [M][G]; a_q16 (optional, may be NULL)
- * receives the same codes as fp16 [M][K] -- exact integers, the operand form
- * the tensor-core path loads with TMA. ("The 4-bit CPU path", section "W4A8":
- * the kernel quantizes activations to int8.) */
+ * [M][K], a_s fp32 [M], a_gsum int32 [M][G]. a_tc (optional, may be NULL;
+ * 2*M*K bytes) receives the same codes in the operand form the tensor-core
+ * path loads with TMA; it is tied to this M and its layout is:
+ *   M <= 64: two e4m3 planes [2][M][K] bytes, plane 0 holding a_q >> 4
+ *            (arithmetic shift, in [-8, 7]) and plane 1 holding a_q & 15, so
+ *            a_q = 16 * plane0 + plane1, both exact in e4m3; inside every aligned run of 8 K values the
+ *            bytes are ordered k0, k0+2, k0+4, k0+6, k0+1, k0+3, k0+5, k0+7
+ *            (the nibble order of the packed weights);
+ *   M > 64:  fp16 [M][K], the codes as exact fp16 integers.
+ * ("The 4-bit CPU path", section "W4A8": the kernel quantizes activations to
+ * int8.) */
 int egopq_quant_act_i8(const uint16_t* x_bf16, int64_t M, int64_t K, int group, int8_t* a_q,
-                       float* a_s, int32_t* a_gsum, uint16_t* a_q16, egopq_stream_t stream);
+                       float* a_s, int32_t* a_gsum, void* a_tc, egopq_stream_t stream);
 
 /* ---- W4A8 GEMM -----------------------------------------------------------------
  * y[m,n] = bf16( a_s[m] * sum_g s[n,g] * (sum_{k in g} a_q[m,k] w_q[n,k]
  *                                         - z[n,g] * a_gsum[m,g]) )
  * Inputs from egopq_quant_act_i8 and egopq_pack_w4; y is bf16 [M][N]. The
- * GEMV path reads a_q and a_gsum; the tensor-core path reads a_q16 (required
- * when it runs) and folds z into its weight operand. Both form each group's
+ * GEMV path reads a_q and a_gsum; the tensor-core path reads a_tc (required
+ * when it runs) and, for M > 64, folds z into its weight operand, for
+ * M <= 64 subtracts z * a_gsum in its epilogue. Every path forms each group's
  * integer partial exactly before scaling. */
-int egopq_w4a8_gemm(const int8_t* a_q, const uint16_t* a_q16, const float* a_s,
+int egopq_w4a8_gemm(const int8_t* a_q, const void* a_tc, const float* a_s,
                     const int32_t* a_gsum, const void* packed, int64_t M, int64_t N, int64_t K,
                     int group, uint16_t* y_bf16, egopq_stream_t stream);
-int egopq_w4a8_gemm_ex(const int8_t* a_q, const uint16_t* a_q16, const float* a_s,
+int egopq_w4a8_gemm_ex(const int8_t* a_q, const void* a_tc, const float* a_s,
                        const int32_t* a_gsum, const void* packed, int64_t M, int64_t N,
                        int64_t K, int group, uint16_t* y_bf16, int path, egopq_stream_t stream);
 
@@ -160,7 +168,7 @@ int egopq_w4a8_linear_noalloc(const uint16_t* x_bf16, const void* packed, int64_
 /* Test readout: the integer group partials Q[m][n][g] (int32 [M][N][G]) the
  * chosen path forms before scaling, from the same main loop:
  *   Q[m,n,g] = sum_{k in g} a_q[m,k] w_q[n,k] - z[n,g] * sum_{k in g} a_q[m,k]. */
-int egopq_w4a8_group_partials(const int8_t* a_q, const uint16_t* a_q16, const int32_t* a_gsum,
+int egopq_w4a8_group_partials(const int8_t* a_q, const void* a_tc, const int32_t* a_gsum,
                               const void* packed, int64_t M, int64_t N, int64_t K, int group,
                               int32_t* Q, int path, egopq_stream_t stream);
 

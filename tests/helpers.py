@@ -54,3 +54,34 @@ def w4_case(config, M, N, K, layer=0, linear=0, outliers=True):
     w = synth.w4_weights(config, layer, linear, N, K)
     x = synth.activations(config, layer, linear, M, K, outliers)
     return x, w
+
+
+def e4m3_to_f64(b) -> np.ndarray:
+    """OCP FP8 E4M3 bytes -> float64 (bias 7, 3 mantissa bits; NaN not used here)."""
+    b = np.asarray(b, np.uint8).astype(np.int64)
+    sign = np.where(b >> 7, -1.0, 1.0)
+    e, m = (b >> 3) & 15, b & 7
+    mag = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * 2.0 ** (e - 7))
+    return sign * mag
+
+
+# byte q of each aligned 8-run of the e4m3 operand planes holds K offset ORDER[q]
+TC_PLANE_ORDER = np.array([0, 2, 4, 6, 1, 3, 5, 7])
+
+
+def decode_tc_operand(buf: np.ndarray, M: int, K: int, fp8_max_m: int) -> np.ndarray:
+    """Integer codes [M][K] held by the tensor-core operand buffer (2*M*K bytes)
+    in the form include/egopq.h documents: two e4m3 planes (a >> 4, a & 15) in
+    the packed weights' nibble order for M <= fp8_max_m, fp16 [M][K] otherwise.
+    Raises if a plane value is not the integer range it must be."""
+    buf = np.ascontiguousarray(buf).view(np.uint8).reshape(-1)
+    assert buf.size == 2 * M * K
+    if M > fp8_max_m:
+        return buf.view(np.float16).reshape(M, K).astype(np.float64)
+    hi = e4m3_to_f64(buf[:M * K]).reshape(M, K // 8, 8)
+    lo = e4m3_to_f64(buf[M * K:]).reshape(M, K // 8, 8)
+    assert np.all((hi >= -8) & (hi <= 7) & (hi == np.round(hi)))
+    assert np.all((lo >= 0) & (lo <= 15) & (lo == np.round(lo)))
+    codes = np.empty((M, K // 8, 8))
+    codes[:, :, TC_PLANE_ORDER] = 16 * hi + lo
+    return codes.reshape(M, K)

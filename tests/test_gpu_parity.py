@@ -10,7 +10,7 @@ import pytest
 
 import oracle
 import synth
-from helpers import check_bf16_output, to_dev, to_host_bits, w4_case
+from helpers import check_bf16_output, decode_tc_operand, to_dev, to_host_bits, w4_case
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -45,7 +45,7 @@ def run_w4a8(x, w, path, M, N, K):
 
 # ------------------------------------------------------------ activation quant
 
-@pytest.mark.parametrize("M,K", [(16, 512), (1, 3584), (5, 18944), (129, 1024), (300, 384)])
+@pytest.mark.parametrize("M,K", [(16, 512), (1, 3584), (5, 18944), (64, 640), (65, 1024), (129, 1024), (300, 384)])
 def test_quant_act_bit_exact(M, K):
     x = synth.activations(0, 1, 0, M, K)
     if M > 3:
@@ -57,7 +57,8 @@ def test_quant_act_bit_exact(M, K):
     assert np.array_equal(a.a_q.cpu().numpy(), a_q)
     assert np.array_equal(a.a_s.cpu().numpy().view(np.uint32), a_s.view(np.uint32))
     assert np.array_equal(a.a_gsum.cpu().numpy(), asum)
-    assert np.array_equal(a.a_q16.float().cpu().numpy(), a_q.astype(np.float32))
+    got = decode_tc_operand(a.a_tc.cpu().numpy(), M, K, eg.TC_FP8_MAX_M)
+    assert np.array_equal(got, a_q.astype(np.float64))
 
 
 def test_quant_act_ties_from_golden_rows():
@@ -88,7 +89,7 @@ def test_pack_bit_exact_and_roundtrip(N, K):
 # ------------------------------------------------------------- group partials
 
 @pytest.mark.parametrize("path", PATHS)
-@pytest.mark.parametrize("M", [1, 3, 4, 5, 16, 17, 64, 129])
+@pytest.mark.parametrize("M", [1, 3, 4, 5, 16, 17, 33, 48, 64, 65, 129])
 def test_w4a8_group_partials_bit_exact(path, M):
     N, K = 256, 512
     x, w = w4_case(0, M, N, K)
@@ -99,11 +100,13 @@ def test_w4a8_group_partials_bit_exact(path, M):
 
 
 @pytest.mark.parametrize("path", PATHS)
-@pytest.mark.parametrize("case", ["max_pos", "max_neg", "alternating"])
-def test_w4a8_group_partials_worst_case_magnitudes(path, case):
+@pytest.mark.parametrize("case", ["max_pos", "max_neg", "alternating", "neg_act"])
+@pytest.mark.parametrize("M", [16, 100])
+def test_w4a8_group_partials_worst_case_magnitudes(path, case, M):
     """|Q| up to 128*127*15 = 243840: the tensor-core path must stay exact
-    (fp16 integer products accumulated in fp32 within one group)."""
-    M, N, K = 16, 128, 512
+    (integer products accumulated in fp32 within one group; e4m3 operands for
+    M = 16, fp16 for M = 100)."""
+    N, K = 128, 512
     G = K // 128
     x = np.full((M, K), 0x3F80, np.uint16)                     # 1.0 -> a_q = 127
     w_q = np.full((N, K), 15, np.uint8)
@@ -116,6 +119,8 @@ def test_w4a8_group_partials_worst_case_magnitudes(path, case):
         w_q[:, 1::2] = 0
         w_q[::2, :] = 15 - w_q[::2, :]                         # half the rows flipped
         z[:, :] = np.arange(N)[:, None] % 16
+    elif case == "neg_act":
+        x[:] = 0xBF80                                          # a_q = -127 = 16*(-8) + 1
     s = np.full((N, G), 0x3C00, np.uint16)                     # 1.0
     w = synth.W4Weights(w_q, s, z, 128)
     a, packed, _ = run_w4a8(x, w, path, M, N, K)
@@ -124,7 +129,7 @@ def test_w4a8_group_partials_worst_case_magnitudes(path, case):
     ref = oracle.group_partials(a_q, w_q, z)
     if case == "max_pos":
         assert ref.max() == 243840
-    if case == "max_neg":
+    if case in ("max_neg", "neg_act"):
         assert ref.min() == -243840
     assert np.array_equal(Q, ref)
 
@@ -288,16 +293,16 @@ def test_rejections():
     s = torch.cuda.current_stream().cuda_stream
     y = torch.empty((4, N), dtype=torch.bfloat16, device="cuda")
     # N not a multiple of 128, misaligned output, missing fp16 codes on the TC path
-    assert lib.egopq_w4a8_gemm_ex(a.a_q.data_ptr(), a.a_q16.data_ptr(), a.a_s.data_ptr(),
+    assert lib.egopq_w4a8_gemm_ex(a.a_q.data_ptr(), a.a_tc.data_ptr(), a.a_s.data_ptr(),
                                   a.a_gsum.data_ptr(), packed.data_ptr(), 4, 192, K, 128,
                                   y.data_ptr(), 0, s) == -2
-    assert lib.egopq_w4a8_gemm_ex(a.a_q.data_ptr(), a.a_q16.data_ptr(), a.a_s.data_ptr(),
+    assert lib.egopq_w4a8_gemm_ex(a.a_q.data_ptr(), a.a_tc.data_ptr(), a.a_s.data_ptr(),
                                   a.a_gsum.data_ptr(), packed.data_ptr(), 4, N, K, 128,
                                   y.data_ptr() + 2, 0, s) == -3
     assert lib.egopq_w4a8_gemm_ex(a.a_q.data_ptr(), None, a.a_s.data_ptr(),
                                   a.a_gsum.data_ptr(), packed.data_ptr(), 4, N, K, 128,
                                   y.data_ptr(), eg.PATH_TC, s) == -1
-    assert lib.egopq_w4a8_gemm_ex(a.a_q.data_ptr(), a.a_q16.data_ptr(), a.a_s.data_ptr(),
+    assert lib.egopq_w4a8_gemm_ex(a.a_q.data_ptr(), a.a_tc.data_ptr(), a.a_s.data_ptr(),
                                   a.a_gsum.data_ptr(), packed.data_ptr(), 4, N, K, 64,
                                   y.data_ptr(), 0, s) == -2
     assert eg.supported(4, N, K) and not eg.supported(4, 80, K)

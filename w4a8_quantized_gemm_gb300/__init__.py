@@ -158,10 +158,21 @@ class QuantAct(NamedTuple):
     a_q: torch.Tensor      # int8 [M, K]
     a_s: torch.Tensor      # fp32 [M]
     a_gsum: torch.Tensor   # int32 [M, G]
-    a_q16: Optional[torch.Tensor]  # fp16 [M, K] (exact integer codes) or None
+    # uint8 [2*M*K]: the codes in the tensor-core operand form (two e4m3 planes
+    # for M <= TC_FP8_MAX_M, fp16 otherwise; layout in include/egopq.h), or None
+    a_tc: Optional[torch.Tensor]
 
 
-def quant_act(x: torch.Tensor, with_f16: bool = True, out: Optional[QuantAct] = None,
+# token count up to which the tensor-core operand form is two e4m3 planes
+TC_FP8_MAX_M = 64
+
+
+def tc_operand(M: int, K: int, device) -> torch.Tensor:
+    """A buffer for the tensor-core operand form of M x K codes."""
+    return torch.empty((2 * M * K,), dtype=torch.uint8, device=device)
+
+
+def quant_act(x: torch.Tensor, with_tc: bool = True, out: Optional[QuantAct] = None,
               stream=None) -> QuantAct:
     """Per-token symmetric int8 quantization of bf16 x [M, K]."""
     _dtype(x, torch.bfloat16, torch.int16, torch.uint16)
@@ -171,9 +182,9 @@ def quant_act(x: torch.Tensor, with_f16: bool = True, out: Optional[QuantAct] = 
         out = QuantAct(torch.empty((M, K), dtype=torch.int8, device=dev),
                        torch.empty((M,), dtype=torch.float32, device=dev),
                        torch.empty((M, max(K // GROUP, 1)), dtype=torch.int32, device=dev),
-                       torch.empty((M, K), dtype=torch.float16, device=dev) if with_f16 else None)
+                       tc_operand(M, K, dev) if with_tc else None)
     _check(load().egopq_quant_act_i8(_ptr(x), M, K, GROUP, _ptr(out.a_q), _ptr(out.a_s),
-                                     _ptr(out.a_gsum), _ptr(out.a_q16), _stream(stream)))
+                                     _ptr(out.a_gsum), _ptr(out.a_tc), _stream(stream)))
     return out
 
 
@@ -182,7 +193,7 @@ def w4a8_gemm(a: QuantAct, packed: torch.Tensor, N: int, K: int, path: int = PAT
     M = a.a_q.shape[0]
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=a.a_q.device)
-    _check(load().egopq_w4a8_gemm_ex(_ptr(a.a_q), _ptr(a.a_q16), _ptr(a.a_s), _ptr(a.a_gsum),
+    _check(load().egopq_w4a8_gemm_ex(_ptr(a.a_q), _ptr(a.a_tc), _ptr(a.a_s), _ptr(a.a_gsum),
                                      _ptr(packed), M, N, K, GROUP, _ptr(out), path,
                                      _stream(stream)))
     return out
@@ -214,7 +225,7 @@ def w4a8_group_partials(a: QuantAct, packed: torch.Tensor, N: int, K: int,
                         path: int = PATH_TC, stream=None) -> torch.Tensor:
     M = a.a_q.shape[0]
     Q = torch.empty((M, N, K // GROUP), dtype=torch.int32, device=a.a_q.device)
-    _check(load().egopq_w4a8_group_partials(_ptr(a.a_q), _ptr(a.a_q16), _ptr(a.a_gsum),
+    _check(load().egopq_w4a8_group_partials(_ptr(a.a_q), _ptr(a.a_tc), _ptr(a.a_gsum),
                                             _ptr(packed), M, N, K, GROUP, _ptr(Q), path,
                                             _stream(stream)))
     return Q

@@ -91,8 +91,8 @@ int run_gemm(const GemmArgs& a, int path, cudaStream_t st) {
   int use = path;
   if (use == EGOPQ_PATH_AUTO)
     use = (a.M <= kGemvAutoMaxM && a.variant == kW4A8) ? EGOPQ_PATH_GEMV : EGOPQ_PATH_TC;
-  if (use == EGOPQ_PATH_TC && a.variant == kW4A8 && !a.a_q16)
-    return fail(EGOPQ_ERR_INVALID_ARG, "a_q16 is required by the tensor-core path");
+  if (use == EGOPQ_PATH_TC && a.variant == kW4A8 && !a.a_tc)
+    return fail(EGOPQ_ERR_INVALID_ARG, "a_tc is required by the tensor-core path");
   cudaError_t e = (use == EGOPQ_PATH_GEMV) ? launch_gemv(a, st) : launch_tc_gemm(a, st);
   if (e == cudaErrorNotSupported)
     return fail(EGOPQ_ERR_UNSUPPORTED_SHAPE, "shape not supported by the requested path");
@@ -138,7 +138,7 @@ int egopq_unpack_w4(const void* packed, int64_t N, int64_t K, int group, uint8_t
 }
 
 int egopq_quant_act_i8(const uint16_t* x_bf16, int64_t M, int64_t K, int group, int8_t* a_q,
-                       float* a_s, int32_t* a_gsum, uint16_t* a_q16, egopq_stream_t stream) {
+                       float* a_s, int32_t* a_gsum, void* a_tc, egopq_stream_t stream) {
   if (M < 0 || K <= 0 || M >= kMaxDim || K >= kMaxDim)
     return fail(EGOPQ_ERR_INVALID_ARG, "bad sizes M=%lld K=%lld", (long long)M, (long long)K);
   if (group != 128) return fail(EGOPQ_ERR_UNSUPPORTED_SHAPE, "group must be 128 (got %d)", group);
@@ -146,13 +146,13 @@ int egopq_quant_act_i8(const uint16_t* x_bf16, int64_t M, int64_t K, int group, 
   if (M == 0) return EGOPQ_OK;
   int rc = check_ptrs(4, "x_bf16", x_bf16, "a_q", a_q, "a_s", a_s, "a_gsum", a_gsum);
   if (rc) return rc;
-  if (a_q16 && !aligned16(a_q16)) return fail(EGOPQ_ERR_MISALIGNED, "a_q16 is not 16-byte aligned");
+  if (a_tc && !aligned16(a_tc)) return fail(EGOPQ_ERR_MISALIGNED, "a_tc is not 16-byte aligned");
   if ((rc = check_arch())) return rc;
-  cudaError_t e = launch_quant_act(x_bf16, M, K, a_q, a_s, a_gsum, a_q16, (cudaStream_t)stream);
+  cudaError_t e = launch_quant_act(x_bf16, M, K, a_q, a_s, a_gsum, a_tc, (cudaStream_t)stream);
   return e == cudaSuccess ? EGOPQ_OK : cuda_fail(e, "quant_act launch");
 }
 
-int egopq_w4a8_gemm_ex(const int8_t* a_q, const uint16_t* a_q16, const float* a_s,
+int egopq_w4a8_gemm_ex(const int8_t* a_q, const void* a_tc, const float* a_s,
                        const int32_t* a_gsum, const void* packed, int64_t M, int64_t N,
                        int64_t K, int group, uint16_t* y_bf16, int path, egopq_stream_t stream) {
   int rc = check_w4_shape(M, N, K, group);
@@ -160,14 +160,14 @@ int egopq_w4a8_gemm_ex(const int8_t* a_q, const uint16_t* a_q16, const float* a_
   if (M == 0) return EGOPQ_OK;
   rc = check_ptrs(5, "a_q", a_q, "a_s", a_s, "a_gsum", a_gsum, "packed", packed, "y_bf16", y_bf16);
   if (rc) return rc;
-  if (a_q16 && !aligned16(a_q16)) return fail(EGOPQ_ERR_MISALIGNED, "a_q16 is not 16-byte aligned");
+  if (a_tc && !aligned16(a_tc)) return fail(EGOPQ_ERR_MISALIGNED, "a_tc is not 16-byte aligned");
   GemmArgs a{};
   a.variant = kW4A8;
   a.M = M;
   a.N = N;
   a.K = K;
   a.a_q = a_q;
-  a.a_q16 = a_q16;
+  a.a_tc = a_tc;
   a.a_s = a_s;
   a.a_gsum = a_gsum;
   a.packed = static_cast<const uint8_t*>(packed);
@@ -176,10 +176,10 @@ int egopq_w4a8_gemm_ex(const int8_t* a_q, const uint16_t* a_q16, const float* a_
   return run_gemm(a, path, (cudaStream_t)stream);
 }
 
-int egopq_w4a8_gemm(const int8_t* a_q, const uint16_t* a_q16, const float* a_s,
+int egopq_w4a8_gemm(const int8_t* a_q, const void* a_tc, const float* a_s,
                     const int32_t* a_gsum, const void* packed, int64_t M, int64_t N, int64_t K,
                     int group, uint16_t* y_bf16, egopq_stream_t stream) {
-  return egopq_w4a8_gemm_ex(a_q, a_q16, a_s, a_gsum, packed, M, N, K, group, y_bf16,
+  return egopq_w4a8_gemm_ex(a_q, a_tc, a_s, a_gsum, packed, M, N, K, group, y_bf16,
                             EGOPQ_PATH_AUTO, stream);
 }
 
@@ -215,11 +215,10 @@ int run_linear(const uint16_t* x_bf16, const void* packed, int64_t M, int64_t N,
   int8_t* a_q = reinterpret_cast<int8_t*>(ws);
   float* a_s = reinterpret_cast<float*>(ws + align256((size_t)(M * K)));
   int32_t* asum = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(a_s) + align256((size_t)(4 * M)));
-  uint16_t* a_q16 = nullptr;
+  void* a_tc = nullptr;
   if (use == EGOPQ_PATH_TC)
-    a_q16 = reinterpret_cast<uint16_t*>(reinterpret_cast<uint8_t*>(asum) +
-                                        align256((size_t)(4 * M * (K / 128))));
-  cudaError_t e = launch_quant_act(x_bf16, M, K, a_q, a_s, asum, a_q16, st);
+    a_tc = reinterpret_cast<uint8_t*>(asum) + align256((size_t)(4 * M * (K / 128)));
+  cudaError_t e = launch_quant_act(x_bf16, M, K, a_q, a_s, asum, a_tc, st);
   if (e != cudaSuccess) return cuda_fail(e, "quant_act launch");
   GemmArgs a{};
   a.variant = kW4A8;
@@ -227,7 +226,7 @@ int run_linear(const uint16_t* x_bf16, const void* packed, int64_t M, int64_t N,
   a.N = N;
   a.K = K;
   a.a_q = a_q;
-  a.a_q16 = a_q16;
+  a.a_tc = a_tc;
   a.a_s = a_s;
   a.a_gsum = asum;
   a.packed = static_cast<const uint8_t*>(packed);
@@ -261,7 +260,7 @@ int egopq_w4a8_linear(const uint16_t* x_bf16, const void* packed, int64_t M, int
                     linear_path(M, path), (cudaStream_t)stream);
 }
 
-int egopq_w4a8_group_partials(const int8_t* a_q, const uint16_t* a_q16, const int32_t* a_gsum,
+int egopq_w4a8_group_partials(const int8_t* a_q, const void* a_tc, const int32_t* a_gsum,
                               const void* packed, int64_t M, int64_t N, int64_t K, int group,
                               int32_t* Q, int path, egopq_stream_t stream) {
   int rc = check_w4_shape(M, N, K, group);
@@ -269,14 +268,14 @@ int egopq_w4a8_group_partials(const int8_t* a_q, const uint16_t* a_q16, const in
   if (M == 0) return EGOPQ_OK;
   rc = check_ptrs(4, "a_q", a_q, "a_gsum", a_gsum, "packed", packed, "Q", Q);
   if (rc) return rc;
-  if (a_q16 && !aligned16(a_q16)) return fail(EGOPQ_ERR_MISALIGNED, "a_q16 is not 16-byte aligned");
+  if (a_tc && !aligned16(a_tc)) return fail(EGOPQ_ERR_MISALIGNED, "a_tc is not 16-byte aligned");
   GemmArgs a{};
   a.variant = kW4A8;
   a.M = M;
   a.N = N;
   a.K = K;
   a.a_q = a_q;
-  a.a_q16 = a_q16;
+  a.a_tc = a_tc;
   a.a_gsum = a_gsum;
   a.packed = static_cast<const uint8_t*>(packed);
   a.partials = Q;

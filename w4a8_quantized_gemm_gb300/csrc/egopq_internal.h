@@ -17,7 +17,7 @@ struct GemmArgs {
   int64_t M, N, K;
   // W4A8
   const int8_t* a_q;
-  const uint16_t* a_q16;
+  const void* a_tc;  // tensor-core operand form of a_q (see kTcFp8MaxM)
   const float* a_s;
   const int32_t* a_gsum;
   // W4A16 / W8A16
@@ -34,7 +34,7 @@ struct GemmArgs {
 };
 
 cudaError_t launch_quant_act(const uint16_t* x, int64_t M, int64_t K, int8_t* a_q, float* a_s,
-                             int32_t* a_gsum, uint16_t* a_q16, cudaStream_t st);
+                             int32_t* a_gsum, void* a_tc, cudaStream_t st);
 cudaError_t launch_pack_w4(const uint8_t* w_q, const uint16_t* s, const uint8_t* z, int64_t N,
                            int64_t K, void* packed, cudaStream_t st);
 cudaError_t launch_unpack_w4(const void* packed, int64_t N, int64_t K, uint8_t* w_q, uint16_t* s,
@@ -48,6 +48,11 @@ cudaError_t launch_tc_gemm(const GemmArgs& a, cudaStream_t st);
 // Bounded-wait self test.
 cudaError_t launch_selftest_timeout(uint64_t timeout_ns, cudaStream_t st);
 
+// Tensor-core W4A8 operand form: up to this many tokens the activation codes
+// are staged as two e4m3 planes (a_q >> 4, a_q & 15) and the MMAs run
+// kind::f8f6f4 at K = 32 (token tiles of at most 64); above it as fp16 codes
+// for kind::f16 MMAs (128-token tiles).
+constexpr int kTcFp8MaxM = 64;
 // Largest M per W4A8 GEMV launch (larger M run as several launches).
 constexpr int kGemvMaxRows = 16;
 // AUTO path: W4A8 batches up to this many tokens take the GEMV.

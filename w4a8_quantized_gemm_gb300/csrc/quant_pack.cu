@@ -7,7 +7,8 @@
 // clamped to +-127, both quotients IEEE fp32 (so the integer codes match any
 // correctly rounded implementation bit for bit). The same pass emits the
 // per-group sums of a_q that fold the zero points into the GEMM epilogue, and
-// optionally the codes as exact fp16 integers for the tensor-core path.
+// optionally the codes in the tensor-core operand form (two exact e4m3 planes
+// for small token counts, exact fp16 integers otherwise).
 //
 // Weight packing lays GPTQ-style int4 codes (per-group _gptq_scale /
 // _gptq_zero, "EgoPQ Real-Serving Handoff", section 2) out in 8512-byte
@@ -21,10 +22,47 @@ namespace egopq {
 
 constexpr int kQuantThreads = 256;
 
+// e4m3 code of an integer in [-16, 16] (exact: the conversion does not
+// round).
+__device__ __forceinline__ uint32_t e4m3_exact(int v) {
+  return __nv_cvt_float_to_fp8((float)v, __NV_SATFINITE, __NV_E4M3);
+}
+
+// Writes the tensor-core operand form of the 8 codes q[0..7] (K = 8*vec ..
+// 8*vec+7) of token m, as documented for a_tc in include/egopq.h: with
+// fp8 = true two e4m3 planes [2][M][K] (high part a >> 4 in [-8, 7], low
+// part a & 15, a = 16 * high + low) with each 8-run in the packed weights' nibble order (even offsets,
+// then odd); otherwise fp16 [M][K].
+__device__ __forceinline__ void store_tc_operand(void* a_tc, bool fp8, int64_t M, int64_t K,
+                                                 int64_t m, int64_t vec, const int (&q)[8]) {
+  if (fp8) {
+    constexpr int kOrder[8] = {0, 2, 4, 6, 1, 3, 5, 7};
+    uint32_t hi[2] = {0, 0}, lo[2] = {0, 0};
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+      const int a = q[kOrder[b]];
+      hi[b >> 2] |= e4m3_exact(a >> 4) << (8 * (b & 3));
+      lo[b >> 2] |= e4m3_exact(a & 15) << (8 * (b & 3));
+    }
+    uint8_t* base = static_cast<uint8_t*>(a_tc);
+    *reinterpret_cast<uint2*>(base + m * K + 8 * vec) = make_uint2(hi[0], hi[1]);
+    *reinterpret_cast<uint2*>(base + M * K + m * K + 8 * vec) = make_uint2(lo[0], lo[1]);
+  } else {
+    uint32_t h[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __half2 hv = __halves2half2(__int2half_rn(q[2 * i]), __int2half_rn(q[2 * i + 1]));
+      h[i] = *reinterpret_cast<uint32_t*>(&hv);
+    }
+    reinterpret_cast<uint4*>(static_cast<uint16_t*>(a_tc) + m * K)[vec] =
+        make_uint4(h[0], h[1], h[2], h[3]);
+  }
+}
+
 __global__ void __launch_bounds__(kQuantThreads)
 quant_act_kernel(const uint16_t* __restrict__ x, int64_t K, int8_t* __restrict__ a_q,
                  float* __restrict__ a_s, int32_t* __restrict__ a_gsum,
-                 uint16_t* __restrict__ a_q16) {
+                 void* __restrict__ a_tc, bool tc_fp8) {
   griddep_wait();
   if (threadIdx.x == 0) griddep_launch_dependents();
   const int64_t m = blockIdx.x;
@@ -73,15 +111,7 @@ quant_act_kernel(const uint16_t* __restrict__ x, int64_t K, int8_t* __restrict__
     packed.y = (uint32_t)(q[4] & 0xFF) | ((uint32_t)(q[5] & 0xFF) << 8) |
                ((uint32_t)(q[6] & 0xFF) << 16) | ((uint32_t)(q[7] & 0xFF) << 24);
     reinterpret_cast<uint2*>(a_q + m * K)[v] = packed;
-    if (a_q16) {
-      uint32_t h[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        __half2 hv = __halves2half2(__int2half_rn(q[2 * i]), __int2half_rn(q[2 * i + 1]));
-        h[i] = *reinterpret_cast<uint32_t*>(&hv);
-      }
-      reinterpret_cast<uint4*>(a_q16 + m * K)[v] = make_uint4(h[0], h[1], h[2], h[3]);
-    }
+    if (a_tc) store_tc_operand(a_tc, tc_fp8, gridDim.x, K, m, v, q);
     // 16 consecutive vectors make one 128-wide group; kQuantThreads % 16 == 0
     // K % 128 == 0, so the 16 lanes of a half-warp are all inside the loop or
     // all outside it; reduce within the half-warp only.
@@ -103,7 +133,7 @@ constexpr int kRegVec = 8;
 __global__ void __launch_bounds__(kQuantRegThreads)
 quant_act_reg_kernel(const uint16_t* __restrict__ x, int64_t K, int8_t* __restrict__ a_q,
                      float* __restrict__ a_s, int32_t* __restrict__ a_gsum,
-                     uint16_t* __restrict__ a_q16) {
+                     void* __restrict__ a_tc, bool tc_fp8) {
   griddep_wait();
   if (threadIdx.x == 0) griddep_launch_dependents();
   const int64_t m = blockIdx.x;
@@ -152,15 +182,7 @@ quant_act_reg_kernel(const uint16_t* __restrict__ x, int64_t K, int8_t* __restri
     packed.y = (uint32_t)(q[4] & 0xFF) | ((uint32_t)(q[5] & 0xFF) << 8) |
                ((uint32_t)(q[6] & 0xFF) << 16) | ((uint32_t)(q[7] & 0xFF) << 24);
     reinterpret_cast<uint2*>(a_q + m * K)[idx] = packed;
-    if (a_q16) {
-      uint32_t h[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        __half2 hv = __halves2half2(__int2half_rn(q[2 * j]), __int2half_rn(q[2 * j + 1]));
-        h[j] = *reinterpret_cast<uint32_t*>(&hv);
-      }
-      reinterpret_cast<uint4*>(a_q16 + m * K)[idx] = make_uint4(h[0], h[1], h[2], h[3]);
-    }
+    if (a_tc) store_tc_operand(a_tc, tc_fp8, gridDim.x, K, m, idx, q);
     int sum = q[0] + q[1] + q[2] + q[3] + q[4] + q[5] + q[6] + q[7];
     const unsigned half_mask = 0xFFFFu << (threadIdx.x & 16);
 #pragma unroll
@@ -250,7 +272,7 @@ static unsigned grid_for(int64_t work, int threads) {
 }
 
 cudaError_t launch_quant_act(const uint16_t* x, int64_t M, int64_t K, int8_t* a_q, float* a_s,
-                             int32_t* a_gsum, uint16_t* a_q16, cudaStream_t st) {
+                             int32_t* a_gsum, void* a_tc, cudaStream_t st) {
   // few tokens: one wide CTA per row, one read of x (latency); many tokens:
   // narrower CTAs, several resident per SM (throughput)
   const bool reg = (M <= 64 && K <= (int64_t)kQuantRegThreads * kRegVec * 8);
@@ -263,8 +285,10 @@ cudaError_t launch_quant_act(const uint16_t* x, int64_t M, int64_t K, int8_t* a_
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (reg) return cudaLaunchKernelEx(&cfg, quant_act_reg_kernel, x, K, a_q, a_s, a_gsum, a_q16);
-  return cudaLaunchKernelEx(&cfg, quant_act_kernel, x, K, a_q, a_s, a_gsum, a_q16);
+  const bool tc_fp8 = M <= kTcFp8MaxM;
+  if (reg)
+    return cudaLaunchKernelEx(&cfg, quant_act_reg_kernel, x, K, a_q, a_s, a_gsum, a_tc, tc_fp8);
+  return cudaLaunchKernelEx(&cfg, quant_act_kernel, x, K, a_q, a_s, a_gsum, a_tc, tc_fp8);
 }
 
 cudaError_t launch_pack_w4(const uint8_t* w_q, const uint16_t* s, const uint8_t* z, int64_t N,

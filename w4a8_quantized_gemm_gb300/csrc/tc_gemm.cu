@@ -9,32 +9,44 @@
 //   Q[m,n,g] = sum_{k in g} a_q[m,k] * (w_q[n,k] - z[n,g])
 //
 // sm_103a has no integer tcgen05.mma, so each group partial is formed EXACTLY
-// on the kind::f16 path: a_q (|a_q| <= 127) and w_q - z (in [-15, 15]) are
-// exact fp16 integers, every product is exact, and a 128-wide group sums to at
-// most 128*127*15 = 243840 < 2^24 in magnitude, so fp32 accumulation of one
-// group in Tensor Memory is exact. The accumulator is drained after every
-// group, scaled by s[n,g] and accumulated in fp32 registers.
+// on floating-point MMAs whose operands are exact small integers:
+//  - token tiles of at most 64 (kind::f8f6f4, K = 32 per MMA): the weight
+//    codes 0..15 are exact e4m3 (two PRMT table lookups per 4 codes), and each
+//    activation code splits as a = 16 * (a >> 4) + (a & 15) into two exact
+//    e4m3 rows of the B operand (N = 2 * tokens); z * sum(a) comes off in the
+//    drain with the per-group activation sums;
+//  - larger tiles (kind::f16, K = 16 per MMA): a_q (|a_q| <= 127) and w_q - z
+//    (in [-15, 15]) as exact fp16, with z folded into the converted weights.
+// Every product is exact and a 128-wide group sums to at most
+// 128*127*15 = 243840 < 2^24 in magnitude, so fp32 accumulation of one group
+// in Tensor Memory is exact. The accumulator is drained after every group,
+// scaled by s[n,g] and accumulated in fp32 registers.
 //
 // Operand roles ("swap AB"): the 128 weight rows of a tile are the MMA's M
 // dimension and live in TENSOR MEMORY as the A operand; the token tile (BT
 // tokens, 16..128) is the MMA's N dimension and comes from shared memory as
 // the B operand, staged by TMA with 128-byte swizzle. The dequantized weights
 // therefore never touch shared memory: converter warps read the packed int4
-// tile (one 8 KiB bulk copy per 128 rows x 128 K), turn codes into
-// (w_q - z) fp16 pairs with one AND/OR and one HSUB2/HFMA2 per pair, and
-// store them straight into TMEM with tcgen05.st.
+// record (one 8512-byte bulk copy per 128 rows x 128 K: codes, scales, zero
+// points), convert the codes and store them straight into TMEM with
+// tcgen05.st.
 //
-// Warp roles (448 threads, 576 for token tiles of at most 32; one CTA per SM):
+// Warp roles (one CTA per SM):
 //   warps 0-7   drain: TMEM accumulator -> registers, *s, accumulate, epilogue;
 //               warps 0-3 own token columns [0, BT/2), warps 4-7 [BT/2, BT)
-//   warps 8-11  convert: packed int4 (or int8) smem tile -> fp16/bf16 in TMEM
-//               (small tiles: a second set, warps 12-15, takes every other group)
-//   next warp   TMA producer (activations tile + weight tile per group)
+//   warps 8-11  convert: packed int4 (or int8) smem tile -> e4m3/fp16/bf16 in
+//               TMEM (small tiles: a second set, warps 12-15, takes every
+//               other group)
+//   next warp   TMA producer (activations tile + weight record per group)
 //   last warp   TMEM allocator and single-thread MMA issuer
 // (a warp reaches TMEM lanes 32*(warp % 4) .. +31, so each role that touches
 // TMEM is a whole warpgroup)
-// Pipelines: S shared-memory stages, 2 TMEM A buffers, 2 TMEM accumulators,
-// all handed over with mbarriers; every wait is bounded.
+// Hand-offs, all on mbarriers with bounded waits: S shared-memory stages,
+// kNumA TMEM A buffers, kNumD TMEM accumulators. Every barrier test is a
+// round trip of about a hundred cycles on the waiting thread, so the MMA
+// issuer waits on one barrier per group: the converters arrive on it only
+// after the stage has landed, the A buffer is free and the accumulator has
+// been drained.
 //
 // Split-K for small grids: a cluster of up to 8 CTAs shares one output tile,
 // each taking a contiguous range of groups; partial sums are reduced through
@@ -60,6 +72,7 @@ struct TcParams {
   int band;        // persistent tile order: bands of `band` m-tiles, m fastest inside a band
   int act3d;       // 1: activation map is 3-D, one copy per 128-wide group; 0: 2-D, two copies
   const float* a_s;
+  const int32_t* a_gsum;  // per-token group sums (e4m3 W4A8 form: zero points in the drain)
   const uint8_t* packed;
   const uint16_t* s8;
   uint16_t* y;
@@ -78,10 +91,20 @@ struct TcCfg {
   // MMA is short, so a chain of dependent ones is latency-bound, while
   // independent ones overlap. The drain adds the chains (integers below 2^24:
   // the sum stays exact).
-  static constexpr int kChains = BT == 16 ? 4 : (BT == 32 ? 2 : 1);
-  static constexpr int kDCols = kChains * BT;  // TMEM columns of one accumulator buffer
-  static constexpr int kNumD = BT <= 64 ? 4 : 2;
-  static constexpr int kNumA = 4;
+  //
+  // W4A8 with token tiles of at most 64 runs kind::f8f6f4: an MMA costs the
+  // same issue time for any N up to 64 (and K = 32 e4m3 per instruction
+  // against K = 16 fp16), so the activation codes a = 16 * (a >> 4) + (a & 15)
+  // enter as two exact e4m3 rows per token (N = 2*BT) and the weight codes
+  // 0..15 as exact e4m3; a group takes 4 MMAs instead of 8, and the zero
+  // points come off in the drain as z * sum(a).
+  static constexpr bool kFp8 = (VARIANT == kW4A8) && BT <= kTcFp8MaxM;
+  static constexpr int kChains = kFp8 ? 1 : (BT == 16 ? 4 : (BT == 32 ? 2 : 1));
+  static constexpr int kDCols = kFp8 ? 2 * BT : kChains * BT;  // columns of one accumulator
+  static constexpr int kACols = kFp8 ? 32 : 64;  // A operand columns of one group
+  static constexpr int kMmaK = kFp8 ? 32 : 16;   // K per MMA
+  static constexpr int kNumD = (kFp8 && BT == 64) ? 2 : (BT <= 64 ? 4 : 2);
+  static constexpr int kNumA = kFp8 ? 8 : 4;
   static constexpr int kActBox = BT * 128;                        // one 64-wide K box, bytes
   static constexpr int kActBytes = 2 * kActBox;                   // a 128-wide group
   // weights of one group: the int8 tile, or one packed int4 record (8192 B of
@@ -98,7 +121,7 @@ struct TcCfg {
   static constexpr int kStages = kStagesRaw > kStageCap ? kStageCap : kStagesRaw;
   static constexpr int kBarOffset = kStages * kStageBytes;
   static constexpr int kSmemBytes = kBarOffset + 512 + 1024;     // + barriers + alignment slack
-  static constexpr int kTmemColsRaw = kNumD * kDCols + kNumA * 64;
+  static constexpr int kTmemColsRaw = kNumD * kDCols + kNumA * kACols;
   static constexpr int kTmemCols = kTmemColsRaw <= 32    ? 32
                                    : kTmemColsRaw <= 64  ? 64
                                    : kTmemColsRaw <= 128 ? 128
@@ -115,7 +138,8 @@ struct TcCfg {
   static constexpr int kBf16 = (VARIANT == kW4A8) ? 0 : 1;
   static_assert(kStages >= 2, "shared memory too small for two stages");
   static_assert(kTmemColsRaw <= 512, "TMEM budget");
-  static_assert(8 * (2 * kStages + 2 * kNumA + 2 * kNumD) + 8 <= 512, "barrier region");
+  static_assert(8 * (2 * kStages + kNumA + 2 * kNumD) + 8 <= 512, "barrier region");
+  static_assert(kStages >= kNumA, "A-buffer reuse is tracked through the stage barriers");
   static_assert(BT % 16 == 0 && BT >= 16 && BT <= 128, "token tile");
   static_assert(kStageBytes % 1024 == 0, "stage alignment");
 };
@@ -204,10 +228,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
   auto afull_bar = [&](int i) { return bar0 + 8u * (2 * S + i); };
-  auto aempty_bar = [&](int i) { return bar0 + 8u * (2 * S + kNumA + i); };
-  auto dfull_bar = [&](int i) { return bar0 + 8u * (2 * S + 2 * kNumA + i); };
-  auto dempty_bar = [&](int i) { return bar0 + 8u * (2 * S + 2 * kNumA + kNumD + i); };
-  uint8_t* misc = smem + C::kBarOffset + 8 * (2 * S + 2 * kNumA + 2 * kNumD);
+  auto dfull_bar = [&](int i) { return bar0 + 8u * (2 * S + kNumA + i); };
+  auto dempty_bar = [&](int i) { return bar0 + 8u * (2 * S + kNumA + kNumD + i); };
+  uint8_t* misc = smem + C::kBarOffset + 8 * (2 * S + kNumA + 2 * kNumD);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
   auto stage_act = [&](int s) { return base + (uint32_t)(s * C::kStageBytes); };
@@ -216,11 +239,13 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1 + 4);
+      // released by the MMA commit and the 4 converter warps (and, in the
+      // e4m3 form, the 8 drain warps, which read the record's scales and
+      // zero points from the stage)
+      mbar_init(empty_bar(s), 1 + 4 + (C::kFp8 ? 8 : 0));
     }
     for (int i = 0; i < kNumA; ++i) {
       mbar_init(afull_bar(i), 4);
-      mbar_init(aempty_bar(i), 1);
     }
     for (int i = 0; i < kNumD; ++i) {
       mbar_init(dfull_bar(i), 1);
@@ -242,7 +267,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t d_tmem = tmem;                  // accumulators: columns [0, kNumD*BT)
-  const uint32_t a_tmem = tmem + kNumD * C::kDCols;  // A operand: kNumA buffers of 64 columns
+  const uint32_t a_tmem = tmem + kNumD * C::kDCols;  // A operand: kNumA buffers of kACols
   const uint64_t tmo = p.timeout_ns;
   const bool cluster_reduce = !PARTIALS && !p.persistent && p.ks > 1;
 
@@ -284,7 +309,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
       auto load_act = [&](int s) {
         const int mt = a_mt, g = g0 + a_gi;
         advance(a_k, a_gi, a_mt, a_nt);
-        if (p.act3d) {
+        if constexpr (C::kFp8) {
+          // both e4m3 planes of BT tokens: [2][BT][128] bytes
+          tma_load_3d(stage_act(s), &act_map, full_bar(s), g * 128, mt * BT, 0);
+        } else if (p.act3d) {
           tma_load_3d(stage_act(s), &act_map, full_bar(s), 0, mt * BT, g * 2);
         } else {
           tma_load_2d(stage_act(s), &act_map, full_bar(s), g * 128, mt * BT);
@@ -325,29 +353,35 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
   } else if (warp == C::kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_f16(128, BT, C::kBf16);
+      constexpr uint32_t idesc = idesc_f16(128, C::kFp8 ? 2 * BT : BT, C::kBf16);
       int last = -1;
       int gi = 0, ti = 0;  // group index inside the tile, tile counter
       for (int i = 0; i < n_items; ++i, gi = (gi + 1 == ng) ? (++ti, 0) : gi + 1) {
         const int s = i % S, ab = i % kNumA;
         const int di = C::kDrainPerGroup ? i : ti;
         const int db = di % kNumD;
-        if (!mbar_wait(full_bar(s), (i / S) & 1, abort_flag, tmo)) break;
+        // one wait per group: the converters arrive on afull only once the
+        // stage has landed, the A buffer is free and the accumulator drained
         if (!mbar_wait(afull_bar(ab), (i / kNumA) & 1, abort_flag, tmo)) break;
-        if (C::kDrainPerGroup || gi == 0)
-          if (!mbar_wait(dempty_bar(db), ((di / kNumD) & 1) ^ 1, abort_flag, tmo)) break;
         tc_fence_after();
+        if constexpr (C::kFp8) {
+          // 4 x K=32: B rows are the 2*BT e4m3 token rows of one 128-byte
+          // swizzled box; K step j advances 32 bytes inside it
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint32_t b_addr = stage_act(s) + (j >> 2) * C::kActBox + (j & 3) * 32;
-          constexpr int CH = C::kChains;
-          const uint32_t acc = C::kDrainPerGroup ? (j >= CH) : (gi > 0 || j >= CH);
-          tc_mma_f16_ts(d_tmem + db * C::kDCols + (j % CH) * BT, a_tmem + ab * 64 + j * 8,
-                        sdesc_kmajor_sw128(b_addr),
-                        idesc, acc);
+          for (int j = 0; j < 4; ++j)
+            tc_mma_f8_ts(d_tmem + db * C::kDCols, a_tmem + ab * C::kACols + j * 8,
+                         sdesc_kmajor_sw128(stage_act(s) + j * 32), idesc, j > 0);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint32_t b_addr = stage_act(s) + (j >> 2) * C::kActBox + (j & 3) * 32;
+            constexpr int CH = C::kChains;
+            const uint32_t acc = C::kDrainPerGroup ? (j >= CH) : (gi > 0 || j >= CH);
+            tc_mma_f16_ts(d_tmem + db * C::kDCols + (j % CH) * BT, a_tmem + ab * 64 + j * 8,
+                          sdesc_kmajor_sw128(b_addr), idesc, acc);
+          }
         }
-        tc_commit(empty_bar(s));
-        tc_commit(aempty_bar(ab));
+        tc_commit(empty_bar(s));  // also frees A buffer ab (converters watch it)
         if (C::kDrainPerGroup || gi == ng - 1) tc_commit(dfull_bar(db));
         last = i;
       }
@@ -373,7 +407,31 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
       const int s = i % S, ab = i % kNumA;
       if (!mbar_wait(full_bar(s), (i / S) & 1, abort_flag, tmo)) break;
       uint32_t out[64];
-      if constexpr (VARIANT == kW8A16) {
+      if constexpr (C::kFp8) {
+        const uint8_t* wt = stage_w_ptr(s) + r * 16;
+        uint4 v[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) v[c] = *reinterpret_cast<const uint4*>(wt + c * 2048);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty_bar(s));
+        // codes 0..15 -> e4m3 by table: prmt picks byte (nibble & 7) of the
+        // 8-byte half-table; a nibble with bit 3 set selects a sign fill,
+        // which is 0x00 because every table byte is positive, so the two
+        // half-table lookups (the second with bit 3 flipped) OR together.
+        constexpr uint32_t kT0 = 0x44403800u, kT1 = 0x4E4C4A48u;  // 0,1,2,3 | 4,5,6,7
+        constexpr uint32_t kT2 = 0x53525150u, kT3 = 0x57565554u;  // 8..11  | 12..15
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint32_t wv[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t w = wv[j], wx = wv[j] ^ 0x88888888u;
+            // nibbles 0..3 (K offsets 0,2,4,6), then 4..7 (offsets 1,3,5,7)
+            out[c * 8 + j * 2] = prmt(kT0, kT1, w) | prmt(kT2, kT3, wx);
+            out[c * 8 + j * 2 + 1] = prmt(kT0, kT1, w >> 16) | prmt(kT2, kT3, wx >> 16);
+          }
+        }
+      } else if constexpr (VARIANT == kW8A16) {
         const uint8_t* wt = stage_w_ptr(s) + r * 128;
         uint4 v[8];
 #pragma unroll
@@ -452,10 +510,24 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
           }
         }
       }
-      if (!mbar_wait(aempty_bar(ab), ((i / kNumA) & 1) ^ 1, abort_flag, tmo)) break;
-      const uint32_t dst = a_tmem + lane_base + ab * 64;
+      // A buffer ab is free once the MMAs of item i - kNumA have completed,
+      // i.e. once stage (i - kNumA) % S has been released for that item
+      // (kStages >= kNumA, so that phase can be neither lapped nor pending
+      // behind an older one here)
+      if (i >= kNumA) {
+        const int j = i - kNumA;
+        if (!mbar_wait(empty_bar(j % S), (j / S) & 1, abort_flag, tmo)) break;
+      }
+      // the accumulator this item feeds must have been drained; one warp of
+      // the set waits (afull completes only with all four arrivals)
+      if (((warp - kConvWarp0) & 3) == 0) {
+        const int di = C::kDrainPerGroup ? i : i / ng;
+        if (!mbar_wait(dempty_bar(di % kNumD), ((di / kNumD) & 1) ^ 1, abort_flag, tmo)) break;
+      }
+      tc_fence_after();
+      const uint32_t dst = a_tmem + lane_base + ab * C::kACols;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < C::kACols / 16; ++c) {
         uint32_t chunk[16];
 #pragma unroll
         for (int q = 0; q < 16; ++q) chunk[q] = out[c * 16 + q];
@@ -485,14 +557,16 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
     griddep_wait();  // a_s and y belong to the stream's order
     float R[HB];     // fp32 running sums for this thread's weight row
     // per-group scales of this thread's row, walked with a pointer and
-    // prefetched one group ahead (the next tile's first one at a tile's end)
+    // prefetched one group ahead (the next tile's first one at a tile's end);
+    // the e4m3 form reads scale and zero point from the staged record instead
+    constexpr bool kScaleFromGlobal = C::kDrainPerGroup && !C::kFp8;
     const uint16_t* sp = nullptr;
     float s_next = 1.f;  // weight-only int8: no per-group scale (per-channel scale at the end)
     int mt = 0, nt = 0;
     if (n_items > 0) {
       unit_tile(0, mt, nt);
       sp = scale_ptr(nt, g0);
-      if constexpr (C::kDrainPerGroup) s_next = f16_bits_to_f32(__ldg(sp));
+      if constexpr (kScaleFromGlobal) s_next = f16_bits_to_f32(__ldg(sp));
     }
     bool ok = true;
     for (int k = 0; k < n_units && ok; ++k) {
@@ -502,7 +576,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
       const uint16_t* sp_tile = scale_ptr(nt, g0);
       // the next tile's first scale, fetched now and used after this tile
       float s_first_next = 0.f;
-      if (C::kDrainPerGroup && k + 1 < n_units) {
+      if (kScaleFromGlobal && k + 1 < n_units) {
         int mt2, nt2;
         unit_tile(k + 1, mt2, nt2);
         s_first_next = f16_bits_to_f32(__ldg(scale_ptr(nt2, g0)));
@@ -514,8 +588,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
         const int i = k * ng + gi;
         const int di = C::kDrainPerGroup ? i : k;
         const int db = di % kNumD;
-        const float s = s_next;
-        if constexpr (C::kDrainPerGroup)
+        float s = s_next;
+        if constexpr (kScaleFromGlobal)
           s_next = (gi + 1 < ng) ? f16_bits_to_f32(__ldg(sp_tile + (int64_t)(gi + 1) * 4256))
                                  : s_first_next;
         if (!mbar_wait(dfull_bar(db), (di / kNumD) & 1, abort_flag, tmo)) {
@@ -523,6 +597,66 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
           break;
         }
         tc_fence_after();
+        float nz = 0.f;
+        if constexpr (C::kFp8) {
+          // this group's scale and zero point from the staged record (the
+          // stage is not refilled before the drain warps release it; the
+          // full-barrier phase is checked so that the copy's bytes are
+          // visible here)
+          const int st = i % S;
+          if (!mbar_wait(full_bar(st), (i / S) & 1, abort_flag, tmo)) {
+            ok = false;
+            break;
+          }
+          const uint8_t* rec = stage_w_ptr(st);
+          s = f16_bits_to_f32(*reinterpret_cast<const uint16_t*>(rec + 8192 + 2 * r));
+          const uint32_t zb = rec[8448 + (r >> 1)];
+          nz = -(float)((r & 1) ? (zb >> 4) : (zb & 0xF));
+          __syncwarp();
+          if (lane == 0) mbar_arrive(empty_bar(st));
+        }
+        if constexpr (C::kFp8) {
+          // accumulator columns [0, BT): sum w * (a >> 4); [BT, 2BT): sum w * (a & 15);
+          // 8 columns per load keep the drain's registers in budget
+          constexpr int CW = 8;
+#pragma unroll
+          for (int cb = 0; cb < HB / CW; ++cb) {
+            asm volatile("" ::: "memory");  // keep the chunks' loads apart
+            uint32_t vh[16], vl[16];
+            const uint32_t src = d_tmem + lane_base + db * C::kDCols + col0 + cb * CW;
+            if constexpr (CW == 16) {
+              tmem_ld16(src, vh);
+              tmem_ld16(src + BT, vl);
+            } else {
+              tmem_ld8(src, vh);
+              tmem_ld8(src + BT, vl);
+            }
+            // the tokens' group sums (the same for every row: L1 hits), read
+            // while the loads are in flight; tokens past M read the last row
+            // (their columns are never stored)
+            float asf[CW];
+            {
+              const int32_t* asum_g = p.a_gsum + (g0 + gi);
+              const int mfirst = (int)(m0 + col0) + cb * CW, mlast = (int)(p.M - 1);
+#pragma unroll
+              for (int q = 0; q < CW; ++q) asf[q] = (float)__ldg(asum_g + min(mfirst + q, mlast) * G);
+            }
+            tmem_wait_ld();
+#pragma unroll
+            for (int q = 0; q < CW; ++q) {
+              const int t = cb * CW + q;
+              // integers below 2^24, so exact: P = sum a*w, Q = P - z*sum(a)
+              const float P = fmaf(16.f, __uint_as_float(vh[q]), __uint_as_float(vl[q]));
+              const float Q = fmaf(nz, asf[q], P);
+              if constexpr (PARTIALS) {
+                const int64_t m = m0 + col0 + t;
+                if (m < p.M) p.partials[(m * N + n) * G + g0 + gi] = __float2int_rn(Q);
+              } else {
+                R[t] = fmaf(s, Q, R[t]);
+              }
+            }
+          }
+        } else {
         constexpr int CW = HB < 16 ? HB : 16;       // columns per tcgen05.ld
         // loads in flight per wait (one at HB = 64, where the 64 accumulators
         // leave no room for a second 16-column buffer)
@@ -576,6 +710,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
             }
           }
         }
+        }  // kind::f16 drain
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(dempty_bar(db));
@@ -690,6 +825,22 @@ static bool make_act_map_3d(CUtensorMap* map, CUtensorMapDataType dt, const void
   return r == CUDA_SUCCESS;
 }
 
+// The two e4m3 activation planes [2][rows][cols] bytes as a 3-D map {cols,
+// rows, 2}; a box {128, box_rows, 2} lands as [2][box_rows][128] swizzled.
+static bool make_act_map_planes(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols,
+                                int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, 2};
+  cuuint64_t strides[2] = {(cuuint64_t)cols, (cuuint64_t)(rows * cols)};
+  cuuint32_t box[3] = {128, (cuuint32_t)box_rows, 2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 static int tc_sm_count() {
   static int count = 0;
   if (!count) {
@@ -743,12 +894,17 @@ static cudaError_t launch_tc(const GemmArgs& a, cudaStream_t st) {
   using C = TcCfg<VARIANT, BT>;
   CUtensorMap act_map, w8_map;
   memset(&w8_map, 0, sizeof(w8_map));
-  const void* act_ptr = (VARIANT == kW4A8) ? (const void*)a.a_q16 : (const void*)a.x;
+  const void* act_ptr = (VARIANT == kW4A8) ? (const void*)a.a_tc : (const void*)a.x;
   const CUtensorMapDataType adt =
       (VARIANT == kW4A8) ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  int act3d = make_act_map_3d(&act_map, adt, act_ptr, a.M, a.K, BT) ? 1 : 0;
-  if (!act3d && !make_map(&act_map, adt, 2, act_ptr, a.M, a.K, 64, BT))
-    return cudaErrorInvalidValue;
+  int act3d = 0;
+  if constexpr (C::kFp8) {
+    if (!make_act_map_planes(&act_map, act_ptr, a.M, a.K, BT)) return cudaErrorInvalidValue;
+  } else {
+    act3d = make_act_map_3d(&act_map, adt, act_ptr, a.M, a.K, BT) ? 1 : 0;
+    if (!act3d && !make_map(&act_map, adt, 2, act_ptr, a.M, a.K, 64, BT))
+      return cudaErrorInvalidValue;
+  }
   if (VARIANT == kW8A16) {
     if (!make_map(&w8_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.w8, a.N, a.K, 128, 128))
       return cudaErrorInvalidValue;
@@ -776,6 +932,7 @@ static cudaError_t launch_tc(const GemmArgs& a, cudaStream_t st) {
                                     (double)128 * a.K / ((VARIANT == kW8A16) ? 1.0 : 2.0))
                       : 1;
   p.a_s = a.a_s;
+  p.a_gsum = a.a_gsum;
   p.packed = a.packed;
   p.s8 = a.s8;
   p.y = a.y;
