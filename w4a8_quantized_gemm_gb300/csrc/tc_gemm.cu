@@ -38,12 +38,13 @@
 //               TMEM (small tiles: a second set, warps 12-15, takes every
 //               other group)
 //   next warp   TMA producer (activations tile + weight record per group)
-//   last warp   TMEM allocator and single-thread MMA issuer
+//   last warps  MMA issuers, one thread each (two for token tiles of at most
+//               32, taking alternate groups); the first allocates TMEM
 // (a warp reaches TMEM lanes 32*(warp % 4) .. +31, so each role that touches
 // TMEM is a whole warpgroup)
 // Hand-offs, all on mbarriers with bounded waits: S shared-memory stages,
 // kNumA TMEM A buffers, kNumD TMEM accumulators. Every barrier test is a
-// round trip of about a hundred cycles on the waiting thread, so the MMA
+// round trip of about a hundred cycles on the waiting thread, so an MMA
 // issuer waits on one barrier per group: the converters arrive on it only
 // after the stage has landed, the A buffer is free and the accumulator has
 // been drained.
@@ -82,16 +83,6 @@ struct TcParams {
 
 template <int VARIANT, int BT>
 struct TcCfg {
-  // TMEM: kNumD accumulators of BT columns + kNumA A-operand buffers of 64
-  // columns. Small token tiles leave room for deeper buffering, which lets the
-  // converters run several groups ahead of the MMAs and the MMAs several
-  // groups ahead of the drain.
-  // Small token tiles split a group's 8 dependent MMAs over kChains
-  // independent accumulators (k-step j feeds chain j % kChains): a small-N
-  // MMA is short, so a chain of dependent ones is latency-bound, while
-  // independent ones overlap. The drain adds the chains (integers below 2^24:
-  // the sum stays exact).
-  //
   // W4A8 with token tiles of at most 64 runs kind::f8f6f4: an MMA costs the
   // same issue time for any N up to 64 (and K = 32 e4m3 per instruction
   // against K = 16 fp16), so the activation codes a = 16 * (a >> 4) + (a & 15)
@@ -99,11 +90,20 @@ struct TcCfg {
   // 0..15 as exact e4m3; a group takes 4 MMAs instead of 8, and the zero
   // points come off in the drain as z * sum(a).
   static constexpr bool kFp8 = (VARIANT == kW4A8) && BT <= kTcFp8MaxM;
-  static constexpr int kChains = kFp8 ? 1 : (BT == 16 ? 4 : (BT == 32 ? 2 : 1));
-  static constexpr int kDCols = kFp8 ? 2 * BT : kChains * BT;  // columns of one accumulator
-  static constexpr int kACols = kFp8 ? 32 : 64;  // A operand columns of one group
-  static constexpr int kMmaK = kFp8 ? 32 : 16;   // K per MMA
-  static constexpr int kNumD = (kFp8 && BT == 64) ? 2 : (BT <= 64 ? 4 : 2);
+  static constexpr int kDCols = kFp8 ? 2 * BT : BT;  // TMEM columns of one accumulator
+  static constexpr int kACols = kFp8 ? 32 : 64;      // A operand columns of one group
+  static constexpr int kMmaK = kFp8 ? 32 : 16;       // K per MMA
+  static constexpr bool kDrainPerGroup = (VARIANT != kW8A16);
+  // MMA issuers. An MMA instruction up to N = 64 costs its issuing thread
+  // about as much as the tensor core, and every barrier test costs it a
+  // round trip, so small token tiles use two issuing warps that take
+  // alternate groups. W8A16 accumulates a whole tile in one accumulator and
+  // keeps one issuer, which orders those MMAs.
+  static constexpr int kMmaWarps = (kDrainPerGroup && BT <= 32) ? 2 : 1;
+  // TMEM: kNumD accumulators of kDCols columns + kNumA A-operand buffers of
+  // kACols columns (deep for small tiles: the converters run ahead of the
+  // MMAs and the MMAs ahead of the drain).
+  static constexpr int kNumD = kFp8 ? (BT == 16 ? 8 : (BT == 32 ? 4 : 2)) : (BT <= 64 ? 4 : 2);
   static constexpr int kNumA = kFp8 ? 8 : 4;
   static constexpr int kActBox = BT * 128;                        // one 64-wide K box, bytes
   static constexpr int kActBytes = 2 * kActBox;                   // a 128-wide group
@@ -120,7 +120,7 @@ struct TcCfg {
   static constexpr int kStageCap = BT <= 32 ? 16 : 8;
   static constexpr int kStages = kStagesRaw > kStageCap ? kStageCap : kStagesRaw;
   static constexpr int kBarOffset = kStages * kStageBytes;
-  static constexpr int kSmemBytes = kBarOffset + 512 + 1024;     // + barriers + alignment slack
+  static constexpr int kSmemBytes = kBarOffset + 1024 + 1024;    // + barriers + alignment slack
   static constexpr int kTmemColsRaw = kNumD * kDCols + kNumA * kACols;
   static constexpr int kTmemCols = kTmemColsRaw <= 32    ? 32
                                    : kTmemColsRaw <= 64  ? 64
@@ -132,14 +132,16 @@ struct TcCfg {
   // (each set's store-to-arrive latency overlaps the other's conversion).
   static constexpr int kConvSets = BT <= 32 ? 2 : 1;
   static constexpr int kProducerWarp = kConvWarp0 + 4 * kConvSets;
-  static constexpr int kMmaWarp = kProducerWarp + 1;
-  static constexpr int kThreads = 32 * (kMmaWarp + 1);
-  static constexpr bool kDrainPerGroup = (VARIANT != kW8A16);
+  static constexpr int kMmaWarp = kProducerWarp + 1;  // first issuer; allocates TMEM
+  static constexpr int kThreads = 32 * (kMmaWarp + kMmaWarps);
   static constexpr int kBf16 = (VARIANT == kW4A8) ? 0 : 1;
   static_assert(kStages >= 2, "shared memory too small for two stages");
+  static_assert(kSmemBytes <= kMaxSmem, "shared memory");
   static_assert(kTmemColsRaw <= 512, "TMEM budget");
-  static_assert(8 * (2 * kStages + kNumA + 2 * kNumD) + 8 <= 512, "barrier region");
-  static_assert(kStages >= kNumA, "A-buffer reuse is tracked through the stage barriers");
+  // a converter set reuses only its own A buffers and accumulators, so every
+  // reuse wait follows that set's previous one in program order
+  static_assert(kNumA % kConvSets == 0 && kNumD % kConvSets == 0, "per-set buffer reuse");
+  static_assert(8 * (2 * kStages + 2 * kNumA + 2 * kNumD + kMmaWarps) + 8 <= 1024, "barrier region");
   static_assert(BT % 16 == 0 && BT >= 16 && BT <= 128, "token tile");
   static_assert(kStageBytes % 1024 == 0, "stage alignment");
 };
@@ -228,9 +230,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
   auto afull_bar = [&](int i) { return bar0 + 8u * (2 * S + i); };
-  auto dfull_bar = [&](int i) { return bar0 + 8u * (2 * S + kNumA + i); };
-  auto dempty_bar = [&](int i) { return bar0 + 8u * (2 * S + kNumA + kNumD + i); };
-  uint8_t* misc = smem + C::kBarOffset + 8 * (2 * S + kNumA + 2 * kNumD);
+  auto aempty_bar = [&](int i) { return bar0 + 8u * (2 * S + kNumA + i); };
+  auto dfull_bar = [&](int i) { return bar0 + 8u * (2 * S + 2 * kNumA + i); };
+  auto dempty_bar = [&](int i) { return bar0 + 8u * (2 * S + 2 * kNumA + kNumD + i); };
+  // one per issuer: its final commit, waited on before teardown
+  auto fin_bar = [&](int i) { return bar0 + 8u * (2 * S + 2 * kNumA + 2 * kNumD + i); };
+  uint8_t* misc = smem + C::kBarOffset + 8 * (2 * S + 2 * kNumA + 2 * kNumD + C::kMmaWarps);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
   auto stage_act = [&](int s) { return base + (uint32_t)(s * C::kStageBytes); };
@@ -246,11 +251,13 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
     }
     for (int i = 0; i < kNumA; ++i) {
       mbar_init(afull_bar(i), 4);
+      mbar_init(aempty_bar(i), 1);
     }
     for (int i = 0; i < kNumD; ++i) {
       mbar_init(dfull_bar(i), 1);
       mbar_init(dempty_bar(i), 8);
     }
+    for (int i = 0; i < C::kMmaWarps; ++i) mbar_init(fin_bar(i), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -350,15 +357,17 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
       cluster_sync_all();
       cluster_sync_all();
     }
-  } else if (warp == C::kMmaWarp) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp >= C::kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuers
+    // issuer q takes groups q, q + kMmaWarps, ...
+    const int q = warp - C::kMmaWarp;
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_f16(128, C::kFp8 ? 2 * BT : BT, C::kBf16);
-      int last = -1;
-      int gi = 0, ti = 0;  // group index inside the tile, tile counter
-      for (int i = 0; i < n_items; ++i, gi = (gi + 1 == ng) ? (++ti, 0) : gi + 1) {
+      bool any = false;
+      for (int i = q; i < n_items; i += C::kMmaWarps) {
         const int s = i % S, ab = i % kNumA;
-        const int di = C::kDrainPerGroup ? i : ti;
+        const int gi = i % ng;
+        const int di = C::kDrainPerGroup ? i : i / ng;
         const int db = di % kNumD;
         // one wait per group: the converters arrive on afull only once the
         // stage has landed, the A buffer is free and the accumulator drained
@@ -375,25 +384,28 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const uint32_t b_addr = stage_act(s) + (j >> 2) * C::kActBox + (j & 3) * 32;
-            constexpr int CH = C::kChains;
-            const uint32_t acc = C::kDrainPerGroup ? (j >= CH) : (gi > 0 || j >= CH);
-            tc_mma_f16_ts(d_tmem + db * C::kDCols + (j % CH) * BT, a_tmem + ab * 64 + j * 8,
+            const uint32_t acc = C::kDrainPerGroup ? (j > 0) : (gi > 0 || j > 0);
+            tc_mma_f16_ts(d_tmem + db * C::kDCols, a_tmem + ab * 64 + j * 8,
                           sdesc_kmajor_sw128(b_addr), idesc, acc);
           }
         }
-        tc_commit(empty_bar(s));  // also frees A buffer ab (converters watch it)
+        tc_commit(empty_bar(s));
+        tc_commit(aempty_bar(ab));
         if (C::kDrainPerGroup || gi == ng - 1) tc_commit(dfull_bar(db));
-        last = i;
+        any = true;
       }
-      if (last >= 0) {  // let the last MMAs finish before teardown
+      if (any) {  // let this issuer's MMAs finish before teardown
+        tc_commit(fin_bar(q));
         volatile int no_abort = 0;
-        mbar_wait(empty_bar(last % S), (last / S) & 1, &no_abort, tmo);
+        mbar_wait(fin_bar(q), 0, &no_abort, tmo);
       }
     }
     __syncwarp();
     teardown_sync();
-    tc_fence_after();
-    tmem_dealloc(tmem, C::kTmemCols);
+    if (warp == C::kMmaWarp) {
+      tc_fence_after();
+      tmem_dealloc(tmem, C::kTmemCols);
+    }
     if (cluster_reduce) {
       cluster_sync_all();
       cluster_sync_all();
@@ -510,14 +522,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
           }
         }
       }
-      // A buffer ab is free once the MMAs of item i - kNumA have completed,
-      // i.e. once stage (i - kNumA) % S has been released for that item
-      // (kStages >= kNumA, so that phase can be neither lapped nor pending
-      // behind an older one here)
-      if (i >= kNumA) {
-        const int j = i - kNumA;
-        if (!mbar_wait(empty_bar(j % S), (j / S) & 1, abort_flag, tmo)) break;
-      }
+      // A buffer ab is free once the MMAs of item i - kNumA have completed
+      if (!mbar_wait(aempty_bar(ab), ((i / kNumA) & 1) ^ 1, abort_flag, tmo)) break;
       // the accumulator this item feeds must have been drained; one warp of
       // the set waits (afull completes only with all four arrivals)
       if (((warp - kConvWarp0) & 3) == 0) {
@@ -669,28 +675,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
             const uint32_t src = d_tmem + lane_base + db * C::kDCols + col0 + (cb + q2) * CW;
             if constexpr (CW == 16) tmem_ld16(src, v[q2]);
             else tmem_ld8(src, v[q2]);
-          }
-          if constexpr (C::kChains > 1) {
-            // the other accumulation chains of the same columns
-            uint32_t w[C::kChains - 1][PAIR][16];
-#pragma unroll
-            for (int ch = 1; ch < C::kChains; ++ch)
-#pragma unroll
-              for (int q2 = 0; q2 < PAIR; ++q2) {
-                const uint32_t src =
-                    d_tmem + lane_base + db * C::kDCols + ch * BT + col0 + (cb + q2) * CW;
-                if constexpr (CW == 16) tmem_ld16(src, w[ch - 1][q2]);
-                else tmem_ld8(src, w[ch - 1][q2]);
-              }
-            tmem_wait_ld();
-#pragma unroll
-            for (int ch = 1; ch < C::kChains; ++ch)
-#pragma unroll
-              for (int q2 = 0; q2 < PAIR; ++q2)
-#pragma unroll
-                for (int q = 0; q < CW; ++q)
-                  v[q2][q] = __float_as_uint(__uint_as_float(v[q2][q]) +
-                                             __uint_as_float(w[ch - 1][q2][q]));
           }
           tmem_wait_ld();
 #pragma unroll
