@@ -105,6 +105,48 @@ def load_peaks():
             "source": "fallback"}
 
 
+def kernel_sources_hash() -> str:
+    """sha256 over the CUDA sources and the public header (names and bytes)."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "w4a8_quantized_gemm_gb300", "csrc")
+    files = sorted(os.path.join(csrc, f) for f in os.listdir(csrc)
+                   if f.endswith((".cu", ".cuh", ".h")))
+    files.append(os.path.join(ROOT, "include", "egopq.h"))
+    for f in files:
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def config_key(args) -> str:
+    return (f"{args.workload}|path={args.path}|fused={int(args.fused)}|api={args.api}|"
+            f"m={args.m}|k={args.k}|n={args.n}|variant={args.variant}")
+
+
+def measured_traffic(args, kernel_label: str):
+    """DRAM bytes per launch of `kernel_label` on this configuration, from the
+    ncu capture summarised in profiles/dram_traffic.txt, or None when there is
+    none or the kernels changed since it was taken (source hash mismatch)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    want_hash, key = None, config_key(args)
+    with open(path) as f:
+        for line in f:
+            line = line.strip()
+            if line.startswith("sources_sha256="):
+                want_hash = line.split("=", 1)[1]
+            elif line.startswith("config=") and want_hash is not None:
+                fields = dict(kv.split("=", 1) for kv in line.split("\t"))
+                if fields["config"] == key and fields["kernel"] == kernel_label:
+                    if want_hash != kernel_sources_hash():
+                        return None
+                    return float(fields["bytes_per_launch"])
+    return None
+
+
 # ------------------------------------------------------------------ clocks ----
 
 class ClockSampler:
@@ -483,7 +525,8 @@ def run_ours(args, rank, world):
         achieved = dom["bytes"] / (dom["ms"] * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / peaks["hbm_gbs"]}
-    roof.update({"kernel": dom_name, "traffic": None, "peak_source": peaks["source"],
+    roof.update({"kernel": dom_name, "traffic": measured_traffic(args, dom_name),
+                 "peak_source": peaks["source"],
                  "avg_launch_us": dom["ms"] * 1e3 / dom["launches"]})
 
     # ---- end to end through the API: each step copies its activations from
