@@ -598,8 +598,8 @@ def run_ours(args, rank, world):
     return result
 
 
-def workload_config(args, wl, per_step_bytes, per_step_ops):
-    cfg = {"workload": {
+def workload_description(args) -> str:
+    return {
         "decode": "decode GEMV sweep: Qwen2.5-7B q,k,v,o,gate,up,down (K=3584/18944), "
                   "M in {1,4,16}, int4 asym group 128, per-token int8 activations",
         "prefill": "prefill W4A8 GEMM: the seven 7B linears + untied head (N=152064), "
@@ -608,7 +608,11 @@ def workload_config(args, wl, per_step_bytes, per_step_ops):
         "dit": "weight-only W4A16 and W8A16 on DiT blocks K=3072/12288, M in {1,16,4096}",
         "tiny": "tiny W4A8: M=16, K=512, N=256",
         "linear": f"one W4A8 linear K={args.k} N={args.n} at M={args.m}",
-    }[args.workload]}
+    }[args.workload]
+
+
+def workload_config(args, wl, per_step_bytes, per_step_ops):
+    cfg = {"workload": workload_description(args)}
     cfg.update({"layer_copies": wl.n_copies, "bytes_per_step": per_step_bytes,
                 "int_ops_per_step": per_step_ops,
                 "l2_defeat": "weights rotated across layer copies larger than L2"
@@ -629,19 +633,21 @@ def cpu_baseline(args, wl, unit_is_ops, budget_s=20.0):
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
     oracle.build()
     done_units, elapsed, samples = 0, 0.0, []
-    ops = wl.step_ops(0)
+    ops = [op for op in wl.step_ops(0) if op[1] != "quant"]
+    # bounded sample: at most 8 rows of each linear and as many columns as
+    # make one call last about target_s (the column count adapts to the
+    # measured speed of the previous call); passes over the step's linears
+    # until the budget is spent
+    target_s = max(0.05, budget_s / (2 * max(1, len(ops))))
+    ops_per_s = 2e9  # first guess, corrected after every call
     i = 0
-    while elapsed < budget_s and i < 10 * len(ops):
+    while elapsed < budget_s or not samples:
         op = ops[i % len(ops)]
         i += 1
         label, kind, M, N, K = op[0], op[1], op[2], op[3], op[4]
-        if kind == "quant":
-            continue
-        # bounded sample: at most 8 rows and as many columns as fit ~2 s
         m = min(M, 8)
-        n = min(N, max(128, int(2e9 / max(1, 2 * m * K * 4))))
-        n = (n // 128) * 128 or 128
-        G = K // G128
+        n = int(target_s * ops_per_s / max(1, 2 * m * K))
+        n = min(N, max(128, (n // 128) * 128))
         w = synth.w4_weights(1, 0, 0, n, K)
         x = synth.activations(1, 0, 0, m, K)
         t0 = time.perf_counter()
@@ -657,6 +663,7 @@ def cpu_baseline(args, wl, unit_is_ops, budget_s=20.0):
             oracle.w8a16(x, w8, s8)
             units = w8a16_bytes(m, n, K)
         dt = time.perf_counter() - t0
+        ops_per_s = 2 * m * n * K / max(dt, 1e-6)
         elapsed += dt
         done_units += units
         samples.append(f"{label}: {m}x{n}x{K}")
@@ -664,7 +671,8 @@ def cpu_baseline(args, wl, unit_is_ops, budget_s=20.0):
     return {"value": round(value, 5), "unit": "TOPS" if unit_is_ops else "GB/s", "cores": cores,
             "kind": "oracle", "seconds": round(elapsed, 2),
             "sample": f"{len(samples)} oracle GEMMs on row/column subsets of the step's linears "
-                      f"(<=8 tokens, columns sized to ~2 s each): " + "; ".join(samples[:8])
+                      f"(<=8 tokens, columns sized to at most ~{target_s:.2f} s a call): "
+                      + "; ".join(samples[:8])
                       + ("; ..." if len(samples) > 8 else "")}
 
 
@@ -688,9 +696,13 @@ def run_reference(args, rank, world):
     kind = "w4a16" if args.workload == "dit" else "w4a8"
     wl.step_ops = lambda c: [(f"M={M} K={K} N={N}", kind, M, N, K, 0, 0, None)
                              for (M, K, N) in shapes]
-    per_step_budget = max(2.0, args.cpu_budget / max(1, args.steps))
+    # each step a bounded sample of the workload, sized so that the whole
+    # warm-up + timed run stays within about two minutes
+    per_step_s = min(5.0, max(0.05, 120.0 / max(1, args.steps + args.warmup)))
+    if args.warmup > 0:
+        cpu_baseline(args, wl, unit_is_ops, budget_s=per_step_s * args.warmup)  # warm-up
     t0 = time.perf_counter()
-    base = cpu_baseline(args, wl, unit_is_ops, budget_s=per_step_budget * args.steps)
+    base = cpu_baseline(args, wl, unit_is_ops, budget_s=per_step_s * args.steps)
     wall = time.perf_counter() - t0
     return {
         "impl": "reference",
@@ -706,7 +718,8 @@ def run_reference(args, rank, world):
         "vs_baseline": None,
         "dtype": "int64 / fp64 (oracle)",
         "data": "synthetic (seeded splitmix64/Box-Muller; 7B/DiT shapes, random weights)",
-        "config": {"workload": args.workload, "arm": "CPU oracle on a bounded sample"},
+        "config": {"workload": workload_description(args),
+                   "arm": "CPU oracle on a bounded sample of each step"},
         "cpu_baseline": base,
         "e2e": {"value": base["value"], "unit": base["unit"], "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
