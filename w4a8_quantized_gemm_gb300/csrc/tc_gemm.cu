@@ -31,15 +31,16 @@
 // points), convert the codes and store them straight into TMEM with
 // tcgen05.st.
 //
-// Warp roles (one CTA per SM):
-//   warps 0-7   drain: TMEM accumulator -> registers, *s, accumulate, epilogue;
-//               warps 0-3 own token columns [0, BT/2), warps 4-7 [BT/2, BT)
-//   warps 8-11  convert: packed int4 (or int8) smem tile -> e4m3/fp16/bf16 in
-//               TMEM (small tiles: a second set, warps 12-15, takes every
-//               other group)
-//   next warp   TMA producer (activations tile + weight record per group)
-//   last warps  MMA issuers, one thread each (two for token tiles of at most
-//               32, taking alternate groups); the first allocates TMEM
+// Warp roles (one CTA per SM; two lean CTAs per SM for 16-token e4m3 tiles):
+//   drain warps      TMEM accumulator -> registers, *s, accumulate, epilogue;
+//                    two warpgroups splitting the token columns (one warpgroup
+//                    with all of them in the lean CTAs)
+//   converter warps  packed int4 (or int8) smem tile -> e4m3/fp16/bf16 in TMEM
+//                    (a second set of four takes every other group for token
+//                    tiles of 32 and the non-lean 16)
+//   producer warp    TMA: activations tile + weight record per group
+//   issuer warps     one MMA-issuing thread each (two for 32-token tiles,
+//                    taking alternate groups); the first allocates TMEM
 // (a warp reaches TMEM lanes 32*(warp % 4) .. +31, so each role that touches
 // TMEM is a whole warpgroup)
 // Hand-offs, all on mbarriers with bounded waits: S shared-memory stages,
@@ -62,8 +63,8 @@
 
 namespace egopq {
 
-constexpr int kConvWarp0 = 8;  // warps 0-7 drain, then the converter warps
-constexpr int kMaxSmem = 232448;
+constexpr int kMaxSmem = 232448;      // dynamic shared memory of a CTA alone on its SM
+constexpr int kMaxSmemHalf = 114688;  // each of two CTAs sharing an SM
 
 struct TcParams {
   int64_t M, N, K;
@@ -99,12 +100,21 @@ struct TcCfg {
   // round trip, so small token tiles use two issuing warps that take
   // alternate groups. W8A16 accumulates a whole tile in one accumulator and
   // keeps one issuer, which orders those MMAs.
-  static constexpr int kMmaWarps = (kDrainPerGroup && BT <= 32) ? 2 : 1;
+  // 16-token e4m3 tiles run two lean CTAs per SM (one drain warpgroup, one
+  // converter set, one issuer each, half the shared memory and TMEM): their
+  // per-group hand-off chain is latency-bound, so two independent pipelines
+  // per SM carry twice the groups.
+  static constexpr bool kLean = kFp8 && BT == 16;
+  static constexpr int kCtasPerSm = kLean ? 2 : 1;
+  static constexpr int kDrainWGs = kLean ? 1 : 2;
+  static constexpr int kConvWarp0 = 4 * kDrainWGs;  // drain warps first
+  static constexpr int kMmaWarps = kLean ? 1 : ((kDrainPerGroup && BT <= 32) ? 2 : 1);
   // TMEM: kNumD accumulators of kDCols columns + kNumA A-operand buffers of
   // kACols columns (deep for small tiles: the converters run ahead of the
   // MMAs and the MMAs ahead of the drain).
-  static constexpr int kNumD = kFp8 ? (BT == 16 ? 8 : (BT == 32 ? 4 : 2)) : (BT <= 64 ? 4 : 2);
-  static constexpr int kNumA = kFp8 ? 8 : 4;
+  static constexpr int kNumD =
+      kLean ? 4 : (kFp8 ? (BT == 32 ? 4 : 2) : (BT <= 64 ? 4 : 2));
+  static constexpr int kNumA = kLean ? 4 : (kFp8 ? 8 : 4);
   static constexpr int kActBox = BT * 128;                        // one 64-wide K box, bytes
   static constexpr int kActBytes = 2 * kActBox;                   // a 128-wide group
   // weights of one group: the int8 tile, or one packed int4 record (8192 B of
@@ -114,7 +124,8 @@ struct TcCfg {
   static constexpr int kWBytes = (VARIANT == kW8A16) ? 16384 : 9216;
   static constexpr int kStageBytes = kActBytes + kWBytes;        // multiple of 1024
   static constexpr int kTxBytes = kActBytes + kWCopyBytes;
-  static constexpr int kStagesRaw = (kMaxSmem - 2048) / kStageBytes;
+  static constexpr int kSmemLimit = kCtasPerSm == 1 ? kMaxSmem : kMaxSmemHalf;
+  static constexpr int kStagesRaw = (kSmemLimit - 3072) / kStageBytes;
   // deep rings for small token tiles (decode streams weights: bytes in flight
   // hide HBM latency); larger tiles are bounded by shared memory
   static constexpr int kStageCap = BT <= 32 ? 16 : 8;
@@ -130,13 +141,15 @@ struct TcCfg {
   // Converter warp sets: with small token tiles the MMA and drain per group are
   // short, so a second set of four converter warps takes every other group
   // (each set's store-to-arrive latency overlaps the other's conversion).
-  static constexpr int kConvSets = BT <= 32 ? 2 : 1;
+  static constexpr int kConvSets = kLean ? 1 : (BT <= 32 ? 2 : 1);
+  static constexpr int kDrainCols = BT / kDrainWGs;  // token columns per drain thread
   static constexpr int kProducerWarp = kConvWarp0 + 4 * kConvSets;
   static constexpr int kMmaWarp = kProducerWarp + 1;  // first issuer; allocates TMEM
   static constexpr int kThreads = 32 * (kMmaWarp + kMmaWarps);
   static constexpr int kBf16 = (VARIANT == kW4A8) ? 0 : 1;
   static_assert(kStages >= 2, "shared memory too small for two stages");
-  static_assert(kSmemBytes <= kMaxSmem, "shared memory");
+  static_assert(kSmemBytes <= kSmemLimit, "shared memory");
+  static_assert(!kLean || kTmemCols <= 256, "two CTAs share the SM's TMEM");
   static_assert(kTmemColsRaw <= 512, "TMEM budget");
   // a converter set reuses only its own A buffers and accumulators, so every
   // reuse wait follows that set's previous one in program order
@@ -169,13 +182,14 @@ __device__ __forceinline__ void store_row(const float (&R)[HB], const TcParams& 
 }
 
 template <int VARIANT, int BT, bool PARTIALS>
-__global__ void __launch_bounds__(TcCfg<VARIANT, BT>::kThreads, 1)
+__global__ void __launch_bounds__(TcCfg<VARIANT, BT>::kThreads, TcCfg<VARIANT, BT>::kCtasPerSm)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
                const __grid_constant__ CUtensorMap w8_map, const TcParams p) {
   using C = TcCfg<VARIANT, BT>;
   constexpr int S = C::kStages;
-  constexpr int HB = BT / 2;  // token columns per drain warpgroup
+  constexpr int HB = C::kDrainCols;  // token columns per drain thread
   constexpr int kNumA = C::kNumA, kNumD = C::kNumD;
+  constexpr int kConvWarp0 = C::kConvWarp0;
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte alignment for the 128-byte-swizzle atoms
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -247,7 +261,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
       // released by the MMA commit and the 4 converter warps (and, in the
       // e4m3 form, the 8 drain warps, which read the record's scales and
       // zero points from the stage)
-      mbar_init(empty_bar(s), 1 + 4 + (C::kFp8 ? 8 : 0));
+      mbar_init(empty_bar(s), 1 + 4 + (C::kFp8 ? 4 * C::kDrainWGs : 0));
     }
     for (int i = 0; i < kNumA; ++i) {
       mbar_init(afull_bar(i), 4);
@@ -255,7 +269,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
     }
     for (int i = 0; i < kNumD; ++i) {
       mbar_init(dfull_bar(i), 1);
-      mbar_init(dempty_bar(i), 8);
+      mbar_init(dempty_bar(i), 4 * C::kDrainWGs);
     }
     for (int i = 0; i < C::kMmaWarps; ++i) mbar_init(fin_bar(i), 1);
     *abort_flag = 0;
@@ -551,7 +565,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
       cluster_sync_all();
     }
   } else {
-    // ------------------------------------------------------------ drain (warps 0-7)
+    // ------------------------------------------------------------ drain
     const int r = (warp & 3) * 32 + lane;
     const int col0 = (warp >> 2) * HB;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
@@ -898,7 +912,7 @@ static cudaError_t launch_tc(const GemmArgs& a, cudaStream_t st) {
   const int64_t n_tiles = a.N / 128;
   const int64_t tiles = m_tiles * n_tiles;
   if (m_tiles > 65535 || n_tiles > 65535 || tiles >= (1LL << 31)) return cudaErrorInvalidValue;
-  const int sms = tc_sm_count();
+  const int sms = tc_sm_count() * C::kCtasPerSm;  // CTA slots of one wave
   int ks = 1, persistent = 0;
   choose_split(tiles, G, sms, &ks, &persistent);
   TcParams p{};
