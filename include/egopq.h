@@ -52,7 +52,7 @@ typedef enum {
   EGOPQ_ERR_TIMEOUT = -6            /* a kernel's bounded wait expired */
 } egopq_status;
 
-/* Kernel path. AUTO picks by M (W4A8: CUDA-core GEMV for M <= 8, the tcgen05
+/* Kernel path. AUTO picks by M (W4A8: CUDA-core GEMV for M <= 4, the tcgen05
  * tensor-core GEMM otherwise; W4A16 and W8A16: tensor-core GEMM); the others force one path for tests and
  * benchmarks. The choice is always this explicit argument, never global or
  * environment state ("The 4-bit CPU path", section "Why the path choice is a

@@ -398,7 +398,7 @@ def test_w4a8_linear_equals_quant_then_gemm(path, M):
     packed = eg.pack_w4(*dev_weights(w))
     xd = to_dev(x, torch.bfloat16)
     y1 = eg.w4a8_linear(xd, packed, N, path=path)
-    two_step_path = path if path != eg.PATH_AUTO else (eg.PATH_GEMV if M <= 8 else eg.PATH_TC)
+    two_step_path = path if path != eg.PATH_AUTO else (eg.PATH_GEMV if M <= eg.GEMV_AUTO_MAX_M else eg.PATH_TC)
     y2 = eg.w4a8_gemm(eg.quant_act(xd), packed, N, K, path=two_step_path)
     assert torch.equal(y1, y2)
     a_q, a_s, _ = oracle.quant_act(x)

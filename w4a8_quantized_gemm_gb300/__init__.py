@@ -165,6 +165,8 @@ class QuantAct(NamedTuple):
 
 # token count up to which the tensor-core operand form is two e4m3 planes
 TC_FP8_MAX_M = 64
+# largest W4A8 token count the AUTO path sends to the CUDA-core GEMV
+GEMV_AUTO_MAX_M = 4
 
 
 def tc_operand(M: int, K: int, device) -> torch.Tensor:

@@ -56,6 +56,6 @@ constexpr int kTcFp8MaxM = 64;
 // Largest M per W4A8 GEMV launch (larger M run as several launches).
 constexpr int kGemvMaxRows = 16;
 // AUTO path: W4A8 batches up to this many tokens take the GEMV.
-constexpr int kGemvAutoMaxM = 8;
+constexpr int kGemvAutoMaxM = 4;
 
 }  // namespace egopq

@@ -108,7 +108,8 @@ struct TcCfg {
   static constexpr int kCtasPerSm = kLean ? 2 : 1;
   static constexpr int kDrainWGs = kLean ? 1 : 2;
   static constexpr int kConvWarp0 = 4 * kDrainWGs;  // drain warps first
-  static constexpr int kMmaWarps = kLean ? 1 : ((kDrainPerGroup && BT <= 32) ? 2 : 1);
+  static constexpr int kMmaWarps =
+      kLean ? 1 : ((kDrainPerGroup && (BT <= 32 || BT == 128)) ? 2 : 1);
   // TMEM: kNumD accumulators of kDCols columns + kNumA A-operand buffers of
   // kACols columns (deep for small tiles: the converters run ahead of the
   // MMAs and the MMAs ahead of the drain).
@@ -141,7 +142,8 @@ struct TcCfg {
   // Converter warp sets: with small token tiles the MMA and drain per group are
   // short, so a second set of four converter warps takes every other group
   // (each set's store-to-arrive latency overlaps the other's conversion).
-  static constexpr int kConvSets = kLean ? 1 : (BT <= 32 ? 2 : 1);
+  static constexpr int kConvSets =
+      kLean ? 1 : ((BT <= 32 || (BT == 128 && kDrainPerGroup)) ? 2 : 1);
   static constexpr int kDrainCols = BT / kDrainWGs;  // token columns per drain thread
   static constexpr int kProducerWarp = kConvWarp0 + 4 * kConvSets;
   static constexpr int kMmaWarp = kProducerWarp + 1;  // first issuer; allocates TMEM
@@ -677,7 +679,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
             }
           }
         } else {
-        constexpr int CW = HB < 16 ? HB : 16;       // columns per tcgen05.ld
+        // columns per tcgen05.ld (8 at 64 columns per thread: the 64 running
+        // sums leave room for no more at 96 registers)
+        constexpr int CW = HB < 16 ? HB : (HB >= 64 ? 8 : 16);
         // loads in flight per wait (one at HB = 64, where the 64 accumulators
         // leave no room for a second 16-column buffer)
         constexpr int PAIR = (HB / CW) >= 2 && HB < 64 ? 2 : 1;
