@@ -583,12 +583,14 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
     // the e4m3 form reads scale and zero point from the staged record instead
     constexpr bool kScaleFromGlobal = C::kDrainPerGroup && !C::kFp8;
     const uint16_t* sp = nullptr;
-    float s_next = 1.f;  // weight-only int8: no per-group scale (per-channel scale at the end)
+    // (kept as raw fp16 bits until used, so that the load's latency overlaps
+    // a whole group; W8A16 has no per-group scale: 1.0)
+    uint16_t s_next = 0x3C00;
     int mt = 0, nt = 0;
     if (n_items > 0) {
       unit_tile(0, mt, nt);
       sp = scale_ptr(nt, g0);
-      if constexpr (kScaleFromGlobal) s_next = f16_bits_to_f32(__ldg(sp));
+      if constexpr (kScaleFromGlobal) s_next = __ldg(sp);
     }
     bool ok = true;
     for (int k = 0; k < n_units && ok; ++k) {
@@ -597,11 +599,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
       const int64_t m0 = (int64_t)mt * BT;
       const uint16_t* sp_tile = scale_ptr(nt, g0);
       // the next tile's first scale, fetched now and used after this tile
-      float s_first_next = 0.f;
+      uint16_t s_first_next = 0;
       if (kScaleFromGlobal && k + 1 < n_units) {
         int mt2, nt2;
         unit_tile(k + 1, mt2, nt2);
-        s_first_next = f16_bits_to_f32(__ldg(scale_ptr(nt2, g0)));
+        s_first_next = __ldg(scale_ptr(nt2, g0));
       }
 #pragma unroll
       for (int t = 0; t < HB; ++t) R[t] = 0.f;
@@ -610,10 +612,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
         const int i = k * ng + gi;
         const int di = C::kDrainPerGroup ? i : k;
         const int db = di % kNumD;
-        float s = s_next;
+        float s = f16_bits_to_f32(s_next);
         if constexpr (kScaleFromGlobal)
-          s_next = (gi + 1 < ng) ? f16_bits_to_f32(__ldg(sp_tile + (int64_t)(gi + 1) * 4256))
-                                 : s_first_next;
+          s_next = (gi + 1 < ng) ? __ldg(sp_tile + (int64_t)(gi + 1) * 4256) : s_first_next;
         if (!mbar_wait(dfull_bar(db), (di / kNumD) & 1, abort_flag, tmo)) {
           ok = false;
           break;
