@@ -318,6 +318,33 @@ class Workload:
         elif name not in ("decode", "prefill", "tiny", "linear", "model"):
             raise ValueError(name)
         self.n_copies = 1 if name == "model" else len(self.layers)
+        self._pack_io()
+
+    def _pack_io(self):
+        """Place every bf16 activation input in one device buffer and every
+        output in another (views keep their shapes; sizes are multiples of 256
+        bytes, so each view stays 16-byte aligned), so that the end-to-end leg
+        moves each step's inputs and outputs with one copy each way."""
+        torch = self.torch
+
+        def pack(tensors):
+            total = sum(t.numel() for t in tensors)
+            buf = torch.empty((total,), dtype=torch.bfloat16, device=self.dev)
+            views, off = [], 0
+            for t in tensors:
+                v = buf[off:off + t.numel()].view(t.shape)
+                v.copy_(t)
+                views.append(v)
+                off += t.numel()
+            return buf, views
+
+        keys = list(self.acts.keys())
+        self.x_all, xs = pack([self.acts[k][1] for k in keys])
+        for k, v in zip(keys, xs):
+            self.acts[k] = (self.acts[k][0], v) + tuple(self.acts[k][2:])
+        ykeys = list(self.ys.keys())
+        self.y_all, yv = pack([self.ys[k] for k in ykeys])
+        self.ys = dict(zip(ykeys, yv))
 
     # one step's launches, as (label, kind, M, N, K, bytes, ops, fn)
     def step_ops(self, copy: int):
@@ -395,15 +422,13 @@ class Workload:
         return self._ws[key]
 
     def host_io(self):
-        """(host pinned inputs, device inputs, device outputs) for the e2e leg."""
+        """([(pinned host inputs, device inputs)], [(device outputs, pinned host
+        outputs)]) for the end-to-end leg: one buffer each way (see _pack_io)."""
         torch = self.torch
-        ins, outs = [], []
-        for key, val in self.acts.items():
-            xd = val[1]
-            ins.append((torch.empty(xd.shape, dtype=xd.dtype).pin_memory().copy_(xd.cpu()), xd))
-        for y in self.ys.values():
-            outs.append((y, torch.empty(y.shape, dtype=y.dtype).pin_memory()))
-        return ins, outs
+        x_host = torch.empty(self.x_all.shape, dtype=self.x_all.dtype).pin_memory()
+        x_host.copy_(self.x_all.cpu())
+        y_host = torch.empty(self.y_all.shape, dtype=self.y_all.dtype).pin_memory()
+        return [(x_host, self.x_all)], [(self.y_all, y_host)]
 
 
 def _to_dev(torch, a, dev, dt=None):

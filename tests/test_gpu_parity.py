@@ -367,6 +367,23 @@ def test_w4a8_persistent_grid_full(n_tiles):
     assert np.array_equal(Q[rows], oracle.group_partials(a_q[rows], w.w_q, w.zero))
 
 
+@pytest.mark.parametrize("per_sm", [(2, 0), (2, 1), (3, 0)])
+def test_w4a8_persistent_grid_small_token_tile(per_sm):
+    """Token tiles of 16 (e4m3 form) run two CTAs per SM, so their grid goes
+    persistent from two tiles per SM on: tile counts of exactly two per SM, one
+    more, and three per SM, with a ragged token count (13 of 16)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    n_tiles = per_sm[0] * sms + per_sm[1]
+    M, K, N = 13, 256, 128 * n_tiles
+    x, w = w4_case(10, M, N, K)
+    a, packed, y = run_w4a8(x, w, eg.PATH_TC, M, N, K)
+    a_q, a_s, _ = oracle.quant_act(x)
+    _, y_ref = oracle.w4a8(a_q, a_s, w.w_q, w.scale_f16, w.zero)
+    check_bf16_output(to_host_bits(y), y_ref, f"persistent 16-token tiles n_tiles={n_tiles}")
+    Q = eg.w4a8_group_partials(a, packed, N, K, path=eg.PATH_TC).cpu().numpy()
+    assert np.array_equal(Q, oracle.group_partials(a_q, w.w_q, w.zero))
+
+
 @pytest.mark.parametrize("variant", ["w4a16", "w8a16"])
 def test_weight_only_persistent_grid_full(variant):
     M, K, N = 256, 384, 128 * 76
