@@ -443,8 +443,10 @@ def kernel_label(eg, kind, M, path):
     if kind == "quant":
         return "quant_act_kernel"
     if kind == "w4a8":
-        gemv = path == eg.PATH_GEMV or (path == eg.PATH_AUTO and M <= 8)
+        gemv = path == eg.PATH_GEMV or (path == eg.PATH_AUTO and M <= eg.GEMV_AUTO_MAX_M)
         return "gemv_w4_kernel (W4A8)" if gemv else "tc_gemm_kernel (W4A8)"
+    if path == eg.PATH_GEMV:  # weight-only GEMVs run only when forced
+        return "gemv_w8_kernel (W8A16)" if kind == "w8a16" else "gemv_w4_kernel (W4A16)"
     return f"tc_gemm_kernel ({kind.upper()})"
 
 
