@@ -685,7 +685,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
         constexpr int CW = HB < 16 ? HB : (HB >= 64 ? 8 : 16);
         // loads in flight per wait (one at HB = 64, where the 64 accumulators
         // leave no room for a second 16-column buffer)
-        constexpr int PAIR = (HB / CW) >= 2 && HB < 64 ? 2 : 1;
+        constexpr int PAIR = (HB / CW) >= 2 ? 2 : 1;
 #pragma unroll
         for (int cb = 0; cb < HB / CW; cb += PAIR) {
           uint32_t v[PAIR][16];
