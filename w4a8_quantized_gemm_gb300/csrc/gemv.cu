@@ -2,12 +2,13 @@
 //
 // Decode is a weight-streaming problem: every packed weight byte is read once
 // per token batch, so the kernels below are built to keep HBM busy. Each CTA
-// (4 warps) owns a 32-row slab of the output and a contiguous range of K
-// groups; its warps take every fourth group of that range, so a warp's loads
-// are 512 contiguous bytes per 16-byte chunk (32 rows x 16 B). A cluster of
-// up to 8 CTAs splits the groups of one slab further and reduces the partial
-// sums through distributed shared memory -- no global scratch, fixed
-// summation order, deterministic output.
+// owns one 128-row tile of the output (one consumer thread per weight row,
+// four consumer warps) and a contiguous range of K groups; a producer warp
+// streams the range's packed records through a shared-memory ring, one bulk
+// copy per group. When the tiles do not fill the GPU, a cluster of up to 8
+// CTAs splits a tile's groups and reduces the partial sums through
+// distributed shared memory -- no global scratch, fixed summation order,
+// deterministic output.
 //
 // W4A8: per (row n, group g) the integer partial
 //   Q = sum_{k in g} a_q*w_q - z[n,g] * a_gsum[m,g]

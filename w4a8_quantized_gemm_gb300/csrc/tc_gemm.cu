@@ -93,7 +93,6 @@ struct TcCfg {
   static constexpr bool kFp8 = (VARIANT == kW4A8) && BT <= kTcFp8MaxM;
   static constexpr int kDCols = kFp8 ? 2 * BT : BT;  // TMEM columns of one accumulator
   static constexpr int kACols = kFp8 ? 32 : 64;      // A operand columns of one group
-  static constexpr int kMmaK = kFp8 ? 32 : 16;       // K per MMA
   static constexpr bool kDrainPerGroup = (VARIANT != kW8A16);
   // MMA issuers. An MMA instruction up to N = 64 costs its issuing thread
   // about as much as the tensor core, and every barrier test costs it a
