@@ -112,9 +112,12 @@ struct TcCfg {
   // TMEM: kNumD accumulators of kDCols columns + kNumA A-operand buffers of
   // kACols columns (deep for small tiles: the converters run ahead of the
   // MMAs and the MMAs ahead of the drain).
+  // (128-token per-group tiles: three 128-column accumulators and two A
+  // buffers -- with two the MMAs of a group wait for the drain two back)
+  static constexpr bool kWide = BT == 128 && kDrainPerGroup;
   static constexpr int kNumD =
-      kLean ? 4 : (kFp8 ? (BT == 32 ? 4 : 2) : (BT <= 64 ? 4 : 2));
-  static constexpr int kNumA = kLean ? 4 : (kFp8 ? 8 : 4);
+      kLean ? 4 : (kWide ? 3 : (kFp8 ? (BT == 32 ? 4 : 2) : (BT <= 64 ? 4 : 2)));
+  static constexpr int kNumA = kLean ? 4 : (kWide ? 2 : (kFp8 ? 8 : 4));
   static constexpr int kActBox = BT * 128;                        // one 64-wide K box, bytes
   static constexpr int kActBytes = 2 * kActBox;                   // a 128-wide group
   // weights of one group: the int8 tile, or one packed int4 record (8192 B of
@@ -152,9 +155,13 @@ struct TcCfg {
   static_assert(kSmemBytes <= kSmemLimit, "shared memory");
   static_assert(!kLean || kTmemCols <= 256, "two CTAs share the SM's TMEM");
   static_assert(kTmemColsRaw <= 512, "TMEM budget");
-  // a converter set reuses only its own A buffers and accumulators, so every
-  // reuse wait follows that set's previous one in program order
-  static_assert(kNumA % kConvSets == 0 && kNumD % kConvSets == 0, "per-set buffer reuse");
+  // Buffer reuse waits test the phase one use back, so the phase two uses back
+  // must be known complete: for A buffers by the set's own previous wait
+  // (kNumA a multiple of the sets); for accumulators either the same way, or
+  // because the A-buffer wait (MMAs of group i - kNumA done, so drains up to
+  // i - kNumA - kNumD done, drains run in order) covers i - 2*kNumD.
+  static_assert(kNumA % kConvSets == 0 && (kNumD % kConvSets == 0 || kNumA <= kNumD),
+                "buffer reuse waits");
   static_assert(8 * (2 * kStages + 2 * kNumA + 2 * kNumD + kMmaWarps) + 8 <= 1024, "barrier region");
   static_assert(BT % 16 == 0 && BT >= 16 && BT <= 128, "token tile");
   static_assert(kStageBytes % 1024 == 0, "stage alignment");
