@@ -59,6 +59,8 @@ def _load():
             lib.oracle_w4a16.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, vp, vp]
             lib.oracle_w8a16.restype = None
             lib.oracle_w8a16.argtypes = [vp, vp, vp, i64, i64, i64, vp, vp]
+            lib.oracle_w8a8.restype = None
+            lib.oracle_w8a8.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, vp, vp]
             lib.oracle_packed_w4_bytes.restype = i64
             lib.oracle_packed_w4_bytes.argtypes = [i64, i64, i64]
             lib.oracle_code_location.restype = None
@@ -143,6 +145,19 @@ def w8a16(x_bf16, w_q, s_f16):
     y = np.empty((M, N), np.uint16)
     _load().oracle_w8a16(_p(x), _p(w_q), _p(s_f16), M, N, K, _p(y64), _p(y))
     return y64, y
+
+
+def w8a8(a_q, a_s, w_q, s_f16):
+    """W8A8 int8-dynamic: (int64 dot [M][N], fp64 y, bf16 bits y)."""
+    a_q, a_s = _c(a_q, np.int8), _c(a_s, np.float32)
+    w_q, s_f16 = _c(w_q, np.int8), _c(s_f16, np.uint16)
+    M, K = a_q.shape
+    N = w_q.shape[0]
+    dot = np.empty((M, N), np.int64)
+    y64 = np.empty((M, N), np.float64)
+    y = np.empty((M, N), np.uint16)
+    _load().oracle_w8a8(_p(a_q), _p(a_s), _p(w_q), _p(s_f16), M, N, K, _p(dot), _p(y64), _p(y))
+    return dot, y64, y
 
 
 def packed_w4_bytes(N: int, K: int, group: int = 128) -> int:

@@ -1,6 +1,6 @@
 /*
  * egopq_oracle.c -- plain CPU oracle for the W4A8 packed-linear GEMM and its
- * W4A16 / W8A16 variants.
+ * W4A16 / W8A16 / W8A8 variants.
  *
  * TEST INFRASTRUCTURE ONLY. Only the tests, the smoke check and the CPU
  * baseline leg of the benchmark may load or call this file. The product path
@@ -20,7 +20,8 @@
  *  - "The 4-bit CPU path", sections "W4A16 - PyTorch tinygemm" and "Building
  *    a checkpoint": weight-only int4 with bf16 activations, group size 128.
  *  - "Serve a pre-quantized int8 weight-only DiT via compressed-tensors ...",
- *    sections "Context" and "Plan": int8 weight-only (W8A16) linears.
+ *    sections "Context" and "Plan": int8 weight-only (W8A16) linears; sections
+ *    "Directive after the int8-wo result" and "Round two": W8A8 int8-dynamic.
  *  - The combination y = a_s * sum_g s * (sum_k a_q*w_q - z * sum_k a_q) is
  *    the plainest reading of those pieces: dequantized weight s*(w_q - z),
  *    dequantized activation a_s*a_q.
@@ -203,6 +204,30 @@ void oracle_w8a16(const uint16_t* x_bf16, const int8_t* w_q, const uint16_t* s_f
       for (int64_t k = 0; k < K; ++k)
         acc += oracle_bf16_to_double(x_bf16[m * K + k]) * (double)w_q[n * K + k];
       double y = oracle_fp16_to_double(s_f16[n]) * acc;
+      if (y64) y64[m * N + n] = y;
+      if (y_bf16) y_bf16[m * N + n] = oracle_bf16_from_double(y);
+    }
+}
+
+/* ---- W8A8: int8 per-token activations, int8 per-output-channel weights --- */
+
+/* "Serve a pre-quantized int8 weight-only DiT via compressed-tensors ...",
+ * sections "Directive after the int8-wo result" and "Round two": W8A8
+ * int8-dynamic -- activations quantized per token at run time (the same
+ * quantizer as above), weights int8 per output channel, int8 products summed
+ * as integers, then both scales applied:
+ *   y[m][n] = a_s[m] * s[n] * sum_k a_q[m,k] * w_q[n,k].
+ * dot (int64 [M][N]), y64 and y_bf16 may each be NULL. */
+void oracle_w8a8(const int8_t* a_q, const float* a_s, const int8_t* w_q, const uint16_t* s_f16,
+                 int64_t M, int64_t N, int64_t K, int64_t* dot, double* y64,
+                 uint16_t* y_bf16) {
+#pragma omp parallel for collapse(2) schedule(static)
+  for (int64_t m = 0; m < M; ++m)
+    for (int64_t n = 0; n < N; ++n) {
+      int64_t d = 0;
+      for (int64_t k = 0; k < K; ++k) d += (int64_t)a_q[m * K + k] * (int64_t)w_q[n * K + k];
+      double y = (double)a_s[m] * oracle_fp16_to_double(s_f16[n]) * (double)d;
+      if (dot) dot[m * N + n] = d;
       if (y64) y64[m * N + n] = y;
       if (y_bf16) y_bf16[m * N + n] = oracle_bf16_from_double(y);
     }

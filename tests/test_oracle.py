@@ -335,6 +335,67 @@ def test_w8a16_matches_dequant_then_matmul(M, N, K):
     assert w8.min() >= -127 and w8.max() <= 127
 
 
+# ---------------------------------------------------------------- W8A8 -----
+
+def test_w8a8_hand_example():
+    """2 tokens x 3 channels x K = 4, worked by hand.
+    a = [[1, 2, -3, 4], [-127, 0, 0, 4]], w = [[3, -1, 2, 1], [1, 0, 0, 0],
+    [0, 0, 0, 1]]: dots [[3-2-6+4, 1, 4], [-381+4, -127, 4]] = [[-1, 1, 4],
+    [-377, -127, 4]]. With a_s = [0.5, 2] and s = [1, 0.25, -2]:
+    y = [[-0.5, 0.125, -4], [-754, -63.5, -16]]; in bf16 -754 lies halfway
+    between -752 and -756 and rounds to the even mantissa, -752 (0xC43C)."""
+    a = np.array([[1, 2, -3, 4], [-127, 0, 0, 4]], np.int8)
+    w = np.array([[3, -1, 2, 1], [1, 0, 0, 0], [0, 0, 0, 1]], np.int8)
+    a_s = np.array([0.5, 2.0], np.float32)
+    s = np.array([0x3C00, 0x3400, 0xC000], np.uint16)  # fp16 1, 0.25, -2
+    dot, y64, y = oracle.w8a8(a, a_s, w, s)
+    assert dot.tolist() == [[-1, 1, 4], [-377, -127, 4]]
+    assert y64.tolist() == [[-0.5, 0.125, -4.0], [-754.0, -63.5, -16.0]]
+    assert y.tolist() == [[0xBF00, 0x3E00, 0xC080], [0xC43C, 0xC27E, 0xC180]]
+
+
+def test_w8a8_extreme_dot_is_exact():
+    """All +-127 over K = 18944: the dot is +-18944 * 16129 = +-305547776,
+    beyond 2^24 (a float accumulator would round) and inside int32."""
+    K = 18944
+    a = np.full((2, K), 127, np.int8)
+    a[1] = -127
+    w = np.full((1, K), 127, np.int8)
+    dot, _, _ = oracle.w8a8(a, np.ones(2, np.float32), w, np.array([0x3C00], np.uint16))
+    assert dot[:, 0].tolist() == [305547776, -305547776]
+
+
+def test_w8a8_reduces_to_w8a16_on_integer_activations():
+    """When every activation is an integer in [-127, 127] and each row's
+    absmax is 127, quantization is the identity (a_s = 1), so W8A8 equals the
+    separately pinned W8A16 on the same data."""
+    rng = np.random.default_rng(5)
+    M, N, K = 3, 5, 256
+    xi = rng.integers(-127, 128, size=(M, K))
+    xi[:, 7] = 127
+    x = (xi.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    w8, s8 = synth.w8_weights(6, 0, 0, N, K)
+    a_q, a_s, _ = oracle.quant_act(x)
+    assert np.array_equal(a_q, xi.astype(np.int8)) and np.all(a_s == 1.0)
+    _, y64, _ = oracle.w8a8(a_q, a_s, w8, s8)
+    y64_ref, _ = oracle.w8a16(x, w8, s8)
+    assert np.array_equal(y64, y64_ref)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 8, 128), (5, 16, 640)])
+def test_w8a8_matches_dequant_then_matmul(M, N, K):
+    """Against fp64 dequantized operands: (a_s * a_q) @ (s * w_q)^T."""
+    x = synth.activations(7, 0, 0, M, K)
+    a_q, a_s, _ = oracle.quant_act(x)
+    w8, s8 = synth.w8_weights(7, 0, 0, N, K)
+    _, y64, _ = oracle.w8a8(a_q, a_s, w8, s8)
+    ref = (a_q.astype(np.float64) * a_s.astype(np.float64)[:, None]) @ (
+        w8.astype(np.float64) * fp16_bits_to_double(s8)[:, None]).T
+    assert np.max(np.abs(y64 - ref)) <= 1e-12 * np.abs(ref).max()
+    _, y64n, _ = oracle.w8a8(a_q, a_s, -w8, s8)                    # sign symmetry
+    assert np.array_equal(y64n, -y64)
+
+
 # ------------------------------------------------------------- packing ------
 
 def unpack_reference(packed, N, K):
