@@ -93,6 +93,10 @@ def w8a16_bytes(M, N, K):
     return N * K + 2 * N + 2 * M * K + 2 * M * N
 
 
+def w8a8_bytes(M, N, K):
+    return N * K + 2 * N + M * K + 4 * M + 2 * M * N
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -299,8 +303,8 @@ class Workload:
             self.ms = [1, 16, 4096] if variant == "w4a8" else [m]
             self.dit_shapes = ([(3072, 3072), (3072, 12288), (12288, 3072)]
                                if variant == "w4a8" else [tuple(lin)])
-            self.dit_variants = ("w4", "w8") if variant == "w4a8" else \
-                ("w4",) if variant == "w4a16" else ("w8",)
+            self.dit_variants = {"w4a8": ("w4", "w8"), "w4a16": ("w4",), "w8a16": ("w8",),
+                                 "w8a8": ("w8a8",)}[variant]
             self.dit_w = {}
             for (K, N) in self.dit_shapes:
                 w = synth.w4_weights(4, 0, 0, N, K)
@@ -312,6 +316,14 @@ class Workload:
                 for K in sorted(set(k for k, _ in self.dit_shapes)):
                     x = synth.activations(4, 0, 0, M, K, outliers=False)
                     self.acts[(M, K)] = (x, t(x, torch.bfloat16))
+            # W8A8: per-token int8 codes (the tensor-core operand form only
+            # where that path runs)
+            self.qacts = {(M, K): eg.QuantAct(
+                torch.empty((M, K), dtype=torch.int8, device=dev),
+                torch.empty((M,), dtype=torch.float32, device=dev),
+                torch.empty((M, K // G128), dtype=torch.int32, device=dev),
+                eg.tc_operand(M, K, dev) if M > eg.TC_FP8_MAX_M else None)
+                for (M, K) in self.acts} if "w8a8" in self.dit_variants else {}
             self.ys = {(M, K, N, v): torch.empty((M, N), dtype=torch.bfloat16, device=dev)
                        for M in self.ms for (K, N) in self.dit_shapes for v in self.dit_variants}
             self.layers = [None]
@@ -392,10 +404,23 @@ class Workload:
                                 (lambda a=a, p=self.head, N=N, K=K, y=y:
                                  eg.w4a8_gemm(a, p, N, K, out=y, path=self.path))))
         else:
+            quantized = set()
             for M in self.ms:
                 for (K, N) in self.dit_shapes:
                     x, xd = self.acts[(M, K)]
                     p4, w8, s8 = self.dit_w[(K, N)]
+                    if "w8a8" in self.dit_variants:
+                        a = self.qacts[(M, K)]
+                        if (M, K) not in quantized:
+                            quantized.add((M, K))
+                            ops.append((f"quant K={K} M={M}", "quant", M, 0, K,
+                                        quant_bytes(M, K), 0,
+                                        (lambda xd=xd, a=a: eg.quant_act(xd, out=a))))
+                        y = self.ys[(M, K, N, "w8a8")]
+                        ops.append((f"w8a8 K={K} N={N} M={M}", "w8a8", M, N, K,
+                                    w8a8_bytes(M, N, K), 2 * M * N * K,
+                                    (lambda a=a, w8=w8, s8=s8, y=y:
+                                     eg.w8a8_gemm(a, w8, s8, out=y, path=self.path))))
                     if "w4" in self.dit_variants:
                         y4 = self.ys[(M, K, N, "w4")]
                         ops.append((f"w4a16 K={K} N={N} M={M}", "w4a16", M, N, K,
@@ -445,6 +470,9 @@ def kernel_label(eg, kind, M, path):
     if kind == "w4a8":
         gemv = path == eg.PATH_GEMV or (path == eg.PATH_AUTO and M <= eg.GEMV_AUTO_MAX_M)
         return "gemv_w4_kernel (W4A8)" if gemv else "tc_gemm_kernel (W4A8)"
+    if kind == "w8a8":
+        gemv = path == eg.PATH_GEMV or (path == eg.PATH_AUTO and M <= eg.TC_FP8_MAX_M)
+        return "gemv_w8a8_kernel (W8A8)" if gemv else "tc_gemm_kernel (W8A8)"
     if path == eg.PATH_GEMV:  # weight-only GEMVs run only when forced
         return "gemv_w8_kernel (W8A16)" if kind == "w8a16" else "gemv_w4_kernel (W4A16)"
     return f"tc_gemm_kernel ({kind.upper()})"
@@ -634,7 +662,9 @@ def workload_description(args) -> str:
         "model": f"full 7B linear pass: 28 layers x 7 linears + head at M={args.m}",
         "dit": "weight-only W4A16 and W8A16 on DiT blocks K=3072/12288, M in {1,16,4096}",
         "tiny": "tiny W4A8: M=16, K=512, N=256",
-        "linear": f"one W4A8 linear K={args.k} N={args.n} at M={args.m}",
+        "linear": f"one {args.variant.upper()} linear K={args.k} N={args.n} at M={args.m}"
+                  + (" (per-token int8 activations, per-channel int8 weights)"
+                     if args.variant == "w8a8" else ""),
     }[args.workload]
 
 
@@ -677,18 +707,24 @@ def cpu_baseline(args, wl, unit_is_ops, budget_s=20.0):
         n = min(N, max(128, (n // 128) * 128))
         w = synth.w4_weights(1, 0, 0, n, K)
         x = synth.activations(1, 0, 0, m, K)
+        if kind in ("w8a16", "w8a8"):
+            w8, s8 = synth.w8_weights(4, 0, 0, n, K)
         t0 = time.perf_counter()
         if kind == "w4a8":
             a_q, a_s, _ = oracle.quant_act(x)
             oracle.w4a8(a_q, a_s, w.w_q, w.scale_f16, w.zero)
-            units = 2 * m * n * K if unit_is_ops else w4a8_bytes(m, n, K)
+            nbytes = w4a8_bytes(m, n, K)
         elif kind == "w4a16":
             oracle.w4a16(x, w.w_q, w.scale_f16, w.zero)
-            units = w4a16_bytes(m, n, K)
+            nbytes = w4a16_bytes(m, n, K)
+        elif kind == "w8a8":
+            a_q, a_s, _ = oracle.quant_act(x)
+            oracle.w8a8(a_q, a_s, w8, s8)
+            nbytes = w8a8_bytes(m, n, K)
         else:
-            w8, s8 = synth.w8_weights(4, 0, 0, n, K)
             oracle.w8a16(x, w8, s8)
-            units = w8a16_bytes(m, n, K)
+            nbytes = w8a16_bytes(m, n, K)
+        units = 2 * m * n * K if unit_is_ops else nbytes
         dt = time.perf_counter() - t0
         ops_per_s = 2 * m * n * K / max(dt, 1e-6)
         elapsed += dt
@@ -720,7 +756,7 @@ def run_reference(args, rank, world):
                       [(3072, 3072), (3072, 12288), (12288, 3072)]],
               "tiny": [(16, 512, 256)],
               "linear": [(args.m, args.k, args.n)]}[args.workload]
-    kind = "w4a16" if args.workload == "dit" else "w4a8"
+    kind = {"dit": "w4a16", "linear": args.variant}.get(args.workload, "w4a8")
     wl.step_ops = lambda c: [(f"M={M} K={K} N={N}", kind, M, N, K, 0, 0, None)
                              for (M, K, N) in shapes]
     # each step a bounded sample of the workload, sized so that the whole
@@ -768,7 +804,7 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--path", choices=["auto", "gemv", "tc"], default="auto")
-    ap.add_argument("--variant", choices=["w4a8", "w4a16", "w8a16"], default="w4a8",
+    ap.add_argument("--variant", choices=["w4a8", "w4a16", "w8a16", "w8a8"], default="w4a8",
                     help="variant for --workload linear")
     ap.add_argument("--api", choices=["gemm", "linear"], default="gemm",
                     help="gemm: egopq_quant_act_i8 + egopq_w4a8_gemm per linear input; "

@@ -62,7 +62,8 @@ typedef enum { EGOPQ_PATH_AUTO = 0, EGOPQ_PATH_GEMV = 1, EGOPQ_PATH_TC = 2 } ego
 typedef enum {
   EGOPQ_VARIANT_W4A8 = 0,
   EGOPQ_VARIANT_W4A16 = 1,
-  EGOPQ_VARIANT_W8A16 = 2
+  EGOPQ_VARIANT_W8A16 = 2,
+  EGOPQ_VARIANT_W8A8 = 3
 } egopq_variant;
 
 typedef void* egopq_stream_t; /* cudaStream_t */
@@ -193,6 +194,24 @@ int egopq_w8a16_gemm(const uint16_t* x_bf16, const int8_t* w_q, const uint16_t* 
 int egopq_w8a16_gemm_ex(const uint16_t* x_bf16, const int8_t* w_q, const uint16_t* scale_f16,
                         int64_t M, int64_t N, int64_t K, uint16_t* y_bf16, int path,
                         egopq_stream_t stream);
+
+/* ---- W8A8 int8-dynamic GEMM ------------------------------------------------------
+ * y[m,n] = bf16( a_s[m] * s[n] * sum_k a_q[m,k] * w_q[n,k] )
+ * Activations as egopq_quant_act_i8 produces them (per-token int8 a_q [M][K],
+ * a_s fp32 [M]; a_tc, the tensor-core operand form, is read only on the
+ * tensor-core path and only exists there for M > 64); weights int8 [N][K]
+ * row-major in [-127, 127] with fp16 per-output-channel scales [N], as for
+ * W8A16. The integer dot products are exact (int32). AUTO runs the GEMV for
+ * M <= 64 and the tensor cores above; EGOPQ_PATH_TC with M <= 64 returns
+ * EGOPQ_ERR_UNSUPPORTED_SHAPE. ("Serve a pre-quantized int8 weight-only DiT
+ * via compressed-tensors ...", sections "Directive after the int8-wo result"
+ * and "Round two": W8A8 int8-dynamic.) */
+int egopq_w8a8_gemm(const int8_t* a_q, const void* a_tc, const float* a_s, const int8_t* w_q,
+                    const uint16_t* scale_f16, int64_t M, int64_t N, int64_t K, uint16_t* y_bf16,
+                    egopq_stream_t stream);
+int egopq_w8a8_gemm_ex(const int8_t* a_q, const void* a_tc, const float* a_s, const int8_t* w_q,
+                       const uint16_t* scale_f16, int64_t M, int64_t N, int64_t K,
+                       uint16_t* y_bf16, int path, egopq_stream_t stream);
 
 /* ---- support, status --------------------------------------------------------------
  * 1 if (M, N, K, group, variant) is accepted by the parity-tested kernels on

@@ -258,6 +258,101 @@ def test_weight_only_dit_shapes_sampled(K, N, M):
     check_bf16_output(y8[np.ix_(rows, cols)], r8, f"W8A16 DiT K={K} N={N} M={M}")
 
 
+# ------------------------------------------------- W8A8 int8-dynamic output
+
+def run_w8a8(x, w8, s8, path):
+    a = eg.quant_act(to_dev(x, torch.bfloat16))
+    return eg.w8a8_gemm(a, to_dev(w8), to_dev(s8, torch.float16), path=path)
+
+
+@pytest.mark.parametrize("path,M", [(eg.PATH_GEMV, m) for m in (1, 2, 3, 5, 8, 9, 16, 17, 64)]
+                         + [(eg.PATH_TC, m) for m in (65, 130, 300)]
+                         + [(eg.PATH_AUTO, m) for m in (1, 64, 65, 129)])
+def test_w8a8_output(path, M):
+    """GEMV (up to 8 tokens a launch, ragged tails) and the tensor-core path
+    (128-token tiles, ragged tails) against the int8-dynamic oracle."""
+    N, K = 384, 1024
+    w8, s8 = synth.w8_weights(5, 0, 0, N, K)
+    x = synth.activations(5, 0, 0, M, K)
+    y = run_w8a8(x, w8, s8, path)
+    a_q, a_s, _ = oracle.quant_act(x)
+    _, _, y_ref = oracle.w8a8(a_q, a_s, w8, s8)
+    check_bf16_output(to_host_bits(y), y_ref, f"W8A8 path={path} M={M}")
+
+
+@pytest.mark.parametrize("path,M", [(eg.PATH_GEMV, 7), (eg.PATH_TC, 200)])
+def test_w8a8_integer_case_bit_exact(path, M):
+    """Tokens whose absmax is 127 quantize to themselves with scale 1; with unit
+    weight scales every output is an integer dot product below 2^24, which the
+    kernel and the oracle both round once to bf16: identical bits."""
+    N, K = 256, 768
+    rng = np.random.default_rng(M)
+    xi = rng.integers(-127, 128, size=(M, K))
+    xi[:, 0] = 127
+    x = torch.tensor(xi, dtype=torch.float32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    w8 = rng.integers(-127, 128, size=(N, K)).astype(np.int8)
+    s8 = np.full(N, 0x3C00, dtype=np.uint16)  # fp16 1.0
+    y = to_host_bits(run_w8a8(x, w8, s8, path))
+    a_q, a_s, _ = oracle.quant_act(x)
+    assert np.array_equal(a_q, xi.astype(np.int8)) and np.all(a_s == 1.0)
+    dot, _, y_ref = oracle.w8a8(a_q, a_s, w8, s8)
+    assert np.abs(dot).max() < 2 ** 24
+    assert np.array_equal(y, y_ref)
+
+
+@pytest.mark.parametrize("path,M", [(eg.PATH_GEMV, 4), (eg.PATH_TC, 130)])
+def test_w8a8_extreme_magnitudes(path, M):
+    """Every code at +-127 over K = 18944: dot products of +-305,547,776 stay
+    exact in the int32 accumulators (and in the tensor-core path's per-group
+    fp32 partials, each at most 128*127*127 < 2^24)."""
+    N, K = 128, 18944
+    rng = np.random.default_rng(3)
+    sign_a = rng.choice([-1, 1], size=(M, K))
+    sign_a[1] = 1
+    x = torch.tensor(sign_a * 2.0, dtype=torch.float32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    w8 = (rng.choice([-1, 1], size=(N, K)) * 127).astype(np.int8)
+    w8[0] = 127
+    s8 = np.full(N, 0x2C00, dtype=np.uint16)  # fp16 1/16
+    y = run_w8a8(x, w8, s8, path)
+    a_q, a_s, _ = oracle.quant_act(x)
+    dot, _, y_ref = oracle.w8a8(a_q, a_s, w8, s8)
+    assert dot[1, 0] == 127 * 127 * K
+    check_bf16_output(to_host_bits(y), y_ref, f"W8A8 extreme path={path}")
+
+
+def test_w8a8_refusals():
+    """The tensor-core path takes the fp16 operand form only (M > 64): forced
+    TC below it is an unsupported shape; TC without a_tc is an invalid argument."""
+    N, K = 128, 256
+    w8, s8 = synth.w8_weights(5, 1, 0, N, K)
+    a = eg.quant_act(to_dev(synth.activations(5, 1, 0, 64, K), torch.bfloat16))
+    with pytest.raises(eg.EgopqError) as e:
+        eg.w8a8_gemm(a, to_dev(w8), to_dev(s8, torch.float16), path=eg.PATH_TC)
+    assert e.value.code == -2
+    a2 = eg.quant_act(to_dev(synth.activations(5, 1, 0, 130, K), torch.bfloat16), with_tc=False)
+    with pytest.raises(eg.EgopqError) as e:
+        eg.w8a8_gemm(a2, to_dev(w8), to_dev(s8, torch.float16), path=eg.PATH_TC)
+    assert e.value.code == -1
+    y = eg.w8a8_gemm(a2, to_dev(w8), to_dev(s8, torch.float16), path=eg.PATH_GEMV)
+    assert y.shape == (130, N)
+
+
+@pytest.mark.parametrize("K,N", [(3072, 3072), (3072, 12288), (12288, 3072)])
+@pytest.mark.parametrize("M", [16, 4096])
+def test_w8a8_dit_shapes_sampled(K, N, M):
+    """The DiT linears at a decode-sized and a 4096-token batch (GEMV and
+    tensor cores under AUTO), checked on sampled rows and columns."""
+    x = synth.activations(5, 2, 0, M, K, outliers=False)
+    w8, s8 = synth.w8_weights(5, 2, 0, N, K)
+    y = to_host_bits(run_w8a8(x, w8, s8, eg.PATH_AUTO))
+    rng = np.random.default_rng(K + N + M)
+    rows = np.unique(np.concatenate([[0, M - 1], rng.choice(M, min(M, 6), replace=False)]))
+    cols = np.unique(np.concatenate([[0, N - 1], rng.choice(N, 160, replace=False)]))
+    a_q, a_s, _ = oracle.quant_act(x[rows])
+    _, _, r = oracle.w8a8(a_q, a_s, w8[cols], s8[cols])
+    check_bf16_output(y[np.ix_(rows, cols)], r, f"W8A8 DiT K={K} N={N} M={M}")
+
+
 # ----------------------------------------------------------------- edge cases
 
 def test_empty_batch_is_a_noop():

@@ -26,7 +26,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libegopq.so")
 HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "egopq.h")
 
 PATH_AUTO, PATH_GEMV, PATH_TC = 0, 1, 2
-VARIANT_W4A8, VARIANT_W4A16, VARIANT_W8A16 = 0, 1, 2
+VARIANT_W4A8, VARIANT_W4A16, VARIANT_W8A16, VARIANT_W8A8 = 0, 1, 2, 3
 STATUS = {0: "OK", -1: "INVALID_ARG", -2: "UNSUPPORTED_SHAPE", -3: "MISALIGNED",
           -4: "ARCH", -5: "CUDA", -6: "TIMEOUT"}
 GROUP = 128
@@ -71,6 +71,8 @@ def load() -> ctypes.CDLL:
             "egopq_w4a16_gemm_ex": (i32, [vp, vp, i64, i64, i64, i32, vp, i32, vp]),
             "egopq_w8a16_gemm": (i32, [vp, vp, vp, i64, i64, i64, vp, vp]),
             "egopq_w8a16_gemm_ex": (i32, [vp, vp, vp, i64, i64, i64, vp, i32, vp]),
+            "egopq_w8a8_gemm": (i32, [vp, vp, vp, vp, vp, i64, i64, i64, vp, vp]),
+            "egopq_w8a8_gemm_ex": (i32, [vp, vp, vp, vp, vp, i64, i64, i64, vp, i32, vp]),
             "egopq_w4a8_linear_workspace_bytes": (sz, [i64, i64, i32, i32]),
             "egopq_w4a8_linear": (i32, [vp, vp, i64, i64, i64, i32, vp, vp, sz, i32, vp]),
             "egopq_w4a8_linear_noalloc": (i32, [vp, vp, i64, i64, i64, i32, vp, i32, vp]),
@@ -255,6 +257,22 @@ def w8a16_gemm(x: torch.Tensor, w_q: torch.Tensor, scale_f16: torch.Tensor,
         out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
     _check(load().egopq_w8a16_gemm_ex(_ptr(x), _ptr(w_q), _ptr(scale_f16), M, N, K, _ptr(out),
                                       path, _stream(stream)))
+    return out
+
+
+def w8a8_gemm(a: QuantAct, w_q: torch.Tensor, scale_f16: torch.Tensor, path: int = PATH_AUTO,
+              out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """W8A8 int8-dynamic GEMM: per-token int8 activations (from quant_act; a_tc
+    is read on the tensor-core path only) times int8 weights [N, K] with fp16
+    per-channel scales [N]."""
+    _dtype(w_q, torch.int8)
+    M, K = a.a_q.shape
+    N = w_q.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=a.a_q.device)
+    _check(load().egopq_w8a8_gemm_ex(_ptr(a.a_q), _ptr(a.a_tc), _ptr(a.a_s), _ptr(w_q),
+                                     _ptr(scale_f16), M, N, K, _ptr(out), path,
+                                     _stream(stream)))
     return out
 
 

@@ -89,9 +89,13 @@ int run_gemm(const GemmArgs& a, int path, cudaStream_t st) {
   if (rc) return rc;
   if (a.M == 0) return EGOPQ_OK;
   int use = path;
-  if (use == EGOPQ_PATH_AUTO)
-    use = (a.M <= kGemvAutoMaxM && a.variant == kW4A8) ? EGOPQ_PATH_GEMV : EGOPQ_PATH_TC;
-  if (use == EGOPQ_PATH_TC && a.variant == kW4A8 && !a.a_tc)
+  if (use == EGOPQ_PATH_AUTO) {
+    if (a.variant == kW8A8)
+      use = (a.M <= kTcFp8MaxM) ? EGOPQ_PATH_GEMV : EGOPQ_PATH_TC;
+    else
+      use = (a.M <= kGemvAutoMaxM && a.variant == kW4A8) ? EGOPQ_PATH_GEMV : EGOPQ_PATH_TC;
+  }
+  if (use == EGOPQ_PATH_TC && (a.variant == kW4A8 || a.variant == kW8A8) && !a.a_tc)
     return fail(EGOPQ_ERR_INVALID_ARG, "a_tc is required by the tensor-core path");
   cudaError_t e = (use == EGOPQ_PATH_GEMV) ? launch_gemv(a, st) : launch_tc_gemm(a, st);
   if (e == cudaErrorNotSupported)
@@ -334,9 +338,40 @@ int egopq_w8a16_gemm(const uint16_t* x_bf16, const int8_t* w_q, const uint16_t* 
   return egopq_w8a16_gemm_ex(x_bf16, w_q, scale_f16, M, N, K, y_bf16, EGOPQ_PATH_AUTO, stream);
 }
 
+int egopq_w8a8_gemm_ex(const int8_t* a_q, const void* a_tc, const float* a_s, const int8_t* w_q,
+                       const uint16_t* scale_f16, int64_t M, int64_t N, int64_t K,
+                       uint16_t* y_bf16, int path, egopq_stream_t stream) {
+  int rc = check_w4_shape(M, N, K, 128);
+  if (rc) return rc;
+  if (M == 0) return EGOPQ_OK;
+  rc = check_ptrs(5, "a_q", a_q, "a_s", a_s, "w_q", w_q, "scale_f16", scale_f16, "y_bf16", y_bf16);
+  if (rc) return rc;
+  if (a_tc && !aligned16(a_tc)) return fail(EGOPQ_ERR_MISALIGNED, "a_tc is not 16-byte aligned");
+  GemmArgs a{};
+  a.variant = kW8A8;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.a_q = a_q;
+  a.a_tc = a_tc;
+  a.a_s = a_s;
+  a.w8 = w_q;
+  a.s8 = scale_f16;
+  a.y = y_bf16;
+  a.timeout_ns = kDefaultTimeoutNs;
+  return run_gemm(a, path, (cudaStream_t)stream);
+}
+
+int egopq_w8a8_gemm(const int8_t* a_q, const void* a_tc, const float* a_s, const int8_t* w_q,
+                    const uint16_t* scale_f16, int64_t M, int64_t N, int64_t K, uint16_t* y_bf16,
+                    egopq_stream_t stream) {
+  return egopq_w8a8_gemm_ex(a_q, a_tc, a_s, w_q, scale_f16, M, N, K, y_bf16, EGOPQ_PATH_AUTO,
+                            stream);
+}
+
 int egopq_supported(int64_t M, int64_t N, int64_t K, int group, int variant) {
-  if (variant < EGOPQ_VARIANT_W4A8 || variant > EGOPQ_VARIANT_W8A16) return 0;
-  if (variant == EGOPQ_VARIANT_W8A16) group = 128;
+  if (variant < EGOPQ_VARIANT_W4A8 || variant > EGOPQ_VARIANT_W8A8) return 0;
+  if (variant == EGOPQ_VARIANT_W8A16 || variant == EGOPQ_VARIANT_W8A8) group = 128;
   if (M < 0 || N <= 0 || K <= 0 || M >= kMaxDim || N >= kMaxDim || K >= kMaxDim) return 0;
   if (group != 128 || K % 128 || N % 128) return 0;
   if (check_arch() != EGOPQ_OK) return 0;

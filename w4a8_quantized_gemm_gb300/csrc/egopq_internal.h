@@ -9,13 +9,13 @@
 
 namespace egopq {
 
-enum Variant { kW4A8 = 0, kW4A16 = 1, kW8A16 = 2 };
+enum Variant { kW4A8 = 0, kW4A16 = 1, kW8A16 = 2, kW8A8 = 3 };
 
 // Operands of one GEMM call, already validated by the ABI layer.
 struct GemmArgs {
   int variant;
   int64_t M, N, K;
-  // W4A8
+  // activation codes (W4A8, W8A8; a_gsum W4A8 only)
   const int8_t* a_q;
   const void* a_tc;  // tensor-core operand form of a_q (see kTcFp8MaxM)
   const float* a_s;
@@ -24,7 +24,7 @@ struct GemmArgs {
   const uint16_t* x;
   // packed int4 weight (W4A8, W4A16)
   const uint8_t* packed;
-  // int8 weight and per-channel scale (W8A16)
+  // int8 weight and per-channel scale (W8A16, W8A8)
   const int8_t* w8;
   const uint16_t* s8;
   // outputs

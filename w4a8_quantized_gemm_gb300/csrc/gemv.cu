@@ -23,6 +23,8 @@
 // W4A16: the same skeleton with fp32 FMAs of bf16 activations against exact
 // (w_q - z) values, scaled per group.
 //
+// W8A8: the same walk on int8 activation codes, dp4a into exact int32 sums.
+//
 // W8A16: int8 row-major weights, one warp per 4 rows, 16-byte coalesced loads
 // along K and a warp-shuffle reduction; y = bf16(s[n] * sum_k x*w_q).
 #include "egopq_internal.h"
@@ -363,6 +365,65 @@ gemv_w8_kernel(const uint16_t* __restrict__ x, const int8_t* __restrict__ w8,
   }
 }
 
+// ---- W8A8 ---------------------------------------------------------------------
+// Same warp-per-4-rows walk as W8A16, on int8 activation codes: dp4a products
+// summed exactly in int32 (|sum| <= K * 127 * 127 < 2^31 for K < 133144),
+// then y = bf16(a_s[m] * s[n] * sum).
+template <int MT>
+__global__ void __launch_bounds__(kW8Threads)
+gemv_w8a8_kernel(const int8_t* __restrict__ a_q, const float* __restrict__ a_s,
+                 const int8_t* __restrict__ w8, const uint16_t* __restrict__ s8, int64_t N,
+                 int64_t K, int rows, uint16_t* __restrict__ y) {
+  const int lane = threadIdx.x & 31;
+  const int64_t gw = ((int64_t)blockIdx.x * kW8Threads + threadIdx.x) >> 5;
+  const int64_t nwarps = ((int64_t)gridDim.x * kW8Threads) >> 5;
+  for (int64_t n0 = gw * kW8RowsPerWarp; n0 < N; n0 += nwarps * kW8RowsPerWarp) {
+    int acc[kW8RowsPerWarp][MT];
+#pragma unroll
+    for (int i = 0; i < kW8RowsPerWarp; ++i)
+#pragma unroll
+      for (int m = 0; m < MT; ++m) acc[i][m] = 0;
+    for (int64_t kc = (int64_t)lane * 16; kc < K; kc += 512) {
+      uint4 av[MT];
+#pragma unroll
+      for (int m = 0; m < MT; ++m)
+        av[m] = (m < rows) ? __ldg(reinterpret_cast<const uint4*>(a_q + m * K + kc))
+                           : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int i = 0; i < kW8RowsPerWarp; ++i) {
+        if (n0 + i < N) {
+          const uint4 wv = ldg_stream(w8 + (n0 + i) * K + kc);
+#pragma unroll
+          for (int m = 0; m < MT; ++m) {
+            int d = acc[i][m];
+            d = __dp4a((int)wv.x, (int)av[m].x, d);
+            d = __dp4a((int)wv.y, (int)av[m].y, d);
+            d = __dp4a((int)wv.z, (int)av[m].z, d);
+            d = __dp4a((int)wv.w, (int)av[m].w, d);
+            acc[i][m] = d;
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kW8RowsPerWarp; ++i)
+#pragma unroll
+      for (int m = 0; m < MT; ++m)
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc[i][m] += __shfl_xor_sync(0xffffffffu, acc[i][m], o);
+    if (lane == 0) {
+#pragma unroll
+      for (int i = 0; i < kW8RowsPerWarp; ++i) {
+        if (n0 + i >= N) break;
+        const float sc = f16_bits_to_f32(s8[n0 + i]);
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+          if (m < rows) y[m * N + n0 + i] = f32_to_bf16_bits(a_s[m] * sc * (float)acc[i][m]);
+      }
+    }
+  }
+}
+
 // ---- launchers ----------------------------------------------------------------
 static int sm_count() {
   static int count = 0;
@@ -417,6 +478,30 @@ static cudaError_t launch_w4_rows(const GemvParams& p, cudaStream_t st) {
 
 cudaError_t launch_gemv(const GemmArgs& a, cudaStream_t st) {
   if (a.M == 0) return cudaSuccess;
+  if (a.variant == kW8A8) {
+    const int64_t warps_needed = (a.N + kW8RowsPerWarp - 1) / kW8RowsPerWarp;
+    int64_t blocks = (warps_needed * 32 + kW8Threads - 1) / kW8Threads;
+    const int64_t cap = (int64_t)sm_count() * 8;
+    if (blocks > cap) blocks = cap;
+    constexpr int kW8A8MaxRows = 8;  // token rows per W8A8 GEMV launch
+    for (int64_t m0 = 0; m0 < a.M; m0 += kW8A8MaxRows) {
+      const int rows = (int)((a.M - m0) < kW8A8MaxRows ? (a.M - m0) : kW8A8MaxRows);
+      const int8_t* aq = a.a_q + m0 * a.K;
+      const float* as = a.a_s + m0;
+      uint16_t* y = a.y + m0 * a.N;
+      if (rows == 1)
+        gemv_w8a8_kernel<1><<<(unsigned)blocks, kW8Threads, 0, st>>>(aq, as, a.w8, a.s8, a.N, a.K, rows, y);
+      else if (rows == 2)
+        gemv_w8a8_kernel<2><<<(unsigned)blocks, kW8Threads, 0, st>>>(aq, as, a.w8, a.s8, a.N, a.K, rows, y);
+      else if (rows <= 4)
+        gemv_w8a8_kernel<4><<<(unsigned)blocks, kW8Threads, 0, st>>>(aq, as, a.w8, a.s8, a.N, a.K, rows, y);
+      else
+        gemv_w8a8_kernel<8><<<(unsigned)blocks, kW8Threads, 0, st>>>(aq, as, a.w8, a.s8, a.N, a.K, rows, y);
+      cudaError_t e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+  }
   if (a.variant == kW8A16) {
     const int64_t warps_needed = (a.N + kW8RowsPerWarp - 1) / kW8RowsPerWarp;
     int64_t blocks = (warps_needed * 32 + kW8Threads - 1) / kW8Threads;

@@ -93,12 +93,21 @@ struct TcCfg {
   static constexpr bool kFp8 = (VARIANT == kW4A8) && BT <= kTcFp8MaxM;
   static constexpr int kDCols = kFp8 ? 2 * BT : BT;  // TMEM columns of one accumulator
   static constexpr int kACols = kFp8 ? 32 : 64;      // A operand columns of one group
-  static constexpr bool kDrainPerGroup = (VARIANT != kW8A16);
+  // Groups per accumulator drain: 1 where every group has its own scale
+  // (W4A8, W4A16); 0 = the whole unit (W8A16: per-channel scale, fp32 sums);
+  // W8A8 drains every 8 groups (1024 K: |partial| <= 1024 * 127^2 < 2^24,
+  // so the fp32 accumulator holds it exactly) and adds the partials as int32
+  // (a whole K row can exceed 2^24); its scales come only in the epilogue.
+  static constexpr int kGroupsPerDrain = (VARIANT == kW8A16) ? 0 : (VARIANT == kW8A8 ? 8 : 1);
+  static constexpr bool kDrainPerGroup = (kGroupsPerDrain == 1);
+  static constexpr bool kIntAcc = (VARIANT == kW8A8);
+  // int8 weight tiles (W8A16, W8A8): staged by a 2-D TMA copy, no pack step
+  static constexpr bool kW8 = (VARIANT == kW8A16 || VARIANT == kW8A8);
   // MMA issuers. An MMA instruction up to N = 64 costs its issuing thread
   // about as much as the tensor core, and every barrier test costs it a
   // round trip, so small token tiles use two issuing warps that take
-  // alternate groups. W8A16 accumulates a whole tile in one accumulator and
-  // keeps one issuer, which orders those MMAs.
+  // alternate groups. Tiles that accumulate several groups in one
+  // accumulator (W8A16, W8A8) keep one issuer, which orders those MMAs.
   // 16-token e4m3 tiles run two lean CTAs per SM (one drain warpgroup, one
   // converter set, one issuer each, half the shared memory and TMEM): their
   // per-group hand-off chain is latency-bound, so two independent pipelines
@@ -123,8 +132,8 @@ struct TcCfg {
   // weights of one group: the int8 tile, or one packed int4 record (8192 B of
   // codes, 256 B of scales, 64 B of zero nibbles), padded to keep stages
   // 1024-byte aligned
-  static constexpr int kWCopyBytes = (VARIANT == kW8A16) ? 16384 : 8512;
-  static constexpr int kWBytes = (VARIANT == kW8A16) ? 16384 : 9216;
+  static constexpr int kWCopyBytes = kW8 ? 16384 : 8512;
+  static constexpr int kWBytes = kW8 ? 16384 : 9216;
   static constexpr int kStageBytes = kActBytes + kWBytes;        // multiple of 1024
   static constexpr int kTxBytes = kActBytes + kWCopyBytes;
   static constexpr int kSmemLimit = kCtasPerSm == 1 ? kMaxSmem : kMaxSmemHalf;
@@ -150,7 +159,7 @@ struct TcCfg {
   static constexpr int kProducerWarp = kConvWarp0 + 4 * kConvSets;
   static constexpr int kMmaWarp = kProducerWarp + 1;  // first issuer; allocates TMEM
   static constexpr int kThreads = 32 * (kMmaWarp + kMmaWarps);
-  static constexpr int kBf16 = (VARIANT == kW4A8) ? 0 : 1;
+  static constexpr int kBf16 = (VARIANT == kW4A8 || VARIANT == kW8A8) ? 0 : 1;  // fp16 codes
   static_assert(kStages >= 2, "shared memory too small for two stages");
   static_assert(kSmemBytes <= kSmemLimit, "shared memory");
   static_assert(!kLean || kTmemCols <= 256, "two CTAs share the SM's TMEM");
@@ -182,7 +191,7 @@ __device__ __forceinline__ void store_row(const float (&R)[HB], const TcParams& 
       const int64_t m = m0 + t;
       if (m < p.M) {
         float v = R[t];
-        if constexpr (VARIANT == kW4A8) v = __ldg(p.a_s + m) * v;
+        if constexpr (VARIANT == kW4A8 || VARIANT == kW8A8) v = __ldg(p.a_s + m) * v;
         p.y[m * p.N + n] = f32_to_bf16_bits(v);
       }
     }
@@ -228,6 +237,14 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
   }
   const int ng = g1 - g0;
   const int n_items = n_units * ng;
+  // accumulator drains per unit, and the drain that item i feeds
+  constexpr int GPD = C::kGroupsPerDrain;
+  const int nc = GPD == 0 ? 1 : (ng + GPD - 1) / GPD;
+  auto drain_of = [&](int i) -> int {
+    if constexpr (GPD == 1) return i;
+    else if constexpr (GPD == 0) return i / ng;
+    else return (i / ng) * nc + (i % ng) / GPD;
+  };
   // tile u -> (mt, nt). Persistent grids walk bands of p.band m-tiles, m
   // fastest inside a band, so the tiles in flight at once share a few
   // activation tiles and a few weight tiles (both stay in L2).
@@ -285,7 +302,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
   }
   if (warp == C::kProducerWarp && lane == 0) {
     prefetch_tensormap(&act_map);
-    if constexpr (VARIANT == kW8A16) prefetch_tensormap(&w8_map);
+    if constexpr (C::kW8) prefetch_tensormap(&w8_map);
   }
   if (warp == C::kMmaWarp) {
     tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
@@ -328,7 +345,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
       auto load_weights = [&](int s) {
         const int nt = w_nt, g = g0 + w_gi;
         advance(w_k, w_gi, w_mt, w_nt);
-        if constexpr (VARIANT == kW8A16) {
+        if constexpr (C::kW8) {
           tma_load_2d(stage_act(s) + C::kActBytes, &w8_map, full_bar(s), g * 128, nt * 128);
         } else {
           bulk_load(stage_act(s) + C::kActBytes, p.packed + ((int64_t)nt * G + g) * 8512, 8512,
@@ -389,8 +406,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
       for (int i = q; i < n_items; i += C::kMmaWarps) {
         const int s = i % S, ab = i % kNumA;
         const int gi = i % ng;
-        const int di = C::kDrainPerGroup ? i : i / ng;
+        const int di = drain_of(i);
         const int db = di % kNumD;
+        // first group of its accumulator; last group of it
+        const bool d_first = GPD == 1 || (GPD == 0 ? gi == 0 : gi % GPD == 0);
+        const bool d_last = GPD == 1 || gi == ng - 1 || (GPD > 1 && gi % GPD == GPD - 1);
         // one wait per group: the converters arrive on afull only once the
         // stage has landed, the A buffer is free and the accumulator drained
         if (!mbar_wait(afull_bar(ab), (i / kNumA) & 1, abort_flag, tmo)) break;
@@ -406,14 +426,14 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const uint32_t b_addr = stage_act(s) + (j >> 2) * C::kActBox + (j & 3) * 32;
-            const uint32_t acc = C::kDrainPerGroup ? (j > 0) : (gi > 0 || j > 0);
+            const uint32_t acc = (j > 0 || !d_first) ? 1u : 0u;
             tc_mma_f16_ts(d_tmem + db * C::kDCols, a_tmem + ab * 64 + j * 8,
                           sdesc_kmajor_sw128(b_addr), idesc, acc);
           }
         }
         tc_commit(empty_bar(s));
         tc_commit(aempty_bar(ab));
-        if (C::kDrainPerGroup || gi == ng - 1) tc_commit(dfull_bar(db));
+        if (d_last) tc_commit(dfull_bar(db));
         any = true;
       }
       if (any) {  // let this issuer's MMAs finish before teardown
@@ -465,7 +485,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
             out[c * 8 + j * 2 + 1] = prmt(kT0, kT1, w >> 16) | prmt(kT2, kT3, wx >> 16);
           }
         }
-      } else if constexpr (VARIANT == kW8A16) {
+      } else if constexpr (C::kW8) {
         const uint8_t* wt = stage_w_ptr(s) + r * 128;
         uint4 v[8];
 #pragma unroll
@@ -486,8 +506,13 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
                   __uint_as_float(prmt(wv[q], 0x4B000000u, 0x7650u | (2 * h))) - 8388736.0f;
               const float hi =
                   __uint_as_float(prmt(wv[q], 0x4B000000u, 0x7650u | (2 * h + 1))) - 8388736.0f;
-              __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
-              out[c * 8 + q * 2 + h] = *reinterpret_cast<uint32_t*>(&b2);
+              if constexpr (VARIANT == kW8A8) {  // fp16 against fp16 activation codes
+                __half2 h2 = __floats2half2_rn(lo, hi);
+                out[c * 8 + q * 2 + h] = *reinterpret_cast<uint32_t*>(&h2);
+              } else {
+                __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
+                out[c * 8 + q * 2 + h] = *reinterpret_cast<uint32_t*>(&b2);
+              }
             }
           }
         }
@@ -549,7 +574,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
       // the accumulator this item feeds must have been drained; one warp of
       // the set waits (afull completes only with all four arrivals)
       if (((warp - kConvWarp0) & 3) == 0) {
-        const int di = C::kDrainPerGroup ? i : i / ng;
+        const int di = drain_of(i);
         if (!mbar_wait(dempty_bar(di % kNumD), ((di / kNumD) & 1) ^ 1, abort_flag, tmo)) break;
       }
       tc_fence_after();
@@ -587,7 +612,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
     // per-group scales of this thread's row, walked with a pointer and
     // prefetched one group ahead (the next tile's first one at a tile's end);
     // the e4m3 form reads scale and zero point from the staged record instead
-    constexpr bool kScaleFromGlobal = C::kDrainPerGroup && !C::kFp8;
+    constexpr bool kScaleFromGlobal = C::kDrainPerGroup && !C::kFp8 && !C::kIntAcc;
     const uint16_t* sp = nullptr;
     // (kept as raw fp16 bits until used, so that the load's latency overlaps
     // a whole group; W8A16 has no per-group scale: 1.0)
@@ -613,10 +638,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
       }
 #pragma unroll
       for (int t = 0; t < HB; ++t) R[t] = 0.f;
-      const int nd = C::kDrainPerGroup ? ng : 1;
-      for (int gi = 0; gi < nd; ++gi) {
+      // per-group drains (nc == ng) index groups with gi and items with i
+      for (int gi = 0; gi < nc; ++gi) {
         const int i = k * ng + gi;
-        const int di = C::kDrainPerGroup ? i : k;
+        const int di = k * nc + gi;
         const int db = di % kNumD;
         float s = f16_bits_to_f32(s_next);
         if constexpr (kScaleFromGlobal)
@@ -712,6 +737,14 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
                 if (m < p.M)
                   p.partials[(m * N + n) * G + g] = __float2int_rn(__uint_as_float(v[q2][q]));
               }
+            } else if constexpr (C::kIntAcc) {
+              // exact: the group partial is an integer below 2^24 in fp32; the
+              // running sum is kept as int32 bits in R
+#pragma unroll
+              for (int q = 0; q < CW; ++q) {
+                float& Rq = R[(cb + q2) * CW + q];
+                Rq = __int_as_float(__float_as_int(Rq) + __float2int_rn(__uint_as_float(v[q2][q])));
+              }
             } else {
 #pragma unroll
               for (int q = 0; q < CW; ++q)
@@ -729,6 +762,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
         const float sc = f16_bits_to_f32(__ldg(p.s8 + n));
 #pragma unroll
         for (int t = 0; t < HB; ++t) R[t] *= sc;
+      }
+      if constexpr (C::kIntAcc) {  // W8A8: int32 sums -> s[n] * sum (a_s in store_row)
+        const float sc = f16_bits_to_f32(__ldg(p.s8 + n));
+#pragma unroll
+        for (int t = 0; t < HB; ++t) R[t] = sc * (float)__float_as_int(R[t]);
       }
       if constexpr (!PARTIALS) {
         if (!cluster_reduce) {
@@ -903,9 +941,10 @@ static cudaError_t launch_tc(const GemmArgs& a, cudaStream_t st) {
   using C = TcCfg<VARIANT, BT>;
   CUtensorMap act_map, w8_map;
   memset(&w8_map, 0, sizeof(w8_map));
-  const void* act_ptr = (VARIANT == kW4A8) ? (const void*)a.a_tc : (const void*)a.x;
+  constexpr bool kCodes = (VARIANT == kW4A8 || VARIANT == kW8A8);  // quantized activations
+  const void* act_ptr = kCodes ? (const void*)a.a_tc : (const void*)a.x;
   const CUtensorMapDataType adt =
-      (VARIANT == kW4A8) ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+      kCodes ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   int act3d = 0;
   if constexpr (C::kFp8) {
     if (!make_act_map_planes(&act_map, act_ptr, a.M, a.K, BT)) return cudaErrorInvalidValue;
@@ -914,7 +953,7 @@ static cudaError_t launch_tc(const GemmArgs& a, cudaStream_t st) {
     if (!act3d && !make_map(&act_map, adt, 2, act_ptr, a.M, a.K, 64, BT))
       return cudaErrorInvalidValue;
   }
-  if (VARIANT == kW8A16) {
+  if (C::kW8) {
     if (!make_map(&w8_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.w8, a.N, a.K, 128, 128))
       return cudaErrorInvalidValue;
   }
@@ -938,7 +977,7 @@ static cudaError_t launch_tc(const GemmArgs& a, cudaStream_t st) {
   p.act3d = act3d;
   p.band = persistent ? choose_band(m_tiles, tiles < sms ? tiles : sms,
                                     (double)BT * a.K * 2.0,
-                                    (double)128 * a.K / ((VARIANT == kW8A16) ? 1.0 : 2.0))
+                                    (double)128 * a.K / (C::kW8 ? 1.0 : 2.0))
                       : 1;
   p.a_s = a.a_s;
   p.a_gsum = a.a_gsum;
@@ -992,6 +1031,12 @@ cudaError_t launch_tc_gemm(const GemmArgs& a, cudaStream_t st) {
       return launch_tc_bt<kW4A16, false>(a, st);
     case kW8A16:
       return launch_tc_bt<kW8A16, false>(a, st);
+    case kW8A8:
+      // the fp16 activation-code form exists for M > kTcFp8MaxM only (the
+      // e4m3 planes below it are specific to 4-bit weights); smaller M run
+      // on the GEMV
+      if (a.M <= kTcFp8MaxM) return cudaErrorNotSupported;
+      return launch_tc<kW8A8, 128, false>(a, st);
   }
   return cudaErrorInvalidValue;
 }
