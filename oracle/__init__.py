@@ -60,6 +60,8 @@ def _load():
             lib.oracle_w8a16.restype = None
             lib.oracle_w8a16.argtypes = [vp, vp, vp, i64, i64, i64, vp, vp]
             lib.oracle_w8a8.restype = None
+            lib.oracle_dequant_w4_bf16.restype = None
+            lib.oracle_dequant_w4_bf16.argtypes = [vp, vp, vp, i64, i64, i64, vp]
             lib.oracle_w8a8.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, vp, vp]
             lib.oracle_packed_w4_bytes.restype = i64
             lib.oracle_packed_w4_bytes.argtypes = [i64, i64, i64]
@@ -135,6 +137,15 @@ def w4a16(x_bf16, w_q, s_f16, z, group: int = 128):
     y = np.empty((M, N), np.uint16)
     _load().oracle_w4a16(_p(x), _p(w_q), _p(s_f16), _p(z), M, N, K, group, _p(y64), _p(y))
     return y64, y
+
+
+def dequant_w4_bf16(w_q, s_f16, z, group: int = 128):
+    """bf16 bits [N][K] of s[n,g] * (w_q[n,k] - z[n,g]) (the dense twin's weight)."""
+    w_q, s_f16, z = _c(w_q, np.uint8), _c(s_f16, np.uint16), _c(z, np.uint8)
+    N, K = w_q.shape
+    out = np.empty((N, K), np.uint16)
+    _load().oracle_dequant_w4_bf16(_p(w_q), _p(s_f16), _p(z), N, K, group, _p(out))
+    return out
 
 
 def w8a16(x_bf16, w_q, s_f16):

@@ -22,6 +22,8 @@
  *  - "Serve a pre-quantized int8 weight-only DiT via compressed-tensors ...",
  *    sections "Context" and "Plan": int8 weight-only (W8A16) linears; sections
  *    "Directive after the int8-wo result" and "Round two": W8A8 int8-dynamic.
+ *  - "The 4-bit CPU path", section "W4A16 - PyTorch tinygemm": the
+ *    dequantize-once bf16 weight of the dense comparison path.
  *  - The combination y = a_s * sum_g s * (sum_k a_q*w_q - z * sum_k a_q) is
  *    the plainest reading of those pieces: dequantized weight s*(w_q - z),
  *    dequantized activation a_s*a_q.
@@ -189,6 +191,25 @@ void oracle_w4a16(const uint16_t* x_bf16, const uint8_t* w_q, const uint16_t* s_
       }
       if (y64) y64[m * N + n] = acc;
       if (y_bf16) y_bf16[m * N + n] = oracle_bf16_from_double(acc);
+    }
+}
+
+/* ---- dense twin operand: the int4 weight dequantized once to bf16 -------- */
+
+/* w[n][k] = bf16( s[n,g] * (w_q[n,k] - z[n,g]) ), g = k / group. The product
+ * is exact in fp64 (an 11-bit fp16 significand times an integer of magnitude
+ * at most 15); the one rounding is fp64 -> bf16, ties to even. ("The 4-bit
+ * CPU path", section "W4A16 - PyTorch tinygemm": large batches dequantize the
+ * weight to bf16 once and hand it to an ordinary dense GEMM.) */
+void oracle_dequant_w4_bf16(const uint8_t* w_q, const uint16_t* s_f16, const uint8_t* z,
+                            int64_t N, int64_t K, int64_t group, uint16_t* w_bf16) {
+  int64_t G = K / group;
+  for (int64_t n = 0; n < N; ++n)
+    for (int64_t k = 0; k < K; ++k) {
+      int64_t g = k / group;
+      double v = oracle_fp16_to_double(s_f16[n * G + g]) *
+                 (double)((int64_t)w_q[n * K + k] - (int64_t)z[n * G + g]);
+      w_bf16[n * K + k] = oracle_bf16_from_double(v);
     }
 }
 

@@ -335,6 +335,58 @@ def test_w8a16_matches_dequant_then_matmul(M, N, K):
     assert w8.min() >= -127 and w8.max() <= 127
 
 
+# ------------------------------------------------- dequantized bf16 weight -
+
+def test_dequant_w4_bf16_hand_values():
+    """One 1x128 group per case, worked by hand (fp16 scale bits, code, zero ->
+    bf16 bits): 0.5*(3-1) = 1.0; 0.5*(0-15) = -7.5; (1+2^-10)*3 = 3.0029296875
+    rounds down to 3.0; q == z gives +0."""
+    cases = [(0x3800, 3, 1, 0x3F80), (0x3800, 0, 15, 0xC0F0),
+             (0x3C01, 3, 0, 0x4040), (0x3C00, 7, 7, 0x0000)]
+    for sb, q, z, want in cases:
+        w = np.full((1, 128), q, np.uint8)
+        got = oracle.dequant_w4_bf16(w, np.array([[sb]], np.uint16), np.array([[z]], np.uint8))
+        assert np.all(got == want), (hex(sb), q, z, hex(int(got[0, 0])))
+
+
+def test_dequant_w4_bf16_ties_to_even():
+    """Products exactly halfway between two bf16 values: 1 + 2^-8 lies between
+    1.0 (0x3F80, even) and 1 + 2^-7 (0x3F81); 1 + 3*2^-8 between 0x3F81 and
+    0x3F82 (even). A truncating or round-half-up conversion fails one of them."""
+    for sb, want in [(0x3C04, 0x3F80), (0x3C0C, 0x3F82)]:
+        w = np.full((1, 128), 1, np.uint8)
+        got = oracle.dequant_w4_bf16(w, np.array([[sb]], np.uint16), np.zeros((1, 1), np.uint8))
+        assert np.all(got == want), hex(int(got[0, 0]))
+
+
+def test_dequant_w4_bf16_matches_library_conversion():
+    """Random codes, zeros and scales over several groups: the fp32 product is
+    exact, so torch's fp32 -> bf16 conversion (round to nearest even) of it
+    gives the same bits; a transposed scale index or a sign slip would not."""
+    torch = pytest.importorskip("torch")
+    N, K = 256, 512
+    w = synth.w4_weights(11, 0, 0, N, K)
+    got = oracle.dequant_w4_bf16(w.w_q, w.scale_f16, w.zero)
+    s32 = torch.from_numpy(w.scale_f16.view(np.float16).astype(np.float32))
+    q = torch.from_numpy(w.w_q.astype(np.float32))
+    z = torch.from_numpy(w.zero.astype(np.float32))
+    ref = (s32.repeat_interleave(128, 1) * (q - z.repeat_interleave(128, 1))).to(torch.bfloat16)
+    assert np.array_equal(got, ref.view(torch.int16).numpy().view(np.uint16))
+
+
+def test_dequant_w4_bf16_reproduces_w4a16_on_a_basis_vector():
+    """x = e_k (a one at column k): the W4A16 oracle's fp64 output is exactly
+    the unrounded dequantized weight column, which rounds to the same bits."""
+    N, K = 128, 256
+    w = synth.w4_weights(12, 0, 0, N, K)
+    dq = oracle.dequant_w4_bf16(w.w_q, w.scale_f16, w.zero)
+    for k in (0, 127, 128, 255):
+        x = np.zeros((1, K), np.uint16)
+        x[0, k] = 0x3F80
+        _, y = oracle.w4a16(x, w.w_q, w.scale_f16, w.zero)
+        assert np.array_equal(y[0], dq[:, k])
+
+
 # ---------------------------------------------------------------- W8A8 -----
 
 def test_w8a8_hand_example():
