@@ -234,6 +234,7 @@ class Workload:
         import w4a8_quantized_gemm_gb300 as eg
         self.torch, self.eg, self.dev, self.name, self.path = torch, eg, dev, name, path
         self.api, self._ws = api, {}
+        self.twin_specs = {}
         self.steps_ops = []   # per layer copy: list of (kind, callable-args)
         self.ops_meta = []    # (kind, M, N, K, bytes, ops)
         self.inputs = []      # per copy: list of device tensors fed from host in e2e
@@ -361,6 +362,10 @@ class Workload:
     # one step's launches, as (label, kind, M, N, K, bytes, ops, fn)
     def step_ops(self, copy: int):
         eg, ops = self.eg, []
+        # the same products on dense bf16 weights, for the twin leg:
+        # (label, M, N, K, bf16 activations, packed int4 weight, output)
+        twins = self.twin_specs.setdefault(copy, [])
+        twins.clear()
         if self.name in ("decode", "prefill", "tiny", "linear", "model"):
             layers = [self.layers[copy]] if self.name != "model" else self.layers
             for M in self.ms:
@@ -389,6 +394,7 @@ class Workload:
                                         quant_bytes(M, K), 0,
                                         (lambda xd=xd, a=a: eg.quant_act(xd, out=a))))
                         y = self.ys[(M, nm)]
+                        twins.append((f"{nm} M={M}", M, N, K, xd, packs[nm], y))
                         ops.append((f"{nm} M={M}", "w4a8", M, N, K, w4a8_bytes(M, N, K),
                                     2 * M * N * K,
                                     (lambda a=a, p=packs[nm], N=N, K=K, y=y:
@@ -399,6 +405,7 @@ class Workload:
                     ops.append((f"quant head M={M}", "quant", M, 0, K, quant_bytes(M, K), 0,
                                 (lambda xd=xd, a=a: eg.quant_act(xd, out=a))))
                     y = self.ys[(M, "head")]
+                    twins.append((f"head M={M}", M, N, K, xd, self.head, y))
                     ops.append((f"head M={M}", "w4a8", M, N, K, w4a8_bytes(M, N, K),
                                 2 * M * N * K,
                                 (lambda a=a, p=self.head, N=N, K=K, y=y:
@@ -423,6 +430,7 @@ class Workload:
                                      eg.w8a8_gemm(a, w8, s8, out=y, path=self.path))))
                     if "w4" in self.dit_variants:
                         y4 = self.ys[(M, K, N, "w4")]
+                        twins.append((f"K={K} N={N} M={M}", M, N, K, xd, p4, y4))
                         ops.append((f"w4a16 K={K} N={N} M={M}", "w4a16", M, N, K,
                                     w4a16_bytes(M, N, K), 2 * M * N * K,
                                     (lambda xd=xd, p=p4, N=N, K=K, y=y4:
@@ -629,8 +637,7 @@ def run_ours(args, rank, world):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "int8 x int4 -> exact int32 group partials, f32 combine, bf16 out"
-                 if args.workload != "dit" else "bf16 x int4/int8 -> f32, bf16 out",
+        "dtype": dtype_string(args),
         "data": "synthetic (seeded splitmix64/Box-Muller; 7B/DiT shapes, random weights)",
         "config": workload_config(args, wl, per_step_bytes, per_step_ops),
         "tops": round(per_step_ops * args.steps * world / (ms_total * 1e-3) / 1e12, 4),
@@ -648,9 +655,88 @@ def run_ours(args, rank, world):
         "path": args.path,
         "device_status": status,
     }
+    if args.twin:
+        twin = measure_twin(args, wl, step_ops, stream, unit_is_ops)
+        if twin is not None:
+            twin["int4_kernels_ms_per_step"] = round(
+                sum(v["ms"] for k, v in per_kernel.items() if k.startswith(("tc_gemm", "gemv_w4")))
+                / args.steps, 5)
+            result["bf16_twin"] = twin
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(args, wl, unit_is_ops, budget_s=args.cpu_budget)
     return result
+
+
+def measure_twin(args, wl, step_ops, stream, unit_is_ops):
+    """The dense bf16 twin: every int4 product of the step on weights
+    dequantized once to bf16 (egopq_dequant_w4), each run as a plain cuBLAS
+    bf16 GEMM (torch.matmul) on the same bf16 activations -- the speed a
+    dequantize-once path gets, and the dense-GEMM yardstick for the packed
+    kernels. Timed like the main leg: one CUDA graph per layer copy, K replays."""
+    import torch
+
+    eg = wl.eg
+    dense, t_dq = {}, 0.0
+    graphs, flops, nbytes = [], 0, 0
+    for c in range(wl.n_copies):
+        specs = wl.twin_specs.get(c, [])
+        for (_, M, N, K, xd, packed, y) in specs:
+            key = packed.data_ptr()
+            if key not in dense:
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                with torch.cuda.stream(stream):
+                    a.record(stream)
+                    dense[key] = eg.dequant_w4(packed, N, K, stream=stream)
+                    b.record(stream)
+                stream.synchronize()
+                t_dq += a.elapsed_time(b)
+        if c == 0:
+            flops = sum(2 * M * N * K for (_, M, N, K, *_r) in specs)
+            nbytes = sum(2 * N * K + 2 * M * K + 2 * M * N for (_, M, N, K, *_r) in specs)
+    if not flops:
+        return None
+    outs = {}
+    with torch.cuda.stream(stream):
+        for c in range(wl.n_copies):
+            for (lab, M, N, K, xd, packed, y) in wl.twin_specs[c]:
+                torch.matmul(xd, dense[packed.data_ptr()].t(), out=y)  # warm-up, cuBLAS heuristics
+    stream.synchronize()
+    for c in range(wl.n_copies):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for (lab, M, N, K, xd, packed, y) in wl.twin_specs[c]:
+                torch.matmul(xd, dense[packed.data_ptr()].t(), out=y)
+        graphs.append(g)
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            graphs[i % len(graphs)].replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(args.steps):
+            graphs[i % len(graphs)].replay()
+        e1.record(stream)
+    stream.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    dense_bytes = sum(t.numel() * 2 for t in dense.values())
+    del dense, outs, graphs
+    torch.cuda.empty_cache()
+    return {"kernel": "cuBLAS bf16 GEMM (torch.matmul) on weights dequantized once by "
+                      "egopq_dequant_w4",
+            "value": round((flops if unit_is_ops else nbytes) / (ms * 1e-3)
+                           / (1e12 if unit_is_ops else 1e9), 3),
+            "unit": "TFLOP/s" if unit_is_ops else "GB/s (bf16 weights)",
+            "ms_per_step": round(ms, 5), "tflops": round(flops / (ms * 1e-3) / 1e12, 2),
+            "products_per_step": sum(len(v) for v in wl.twin_specs.values()) // max(1, wl.n_copies),
+            "dequant_once_ms": round(t_dq, 3), "dense_weight_bytes": dense_bytes}
+
+
+def dtype_string(args) -> str:
+    v = args.variant if args.workload == "linear" else ("w4a16" if args.workload == "dit" else "w4a8")
+    return {"w4a8": "int8 x int4 -> exact int32 group partials, f32 combine, bf16 out",
+            "w8a8": "int8 x int8 -> exact int32 sums, f32 combine, bf16 out",
+            "w4a16": "bf16 x int4/int8 -> f32, bf16 out" if args.workload == "dit"
+                     else "bf16 x int4 -> f32, bf16 out",
+            "w8a16": "bf16 x int8 -> f32, bf16 out"}[v]
 
 
 def workload_description(args) -> str:
@@ -756,7 +842,8 @@ def run_reference(args, rank, world):
                       [(3072, 3072), (3072, 12288), (12288, 3072)]],
               "tiny": [(16, 512, 256)],
               "linear": [(args.m, args.k, args.n)]}[args.workload]
-    kind = {"dit": "w4a16", "linear": args.variant}.get(args.workload, "w4a8")
+    kind = args.variant if args.workload == "linear" else (
+        "w4a16" if args.workload == "dit" else "w4a8")
     wl.step_ops = lambda c: [(f"M={M} K={K} N={N}", kind, M, N, K, 0, 0, None)
                              for (M, K, N) in shapes]
     # each step a bounded sample of the workload, sized so that the whole
@@ -803,6 +890,9 @@ def main():
     ap.add_argument("--n", type=int, default=3584, help="N for --workload linear")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--twin", action="store_true",
+                    help="also time the dense bf16 twin: the step's int4 products as cuBLAS "
+                         "bf16 GEMMs on weights dequantized once")
     ap.add_argument("--path", choices=["auto", "gemv", "tc"], default="auto")
     ap.add_argument("--variant", choices=["w4a8", "w4a16", "w8a16", "w8a8"], default="w4a8",
                     help="variant for --workload linear")

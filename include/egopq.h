@@ -98,6 +98,17 @@ size_t egopq_packed_w4_bytes(int64_t N, int64_t K, int group);
 int egopq_pack_w4(const uint8_t* w_q, const uint16_t* scale_f16, const uint8_t* zero,
                   int64_t N, int64_t K, int group, void* packed, egopq_stream_t stream);
 
+/* Dequantize a packed weight once to dense bf16 (device w_bf16 [N][K],
+ * row-major, caller-allocated 2*N*K bytes):
+ *   w[n][k] = bf16( s[n,g] * (w_q[n,k] - z[n,g]) ),  g = k / 128,
+ * the product exact in fp32, one round-to-nearest-even conversion. This is the
+ * operand of the dense comparison path that large batches can take (dequantize
+ * once, then an ordinary bf16 GEMM: "The 4-bit CPU path", section "W4A16 -
+ * PyTorch tinygemm"). Asynchronous on `stream`; shape errors as for
+ * egopq_pack_w4. */
+int egopq_dequant_w4(const void* packed, int64_t N, int64_t K, int group, uint16_t* w_bf16,
+                     egopq_stream_t stream);
+
 /* Inverse of egopq_pack_w4 (test and inspection aid). */
 int egopq_unpack_w4(const void* packed, int64_t N, int64_t K, int group, uint8_t* w_q,
                     uint16_t* scale_f16, uint8_t* zero, egopq_stream_t stream);

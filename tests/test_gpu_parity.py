@@ -258,6 +258,30 @@ def test_weight_only_dit_shapes_sampled(K, N, M):
     check_bf16_output(y8[np.ix_(rows, cols)], r8, f"W8A16 DiT K={K} N={N} M={M}")
 
 
+# ------------------------------------------- dense bf16 twin: dequantize once
+
+@pytest.mark.parametrize("N,K", [(128, 128), (384, 1024), (3584, 18944)])
+def test_dequant_w4_bit_exact(N, K):
+    """egopq_dequant_w4 against the oracle, every element, bit for bit."""
+    w = synth.w4_weights(6, 0, 0, N, K)
+    packed = eg.pack_w4(*dev_weights(w))
+    got = to_host_bits(eg.dequant_w4(packed, N, K))
+    assert np.array_equal(got, oracle.dequant_w4_bf16(w.w_q, w.scale_f16, w.zero))
+
+
+def test_dequant_w4_head_sampled_rows():
+    """The 152064 x 3584 output head (1.09 GB of bf16): sampled rows from the
+    first, last and random 128-row blocks."""
+    N, K = 152064, 3584
+    w = synth.w4_weights(6, 1, synth.LINEARS["head"], N, K)
+    dq = eg.dequant_w4(eg.pack_w4(*dev_weights(w)), N, K)
+    rng = np.random.default_rng(5)
+    rows = np.unique(np.concatenate([[0, 1, 127, 128, N - 1], rng.choice(N, 64, replace=False)]))
+    got = to_host_bits(dq[torch.from_numpy(rows).cuda()])
+    ref = oracle.dequant_w4_bf16(w.w_q[rows], w.scale_f16[rows], w.zero[rows])
+    assert np.array_equal(got, ref)
+
+
 # ------------------------------------------------- W8A8 int8-dynamic output
 
 def run_w8a8(x, w8, s8, path):

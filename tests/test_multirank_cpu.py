@@ -42,8 +42,8 @@ def test_reference_arm_prints_on_rank0_only():
     import argparse
 
     import bench
-    args = argparse.Namespace(workload="tiny", steps=1, warmup=0, m=1, k=512, n=256,
-                              cpu_budget=0.5, impl="reference")
+    args = argparse.Namespace(workload="tiny", variant="w4a8", steps=1, warmup=0, m=1, k=512,
+                              n=256, cpu_budget=0.5, impl="reference")
     assert bench.run_reference(args, rank=1, world=2) is None
     res = bench.run_reference(args, rank=0, world=2)
     assert res["impl"] == "reference" and res["value"] > 0

@@ -63,6 +63,7 @@ def load() -> ctypes.CDLL:
             "egopq_packed_w4_bytes": (sz, [i64, i64, i32]),
             "egopq_pack_w4": (i32, [vp, vp, vp, i64, i64, i32, vp, vp]),
             "egopq_unpack_w4": (i32, [vp, i64, i64, i32, vp, vp, vp, vp]),
+            "egopq_dequant_w4": (i32, [vp, i64, i64, i32, vp, vp]),
             "egopq_quant_act_i8": (i32, [vp, i64, i64, i32, vp, vp, vp, vp, vp]),
             "egopq_w4a8_gemm": (i32, [vp, vp, vp, vp, vp, i64, i64, i64, i32, vp, vp]),
             "egopq_w4a8_gemm_ex": (i32, [vp, vp, vp, vp, vp, i64, i64, i64, i32, vp, i32, vp]),
@@ -154,6 +155,15 @@ def unpack_w4(packed: torch.Tensor, N: int, K: int, stream=None):
     _check(load().egopq_unpack_w4(_ptr(packed), N, K, GROUP, _ptr(w), _ptr(s), _ptr(z),
                                   _stream(stream)))
     return w, s, z
+
+
+def dequant_w4(packed: torch.Tensor, N: int, K: int, out: Optional[torch.Tensor] = None,
+               stream=None) -> torch.Tensor:
+    """The packed weight dequantized once to dense bf16 [N, K]."""
+    if out is None:
+        out = torch.empty((N, K), dtype=torch.bfloat16, device=packed.device)
+    _check(load().egopq_dequant_w4(_ptr(packed), N, K, GROUP, _ptr(out), _stream(stream)))
+    return out
 
 
 class QuantAct(NamedTuple):

@@ -2,8 +2,9 @@
 
 Every translation unit compiles in parallel with
 `-gencode arch=compute_103a,code=sm_103a` (the explicit `a` target is what
-enables tcgen05 and TMA), as relocatable device code so that all kernels share
-the library's one device error word, then nvcc links the shared library.
+enables tcgen05 and TMA) as a whole program -- no relocatable device code,
+under which ptxas ignores per-warpgroup register budgets (setmaxnreg) -- and
+nvcc links the shared library. Each unit keeps its own device error word.
 """
 from __future__ import annotations
 
@@ -19,7 +20,7 @@ LIB = os.path.join(BUILD, "libegopq.so")
 SOURCES = ["egopq_api.cu", "quant_pack.cu", "gemv.cu", "tc_gemm.cu", "no_alloc.cu"]
 HEADERS = ["egopq_common.cuh", "egopq_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-rdc=true", "-Xcompiler", "-fPIC",
+FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                 "-Xcompiler", "-Wall", "-Xcompiler", "-Wno-unknown-pragmas"]
 
 
@@ -67,7 +68,7 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
             sys.stderr.write(log)
     if jobs or force or _stale(LIB, objs):
         tmp = LIB + f".tmp{os.getpid()}"
-        cmd = [nvcc] + ARCH + ["-shared", "-rdc=true", "-o", tmp] + objs
+        cmd = [nvcc] + ARCH + ["-shared", "-o", tmp] + objs
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed: {' '.join(cmd)}\n{r.stdout}\n{r.stderr}")

@@ -9,7 +9,6 @@
 #include "egopq_internal.h"
 
 namespace egopq {
-__device__ unsigned int g_error_word = 0;
 }
 
 using namespace egopq;
@@ -139,6 +138,17 @@ int egopq_unpack_w4(const void* packed, int64_t N, int64_t K, int group, uint8_t
   if ((rc = check_arch())) return rc;
   cudaError_t e = launch_unpack_w4(packed, N, K, w_q, scale_f16, zero, (cudaStream_t)stream);
   return e == cudaSuccess ? EGOPQ_OK : cuda_fail(e, "unpack_w4 launch");
+}
+
+int egopq_dequant_w4(const void* packed, int64_t N, int64_t K, int group, uint16_t* w_bf16,
+                     egopq_stream_t stream) {
+  int rc = check_w4_shape(0, N, K, group);
+  if (rc) return rc;
+  rc = check_ptrs(2, "packed", packed, "w_bf16", w_bf16);
+  if (rc) return rc;
+  if ((rc = check_arch())) return rc;
+  cudaError_t e = launch_dequant_w4(packed, N, K, w_bf16, (cudaStream_t)stream);
+  return e == cudaSuccess ? EGOPQ_OK : cuda_fail(e, "dequant_w4 launch");
 }
 
 int egopq_quant_act_i8(const uint16_t* x_bf16, int64_t M, int64_t K, int group, int8_t* a_q,
@@ -382,14 +392,15 @@ int egopq_device_status(egopq_stream_t stream) {
   cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
   unsigned int word = 0;
-  e = cudaMemcpyFromSymbol(&word, g_error_word, sizeof(word));
-  if (e != cudaSuccess) return cuda_fail(e, "read error word");
-  if (word) {
-    const unsigned int zero = 0;
-    e = cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero));
-    if (e != cudaSuccess) return cuda_fail(e, "clear error word");
-    if (word & kErrTimeout) return fail(EGOPQ_ERR_TIMEOUT, "a kernel's bounded wait expired");
+  cudaError_t (*const take[])(unsigned*) = {take_error_word_quant_pack, take_error_word_gemv,
+                                            take_error_word_tc_gemm};
+  for (auto fn : take) {
+    unsigned int w = 0;
+    e = fn(&w);
+    if (e != cudaSuccess) return cuda_fail(e, "read and clear a device error word");
+    word |= w;
   }
+  if (word & kErrTimeout) return fail(EGOPQ_ERR_TIMEOUT, "a kernel's bounded wait expired");
   return EGOPQ_OK;
 }
 

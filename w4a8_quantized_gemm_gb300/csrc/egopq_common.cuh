@@ -18,8 +18,20 @@ namespace egopq {
 
 // ---- device error word ----------------------------------------------------
 // Bit 0: a bounded wait expired (EGOPQ_ERR_TIMEOUT on the host side).
+// One word per translation unit: the library compiles every unit as a whole
+// program (no relocatable device code), which is what lets ptxas honour
+// per-warpgroup register budgets (setmaxnreg). Each unit with kernels exports
+// a take_error_word_* function; the host ORs and clears them all.
 constexpr unsigned kErrTimeout = 1u;
-extern __device__ unsigned int g_error_word;
+static __device__ unsigned int g_error_word = 0;
+
+// Host: read this unit's word and clear it if set.
+static inline cudaError_t take_local_error_word(unsigned* out) {
+  cudaError_t e = cudaMemcpyFromSymbol(out, g_error_word, sizeof(unsigned));
+  if (e != cudaSuccess || *out == 0) return e;
+  const unsigned zero = 0;
+  return cudaMemcpyToSymbol(g_error_word, &zero, sizeof(unsigned));
+}
 
 __device__ __forceinline__ void raise_error(unsigned bits) { atomicOr(&g_error_word, bits); }
 
@@ -212,6 +224,19 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
       "r"(r[15])
       : "memory");
+}
+
+// Per-warpgroup register budget (all four warps execute the same one; R a
+// multiple of 8 in [24, 256]). An increase waits until other warpgroups of
+// the block have released enough, so the budgets must add up to at most what
+// the block was launched with.
+template <int R>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(R));
+}
+template <int R>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(R));
 }
 
 // Shared-memory matrix descriptor (tcgen05 form) for a K-major operand staged

@@ -39,6 +39,13 @@ cudaError_t launch_pack_w4(const uint8_t* w_q, const uint16_t* s, const uint8_t*
                            int64_t K, void* packed, cudaStream_t st);
 cudaError_t launch_unpack_w4(const void* packed, int64_t N, int64_t K, uint8_t* w_q, uint16_t* s,
                              uint8_t* z, cudaStream_t st);
+cudaError_t launch_dequant_w4(const void* packed, int64_t N, int64_t K, uint16_t* w,
+                              cudaStream_t st);
+
+// Each kernel unit's device error word, read and cleared (see egopq_common.cuh).
+cudaError_t take_error_word_quant_pack(unsigned* out);
+cudaError_t take_error_word_gemv(unsigned* out);
+cudaError_t take_error_word_tc_gemm(unsigned* out);
 
 // CUDA-core GEMV (small M). Returns cudaErrorNotSupported for shapes it does
 // not take.

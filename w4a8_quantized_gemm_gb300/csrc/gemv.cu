@@ -573,4 +573,6 @@ cudaError_t launch_gemv(const GemmArgs& a, cudaStream_t st) {
   return cudaSuccess;
 }
 
+cudaError_t take_error_word_gemv(unsigned* out) { return take_local_error_word(out); }
+
 }  // namespace egopq

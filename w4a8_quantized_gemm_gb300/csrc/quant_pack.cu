@@ -266,6 +266,41 @@ __global__ void unpack_meta_kernel(const uint8_t* __restrict__ in, int64_t N, in
   }
 }
 
+// Dequantize once: w[n][k] = bf16(s[n,g] * (w_q[n,k] - z[n,g])). One CTA per
+// packed record (a 128-row x 128-K block); thread (c, r) reads the 16 code
+// bytes of row r, K offsets c*32 .. c*32+31 (consecutive threads, consecutive
+// 16-byte units) and writes those 32 values as 64 contiguous bytes of row n.
+// The fp32 product is exact (11-bit scale significand times |q - z| <= 15),
+// so the one rounding is the bf16 conversion (nearest, ties to even).
+constexpr int kDequantThreads = 512;
+
+__global__ void __launch_bounds__(kDequantThreads)
+dequant_w4_kernel(const uint8_t* __restrict__ in, int64_t G, int64_t K, uint16_t* __restrict__ w) {
+  const int64_t rec = blockIdx.x;
+  const int64_t t = rec / G, g = rec % G;
+  const int c = threadIdx.x / 128, r = threadIdx.x % 128;
+  const uint8_t* rp = in + rec * kRecBytes;
+  const uint4 v = *reinterpret_cast<const uint4*>(rp + (c * 128 + r) * 16);
+  const float s = __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t*>(rp + 8192 + 2 * r)));
+  const uint8_t zb = rp[8448 + r / 2];
+  const int z = (r & 1) ? (zb >> 4) : (zb & 0xF);
+  const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+  uint16_t* dst = w + (t * 128 + r) * K + g * 128 + c * 32;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    uint32_t o[4] = {0u, 0u, 0u, 0u};  // bf16 pairs in K order
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+      const int q = (int)((words[j] >> (4 * p)) & 0xF);
+      // nibble p of a word: K offset 2p (p < 4) or 2(p - 4) + 1
+      const int kk = p < 4 ? 2 * p : 2 * (p - 4) + 1;
+      const uint32_t bits = __bfloat16_as_ushort(__float2bfloat16_rn(s * (float)(q - z)));
+      o[kk >> 1] |= bits << (16 * (kk & 1));
+    }
+    *reinterpret_cast<uint4*>(dst + j * 8) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
 static unsigned grid_for(int64_t work, int threads) {
   int64_t b = (work + threads - 1) / threads;
   return (unsigned)(b < 1 ? 1 : (b > 65535 * 8 ? 65535 * 8 : b));
@@ -312,5 +347,18 @@ cudaError_t launch_unpack_w4(const void* packed, int64_t N, int64_t K, uint8_t* 
   unpack_meta_kernel<<<grid_for(G * N, 256), 256, 0, st>>>(base, N, G, s, z);
   return cudaGetLastError();
 }
+
+cudaError_t launch_dequant_w4(const void* packed, int64_t N, int64_t K, uint16_t* w,
+                              cudaStream_t st) {
+  const int64_t G = K / 128;
+  const int64_t recs = (N / 128) * G;
+  if (recs <= 0) return cudaSuccess;
+  if (recs > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  dequant_w4_kernel<<<(unsigned)recs, kDequantThreads, 0, st>>>(
+      static_cast<const uint8_t*>(packed), G, K, w);
+  return cudaGetLastError();
+}
+
+cudaError_t take_error_word_quant_pack(unsigned* out) { return take_local_error_word(out); }
 
 }  // namespace egopq

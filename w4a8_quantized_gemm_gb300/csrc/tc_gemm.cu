@@ -158,7 +158,25 @@ struct TcCfg {
   static constexpr int kDrainCols = BT / kDrainWGs;  // token columns per drain thread
   static constexpr int kProducerWarp = kConvWarp0 + 4 * kConvSets;
   static constexpr int kMmaWarp = kProducerWarp + 1;  // first issuer; allocates TMEM
-  static constexpr int kThreads = 32 * (kMmaWarp + kMmaWarps);
+  // Register split (128-token per-group tiles): the drain threads hold 64
+  // running sums each, so with an even split they can keep only 16 TMEM
+  // columns in flight and the drain, latency-bound, paces the pipeline. The
+  // block is padded to whole warpgroups (setmaxnreg acts per warpgroup) and
+  // the drain warpgroups take registers from the converter warpgroups (which
+  // then convert 16 words at a time) and from the producer/issuer warpgroup.
+  static constexpr bool kRegSplit = kWide;
+  static constexpr int kWarpsUsed = kMmaWarp + kMmaWarps;
+  static constexpr int kWarps = kRegSplit ? (kWarpsUsed + 3) / 4 * 4 : kWarpsUsed;
+  static constexpr int kThreads = 32 * kWarps;
+  static constexpr int kRegDrain = 120, kRegConv = 96, kRegOther = 48;
+  // converters below 96 registers cannot hold a converted group: they then
+  // wait for their buffers first and convert 16 words at a time
+  static constexpr bool kConvChunked = kRegSplit && kRegConv < 96;
+  // drain: TMEM columns in flight per wait at 64 running sums per thread
+  static constexpr int kDrainInFlight = !kRegSplit ? 16 : (kRegDrain >= 144 ? 64 : 32);
+  // registers every thread has at launch (ptxas holds a kernel that uses
+  // setmaxnreg at its launch-bounds maximum; the launcher checks it)
+  static constexpr int kRegLaunch = (65536 / kThreads) / 8 * 8;
   static constexpr int kBf16 = (VARIANT == kW4A8 || VARIANT == kW8A8) ? 0 : 1;  // fp16 codes
   static_assert(kStages >= 2, "shared memory too small for two stages");
   static_assert(kSmemBytes <= kSmemLimit, "shared memory");
@@ -173,8 +191,56 @@ struct TcCfg {
                 "buffer reuse waits");
   static_assert(8 * (2 * kStages + 2 * kNumA + 2 * kNumD + kMmaWarps) + 8 <= 1024, "barrier region");
   static_assert(BT % 16 == 0 && BT >= 16 && BT <= 128, "token tile");
+  // the split hands out exactly the registers the block was launched with
+  static_assert(!kRegSplit || (kWarps / 4 == kDrainWGs + kConvSets + 1 &&
+                               kDrainWGs * kRegDrain + kConvSets * kRegConv + kRegOther <=
+                                   (kWarps / 4) * kRegLaunch),
+                "register split");
   static_assert(kStageBytes % 1024 == 0, "stage alignment");
 };
+
+// 32 packed int4 codes of one weight row (one 16-byte unit of the record:
+// K offsets 0..31 of a 32-wide slice, nibble order as packed) -> 16 words of
+// the tensor-core A operand, zero point folded in: fp16 (w - z) pairs for
+// W4A8, bf16 pairs for W4A16; both exact.
+template <int VARIANT>
+__device__ __forceinline__ void cvt_w4_unit(const uint4& v, uint32_t z, uint32_t (&o)[16]) {
+  const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+  if constexpr (VARIANT == kW4A8) {
+    // fp16: 0x6400|e = 1024+e, 0x6400|(e<<4) = 1024+16e (exact)
+    const __half2 zlo = __half2half2(__ushort_as_half((uint16_t)(0x6400u | z)));
+    const __half2 nzhi = __half2half2(__float2half_rn(-64.0f - (float)z));
+    const __half2 sixteenth = __float2half2_rn(0.0625f);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t w = wv[j], w2 = wv[j] >> 8;
+      uint32_t h0 = lop3_and_or(w, 0x000F000Fu, 0x64006400u);
+      uint32_t h1 = lop3_and_or(w, 0x00F000F0u, 0x64006400u);
+      uint32_t h2 = lop3_and_or(w2, 0x000F000Fu, 0x64006400u);
+      uint32_t h3 = lop3_and_or(w2, 0x00F000F0u, 0x64006400u);
+      __half2 r0 = __hsub2(*reinterpret_cast<__half2*>(&h0), zlo);
+      __half2 r1 = __hfma2(*reinterpret_cast<__half2*>(&h1), sixteenth, nzhi);
+      __half2 r2 = __hsub2(*reinterpret_cast<__half2*>(&h2), zlo);
+      __half2 r3 = __hfma2(*reinterpret_cast<__half2*>(&h3), sixteenth, nzhi);
+      o[j * 4 + 0] = *reinterpret_cast<uint32_t*>(&r0);
+      o[j * 4 + 1] = *reinterpret_cast<uint32_t*>(&r1);
+      o[j * 4 + 2] = *reinterpret_cast<uint32_t*>(&r2);
+      o[j * 4 + 3] = *reinterpret_cast<uint32_t*>(&r3);
+    }
+  } else {
+    // bf16: 0x4300|e = 128+e (exact for e < 128)
+    const __nv_bfloat162 zz = __bfloat162bfloat162(__ushort_as_bfloat16((uint16_t)(0x4300u | z)));
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t h = lop3_and_or(wv[j] >> (4 * q), 0x000F000Fu, 0x43004300u);
+        __nv_bfloat162 rr = __hsub2(*reinterpret_cast<__nv_bfloat162*>(&h), zz);
+        o[j * 4 + q] = *reinterpret_cast<uint32_t*>(&rr);
+      }
+    }
+  }
+}
 
 // y[m0+t][n] = bf16(a_s[m0+t] * R[t]) (W4A8) or bf16(R[t]), t < HB, rows < M.
 // Eight rows at a time, with a compiler barrier between chunks so the a_s
@@ -214,7 +280,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
   uint8_t* smem = smem_raw + (base - raw_addr);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t N = p.N, K = p.K;
+  const int64_t N = p.N;
   const int G = p.G;
 
   // ---- this CTA's work: a flat sequence of (tile, group) items ---------------
@@ -243,7 +309,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
   auto drain_of = [&](int i) -> int {
     if constexpr (GPD == 1) return i;
     else if constexpr (GPD == 0) return i / ng;
-    else return (i / ng) * nc + (i % ng) / GPD;
+    else return (i / ng) * nc + (i % ng) / (GPD > 1 ? GPD : 1);
   };
   // tile u -> (mt, nt). Persistent grids walk bands of p.band m-tiles, m
   // fastest inside a band, so the tiles in flight at once share a few
@@ -317,7 +383,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
   const uint64_t tmo = p.timeout_ns;
   const bool cluster_reduce = !PARTIALS && !p.persistent && p.ks > 1;
 
-  // Each role ends with the same named CTA barrier (all 448 threads) and, for
+  // Each role ends with the same named CTA barrier (every thread) and, for
   // split-K clusters, the same two cluster barriers, so the drain warps can
   // keep their accumulators in registers through the epilogue.
   auto teardown_sync = [&]() {
@@ -325,7 +391,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
     asm volatile("bar.sync 1, %0;" ::"n"(C::kThreads) : "memory");
   };
 
-  if (warp == C::kProducerWarp) {
+  auto producer_role = [&]() {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       // item i = (unit i / ng, group g0 + i % ng), walked with counters
@@ -396,7 +462,16 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
       cluster_sync_all();
       cluster_sync_all();
     }
-  } else if (warp >= C::kMmaWarp) {
+  };
+  auto pad_role = [&]() {
+    // ------------------------------------------------------------ padding warps
+    teardown_sync();
+    if (cluster_reduce) {
+      cluster_sync_all();
+      cluster_sync_all();
+    }
+  };
+  auto mma_role = [&]() {
     // ------------------------------------------------------------ MMA issuers
     // issuer q takes groups q, q + kMmaWarps, ...
     const int q = warp - C::kMmaWarp;
@@ -409,8 +484,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
         const int di = drain_of(i);
         const int db = di % kNumD;
         // first group of its accumulator; last group of it
-        const bool d_first = GPD == 1 || (GPD == 0 ? gi == 0 : gi % GPD == 0);
-        const bool d_last = GPD == 1 || gi == ng - 1 || (GPD > 1 && gi % GPD == GPD - 1);
+        constexpr int kGpd = GPD > 1 ? GPD : 1;  // (a divisor in every instantiation)
+        const bool d_first = GPD == 1 || (GPD == 0 ? gi == 0 : gi % kGpd == 0);
+        const bool d_last = GPD == 1 || gi == ng - 1 || (GPD > 1 && gi % kGpd == kGpd - 1);
         // one wait per group: the converters arrive on afull only once the
         // stage has landed, the A buffer is free and the accumulator drained
         if (!mbar_wait(afull_bar(ab), (i / kNumA) & 1, abort_flag, tmo)) break;
@@ -452,7 +528,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
       cluster_sync_all();
       cluster_sync_all();
     }
-  } else if (warp >= kConvWarp0) {
+  };
+  auto conv_role = [&]() {
     // ------------------------------------------------------------ converters
     const int r = ((warp - kConvWarp0) & 3) * 32 + lane;  // weight row == TMEM lane
     const int set = (warp - kConvWarp0) >> 2;             // this set converts items set, +sets..
@@ -525,48 +602,34 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
         __syncwarp();
         if (lane == 0) mbar_arrive(empty_bar(s));
         const uint32_t z = (r & 1) ? (zb >> 4) : (zb & 0xF);
-        if constexpr (VARIANT == kW4A8) {
-          // fp16: 0x6400|e = 1024+e, 0x6400|(e<<4) = 1024+16e (exact)
-          const __half2 zlo = __half2half2(__ushort_as_half((uint16_t)(0x6400u | z)));
-          const __half2 nzhi = __half2half2(__float2half_rn(-64.0f - (float)z));
-          const __half2 sixteenth = __float2half2_rn(0.0625f);
+        if constexpr (C::kConvChunked) {
+          // few registers: wait for the buffers first, then convert and store
+          // one 16-word unit at a time
+          if (!mbar_wait(aempty_bar(ab), ((i / kNumA) & 1) ^ 1, abort_flag, tmo)) break;
+          if (((warp - kConvWarp0) & 3) == 0) {
+            const int di = drain_of(i);
+            if (!mbar_wait(dempty_bar(di % kNumD), ((di / kNumD) & 1) ^ 1, abort_flag, tmo)) break;
+          }
+          tc_fence_after();
+          const uint32_t dst = a_tmem + lane_base + ab * C::kACols;
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
-            const uint32_t wv[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const uint32_t w = wv[j], w2 = wv[j] >> 8;
-              uint32_t h0 = lop3_and_or(w, 0x000F000Fu, 0x64006400u);
-              uint32_t h1 = lop3_and_or(w, 0x00F000F0u, 0x64006400u);
-              uint32_t h2 = lop3_and_or(w2, 0x000F000Fu, 0x64006400u);
-              uint32_t h3 = lop3_and_or(w2, 0x00F000F0u, 0x64006400u);
-              __half2 r0 = __hsub2(*reinterpret_cast<__half2*>(&h0), zlo);
-              __half2 r1 = __hfma2(*reinterpret_cast<__half2*>(&h1), sixteenth, nzhi);
-              __half2 r2 = __hsub2(*reinterpret_cast<__half2*>(&h2), zlo);
-              __half2 r3 = __hfma2(*reinterpret_cast<__half2*>(&h3), sixteenth, nzhi);
-              out[c * 16 + j * 4 + 0] = *reinterpret_cast<uint32_t*>(&r0);
-              out[c * 16 + j * 4 + 1] = *reinterpret_cast<uint32_t*>(&r1);
-              out[c * 16 + j * 4 + 2] = *reinterpret_cast<uint32_t*>(&r2);
-              out[c * 16 + j * 4 + 3] = *reinterpret_cast<uint32_t*>(&r3);
-            }
+            uint32_t chunk[16];
+            cvt_w4_unit<VARIANT>(v[c], z, chunk);
+            tmem_st16(dst + c * 16, chunk);
           }
-        } else {
-          // bf16: 0x4300|e = 128+e (exact for e < 128)
-          const __nv_bfloat162 zz =
-              __bfloat162bfloat162(__ushort_as_bfloat16((uint16_t)(0x4300u | z)));
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(afull_bar(ab));
+          continue;
+        }
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const uint32_t wv[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+        for (int c = 0; c < 4; ++c) {
+          uint32_t chunk[16];
+          cvt_w4_unit<VARIANT>(v[c], z, chunk);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                uint32_t h = lop3_and_or(wv[j] >> (4 * q), 0x000F000Fu, 0x43004300u);
-                __nv_bfloat162 rr = __hsub2(*reinterpret_cast<__nv_bfloat162*>(&h), zz);
-                out[c * 16 + j * 4 + q] = *reinterpret_cast<uint32_t*>(&rr);
-              }
-            }
-          }
+          for (int q = 0; q < 16; ++q) out[c * 16 + q] = chunk[q];
         }
       }
       // A buffer ab is free once the MMAs of item i - kNumA have completed
@@ -597,7 +660,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
       cluster_sync_all();
       cluster_sync_all();
     }
-  } else {
+  };
+  auto drain_role = [&]() {
     // ------------------------------------------------------------ drain
     const int r = (warp & 3) * 32 + lane;
     const int col0 = (warp >> 2) * HB;
@@ -713,10 +777,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
         } else {
         // columns per tcgen05.ld (8 at 64 columns per thread: the 64 running
         // sums leave room for no more at 96 registers)
-        constexpr int CW = HB < 16 ? HB : (HB >= 64 ? 8 : 16);
-        // loads in flight per wait (one at HB = 64, where the 64 accumulators
-        // leave no room for a second 16-column buffer)
-        constexpr int PAIR = (HB / CW) >= 2 ? 2 : 1;
+        // (with the register split: 32 or 64 columns in flight)
+        constexpr int CW = HB < 16 ? HB : ((HB >= 64 && !C::kRegSplit) ? 8 : 16);
+        // loads in flight per wait
+        constexpr int PAIR = (HB >= 64 && C::kRegSplit) ? C::kDrainInFlight / CW
+                                                        : ((HB / CW) >= 2 ? 2 : 1);
 #pragma unroll
         for (int cb = 0; cb < HB / CW; cb += PAIR) {
           uint32_t v[PAIR][16];
@@ -798,6 +863,29 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
         store_row<VARIANT, HB>(R, p, m0 + col0, n);
       }
     }
+  };
+
+  // Role dispatch. With the register split each warpgroup changes its budget
+  // first, inside its own branch (so the budget covers all of the role's code).
+  if constexpr (C::kRegSplit) {
+    const int wg = warp >> 2;
+    if (wg >= C::kDrainWGs + C::kConvSets) {
+      setmaxnreg_dec<C::kRegOther>();
+      if (warp == C::kProducerWarp) producer_role();
+      else if (warp >= C::kWarpsUsed) pad_role();
+      else mma_role();
+    } else if (wg >= C::kDrainWGs) {
+      setmaxnreg_dec<C::kRegConv>();
+      conv_role();
+    } else {
+      setmaxnreg_inc<C::kRegDrain>();
+      drain_role();
+    }
+  } else {
+    if (warp == C::kProducerWarp) producer_role();
+    else if (warp >= C::kMmaWarp) mma_role();
+    else if (warp >= kConvWarp0) conv_role();
+    else drain_role();
   }
 }
 
@@ -992,6 +1080,16 @@ static cudaError_t launch_tc(const GemmArgs& a, cudaStream_t st) {
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
     if (e != cudaSuccess) return e;
+    if constexpr (C::kRegSplit) {
+      // the warpgroups' register budgets must fit in what the block is
+      // launched with, or a setmaxnreg increase would wait for ever
+      cudaFuncAttributes fa;
+      e = cudaFuncGetAttributes(&fa, kern);
+      if (e != cudaSuccess) return e;
+      if (C::kDrainWGs * C::kRegDrain + C::kConvSets * C::kRegConv + C::kRegOther >
+          (C::kWarps / 4) * fa.numRegs)
+        return cudaErrorInvalidConfiguration;
+    }
     attr_set = true;
   }
   cudaLaunchConfig_t cfg = {};
@@ -1040,5 +1138,7 @@ cudaError_t launch_tc_gemm(const GemmArgs& a, cudaStream_t st) {
   }
   return cudaErrorInvalidValue;
 }
+
+cudaError_t take_error_word_tc_gemm(unsigned* out) { return take_local_error_word(out); }
 
 }  // namespace egopq
