@@ -61,6 +61,8 @@ def _load():
             lib.oracle_w8a16.argtypes = [vp, vp, vp, i64, i64, i64, vp, vp]
             lib.oracle_w8a8.restype = None
             lib.oracle_dequant_w4_bf16.restype = None
+            lib.oracle_gptq_unpack.restype = i64
+            lib.oracle_gptq_unpack.argtypes = [vp, vp, vp, i64, i64, i64, i64, vp, vp, vp]
             lib.oracle_dequant_w4_bf16.argtypes = [vp, vp, vp, i64, i64, i64, vp]
             lib.oracle_w8a8.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, vp, vp]
             lib.oracle_packed_w4_bytes.restype = i64
@@ -146,6 +148,21 @@ def dequant_w4_bf16(w_q, s_f16, z, group: int = 128):
     out = np.empty((N, K), np.uint16)
     _load().oracle_dequant_w4_bf16(_p(w_q), _p(s_f16), _p(z), N, K, group, _p(out))
     return out
+
+
+def gptq_unpack(qweight, qzeros, scales, N: int, K: int, group: int = 128,
+                zero_offset: int = 1):
+    """GPTQ checkpoint tensors -> (w_q [N][K], s [N][G] fp16 bits, z [N][G], number of
+    zero points outside [0, 15])."""
+    qweight, qzeros = _c(qweight, np.int32), _c(qzeros, np.int32)
+    scales = _c(scales, np.uint16)
+    G = K // group
+    w_q = np.empty((N, K), np.uint8)
+    s = np.empty((N, G), np.uint16)
+    z = np.empty((N, G), np.uint8)
+    bad = _load().oracle_gptq_unpack(_p(qweight), _p(qzeros), _p(scales), N, K, group,
+                                     zero_offset, _p(w_q), _p(s), _p(z))
+    return w_q, s, z, int(bad)
 
 
 def w8a16(x_bf16, w_q, s_f16):

@@ -24,6 +24,9 @@
  *    "Directive after the int8-wo result" and "Round two": W8A8 int8-dynamic.
  *  - "The 4-bit CPU path", section "W4A16 - PyTorch tinygemm": the
  *    dequantize-once bf16 weight of the dense comparison path.
+ *  - GPTQ checkpoint tensors (qweight / qzeros / scales): the pages name the
+ *    metadata only; the byte layout read here is the common export
+ *    convention, stated at oracle_gptq_unpack.
  *  - The combination y = a_s * sum_g s * (sum_k a_q*w_q - z * sum_k a_q) is
  *    the plainest reading of those pieces: dequantized weight s*(w_q - z),
  *    dequantized activation a_s*a_q.
@@ -192,6 +195,41 @@ void oracle_w4a16(const uint16_t* x_bf16, const uint8_t* w_q, const uint16_t* s_
       if (y64) y64[m * N + n] = acc;
       if (y_bf16) y_bf16[m * N + n] = oracle_bf16_from_double(acc);
     }
+}
+
+/* ---- GPTQ checkpoint tensors -> logical codes, scales and zero points ---- */
+
+/* Reading of the checkpoint format (the pages name the _gptq_scale and
+ * _gptq_zero metadata -- "EgoPQ Real-Serving Handoff", section 2 "External
+ * Artifacts"; "The 4-bit CPU path", section "W4A8" -- but print no byte
+ * layout; this is the common GPTQ export convention):
+ *   qweight int32 [K/8][N]: word (r, n) holds the codes of rows k = 8r + i,
+ *           i = 0..7, of output n in bits 4i .. 4i+3 (low nibble first);
+ *   qzeros  int32 [G][N/8]: word (g, c) holds the zero points of outputs
+ *           n = 8c + j in bits 4j .. 4j+3;
+ *   scales  fp16  [G][N].
+ * The zero point is the stored nibble plus zero_offset (1 for exporters that
+ * store z - 1). Outputs in the logical layout: w_q [N][K], s [N][G], z [N][G].
+ * Returns how many zero points fall outside [0, 15] (not representable in the
+ * 4-bit record; those entries of z hold the value modulo 16). */
+int64_t oracle_gptq_unpack(const int32_t* qweight, const int32_t* qzeros, const uint16_t* scales,
+                           int64_t N, int64_t K, int64_t group, int64_t zero_offset,
+                           uint8_t* w_q, uint16_t* s_f16, uint8_t* z) {
+  int64_t G = K / group, bad = 0;
+  for (int64_t n = 0; n < N; ++n)
+    for (int64_t k = 0; k < K; ++k) {
+      uint32_t word = (uint32_t)qweight[(k / 8) * N + n];
+      w_q[n * K + k] = (uint8_t)((word >> (4 * (k % 8))) & 0xFu);
+    }
+  for (int64_t g = 0; g < G; ++g)
+    for (int64_t n = 0; n < N; ++n) {
+      uint32_t word = (uint32_t)qzeros[g * (N / 8) + n / 8];
+      int64_t zz = (int64_t)((word >> (4 * (n % 8))) & 0xFu) + zero_offset;
+      if (zz < 0 || zz > 15) ++bad;
+      z[n * G + g] = (uint8_t)(zz & 0xF);
+      s_f16[n * G + g] = scales[g * N + n];
+    }
+  return bad;
 }
 
 /* ---- dense twin operand: the int4 weight dequantized once to bf16 -------- */

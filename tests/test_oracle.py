@@ -335,6 +335,53 @@ def test_w8a16_matches_dequant_then_matmul(M, N, K):
     assert w8.min() >= -127 and w8.max() <= 127
 
 
+# ------------------------------------------------------------ GPTQ import --
+
+def _i32(u):
+    return np.array(u, dtype=np.uint32).view(np.int32)
+
+
+def test_gptq_unpack_hand_words():
+    """Words written by hand from the format (codes of k = 8r + i in bits
+    4i..4i+3 of qweight[r][n]; zero points of n = 8c + j in bits 4j..4j+3 of
+    qzeros[g][c]): 0x87654321 is codes 1..8 in K order, 0x0FEDCBA9 is
+    9..15, 0; words with the sign bit set (0xF0000000, 0x80000000) give a top
+    code of 15 and 8. A reversed nibble order, a transposed qweight, an
+    arithmetic-shift sign smear or a dropped offset fails one of them."""
+    N, K = 8, 128
+    qweight = np.zeros((K // 8, N), np.uint32)
+    qweight[0, 0] = 0x87654321
+    qweight[1, 0] = 0x0FEDCBA9
+    qweight[0, 1] = 0x11111111
+    qweight[2, 1] = 0xF0000000
+    qweight[3, 7] = 0x80000000
+    qzeros = np.array([[0x76543210]], np.uint32)
+    scales = (0x3C00 + np.arange(N, dtype=np.uint16)).reshape(1, N)
+    for off in (0, 1):
+        w_q, sc, z, bad = oracle.gptq_unpack(_i32(qweight), _i32(qzeros), scales, N, K, 128, off)
+        assert bad == 0
+        assert list(w_q[0, :16]) == [1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12, 13, 14, 15, 0]
+        assert list(w_q[1, :8]) == [1] * 8 and list(w_q[1, 16:24]) == [0] * 7 + [15]
+        assert list(w_q[7, 24:32]) == [0] * 7 + [8]
+        assert w_q[2:7].max() == 0 and w_q[0, 16:].max() == 0
+        assert list(z[:, 0]) == [n + off for n in range(N)]
+        assert list(sc[:, 0]) == list(scales[0])
+
+
+def test_gptq_unpack_counts_unrepresentable_zeros():
+    """Offset 1 (stored z - 1): a stored 15 is z = 16, outside the 4-bit
+    range; each such entry is counted."""
+    N, K = 16, 256
+    qweight = np.zeros((K // 8, N), np.int32)
+    qzeros = np.zeros((2, N // 8), np.uint32)
+    qzeros[1, 1] = 0xF00000F0  # n = 9 and n = 15 of group 1
+    scales = np.full((2, N), 0x3C00, np.uint16)
+    _, _, z, bad = oracle.gptq_unpack(qweight, _i32(qzeros), scales, N, K, 128, 1)
+    assert bad == 2
+    _, _, z0, bad0 = oracle.gptq_unpack(qweight, _i32(qzeros), scales, N, K, 128, 0)
+    assert bad0 == 0 and z0[9, 1] == 15 and z0[15, 1] == 15 and z0[8, 1] == 0
+
+
 # ------------------------------------------------- dequantized bf16 weight -
 
 def test_dequant_w4_bf16_hand_values():
