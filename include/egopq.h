@@ -109,6 +109,26 @@ int egopq_pack_w4(const uint8_t* w_q, const uint16_t* scale_f16, const uint8_t* 
 int egopq_dequant_w4(const void* packed, int64_t N, int64_t K, int group, uint16_t* w_bf16,
                      egopq_stream_t stream);
 
+/* Pack a GPTQ checkpoint's tensors (device) directly into `packed`:
+ *   qweight     int32 [K/8][N]: word (r, n) holds the codes of rows k = 8r+i
+ *               (i = 0..7) of output n in bits 4i..4i+3, low nibble first;
+ *   qzeros      int32 [G][N/8]: word (g, c) holds the zero points of outputs
+ *               n = 8c+j in bits 4j..4j+3;
+ *   scales_f16  fp16  [G][N]   (_gptq_scale);
+ *   zero_offset 0 or 1: z = stored nibble + zero_offset (1 for exporters that
+ *               store z - 1)                          (_gptq_zero).
+ * The pages name this metadata ("EgoPQ Real-Serving Handoff", section 2;
+ * "The 4-bit CPU path", section "W4A8") but not its byte layout; the layout
+ * above is the common GPTQ export convention. Group-ordered checkpoints only
+ * (row k in group k / 128; no activation-order permutation). The result equals
+ * egopq_pack_w4 of the unpacked codes, scales and zero points. A zero point
+ * outside [0, 15] after the offset cannot be stored: it is kept modulo 16 and
+ * the next egopq_device_status returns EGOPQ_ERR_INVALID_ARG. Shape errors as
+ * for egopq_pack_w4. */
+int egopq_pack_w4_gptq(const int32_t* qweight, const int32_t* qzeros, const uint16_t* scales_f16,
+                       int64_t N, int64_t K, int group, int zero_offset, void* packed,
+                       egopq_stream_t stream);
+
 /* Inverse of egopq_pack_w4 (test and inspection aid). */
 int egopq_unpack_w4(const void* packed, int64_t N, int64_t K, int group, uint8_t* w_q,
                     uint16_t* scale_f16, uint8_t* zero, egopq_stream_t stream);
@@ -233,7 +253,8 @@ int egopq_w8a8_gemm_ex(const int8_t* a_q, const void* a_tc, const float* a_s, co
 int egopq_supported(int64_t M, int64_t N, int64_t K, int group, int variant);
 
 /* Synchronize `stream`, then read and clear the device error word: EGOPQ_OK,
- * EGOPQ_ERR_TIMEOUT if a kernel's bounded wait expired since the last call, or
+ * EGOPQ_ERR_TIMEOUT if a kernel's bounded wait expired since the last call,
+ * EGOPQ_ERR_INVALID_ARG if egopq_pack_w4_gptq met a zero point it cannot store, or
  * EGOPQ_ERR_CUDA if the synchronization itself failed. Every wait inside the
  * kernels is bounded (2 s); once one expires its kernel's results are invalid,
  * and kernels launched before this call reads the word may give up early. */

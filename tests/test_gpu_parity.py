@@ -45,7 +45,10 @@ def run_w4a8(x, w, path, M, N, K):
 
 # ------------------------------------------------------------ activation quant
 
-@pytest.mark.parametrize("M,K", [(16, 512), (1, 3584), (5, 18944), (64, 640), (65, 1024), (129, 1024), (300, 384)])
+@pytest.mark.parametrize("M,K", [(16, 512), (1, 3584), (5, 18944), (64, 640), (65, 1024), (129, 1024),
+                                 (300, 384),
+                                 # rows split over clusters of 3, 5 and 8 CTAs
+                                 (1, 8320), (4, 18944), (64, 18944), (7, 32768)])
 def test_quant_act_bit_exact(M, K):
     x = synth.activations(0, 1, 0, M, K)
     if M > 3:
@@ -256,6 +259,56 @@ def test_weight_only_dit_shapes_sampled(K, N, M):
     _, r8 = oracle.w8a16(x[rows], w8[cols], s8[cols])
     check_bf16_output(y4[np.ix_(rows, cols)], r4, f"W4A16 DiT K={K} N={N} M={M}")
     check_bf16_output(y8[np.ix_(rows, cols)], r8, f"W8A16 DiT K={K} N={N} M={M}")
+
+
+# ------------------------------------------------------------ GPTQ import
+
+def to_gptq(w_q, s_f16, z, zero_offset):
+    """Logical codes [N][K], scales and zero points [N][G] as GPTQ checkpoint
+    tensors (qweight [K/8][N], qzeros [G][N/8], scales [G][N]); the zero
+    points are stored minus the offset."""
+    N, K = w_q.shape
+    cw = w_q.astype(np.uint32).T.reshape(K // 8, 8, N)             # [r][i][n]
+    qweight = np.zeros((K // 8, N), np.uint32)
+    for i in range(8):
+        qweight |= (cw[:, i, :] & 0xF) << (4 * i)
+    zs = (z.astype(np.int64) - zero_offset).T.reshape(-1, N // 8, 8)  # [g][c][j]
+    qzeros = np.zeros(zs.shape[:2], np.uint32)
+    for j in range(8):
+        qzeros |= (zs[:, :, j].astype(np.uint32) & 0xF) << (4 * j)
+    return qweight.view(np.int32), qzeros.view(np.int32), np.ascontiguousarray(s_f16.T)
+
+
+@pytest.mark.parametrize("N,K,off", [(128, 128, 1), (384, 1024, 0), (3584, 18944, 1)])
+def test_gptq_import_equals_pack(N, K, off):
+    w = synth.w4_weights(8, 0, 0, N, K)
+    z = np.maximum(w.zero, off).astype(np.uint8)   # representable after the offset
+    qweight, qzeros, scales = to_gptq(w.w_q, w.scale_f16, z, off)
+    # the helper's words decode (by the oracle) to the logical tensors
+    wq2, s2, z2, bad = oracle.gptq_unpack(qweight, qzeros, scales, N, K, 128, off)
+    assert bad == 0 and np.array_equal(wq2, w.w_q) and np.array_equal(s2, w.scale_f16)
+    assert np.array_equal(z2, z)
+    got = eg.pack_w4_gptq(to_dev(qweight), to_dev(qzeros), to_dev(scales, torch.float16), off)
+    ref = eg.pack_w4(to_dev(w.w_q), to_dev(w.scale_f16, torch.float16), to_dev(z))
+    assert torch.equal(got, ref)
+    assert eg.device_status() == 0
+
+
+def test_gptq_import_flags_unrepresentable_zero():
+    """With offset 1 a stored zero nibble of 15 means z = 16, which the 4-bit
+    record cannot hold: the import completes, and the next egopq_device_status
+    reports EGOPQ_ERR_INVALID_ARG (once: the word is cleared)."""
+    N, K = 128, 256
+    w = synth.w4_weights(8, 1, 0, N, K)
+    z = np.ones_like(w.zero)                       # stored as 0 with offset 1
+    qweight, qzeros, scales = to_gptq(w.w_q, w.scale_f16, z, 1)
+    qz = qzeros.view(np.uint32).copy()
+    qz[1, 3] |= np.uint32(0xF << 8)                # output 8*3 + 2 = 26, group 1: stored 15
+    qz = qz.view(np.int32)
+    assert oracle.gptq_unpack(qweight, qz, scales, N, K, 128, 1)[3] == 1
+    eg.pack_w4_gptq(to_dev(qweight), to_dev(qz), to_dev(scales, torch.float16), 1)
+    assert eg.device_status() == -1
+    assert eg.device_status() == 0
 
 
 # ------------------------------------------- dense bf16 twin: dequantize once

@@ -64,6 +64,7 @@ def load() -> ctypes.CDLL:
             "egopq_pack_w4": (i32, [vp, vp, vp, i64, i64, i32, vp, vp]),
             "egopq_unpack_w4": (i32, [vp, i64, i64, i32, vp, vp, vp, vp]),
             "egopq_dequant_w4": (i32, [vp, i64, i64, i32, vp, vp]),
+            "egopq_pack_w4_gptq": (i32, [vp, vp, vp, i64, i64, i32, i32, vp, vp]),
             "egopq_quant_act_i8": (i32, [vp, i64, i64, i32, vp, vp, vp, vp, vp]),
             "egopq_w4a8_gemm": (i32, [vp, vp, vp, vp, vp, i64, i64, i64, i32, vp, vp]),
             "egopq_w4a8_gemm_ex": (i32, [vp, vp, vp, vp, vp, i64, i64, i64, i32, vp, i32, vp]),
@@ -155,6 +156,19 @@ def unpack_w4(packed: torch.Tensor, N: int, K: int, stream=None):
     _check(load().egopq_unpack_w4(_ptr(packed), N, K, GROUP, _ptr(w), _ptr(s), _ptr(z),
                                   _stream(stream)))
     return w, s, z
+
+
+def pack_w4_gptq(qweight: torch.Tensor, qzeros: torch.Tensor, scales: torch.Tensor,
+                 zero_offset: int = 1, stream=None) -> torch.Tensor:
+    """Packed weight from a GPTQ checkpoint's qweight int32 [K/8, N], qzeros
+    int32 [G, N/8] and scales fp16 [G, N] (layout in include/egopq.h)."""
+    _dtype(qweight, torch.int32)
+    _dtype(qzeros, torch.int32)
+    K, N = qweight.shape[0] * 8, qweight.shape[1]
+    packed = torch.empty(packed_w4_bytes(N, K), dtype=torch.uint8, device=qweight.device)
+    _check(load().egopq_pack_w4_gptq(_ptr(qweight), _ptr(qzeros), _ptr(scales), N, K, GROUP,
+                                     zero_offset, _ptr(packed), _stream(stream)))
+    return packed
 
 
 def dequant_w4(packed: torch.Tensor, N: int, K: int, out: Optional[torch.Tensor] = None,

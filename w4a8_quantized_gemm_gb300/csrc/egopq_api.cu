@@ -140,6 +140,22 @@ int egopq_unpack_w4(const void* packed, int64_t N, int64_t K, int group, uint8_t
   return e == cudaSuccess ? EGOPQ_OK : cuda_fail(e, "unpack_w4 launch");
 }
 
+int egopq_pack_w4_gptq(const int32_t* qweight, const int32_t* qzeros, const uint16_t* scales_f16,
+                       int64_t N, int64_t K, int group, int zero_offset, void* packed,
+                       egopq_stream_t stream) {
+  int rc = check_w4_shape(0, N, K, group);
+  if (rc) return rc;
+  if (zero_offset != 0 && zero_offset != 1)
+    return fail(EGOPQ_ERR_INVALID_ARG, "zero_offset must be 0 or 1 (got %d)", zero_offset);
+  rc = check_ptrs(4, "qweight", qweight, "qzeros", qzeros, "scales_f16", scales_f16, "packed",
+                  packed);
+  if (rc) return rc;
+  if ((rc = check_arch())) return rc;
+  cudaError_t e =
+      launch_pack_w4_gptq(qweight, qzeros, scales_f16, N, K, zero_offset, packed, (cudaStream_t)stream);
+  return e == cudaSuccess ? EGOPQ_OK : cuda_fail(e, "pack_w4_gptq launch");
+}
+
 int egopq_dequant_w4(const void* packed, int64_t N, int64_t K, int group, uint16_t* w_bf16,
                      egopq_stream_t stream) {
   int rc = check_w4_shape(0, N, K, group);
@@ -401,6 +417,8 @@ int egopq_device_status(egopq_stream_t stream) {
     word |= w;
   }
   if (word & kErrTimeout) return fail(EGOPQ_ERR_TIMEOUT, "a kernel's bounded wait expired");
+  if (word & kErrRange)
+    return fail(EGOPQ_ERR_INVALID_ARG, "an imported zero point is outside [0, 15]");
   return EGOPQ_OK;
 }
 

@@ -18,11 +18,14 @@ namespace egopq {
 
 // ---- device error word ----------------------------------------------------
 // Bit 0: a bounded wait expired (EGOPQ_ERR_TIMEOUT on the host side).
+// Bit 1: an imported value the packed format cannot hold (a GPTQ zero point
+// outside [0, 15] after its offset; EGOPQ_ERR_INVALID_ARG).
 // One word per translation unit: the library compiles every unit as a whole
 // program (no relocatable device code), which is what lets ptxas honour
 // per-warpgroup register budgets (setmaxnreg). Each unit with kernels exports
 // a take_error_word_* function; the host ORs and clears them all.
 constexpr unsigned kErrTimeout = 1u;
+constexpr unsigned kErrRange = 2u;
 static __device__ unsigned int g_error_word = 0;
 
 // Host: read this unit's word and clear it if set.
@@ -279,6 +282,11 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
   return r;
 }
 __device__ __forceinline__ void cluster_sync_all() {

@@ -39,6 +39,9 @@ cudaError_t launch_pack_w4(const uint8_t* w_q, const uint16_t* s, const uint8_t*
                            int64_t K, void* packed, cudaStream_t st);
 cudaError_t launch_unpack_w4(const void* packed, int64_t N, int64_t K, uint8_t* w_q, uint16_t* s,
                              uint8_t* z, cudaStream_t st);
+cudaError_t launch_pack_w4_gptq(const int32_t* qweight, const int32_t* qzeros,
+                               const uint16_t* scales, int64_t N, int64_t K, int zero_offset,
+                               void* packed, cudaStream_t st);
 cudaError_t launch_dequant_w4(const void* packed, int64_t N, int64_t K, uint16_t* w,
                               cudaStream_t st);
 

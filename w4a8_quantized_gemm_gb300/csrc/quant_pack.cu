@@ -191,6 +191,87 @@ quant_act_reg_kernel(const uint16_t* __restrict__ x, int64_t K, int8_t* __restri
   }
 }
 
+// Long rows for few tokens: one token's row is split over a cluster of CTAs
+// (whole 128-wide groups each, at most kSplitVec 16-byte vectors per thread),
+// so that the per-element divisions spread over several SMs; the CTAs combine
+// their partial absmax through distributed shared memory. Same arithmetic as
+// the kernels above, element for element.
+constexpr int kSplitThreads = 256;
+constexpr int kSplitVec = 2;
+constexpr int kSplitMaxVec = kSplitThreads * kSplitVec;  // vectors one CTA holds
+
+__global__ void __launch_bounds__(kSplitThreads)
+quant_act_split_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K,
+                       int8_t* __restrict__ a_q, float* __restrict__ a_s,
+                       int32_t* __restrict__ a_gsum, void* __restrict__ a_tc, bool tc_fp8) {
+  griddep_wait();
+  if (threadIdx.x == 0) griddep_launch_dependents();
+  const int C = (int)cluster_nctarank();
+  const int rank = (int)cluster_ctarank();
+  const int64_t m = blockIdx.x / C;
+  const int G = (int)(K / 128);
+  const int v0 = (int)((int64_t)rank * G / C) * 16, v1 = (int)((int64_t)(rank + 1) * G / C) * 16;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + m * K);
+  __shared__ float warp_max[kSplitThreads / 32];
+  __shared__ float cta_max;
+  uint4 v[kSplitVec];
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < kSplitVec; ++i) {
+    const int idx = v0 + threadIdx.x + i * kSplitThreads;
+    v[i] = idx < v1 ? __ldg(xr + idx) : make_uint4(0, 0, 0, 0);
+    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      amax = fmaxf(amax, fabsf(__uint_as_float(w[j] << 16)));
+      amax = fmaxf(amax, fabsf(__uint_as_float(w[j] & 0xFFFF0000u)));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float a = warp_max[0];
+#pragma unroll
+    for (int i = 1; i < kSplitThreads / 32; ++i) a = fmaxf(a, warp_max[i]);
+    cta_max = a;
+  }
+  cluster_sync_all();  // every CTA's partial maximum is in its shared memory
+  amax = 0.f;
+  for (int r = 0; r < C; ++r) amax = fmaxf(amax, ld_dsmem_f32(map_to_rank(smem_u32(&cta_max), r)));
+  cluster_sync_all();  // no CTA leaves while another still reads its partial
+  const float s = __fdiv_rn(amax, 127.0f);
+  if (rank == 0 && threadIdx.x == 0) a_s[m] = s;
+  const bool zero_row = (amax == 0.f);
+#pragma unroll
+  for (int i = 0; i < kSplitVec; ++i) {
+    const int idx = v0 + threadIdx.x + i * kSplitThreads;
+    if (idx >= v1) break;  // whole half-warps leave together (v0, v1 multiples of 16)
+    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+    int q[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float lo = __uint_as_float(w[j] << 16);
+      const float hi = __uint_as_float(w[j] & 0xFFFF0000u);
+      q[2 * j] = zero_row ? 0 : max(-127, min(127, __float2int_rn(__fdiv_rn(lo, s))));
+      q[2 * j + 1] = zero_row ? 0 : max(-127, min(127, __float2int_rn(__fdiv_rn(hi, s))));
+    }
+    uint2 packed;
+    packed.x = (uint32_t)(q[0] & 0xFF) | ((uint32_t)(q[1] & 0xFF) << 8) |
+               ((uint32_t)(q[2] & 0xFF) << 16) | ((uint32_t)(q[3] & 0xFF) << 24);
+    packed.y = (uint32_t)(q[4] & 0xFF) | ((uint32_t)(q[5] & 0xFF) << 8) |
+               ((uint32_t)(q[6] & 0xFF) << 16) | ((uint32_t)(q[7] & 0xFF) << 24);
+    reinterpret_cast<uint2*>(a_q + m * K)[idx] = packed;
+    if (a_tc) store_tc_operand(a_tc, tc_fp8, M, K, m, idx, q);
+    int sum = q[0] + q[1] + q[2] + q[3] + q[4] + q[5] + q[6] + q[7];
+    const unsigned half_mask = 0xFFFFu << (threadIdx.x & 16);
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) sum += __shfl_xor_sync(half_mask, sum, o);
+    if ((threadIdx.x & 15) == 0) a_gsum[m * G + idx / 16] = sum;
+  }
+}
+
 // nibble p of a packed word carries K offset kNibbleK[p] inside its 8-wide run
 __device__ __constant__ int kNibbleK[8] = {0, 2, 4, 6, 1, 3, 5, 7};
 
@@ -301,6 +382,53 @@ dequant_w4_kernel(const uint8_t* __restrict__ in, int64_t G, int64_t K, uint16_t
   }
 }
 
+// GPTQ checkpoint tensors straight into the packed records. qweight int32
+// [K/8][N]: word (r, n) holds the codes of rows k = 8r + i of output n in bits
+// 4i..4i+3, so the 8 codes of one packed word (K offsets k0 .. k0+7, k0 a
+// multiple of 8) are one qweight word, its nibbles permuted to the record's
+// order.
+__global__ void pack_gptq_codes_kernel(const int32_t* __restrict__ qweight, int64_t N, int64_t K,
+                                       uint8_t* __restrict__ out) {
+  const int64_t G = K / 128;
+  const int64_t nwords = N * K / 8;
+  for (int64_t w = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; w < nwords;
+       w += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t rec = w / 2048, u = w % 2048;
+    const int64_t t = rec / G, g = rec % G;
+    const int64_t unit = u / 4, j = u % 4;
+    const int64_t c = unit / 128, r = unit % 128;
+    const int64_t n = t * 128 + r, k0 = g * 128 + c * 32 + j * 8;
+    const uint32_t in = static_cast<uint32_t>(qweight[(k0 / 8) * N + n]);
+    uint32_t word = 0;
+#pragma unroll
+    for (int p = 0; p < 8; ++p) word |= ((in >> (4 * kNibbleK[p])) & 0xFu) << (4 * p);
+    *reinterpret_cast<uint32_t*>(out + rec * kRecBytes + u * 4) = word;
+  }
+}
+
+// scales fp16 [G][N] and qzeros int32 [G][N/8] (zero point of output n = 8c + j
+// in bits 4j..4j+3 of word (g, c), plus zero_offset) into the records; a zero
+// point outside [0, 15] raises kErrRange (and is stored modulo 16).
+__global__ void pack_gptq_meta_kernel(const int32_t* __restrict__ qzeros,
+                                      const uint16_t* __restrict__ scales, int64_t N, int64_t G,
+                                      int zero_offset, uint8_t* __restrict__ out) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < G * N;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t g = i / N, n = i % N;
+    uint8_t* rec = out + ((n / 128) * G + g) * kRecBytes;
+    const int64_t r = n % 128;
+    *reinterpret_cast<uint16_t*>(rec + 8192 + 2 * r) = scales[g * N + n];
+    if ((r & 1) == 0) {
+      // n is even, so n and n + 1 share a qzeros word
+      const uint32_t word = static_cast<uint32_t>(qzeros[g * (N / 8) + n / 8]);
+      const int z0 = (int)((word >> (4 * (n % 8))) & 0xFu) + zero_offset;
+      const int z1 = (int)((word >> (4 * (n % 8 + 1))) & 0xFu) + zero_offset;
+      if (z0 < 0 || z0 > 15 || z1 < 0 || z1 > 15) raise_error(kErrRange);
+      rec[8448 + r / 2] = (uint8_t)((z0 & 0xF) | ((z1 & 0xF) << 4));
+    }
+  }
+}
+
 static unsigned grid_for(int64_t work, int threads) {
   int64_t b = (work + threads - 1) / threads;
   return (unsigned)(b < 1 ? 1 : (b > 65535 * 8 ? 65535 * 8 : b));
@@ -321,6 +449,29 @@ cudaError_t launch_quant_act(const uint16_t* x, int64_t M, int64_t K, int8_t* a_
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   const bool tc_fp8 = M <= kTcFp8MaxM;
+  // rows longer than 1024 vectors for few tokens: split over a cluster of up
+  // to 8 CTAs, each holding whole groups and at most kSplitMaxVec vectors
+  const int64_t nvec = K / 8;
+  if (M <= 64 && nvec > 1024) {
+    const int64_t G = K / 128;
+    int split = (int)((nvec + kSplitMaxVec - 1) / kSplitMaxVec);
+    if (split < 2) split = 2;
+    // each CTA's share, ceil(G / split) groups, must fit its registers
+    if (split <= 8 && (G + split - 1) / split * 16 <= kSplitMaxVec) {
+      cudaLaunchAttribute cattr[2];
+      cattr[0] = attr[0];
+      cattr[1].id = cudaLaunchAttributeClusterDimension;
+      cattr[1].val.clusterDim.x = (unsigned)split;
+      cattr[1].val.clusterDim.y = 1;
+      cattr[1].val.clusterDim.z = 1;
+      cfg.attrs = cattr;
+      cfg.numAttrs = 2;
+      cfg.gridDim = dim3((unsigned)(M * split), 1, 1);
+      cfg.blockDim = dim3(kSplitThreads, 1, 1);
+      return cudaLaunchKernelEx(&cfg, quant_act_split_kernel, x, M, K, a_q, a_s, a_gsum, a_tc,
+                                tc_fp8);
+    }
+  }
   if (reg)
     return cudaLaunchKernelEx(&cfg, quant_act_reg_kernel, x, K, a_q, a_s, a_gsum, a_tc, tc_fp8);
   return cudaLaunchKernelEx(&cfg, quant_act_kernel, x, K, a_q, a_s, a_gsum, a_tc, tc_fp8);
@@ -345,6 +496,19 @@ cudaError_t launch_unpack_w4(const void* packed, int64_t N, int64_t K, uint8_t* 
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   unpack_meta_kernel<<<grid_for(G * N, 256), 256, 0, st>>>(base, N, G, s, z);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack_w4_gptq(const int32_t* qweight, const int32_t* qzeros,
+                               const uint16_t* scales, int64_t N, int64_t K, int zero_offset,
+                               void* packed, cudaStream_t st) {
+  const int64_t G = K / 128;
+  uint8_t* out = static_cast<uint8_t*>(packed);
+  pack_gptq_codes_kernel<<<grid_for(N * K / 8, 256), 256, 0, st>>>(qweight, N, K, out);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  pack_gptq_meta_kernel<<<grid_for(G * N, 256), 256, 0, st>>>(qzeros, scales, N, G, zero_offset,
+                                                               out);
   return cudaGetLastError();
 }
 

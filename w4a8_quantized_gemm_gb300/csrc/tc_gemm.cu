@@ -475,48 +475,57 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
     // ------------------------------------------------------------ MMA issuers
     // issuer q takes groups q, q + kMmaWarps, ...
     const int q = warp - C::kMmaWarp;
-    if (lane == 0) {
-      constexpr uint32_t idesc = idesc_f16(128, C::kFp8 ? 2 * BT : BT, C::kBf16);
-      bool any = false;
-      for (int i = q; i < n_items; i += C::kMmaWarps) {
-        const int s = i % S, ab = i % kNumA;
-        const int gi = i % ng;
-        const int di = drain_of(i);
-        const int db = di % kNumD;
-        // first group of its accumulator; last group of it
-        constexpr int kGpd = GPD > 1 ? GPD : 1;  // (a divisor in every instantiation)
-        const bool d_first = GPD == 1 || (GPD == 0 ? gi == 0 : gi % kGpd == 0);
-        const bool d_last = GPD == 1 || gi == ng - 1 || (GPD > 1 && gi % kGpd == kGpd - 1);
-        // one wait per group: the converters arrive on afull only once the
-        // stage has landed, the A buffer is free and the accumulator drained
-        if (!mbar_wait(afull_bar(ab), (i / kNumA) & 1, abort_flag, tmo)) break;
-        tc_fence_after();
-        if constexpr (C::kFp8) {
-          // 4 x K=32: B rows are the 2*BT e4m3 token rows of one 128-byte
-          // swizzled box; K step j advances 32 bytes inside it
+    constexpr uint32_t idesc = idesc_f16(128, C::kFp8 ? 2 * BT : BT, C::kBf16);
+    // (lane 0) the waits that let group i go: false once a wait gave up
+    auto wait_group = [&](int i) -> bool {
+      const int ab = i % kNumA;
+      // one wait per group: the converters arrive on afull only once the
+      // stage has landed, the A buffer is free and the accumulator drained
+      return mbar_wait(afull_bar(ab), (i / kNumA) & 1, abort_flag, tmo);
+    };
+    // (lane 0) group i's MMAs and the commits that release its buffers
+    auto issue_group = [&](int i) {
+      const int s = i % S, ab = i % kNumA;
+      const int gi = i % ng;
+      const int di = drain_of(i);
+      const int db = di % kNumD;
+      // first group of its accumulator; last group of it
+      constexpr int kGpd = GPD > 1 ? GPD : 1;  // (a divisor in every instantiation)
+      const bool d_first = GPD == 1 || (GPD == 0 ? gi == 0 : gi % kGpd == 0);
+      const bool d_last = GPD == 1 || gi == ng - 1 || (GPD > 1 && gi % kGpd == kGpd - 1);
+      tc_fence_after();
+      if constexpr (C::kFp8) {
+        // 4 x K=32: B rows are the 2*BT e4m3 token rows of one 128-byte
+        // swizzled box; K step j advances 32 bytes inside it
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            tc_mma_f8_ts(d_tmem + db * C::kDCols, a_tmem + ab * C::kACols + j * 8,
-                         sdesc_kmajor_sw128(stage_act(s) + j * 32), idesc, j > 0);
-        } else {
+        for (int j = 0; j < 4; ++j)
+          tc_mma_f8_ts(d_tmem + db * C::kDCols, a_tmem + ab * C::kACols + j * 8,
+                       sdesc_kmajor_sw128(stage_act(s) + j * 32), idesc, j > 0);
+      } else {
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const uint32_t b_addr = stage_act(s) + (j >> 2) * C::kActBox + (j & 3) * 32;
-            const uint32_t acc = (j > 0 || !d_first) ? 1u : 0u;
-            tc_mma_f16_ts(d_tmem + db * C::kDCols, a_tmem + ab * 64 + j * 8,
-                          sdesc_kmajor_sw128(b_addr), idesc, acc);
-          }
+        for (int j = 0; j < 8; ++j) {
+          const uint32_t b_addr = stage_act(s) + (j >> 2) * C::kActBox + (j & 3) * 32;
+          const uint32_t acc = (j > 0 || !d_first) ? 1u : 0u;
+          tc_mma_f16_ts(d_tmem + db * C::kDCols, a_tmem + ab * 64 + j * 8,
+                        sdesc_kmajor_sw128(b_addr), idesc, acc);
         }
-        tc_commit(empty_bar(s));
-        tc_commit(aempty_bar(ab));
-        if (d_last) tc_commit(dfull_bar(db));
+      }
+      tc_commit(empty_bar(s));
+      tc_commit(aempty_bar(ab));
+      if (d_last) tc_commit(dfull_bar(db));
+    };
+    bool any = false;
+    if (lane == 0) {
+      for (int i = q; i < n_items; i += C::kMmaWarps) {
+        if (!wait_group(i)) break;
+        issue_group(i);
         any = true;
       }
-      if (any) {  // let this issuer's MMAs finish before teardown
-        tc_commit(fin_bar(q));
-        volatile int no_abort = 0;
-        mbar_wait(fin_bar(q), 0, &no_abort, tmo);
-      }
+    }
+    if (lane == 0 && any) {  // let this issuer's MMAs finish before teardown
+      tc_commit(fin_bar(q));
+      volatile int no_abort = 0;
+      mbar_wait(fin_bar(q), 0, &no_abort, tmo);
     }
     __syncwarp();
     teardown_sync();
