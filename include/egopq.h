@@ -13,12 +13,14 @@
  *    checkpoint": weight-only int4, group size 128.
  *  - "Serve a pre-quantized int8 weight-only DiT via compressed-tensors ..."
  *    (vllm-omni issue 5), sections "Context" and "Plan": int8 weight-only
- *    (W8A16) linears.
+ *    (W8A16) linears; sections "Directive after the int8-wo result" and
+ *    "Round two": W8A8 int8-dynamic.
  *
  * Conventions for every call:
  *  - Pointers are caller-owned DEVICE memory unless stated otherwise, 16-byte
- *    aligned. The library allocates nothing per call (one static 4-byte device
- *    error word is its only device state).
+ *    aligned. The library allocates nothing per call (its only device state:
+ *    a 4-byte error word per kernel unit and the 16 MiB staging array of
+ *    egopq_w4a8_linear_noalloc).
  *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
  *    stream). They validate arguments on the host first and return a negative
  *    egopq_status without launching anything when a check fails; a failed
