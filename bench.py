@@ -547,7 +547,7 @@ def run_ours(args, rank, world):
     ms_step = ms_total / args.steps
     per_step_bytes = sum(op[5] for op in step_ops[0])
     per_step_ops = sum(op[6] for op in step_ops[0])
-    unit_is_ops = args.workload == "prefill" or (args.workload == "linear" and args.m > 64)
+    unit_is_ops = ops_unit(args)
     per_step_units = per_step_ops if unit_is_ops else per_step_bytes
     value = per_step_units * args.steps * world / (ms_total * 1e-3) / (1e12 if unit_is_ops else 1e9)
 
@@ -739,6 +739,12 @@ def dtype_string(args) -> str:
             "w8a16": "bf16 x int8 -> f32, bf16 out"}[v]
 
 
+def ops_unit(args) -> bool:
+    """Tensor-core-sized workloads (more than 64 tokens) report TOPS, the rest
+    GB/s."""
+    return args.workload == "prefill" or (args.workload in ("linear", "model") and args.m > 64)
+
+
 def workload_description(args) -> str:
     return {
         "decode": "decode GEMV sweep: Qwen2.5-7B q,k,v,o,gate,up,down (K=3584/18944), "
@@ -834,7 +840,7 @@ def run_reference(args, rank, world):
         pass
     wl = _WL()
     wl.n_copies = 1
-    unit_is_ops = args.workload == "prefill" or (args.workload == "linear" and args.m > 64)
+    unit_is_ops = ops_unit(args)
     shapes = {"decode": [(M, K, N) for M in (1, 4, 16) for (_, K, N) in SHAPES_7B],
               "prefill": [(M, K, N) for M in (512, 2048, 4096) for (_, K, N) in SHAPES_7B + [HEAD]],
               "model": [(args.m, K, N) for (_, K, N) in SHAPES_7B] + [(args.m, HEAD[1], HEAD[2])],
