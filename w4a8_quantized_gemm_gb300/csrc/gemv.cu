@@ -78,6 +78,9 @@ gemv_w4_kernel(const GemvParams p) {
   auto empty_bar = [&](int s) { return smem_u32(bars + kGemvStages + s); };
   const uint64_t tmo = p.timeout_ns;
 
+  float red_scale[MT];  // (consumers) token scales for the split-K epilogue
+#pragma unroll
+  for (int m = 0; m < MT; ++m) red_scale[m] = 1.f;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kGemvStages; ++s) {
       mbar_init(full_bar(s), 1);
@@ -118,6 +121,12 @@ gemv_w4_kernel(const GemvParams p) {
     const int64_t n = (int64_t)t * 128 + r;
     griddep_wait();             // activations come from the preceding kernel
     if (threadIdx.x == 0) griddep_launch_dependents();
+    // the tokens' scales, needed only by the epilogue: loaded now so that
+    // their latency overlaps the group loop
+    float asc[MT];
+#pragma unroll
+    for (int m = 0; m < MT; ++m)
+      asc[m] = (VARIANT == kW4A8 && !PARTIALS && m < p.rows) ? __ldg(p.a_s + m) : 1.f;
     // stage this CTA's activations, permuted to the nibble order
     if constexpr (VARIANT == kW4A8) {
       uint2* aw = reinterpret_cast<uint2*>(act);
@@ -245,10 +254,14 @@ gemv_w4_kernel(const GemvParams p) {
         for (int m = 0; m < MT; ++m) {
           if (m < p.rows) {
             float v = acc[m];
-            if constexpr (VARIANT == kW4A8) v = p.a_s[m] * v;
+            if constexpr (VARIANT == kW4A8) v = asc[m] * v;
             p.y[m * N + n] = f32_to_bf16_bits(v);
           }
         }
+      }
+      if (p.ks > 1) {  // rank 0 applies the scales after the reduction
+#pragma unroll
+        for (int m = 0; m < MT; ++m) red_scale[m] = asc[m];
       }
     }
   }
@@ -263,16 +276,35 @@ gemv_w4_kernel(const GemvParams p) {
 #pragma unroll
         for (int m = 0; m < MT; ++m) acc[m] = red[m * 128 + r];
         const uint32_t local = smem_u32(red);
-        for (int rk = 1; rk < p.ks; ++rk) {
-          const uint32_t remote = map_to_rank(local, rk);
+        // every rank's partials of a chunk of tokens are loaded before any is
+        // added (one DSMEM round trip a chunk, not one a rank); the sums keep
+        // rank order
+        constexpr int MC = MT < 4 ? MT : 4;
 #pragma unroll
-          for (int m = 0; m < MT; ++m) acc[m] += ld_dsmem_f32(remote + (m * 128 + r) * 4);
+        for (int m0 = 0; m0 < MT; m0 += MC) {
+          float v[7][MC];
+#pragma unroll
+          for (int rk = 1; rk < 8; ++rk) {
+            if (rk < p.ks) {
+              const uint32_t remote = map_to_rank(local, rk);
+#pragma unroll
+              for (int mm = 0; mm < MC; ++mm)
+                v[rk - 1][mm] = ld_dsmem_f32(remote + ((m0 + mm) * 128 + r) * 4);
+            }
+          }
+#pragma unroll
+          for (int rk = 1; rk < 8; ++rk) {
+            if (rk < p.ks) {
+#pragma unroll
+              for (int mm = 0; mm < MC; ++mm) acc[m0 + mm] += v[rk - 1][mm];
+            }
+          }
         }
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
           if (m < p.rows) {
             float v = acc[m];
-            if constexpr (VARIANT == kW4A8) v = p.a_s[m] * v;
+            if constexpr (VARIANT == kW4A8) v = red_scale[m] * v;
             p.y[m * N + n] = f32_to_bf16_bits(v);
           }
         }

@@ -264,11 +264,24 @@ __device__ __forceinline__ void store_row(const float (&R)[HB], const TcParams& 
   }
 }
 
+// The same store with the tokens' scales already in registers (1 where the
+// variant has none).
+template <int HB>
+__device__ __forceinline__ void store_row_scaled(const float (&R)[HB], const float (&asv)[HB],
+                                                 const TcParams& p, int64_t m0, int64_t n) {
+#pragma unroll
+  for (int t = 0; t < HB; ++t) {
+    const int64_t m = m0 + t;
+    if (m < p.M) p.y[m * p.N + n] = f32_to_bf16_bits(asv[t] * R[t]);
+  }
+}
+
 template <int VARIANT, int BT, bool PARTIALS>
 __global__ void __launch_bounds__(TcCfg<VARIANT, BT>::kThreads, TcCfg<VARIANT, BT>::kCtasPerSm)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
                const __grid_constant__ CUtensorMap w8_map, const TcParams p) {
   using C = TcCfg<VARIANT, BT>;
+  constexpr bool kCodes = (VARIANT == kW4A8 || VARIANT == kW8A8);  // per-token scales
   constexpr int S = C::kStages;
   constexpr int HB = C::kDrainCols;  // token columns per drain thread
   constexpr int kNumA = C::kNumA, kNumD = C::kNumD;
@@ -858,18 +871,58 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
       float* red = reinterpret_cast<float*>(smem);  // [BT][128]
 #pragma unroll
       for (int t = 0; t < HB; ++t) red[(col0 + t) * 128 + r] = R[t];
-      cluster_sync_all();
-      if (cluster_ctarank() == 0) {
-        const uint32_t local = smem_u32(red);
-        for (int rk = 1; rk < p.ks; ++rk) {
-          const uint32_t remote = map_to_rank(local, rk);
+      if constexpr (HB <= 16) {  // decode-sized tiles: the epilogue is on the critical path
+        cluster_sync_all();
+        float asv[HB];  // the tokens' scales, loaded before the reduction so
+                        // that their latency overlaps it
+        if (cluster_ctarank() == 0) {
 #pragma unroll
-          for (int t = 0; t < HB; ++t) R[t] += ld_dsmem_f32(remote + ((col0 + t) * 128 + r) * 4);
+          for (int t = 0; t < HB; ++t)
+            asv[t] = (kCodes && m0 + col0 + t < p.M) ? __ldg(p.a_s + m0 + col0 + t) : 1.f;
+          // every rank's partials of 4 columns are loaded before any is added
+          // (one DSMEM round trip per 4 columns, not one per rank); the sums
+          // keep rank order
+          const uint32_t local = smem_u32(red);
+          constexpr int TC = HB < 4 ? HB : 4;
+#pragma unroll
+          for (int t0 = 0; t0 < HB; t0 += TC) {
+            float v[7][TC];
+#pragma unroll
+            for (int rk = 1; rk < 8; ++rk) {
+              if (rk < p.ks) {
+                const uint32_t remote = map_to_rank(local, rk);
+#pragma unroll
+                for (int tt = 0; tt < TC; ++tt)
+                  v[rk - 1][tt] = ld_dsmem_f32(remote + ((col0 + t0 + tt) * 128 + r) * 4);
+              }
+            }
+#pragma unroll
+            for (int rk = 1; rk < 8; ++rk) {
+              if (rk < p.ks) {
+#pragma unroll
+                for (int tt = 0; tt < TC; ++tt) R[t0 + tt] += v[rk - 1][tt];
+              }
+            }
+          }
         }
-      }
-      cluster_sync_all();
-      if (cluster_ctarank() == 0) {
-        store_row<VARIANT, HB>(R, p, m0 + col0, n);
+        cluster_sync_all();
+        if (cluster_ctarank() == 0) {
+          store_row_scaled<HB>(R, asv, p, m0 + col0, n);
+        }
+      } else {  // (wide tiles: their drain registers have no room for the batch)
+        cluster_sync_all();
+        if (cluster_ctarank() == 0) {
+          const uint32_t local = smem_u32(red);
+          for (int rk = 1; rk < p.ks; ++rk) {
+            const uint32_t remote = map_to_rank(local, rk);
+#pragma unroll
+            for (int t = 0; t < HB; ++t) R[t] += ld_dsmem_f32(remote + ((col0 + t) * 128 + r) * 4);
+          }
+        }
+        cluster_sync_all();
+        if (cluster_ctarank() == 0) {
+          store_row<VARIANT, HB>(R, p, m0 + col0, n);
+        }
       }
     }
   };
