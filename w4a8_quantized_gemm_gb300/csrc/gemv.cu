@@ -326,6 +326,15 @@ __device__ __forceinline__ uint4 ldg_stream(const void* p) {
 constexpr int kW8Threads = 256;
 constexpr int kW8RowsPerWarp = 4;
 
+// One lane's 16 bytes of each of a warp's rows at K offset kc (zeros past N or
+// K), so that all the warp's row loads of a slice are in flight together.
+__device__ __forceinline__ void load_w8_rows(uint4 (&w)[kW8RowsPerWarp], const int8_t* w8,
+                                             int64_t n0, int64_t N, int64_t K, int64_t kc) {
+#pragma unroll
+  for (int i = 0; i < kW8RowsPerWarp; ++i)
+    w[i] = (n0 + i < N && kc < K) ? ldg_stream(w8 + (n0 + i) * K + kc) : make_uint4(0, 0, 0, 0);
+}
+
 template <int MT>
 __global__ void __launch_bounds__(kW8Threads)
 gemv_w8_kernel(const uint16_t* __restrict__ x, const int8_t* __restrict__ w8,
@@ -340,7 +349,11 @@ gemv_w8_kernel(const uint16_t* __restrict__ x, const int8_t* __restrict__ w8,
     for (int i = 0; i < kW8RowsPerWarp; ++i)
 #pragma unroll
       for (int m = 0; m < MT; ++m) acc[i][m] = 0.f;
+    // the next slice's weights are requested before the current slice is used
+    uint4 wcur[kW8RowsPerWarp], wnext[kW8RowsPerWarp];
+    load_w8_rows(wcur, w8, n0, N, K, (int64_t)lane * 16);
     for (int64_t kc = (int64_t)lane * 16; kc < K; kc += 512) {
+      load_w8_rows(wnext, w8, n0, N, K, kc + 512);
       float xv[MT][16];
 #pragma unroll
       for (int m = 0; m < MT; ++m) {
@@ -361,7 +374,7 @@ gemv_w8_kernel(const uint16_t* __restrict__ x, const int8_t* __restrict__ w8,
 #pragma unroll
       for (int i = 0; i < kW8RowsPerWarp; ++i) {
         if (n0 + i < N) {
-          const uint4 wv = ldg_stream(w8 + (n0 + i) * K + kc);
+          const uint4 wv = wcur[i];
           const uint32_t ww[4] = {wv.x ^ 0x80808080u, wv.y ^ 0x80808080u, wv.z ^ 0x80808080u,
                                   wv.w ^ 0x80808080u};
 #pragma unroll
@@ -377,6 +390,8 @@ gemv_w8_kernel(const uint16_t* __restrict__ x, const int8_t* __restrict__ w8,
           }
         }
       }
+#pragma unroll
+      for (int i = 0; i < kW8RowsPerWarp; ++i) wcur[i] = wnext[i];
     }
 #pragma unroll
     for (int i = 0; i < kW8RowsPerWarp; ++i)
@@ -415,7 +430,11 @@ gemv_w8a8_kernel(const int8_t* __restrict__ a_q, const float* __restrict__ a_s,
     for (int i = 0; i < kW8RowsPerWarp; ++i)
 #pragma unroll
       for (int m = 0; m < MT; ++m) acc[i][m] = 0;
+    // the next slice's weights are requested before the current slice is used
+    uint4 wcur[kW8RowsPerWarp], wnext[kW8RowsPerWarp];
+    load_w8_rows(wcur, w8, n0, N, K, (int64_t)lane * 16);
     for (int64_t kc = (int64_t)lane * 16; kc < K; kc += 512) {
+      load_w8_rows(wnext, w8, n0, N, K, kc + 512);
       uint4 av[MT];
 #pragma unroll
       for (int m = 0; m < MT; ++m)
@@ -424,7 +443,7 @@ gemv_w8a8_kernel(const int8_t* __restrict__ a_q, const float* __restrict__ a_s,
 #pragma unroll
       for (int i = 0; i < kW8RowsPerWarp; ++i) {
         if (n0 + i < N) {
-          const uint4 wv = ldg_stream(w8 + (n0 + i) * K + kc);
+          const uint4 wv = wcur[i];
 #pragma unroll
           for (int m = 0; m < MT; ++m) {
             int d = acc[i][m];
@@ -436,6 +455,8 @@ gemv_w8a8_kernel(const int8_t* __restrict__ a_q, const float* __restrict__ a_s,
           }
         }
       }
+#pragma unroll
+      for (int i = 0; i < kW8RowsPerWarp; ++i) wcur[i] = wnext[i];
     }
 #pragma unroll
     for (int i = 0; i < kW8RowsPerWarp; ++i)
