@@ -1,4 +1,5 @@
-// tc_gemm.cu -- tcgen05 tensor-core GEMM for the W4A8, W4A16 and W8A16 linears.
+// tc_gemm.cu -- tcgen05 tensor-core GEMM for the W4A8, W4A16, W8A16 and W8A8
+// linears.
 //
 // The pages describe the W4A8 linear only as prior art for other hardware (an
 // AMX CPU kernel, "The 4-bit CPU path", section "W4A8 - _C::int4_scaled_mm_cpu";
@@ -37,10 +38,13 @@
 //                    with all of them in the lean CTAs)
 //   converter warps  packed int4 (or int8) smem tile -> e4m3/fp16/bf16 in TMEM
 //                    (a second set of four takes every other group for token
-//                    tiles of 32 and the non-lean 16)
+//                    tiles of 32 and for per-group 128-token tiles)
 //   producer warp    TMA: activations tile + weight record per group
-//   issuer warps     one MMA-issuing thread each (two for 32-token tiles,
-//                    taking alternate groups); the first allocates TMEM
+//   issuer warps     one MMA-issuing thread each (two for 32-token and
+//                    per-group 128-token tiles, taking alternate groups); the
+//                    first allocates TMEM
+// (128-token per-group tiles add a padding warp and split the registers per
+// warpgroup with setmaxnreg: drains 120, converters 96, producer/issuers 48)
 // (a warp reaches TMEM lanes 32*(warp % 4) .. +31, so each role that touches
 // TMEM is a whole warpgroup)
 // Hand-offs, all on mbarriers with bounded waits: S shared-memory stages,
@@ -56,7 +60,10 @@
 //
 // Variants: W4A16 uses bf16 operands (activations as given, w_q - z exact in
 // bf16) and no a_s; W8A16 converts int8 weights to bf16 and accumulates all
-// of K in TMEM, applying the per-channel scale once at the end.
+// of K in TMEM, applying the per-channel scale once at the end; W8A8 converts
+// int8 weights to fp16 against the fp16 activation codes, drains every 8
+// groups (exact: 1024 * 127^2 < 2^24), adds the partials as int32 and scales
+// by a_s[m] * s[n] at the end.
 #include <cmath>
 
 #include "egopq_internal.h"
@@ -162,18 +169,17 @@ struct TcCfg {
   // running sums each, so with an even split they can keep only 16 TMEM
   // columns in flight and the drain, latency-bound, paces the pipeline. The
   // block is padded to whole warpgroups (setmaxnreg acts per warpgroup) and
-  // the drain warpgroups take registers from the converter warpgroups (which
-  // then convert 16 words at a time) and from the producer/issuer warpgroup.
+  // the drain warpgroups take registers from the producer/issuer warpgroup,
+  // keeping 32 columns in flight. (Drains at 152 with all 64 columns in
+  // flight, converters at 64 converting 16 words at a time after their
+  // waits, measured slower: conversion then sits on the A-buffer hand-off.)
   static constexpr bool kRegSplit = kWide;
   static constexpr int kWarpsUsed = kMmaWarp + kMmaWarps;
   static constexpr int kWarps = kRegSplit ? (kWarpsUsed + 3) / 4 * 4 : kWarpsUsed;
   static constexpr int kThreads = 32 * kWarps;
   static constexpr int kRegDrain = 120, kRegConv = 96, kRegOther = 48;
-  // converters below 96 registers cannot hold a converted group: they then
-  // wait for their buffers first and convert 16 words at a time
-  static constexpr bool kConvChunked = kRegSplit && kRegConv < 96;
-  // drain: TMEM columns in flight per wait at 64 running sums per thread
-  static constexpr int kDrainInFlight = !kRegSplit ? 16 : (kRegDrain >= 144 ? 64 : 32);
+  // (converters keep a whole converted group, 64 registers, in flight)
+  static_assert(!kRegSplit || kRegConv >= 96, "converter registers");
   // registers every thread has at launch (ptxas holds a kernel that uses
   // setmaxnreg at its launch-bounds maximum; the launcher checks it)
   static constexpr int kRegLaunch = (65536 / kThreads) / 8 * 8;
@@ -624,28 +630,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
         __syncwarp();
         if (lane == 0) mbar_arrive(empty_bar(s));
         const uint32_t z = (r & 1) ? (zb >> 4) : (zb & 0xF);
-        if constexpr (C::kConvChunked) {
-          // few registers: wait for the buffers first, then convert and store
-          // one 16-word unit at a time
-          if (!mbar_wait(aempty_bar(ab), ((i / kNumA) & 1) ^ 1, abort_flag, tmo)) break;
-          if (((warp - kConvWarp0) & 3) == 0) {
-            const int di = drain_of(i);
-            if (!mbar_wait(dempty_bar(di % kNumD), ((di / kNumD) & 1) ^ 1, abort_flag, tmo)) break;
-          }
-          tc_fence_after();
-          const uint32_t dst = a_tmem + lane_base + ab * C::kACols;
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t chunk[16];
-            cvt_w4_unit<VARIANT>(v[c], z, chunk);
-            tmem_st16(dst + c * 16, chunk);
-          }
-          tmem_wait_st();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(afull_bar(ab));
-          continue;
-        }
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t chunk[16];
@@ -797,13 +781,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
             }
           }
         } else {
-        // columns per tcgen05.ld (8 at 64 columns per thread: the 64 running
-        // sums leave room for no more at 96 registers)
-        // (with the register split: 32 or 64 columns in flight)
+        // columns per tcgen05.ld (8 at 64 columns per thread without the
+        // register split: the 64 running sums leave room for no more at 96
+        // registers; with it, 16)
         constexpr int CW = HB < 16 ? HB : ((HB >= 64 && !C::kRegSplit) ? 8 : 16);
-        // loads in flight per wait
-        constexpr int PAIR = (HB >= 64 && C::kRegSplit) ? C::kDrainInFlight / CW
-                                                        : ((HB / CW) >= 2 ? 2 : 1);
+        // loads in flight per wait (32 columns at most)
+        constexpr int PAIR = (HB / CW) >= 2 ? 2 : 1;
 #pragma unroll
         for (int cb = 0; cb < HB / CW; cb += PAIR) {
           uint32_t v[PAIR][16];
