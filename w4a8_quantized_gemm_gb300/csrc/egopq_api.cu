@@ -1,5 +1,5 @@
 // egopq_api.cu -- the C ABI declared in include/egopq.h: argument validation,
-// path dispatch, the device error word and error strings. No allocation
+// path dispatch, the device error words and error strings. No allocation
 // happens here; every buffer belongs to the caller.
 #include <cstdarg>
 #include <cstdio>

@@ -16,6 +16,11 @@
 // that one 1-D bulk copy stages everything a (row block, group) needs, and so
 // that one AND/OR per 32-bit word yields two consecutive K values as an fp16
 // pair. The layout is documented in include/egopq.h.
+//
+// Also here: rows longer than 8192 for up to 64 tokens are quantized by a
+// cluster of CTAs (partial absmax through distributed shared memory); GPTQ
+// checkpoint tensors (qweight / qzeros / scales) are packed directly; and a
+// packed weight can be dequantized once to dense bf16.
 #include "egopq_internal.h"
 
 namespace egopq {
