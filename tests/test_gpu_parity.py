@@ -442,6 +442,77 @@ def test_empty_batch_is_a_noop():
     assert y.shape == (0, N)
 
 
+def test_empty_batches_other_variants_are_noops():
+    """M = 0 through every GEMM entry point: an empty result, nothing launched,
+    no error."""
+    K, N = 512, 256
+    w = synth.w4_weights(0, 0, 0, N, K)
+    packed = eg.pack_w4(*dev_weights(w))
+    w8, s8 = synth.w8_weights(0, 0, 0, N, K)
+    x = torch.empty((0, K), dtype=torch.bfloat16, device="cuda")
+    a = eg.quant_act(x)
+    for path in (eg.PATH_AUTO, eg.PATH_GEMV, eg.PATH_TC):
+        assert eg.w4a16_gemm(x, packed, N, K, path=path).shape == (0, N)
+        assert eg.w8a16_gemm(x, to_dev(w8), to_dev(s8, torch.float16), path=path).shape == (0, N)
+        assert eg.w8a8_gemm(a, to_dev(w8), to_dev(s8, torch.float16), path=path).shape == (0, N)
+    assert eg.device_status() == 0
+
+
+def test_rejections_new_entry_points():
+    """Host-side refusals of the W8A8, GPTQ-import and dequantization calls:
+    untiled N, a group other than 128, a bad zero offset, misaligned pointers;
+    nothing is launched and the status names the cause."""
+    lib = eg.load()
+    st = torch.cuda.current_stream().cuda_stream
+    K, N = 512, 256
+    w8, s8 = synth.w8_weights(0, 0, 0, N, K)
+    w8d, s8d = to_dev(w8), to_dev(s8, torch.float16)
+    a = eg.quant_act(to_dev(synth.activations(0, 0, 0, 4, K), torch.bfloat16))
+    y = torch.empty((4, N), dtype=torch.bfloat16, device="cuda")
+    # W8A8: N = 192 untiled; misaligned output
+    assert lib.egopq_w8a8_gemm_ex(a.a_q.data_ptr(), None, a.a_s.data_ptr(), w8d.data_ptr(),
+                                  s8d.data_ptr(), 4, 192, K, y.data_ptr(), 0, st) == -2
+    assert lib.egopq_w8a8_gemm_ex(a.a_q.data_ptr(), None, a.a_s.data_ptr(), w8d.data_ptr(),
+                                  s8d.data_ptr(), 4, N, K, y.data_ptr() + 2, 0, st) == -3
+    # GPTQ import: group 64, zero offset 2, misaligned qweight
+    qweight = torch.zeros((K // 8, N), dtype=torch.int32, device="cuda")
+    qzeros = torch.zeros((K // 128, N // 8), dtype=torch.int32, device="cuda")
+    scales = torch.ones((K // 128, N), dtype=torch.float16, device="cuda")
+    packed = torch.empty(eg.packed_w4_bytes(N, K), dtype=torch.uint8, device="cuda")
+    args = (qzeros.data_ptr(), scales.data_ptr(), N, K)
+    assert lib.egopq_pack_w4_gptq(qweight.data_ptr(), *args, 64, 1, packed.data_ptr(), st) == -2
+    assert lib.egopq_pack_w4_gptq(qweight.data_ptr(), *args, 128, 2, packed.data_ptr(), st) == -1
+    assert lib.egopq_pack_w4_gptq(qweight.data_ptr() + 4, *args, 128, 1, packed.data_ptr(),
+                                  st) == -3
+    # dequantization: untiled K, misaligned output
+    wd = torch.empty((N, K), dtype=torch.bfloat16, device="cuda")
+    assert lib.egopq_dequant_w4(packed.data_ptr(), N, K - 64, 128, wd.data_ptr(), st) == -2
+    assert lib.egopq_dequant_w4(packed.data_ptr(), N, K, 128, wd.data_ptr() + 2, st) == -3
+    assert eg.device_status() == 0
+
+
+def test_guard_bands_new_outputs():
+    """The W8A8 (GEMV and tensor-core) and dequantization kernels write
+    exactly their outputs: sentinel bands on both sides stay intact."""
+    pad = 4096
+    K, N = 1024, 256
+    w8, s8 = synth.w8_weights(0, 1, 0, N, K)
+    for M, path in [(9, eg.PATH_GEMV), (130, eg.PATH_TC)]:
+        a = eg.quant_act(to_dev(synth.activations(0, 1, 0, M, K), torch.bfloat16))
+        buf = torch.full((M * N + 2 * pad,), 12345, dtype=torch.int16, device="cuda")
+        out = buf[pad:pad + M * N].view(torch.bfloat16).view(M, N)
+        eg.w8a8_gemm(a, to_dev(w8), to_dev(s8, torch.float16), path=path, out=out)
+        torch.cuda.synchronize()
+        assert torch.all(buf[:pad] == 12345) and torch.all(buf[pad + M * N:] == 12345), path
+    w = synth.w4_weights(0, 1, 0, N, K)
+    packed = eg.pack_w4(*dev_weights(w))
+    buf = torch.full((N * K + 2 * pad,), 12345, dtype=torch.int16, device="cuda")
+    eg.dequant_w4(packed, N, K, out=buf[pad:pad + N * K].view(torch.bfloat16).view(N, K))
+    torch.cuda.synchronize()
+    assert torch.all(buf[:pad] == 12345) and torch.all(buf[pad + N * K:] == 12345)
+    assert eg.device_status() == 0
+
+
 def test_output_guard_bands_untouched():
     M, N, K = 17, 256, 512
     x, w = w4_case(0, M, N, K)
