@@ -29,8 +29,9 @@
  *  - Matrices are row-major. bf16 and fp16 values travel as their 16-bit
  *    patterns (uint16_t).
  *  - Shape gate: group == 128, K % 128 == 0, N % 128 == 0, M >= 0 (M == 0 is a
- *    no-op). Shapes that do not tile the 128-row weight block are refused
- *    rather than computed wrong ("The 4-bit CPU path", section "The weight
+ *    no-op), every size below 2^31 (larger: EGOPQ_ERR_UNSUPPORTED_SHAPE).
+ *    Shapes that do not tile the 128-row weight block are refused rather
+ *    than computed wrong ("The 4-bit CPU path", section "The weight
  *    layout, measured": a reshape gate keeps an untiled N from being
  *    mis-read).
  */
@@ -47,7 +48,7 @@ extern "C" {
 typedef enum {
   EGOPQ_OK = 0,
   EGOPQ_ERR_INVALID_ARG = -1,       /* null pointer, bad enum, negative size */
-  EGOPQ_ERR_UNSUPPORTED_SHAPE = -2, /* group != 128, K % 128, N % 128 */
+  EGOPQ_ERR_UNSUPPORTED_SHAPE = -2, /* group != 128, K % 128, N % 128, size >= 2^31 */
   EGOPQ_ERR_MISALIGNED = -3,        /* an operand pointer is not 16-byte aligned */
   EGOPQ_ERR_ARCH = -4,              /* current device is not sm_103 */
   EGOPQ_ERR_CUDA = -5,              /* a CUDA runtime call or launch failed */
@@ -55,10 +56,11 @@ typedef enum {
 } egopq_status;
 
 /* Kernel path. AUTO picks by M (W4A8: CUDA-core GEMV for M <= 4, the tcgen05
- * tensor-core GEMM otherwise; W4A16 and W8A16: tensor-core GEMM); the others force one path for tests and
- * benchmarks. The choice is always this explicit argument, never global or
- * environment state ("The 4-bit CPU path", section "Why the path choice is a
- * config field"). */
+ * tensor-core GEMM otherwise; W8A8: GEMV for M <= 64; W4A16 and W8A16:
+ * tensor-core GEMM); egopq_auto_path reports the choice. The others force one
+ * path for tests and benchmarks. The choice is always this explicit argument,
+ * never global or environment state ("The 4-bit CPU path", section "Why the
+ * path choice is a config field"). */
 typedef enum { EGOPQ_PATH_AUTO = 0, EGOPQ_PATH_GEMV = 1, EGOPQ_PATH_TC = 2 } egopq_path;
 
 typedef enum {
@@ -67,6 +69,11 @@ typedef enum {
   EGOPQ_VARIANT_W8A16 = 2,
   EGOPQ_VARIANT_W8A8 = 3
 } egopq_variant;
+
+/* The path EGOPQ_PATH_AUTO takes for M tokens of `variant` (EGOPQ_PATH_GEMV
+ * or EGOPQ_PATH_TC), or EGOPQ_ERR_INVALID_ARG for an unknown variant or
+ * M < 0. Host-only; no device is touched. */
+int egopq_auto_path(int64_t M, int variant);
 
 typedef void* egopq_stream_t; /* cudaStream_t */
 
@@ -143,16 +150,30 @@ int egopq_unpack_w4(const void* packed, int64_t N, int64_t K, int group, uint8_t
  *   a_gsum[m,g] = sum_{k in g} a_q[m,k]
  * A row of zeros gives a_s = 0 and a_q = 0. Outputs (device): a_q int8
  * [M][K], a_s fp32 [M], a_gsum int32 [M][G]. a_tc (optional, may be NULL;
- * 2*M*K bytes) receives the same codes in the operand form the tensor-core
- * path loads with TMA; it is tied to this M and its layout is:
- *   M <= 64: two e4m3 planes [2][M][K] bytes, plane 0 holding a_q >> 4
- *            (arithmetic shift, in [-8, 7]) and plane 1 holding a_q & 15, so
- *            a_q = 16 * plane0 + plane1, both exact in e4m3; inside every aligned run of 8 K values the
- *            bytes are ordered k0, k0+2, k0+4, k0+6, k0+1, k0+3, k0+5, k0+7
- *            (the nibble order of the packed weights);
- *   M > 64:  fp16 [M][K], the codes as exact fp16 integers.
+ * egopq_tc_operand_bytes(M, K, group) bytes) receives the same codes in the
+ * operand form the tensor-core path loads with TMA. The library chooses that
+ * form from M (egopq_tc_operand_form); a buffer written for one M is valid
+ * only for GEMM calls with the same M. Its layout, for inspection only:
+ *   EGOPQ_TC_FORM_E4M3_PLANES (M <= 64): two e4m3 planes [2][M][K] bytes,
+ *            plane 0 holding a_q >> 4 (arithmetic shift, in [-8, 7]) and
+ *            plane 1 holding a_q & 15, so a_q = 16 * plane0 + plane1, both
+ *            exact in e4m3; inside every aligned run of 8 K values the bytes
+ *            are ordered k0, k0+2, k0+4, k0+6, k0+1, k0+3, k0+5, k0+7 (the
+ *            nibble order of the packed weights);
+ *   EGOPQ_TC_FORM_F16 (M > 64): fp16 [M][K], the codes as exact fp16 integers.
+ * Callers that do not want to hold this buffer use egopq_w4a8_linear, which
+ * keeps it inside its workspace.
  * ("The 4-bit CPU path", section "W4A8": the kernel quantizes activations to
  * int8.) */
+typedef enum { EGOPQ_TC_FORM_E4M3_PLANES = 1, EGOPQ_TC_FORM_F16 = 2 } egopq_tc_form;
+
+/* Bytes of the tensor-core operand buffer a_tc for M x K codes (2*M*K), or 0
+ * for a refused shape (M <= 0, K not a multiple of 128, group != 128). */
+size_t egopq_tc_operand_bytes(int64_t M, int64_t K, int group);
+/* The form egopq_quant_act_i8 writes a_tc in for M tokens (an
+ * egopq_tc_form), or EGOPQ_ERR_INVALID_ARG for M <= 0. */
+int egopq_tc_operand_form(int64_t M);
+
 int egopq_quant_act_i8(const uint16_t* x_bf16, int64_t M, int64_t K, int group, int8_t* a_q,
                        float* a_s, int32_t* a_gsum, void* a_tc, egopq_stream_t stream);
 
@@ -171,6 +192,24 @@ int egopq_w4a8_gemm_ex(const int8_t* a_q, const void* a_tc, const float* a_s,
                        const int32_t* a_gsum, const void* packed, int64_t M, int64_t N,
                        int64_t K, int group, uint16_t* y_bf16, int path, egopq_stream_t stream);
 
+/* Sibling W4A8 linears that read the same activations -- a layer's query, key
+ * and value projections, or the gate and up projections of its MLP -- in ONE
+ * kernel launch over all their output tiles (fewer dependent launches per
+ * decode step; the fused query/key/value loading of "Serve a pre-quantized
+ * int8 weight-only DiT via compressed-tensors ...", section "Round two").
+ * For j < count (1..8): y_bf16[j] = the egopq_w4a8_gemm_ex result of
+ * (a, packed[j]) with N[j] output rows (N[j] % 128 == 0), on `path`. packed,
+ * N and y_bf16 are HOST arrays of `count` entries; the pointers they hold are
+ * device memory (16-byte aligned). Each output is formed from the same exact
+ * integer group partials as a separate call; the kernel grid (and so the
+ * fp32 order in which split-K partial sums are added) depends on all the
+ * linears together, so outputs can differ from separate calls in rounding,
+ * always within the output bar. Deterministic. */
+int egopq_w4a8_gemm_grouped(const int8_t* a_q, const void* a_tc, const float* a_s,
+                            const int32_t* a_gsum, int count, const void* const* packed,
+                            const int64_t* N, int64_t M, int64_t K, int group,
+                            uint16_t* const* y_bf16, int path, egopq_stream_t stream);
+
 /* One-call W4A8 linear from bf16 activations: per-token int8 quantization as
  * in egopq_quant_act_i8 into `workspace`, then the W4A8 GEMM on `path`, y bf16
  * [M][N]. `workspace` is caller-owned device memory of at least
@@ -184,6 +223,15 @@ int egopq_w4a8_linear(const uint16_t* x_bf16, const void* packed, int64_t M, int
                       int group, uint16_t* y_bf16, void* workspace, size_t workspace_bytes,
                       int path, egopq_stream_t stream);
 
+/* egopq_w4a8_linear for sibling linears: one quantization of x, then
+ * egopq_w4a8_gemm_grouped over the `count` weights (arrays as there). The
+ * workspace is egopq_w4a8_linear_workspace_bytes(M, K, group, path) bytes,
+ * the same as for a single linear. */
+int egopq_w4a8_linear_grouped(const uint16_t* x_bf16, int count, const void* const* packed,
+                              const int64_t* N, int64_t M, int64_t K, int group,
+                              uint16_t* const* y_bf16, void* workspace, size_t workspace_bytes,
+                              int path, egopq_stream_t stream);
+
 /* egopq_w4a8_linear for callers that cannot allocate device memory -- a
  * plugin inside a framework that owns every device buffer, or a serving loop
  * that must never enter cudaMalloc. The pages have no counterpart; this is a
@@ -193,8 +241,11 @@ int egopq_w4a8_linear(const uint16_t* x_bf16, const void* packed, int64_t M, int
  * process exits. Calls whose staging exceeds 16 MiB (about 3*M*K bytes on the
  * tensor-core path, M*K on the GEMV path) return EGOPQ_ERR_UNSUPPORTED_SHAPE.
  * All calls share the array: calls that overlap on the GPU race on it. The
- * first call on each device looks the array's address up with that device
- * current; make that first call before any stream capture. Allocates nothing. */
+ * first call in each CUDA context looks the array's address up with that
+ * context's device current (and a call after a device reset, in the new
+ * context, looks it up again); make that first call before any stream
+ * capture. Shape and size checks are those of egopq_w4a8_linear. Allocates
+ * nothing. */
 int egopq_w4a8_linear_noalloc(const uint16_t* x_bf16, const void* packed, int64_t M, int64_t N,
                               int64_t K, int group, uint16_t* y_bf16, int path,
                               egopq_stream_t stream);

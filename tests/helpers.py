@@ -69,14 +69,14 @@ def e4m3_to_f64(b) -> np.ndarray:
 TC_PLANE_ORDER = np.array([0, 2, 4, 6, 1, 3, 5, 7])
 
 
-def decode_tc_operand(buf: np.ndarray, M: int, K: int, fp8_max_m: int) -> np.ndarray:
+def decode_tc_operand(buf: np.ndarray, M: int, K: int, e4m3_planes: bool) -> np.ndarray:
     """Integer codes [M][K] held by the tensor-core operand buffer (2*M*K bytes)
     in the form include/egopq.h documents: two e4m3 planes (a >> 4, a & 15) in
-    the packed weights' nibble order for M <= fp8_max_m, fp16 [M][K] otherwise.
+    the packed weights' nibble order when e4m3_planes, fp16 [M][K] otherwise.
     Raises if a plane value is not the integer range it must be."""
     buf = np.ascontiguousarray(buf).view(np.uint8).reshape(-1)
     assert buf.size == 2 * M * K
-    if M > fp8_max_m:
+    if not e4m3_planes:
         return buf.view(np.float16).reshape(M, K).astype(np.float64)
     hi = e4m3_to_f64(buf[:M * K]).reshape(M, K // 8, 8)
     lo = e4m3_to_f64(buf[M * K:]).reshape(M, K // 8, 8)

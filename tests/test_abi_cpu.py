@@ -55,6 +55,36 @@ def test_host_validation_rejects_before_launch(lib):
     assert lib.egopq_selftest_timeout(0, s) == -1
 
 
+def test_auto_path_and_operand_queries(lib):
+    """The AUTO choice and the tensor-core operand form come from the library
+    (host-only queries, no device touched)."""
+    GEMV, TC = eg.PATH_GEMV, eg.PATH_TC
+    assert [lib.egopq_auto_path(m, eg.VARIANT_W4A8) for m in (1, 4, 5, 16, 4096)] == \
+        [GEMV, GEMV, TC, TC, TC]
+    assert [lib.egopq_auto_path(m, eg.VARIANT_W8A8) for m in (1, 64, 65)] == [GEMV, GEMV, TC]
+    assert lib.egopq_auto_path(1, eg.VARIANT_W4A16) == TC
+    assert lib.egopq_auto_path(1, eg.VARIANT_W8A16) == TC
+    assert lib.egopq_auto_path(1, 9) == -1
+    assert lib.egopq_auto_path(-1, eg.VARIANT_W4A8) == -1
+    assert lib.egopq_tc_operand_bytes(16, 3584, 128) == 2 * 16 * 3584
+    assert lib.egopq_tc_operand_bytes(16, 3500, 128) == 0
+    assert lib.egopq_tc_operand_bytes(0, 3584, 128) == 0
+    assert lib.egopq_tc_operand_form(64) == eg.TC_FORM_E4M3_PLANES
+    assert lib.egopq_tc_operand_form(65) == eg.TC_FORM_F16
+    assert lib.egopq_tc_operand_form(0) == -1
+
+
+def test_sizes_beyond_the_limit_are_unsupported_shapes(lib):
+    A, s = 0x10000, None
+    big = 1 << 31
+    assert lib.egopq_w4a8_gemm_ex(A, A, A, A, A, 4, big, 512, 128, A, 0, s) == -2
+    assert lib.egopq_w4a8_linear(A, A, 4, big, 512, 128, A, A, 1 << 20, 0, s) == -2
+    assert lib.egopq_w4a8_linear_noalloc(A, A, 4, big, 512, 128, A, 0, s) == -2
+    assert lib.egopq_w4a8_linear_noalloc(A, A, big, 256, 512, 128, A, 0, s) == -2
+    assert b"2^31" in lib.egopq_last_error_string()
+    assert lib.egopq_quant_act_i8(A, big, 512, 128, A, A, A, None, s) == -2
+
+
 def test_binding_fails_loudly_without_library(monkeypatch):
     monkeypatch.setattr(eg, "LIB_PATH", os.path.join(os.path.dirname(eg.LIB_PATH), "nope.so"))
     monkeypatch.setattr(eg, "_lib", None)

@@ -60,7 +60,9 @@ def test_quant_act_bit_exact(M, K):
     assert np.array_equal(a.a_q.cpu().numpy(), a_q)
     assert np.array_equal(a.a_s.cpu().numpy().view(np.uint32), a_s.view(np.uint32))
     assert np.array_equal(a.a_gsum.cpu().numpy(), asum)
-    got = decode_tc_operand(a.a_tc.cpu().numpy(), M, K, eg.TC_FP8_MAX_M)
+    form = eg.tc_operand_form(M)
+    assert form == (eg.TC_FORM_E4M3_PLANES if M <= 64 else eg.TC_FORM_F16)
+    got = decode_tc_operand(a.a_tc.cpu().numpy(), M, K, form == eg.TC_FORM_E4M3_PLANES)
     assert np.array_equal(got, a_q.astype(np.float64))
 
 
@@ -658,7 +660,7 @@ def test_w4a8_linear_equals_quant_then_gemm(path, M):
     packed = eg.pack_w4(*dev_weights(w))
     xd = to_dev(x, torch.bfloat16)
     y1 = eg.w4a8_linear(xd, packed, N, path=path)
-    two_step_path = path if path != eg.PATH_AUTO else (eg.PATH_GEMV if M <= eg.GEMV_AUTO_MAX_M else eg.PATH_TC)
+    two_step_path = path if path != eg.PATH_AUTO else eg.auto_path(M)
     y2 = eg.w4a8_gemm(eg.quant_act(xd), packed, N, K, path=two_step_path)
     assert torch.equal(y1, y2)
     a_q, a_s, _ = oracle.quant_act(x)

@@ -28,7 +28,7 @@ def test_decode_tc_operand_planes_roundtrip():
             q = int(np.nonzero(TC_PLANE_ORDER == off)[0][0])
             buf[m * K + run * 8 + q] = enc[int(a[m, k]) >> 4]
             buf[M * K + m * K + run * 8 + q] = enc[int(a[m, k]) & 15]
-    assert np.array_equal(decode_tc_operand(buf, M, K, 64), a)
-    # above the threshold the buffer is fp16 codes
+    assert np.array_equal(decode_tc_operand(buf, M, K, e4m3_planes=True), a)
+    # the other form holds fp16 codes
     f16 = a.astype(np.float16).view(np.uint8).reshape(-1)
-    assert np.array_equal(decode_tc_operand(f16, M, K, 2), a)
+    assert np.array_equal(decode_tc_operand(f16, M, K, e4m3_planes=False), a)

@@ -43,8 +43,10 @@ def test_reference_arm_prints_on_rank0_only():
 
     import bench
     args = argparse.Namespace(workload="tiny", variant="w4a8", steps=1, warmup=0, m=1, k=512,
-                              n=256, cpu_budget=0.5, impl="reference")
+                              n=256, cpu_budget=0.5, impl="reference", api="grouped",
+                              fused=False, path="auto")
     assert bench.run_reference(args, rank=1, world=2) is None
     res = bench.run_reference(args, rank=0, world=2)
     assert res["impl"] == "reference" and res["value"] > 0
     assert res["e2e"]["h2d_bytes_per_step"] == 0 and res["cpu_baseline"]["kind"] == "oracle"
+    assert res["config"] == bench.workload_config(args)

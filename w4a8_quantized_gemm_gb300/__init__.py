@@ -78,7 +78,14 @@ def load() -> ctypes.CDLL:
             "egopq_w4a8_linear_workspace_bytes": (sz, [i64, i64, i32, i32]),
             "egopq_w4a8_linear": (i32, [vp, vp, i64, i64, i64, i32, vp, vp, sz, i32, vp]),
             "egopq_w4a8_linear_noalloc": (i32, [vp, vp, i64, i64, i64, i32, vp, i32, vp]),
+            "egopq_w4a8_gemm_grouped": (i32, [vp, vp, vp, vp, i32, vp, vp, i64, i64, i32, vp,
+                                              i32, vp]),
+            "egopq_w4a8_linear_grouped": (i32, [vp, i32, vp, vp, i64, i64, i32, vp, vp, sz, i32,
+                                                vp]),
             "egopq_supported": (i32, [i64, i64, i64, i32, i32]),
+            "egopq_auto_path": (i32, [i64, i32]),
+            "egopq_tc_operand_bytes": (sz, [i64, i64, i32]),
+            "egopq_tc_operand_form": (i32, [i64]),
             "egopq_device_status": (i32, [vp]),
             "egopq_selftest_timeout": (i32, [i32, vp]),
         }
@@ -184,20 +191,41 @@ class QuantAct(NamedTuple):
     a_q: torch.Tensor      # int8 [M, K]
     a_s: torch.Tensor      # fp32 [M]
     a_gsum: torch.Tensor   # int32 [M, G]
-    # uint8 [2*M*K]: the codes in the tensor-core operand form (two e4m3 planes
-    # for M <= TC_FP8_MAX_M, fp16 otherwise; layout in include/egopq.h), or None
+    # uint8: the codes in the tensor-core operand form the library picks for
+    # this M (tc_operand_form; layout in include/egopq.h), or None
     a_tc: Optional[torch.Tensor]
 
 
-# token count up to which the tensor-core operand form is two e4m3 planes
-TC_FP8_MAX_M = 64
-# largest W4A8 token count the AUTO path sends to the CUDA-core GEMV
-GEMV_AUTO_MAX_M = 4
+TC_FORM_E4M3_PLANES, TC_FORM_F16 = 1, 2
+
+
+def auto_path(M: int, variant: int = VARIANT_W4A8) -> int:
+    """The path (PATH_GEMV or PATH_TC) the library's AUTO choice takes for M
+    tokens of `variant`."""
+    rc = int(load().egopq_auto_path(M, variant))
+    if rc < 0:
+        _check(rc)
+    return rc
+
+
+def tc_operand_form(M: int) -> int:
+    """TC_FORM_E4M3_PLANES or TC_FORM_F16: the form quant_act writes the
+    tensor-core operand in for M tokens."""
+    rc = int(load().egopq_tc_operand_form(M))
+    if rc < 0:
+        _check(rc)
+    return rc
 
 
 def tc_operand(M: int, K: int, device) -> torch.Tensor:
-    """A buffer for the tensor-core operand form of M x K codes."""
-    return torch.empty((2 * M * K,), dtype=torch.uint8, device=device)
+    """A buffer for the tensor-core operand form of M x K codes (empty for an
+    empty batch)."""
+    if M == 0:
+        return torch.empty((0,), dtype=torch.uint8, device=device)
+    nbytes = int(load().egopq_tc_operand_bytes(M, K, GROUP))
+    if nbytes == 0:
+        raise EgopqError(-2, f"no tensor-core operand for M={M} K={K}")
+    return torch.empty((nbytes,), dtype=torch.uint8, device=device)
 
 
 def quant_act(x: torch.Tensor, with_tc: bool = True, out: Optional[QuantAct] = None,
@@ -246,6 +274,61 @@ def w4a8_linear(x: torch.Tensor, packed: torch.Tensor, N: int, path: int = PATH_
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(load().egopq_w4a8_linear(_ptr(x), _ptr(packed), M, N, K, GROUP, _ptr(out),
                                     _ptr(workspace), ws_bytes, path, _stream(stream)))
+    return out
+
+
+class _Group:
+    """Host arrays (packed pointers, row counts, output pointers) of sibling
+    linears for the grouped calls; built once, reused by every call."""
+
+    def __init__(self, packed, N, outs):
+        n = len(packed)
+        if not (1 <= n <= 8) or len(N) != n or len(outs) != n:
+            raise ValueError("1 to 8 linears, with one N and one output each")
+        self.count = n
+        self.packed = (ctypes.c_void_p * n)(*[_ptr(p) for p in packed])
+        self.N = (ctypes.c_int64 * n)(*[int(v) for v in N])
+        self.y = (ctypes.c_void_p * n)(*[_ptr(o) for o in outs])
+
+
+def _grouped_outputs(M, N, device, out):
+    if out is None:
+        out = [torch.empty((M, n), dtype=torch.bfloat16, device=device) for n in N]
+    for o, n in zip(out, N):
+        _dtype(o, torch.bfloat16)
+        if tuple(o.shape) != (M, n):
+            raise ValueError(f"output of shape {tuple(o.shape)}, expected {(M, n)}")
+    return out
+
+
+def w4a8_gemm_grouped(a: QuantAct, packed: list, N: list, K: int, path: int = PATH_AUTO,
+                      out: Optional[list] = None, stream=None) -> list:
+    """Sibling linears sharing the activations `a` (q|k|v, gate|up) in one
+    launch: returns [y_j bf16 [M, N_j]]."""
+    M = a.a_q.shape[0]
+    out = _grouped_outputs(M, N, a.a_q.device, out)
+    g = _Group(packed, N, out)
+    _check(load().egopq_w4a8_gemm_grouped(_ptr(a.a_q), _ptr(a.a_tc), _ptr(a.a_s), _ptr(a.a_gsum),
+                                          g.count, g.packed, g.N, M, K, GROUP, g.y, path,
+                                          _stream(stream)))
+    return out
+
+
+def w4a8_linear_grouped(x: torch.Tensor, packed: list, N: list, path: int = PATH_AUTO,
+                        out: Optional[list] = None, workspace: Optional[torch.Tensor] = None,
+                        stream=None) -> list:
+    """One quantization of bf16 x [M, K] and one grouped GEMM over the sibling
+    weights: returns [y_j bf16 [M, N_j]]."""
+    _dtype(x, torch.bfloat16)
+    M, K = x.shape
+    out = _grouped_outputs(M, N, x.device, out)
+    need = w4a8_linear_workspace_bytes(M, K, path)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    g = _Group(packed, N, out)
+    _check(load().egopq_w4a8_linear_grouped(_ptr(x), g.count, g.packed, g.N, M, K, GROUP, g.y,
+                                            _ptr(workspace), workspace.numel(), path,
+                                            _stream(stream)))
     return out
 
 

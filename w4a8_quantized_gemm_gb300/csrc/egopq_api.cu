@@ -9,7 +9,26 @@
 #include "egopq_internal.h"
 
 namespace egopq {
+
+int current_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+  return dev;
 }
+
+int device_sm_count() {
+  static std::atomic<int> cached[kMaxDevices] = {};
+  const int dev = current_device();
+  if (dev < 0) return 0;
+  int n = cached[dev].load(std::memory_order_relaxed);
+  if (n > 0) return n;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return 0;
+  cached[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
+
+}  // namespace egopq
 
 using namespace egopq;
 
@@ -34,33 +53,51 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s per bounded wait
 constexpr int64_t kMaxDim = (int64_t)1 << 31;
 
+}  // namespace
+
+namespace egopq {
+
 // sm_103 check, cached per device
 int check_arch() {
-  static int cached[64];  // 0 unknown, 1 ok, 2 bad
+  static std::atomic<int> cached[kMaxDevices] = {};  // 0 unknown, 1 ok, 2 bad
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-  if (dev >= 0 && dev < 64 && cached[dev]) return cached[dev] == 1 ? EGOPQ_OK : EGOPQ_ERR_ARCH;
+  if (dev < 0 || dev >= kMaxDevices)
+    return fail(EGOPQ_ERR_CUDA, "device ordinal %d is beyond the %d this library tracks", dev,
+                kMaxDevices);
+  const int c = cached[dev].load(std::memory_order_relaxed);
+  if (c) {
+    if (c == 1) return EGOPQ_OK;
+    return fail(EGOPQ_ERR_ARCH, "device %d is not sm_103; this library is built for sm_103a", dev);
+  }
   int major = 0, minor = 0;
   cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
   cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
   const bool ok = (major == 10 && minor == 3);
-  if (dev >= 0 && dev < 64) cached[dev] = ok ? 1 : 2;
+  cached[dev].store(ok ? 1 : 2, std::memory_order_relaxed);
   if (!ok) return fail(EGOPQ_ERR_ARCH, "device %d is sm_%d%d; this library is built for sm_103a", dev,
                        major, minor);
   return EGOPQ_OK;
 }
 
 int check_w4_shape(int64_t M, int64_t N, int64_t K, int group) {
-  if (M < 0 || N <= 0 || K <= 0 || M >= kMaxDim || N >= kMaxDim || K >= kMaxDim)
+  if (M < 0 || N <= 0 || K <= 0)
     return fail(EGOPQ_ERR_INVALID_ARG, "bad sizes M=%lld N=%lld K=%lld", (long long)M,
                 (long long)N, (long long)K);
+  if (M >= kMaxDim || N >= kMaxDim || K >= kMaxDim)
+    return fail(EGOPQ_ERR_UNSUPPORTED_SHAPE, "sizes M=%lld N=%lld K=%lld exceed 2^31 - 1",
+                (long long)M, (long long)N, (long long)K);
   if (group != 128) return fail(EGOPQ_ERR_UNSUPPORTED_SHAPE, "group must be 128 (got %d)", group);
   if (K % 128 || N % 128)
     return fail(EGOPQ_ERR_UNSUPPORTED_SHAPE,
                 "K (%lld) and N (%lld) must be multiples of 128", (long long)K, (long long)N);
   return EGOPQ_OK;
 }
+
+}  // namespace egopq
+
+namespace {
 
 int check_ptrs(int n, ...) {
   va_list ap;
@@ -87,13 +124,7 @@ int run_gemm(const GemmArgs& a, int path, cudaStream_t st) {
   int rc = check_arch();
   if (rc) return rc;
   if (a.M == 0) return EGOPQ_OK;
-  int use = path;
-  if (use == EGOPQ_PATH_AUTO) {
-    if (a.variant == kW8A8)
-      use = (a.M <= kTcFp8MaxM) ? EGOPQ_PATH_GEMV : EGOPQ_PATH_TC;
-    else
-      use = (a.M <= kGemvAutoMaxM && a.variant == kW4A8) ? EGOPQ_PATH_GEMV : EGOPQ_PATH_TC;
-  }
+  const int use = auto_path(a.M, a.variant, path);
   if (use == EGOPQ_PATH_TC && (a.variant == kW4A8 || a.variant == kW8A8) && !a.a_tc)
     return fail(EGOPQ_ERR_INVALID_ARG, "a_tc is required by the tensor-core path");
   cudaError_t e = (use == EGOPQ_PATH_GEMV) ? launch_gemv(a, st) : launch_tc_gemm(a, st);
@@ -169,8 +200,11 @@ int egopq_dequant_w4(const void* packed, int64_t N, int64_t K, int group, uint16
 
 int egopq_quant_act_i8(const uint16_t* x_bf16, int64_t M, int64_t K, int group, int8_t* a_q,
                        float* a_s, int32_t* a_gsum, void* a_tc, egopq_stream_t stream) {
-  if (M < 0 || K <= 0 || M >= kMaxDim || K >= kMaxDim)
+  if (M < 0 || K <= 0)
     return fail(EGOPQ_ERR_INVALID_ARG, "bad sizes M=%lld K=%lld", (long long)M, (long long)K);
+  if (M >= kMaxDim || K >= kMaxDim)
+    return fail(EGOPQ_ERR_UNSUPPORTED_SHAPE, "sizes M=%lld K=%lld exceed 2^31 - 1", (long long)M,
+                (long long)K);
   if (group != 128) return fail(EGOPQ_ERR_UNSUPPORTED_SHAPE, "group must be 128 (got %d)", group);
   if (K % 128) return fail(EGOPQ_ERR_UNSUPPORTED_SHAPE, "K must be a multiple of 128");
   if (M == 0) return EGOPQ_OK;
@@ -206,6 +240,74 @@ int egopq_w4a8_gemm_ex(const int8_t* a_q, const void* a_tc, const float* a_s,
   return run_gemm(a, path, (cudaStream_t)stream);
 }
 
+}  // extern "C"
+
+namespace {
+
+// Validate a sibling-linear list and build its segment table (total output
+// rows in *n_total).
+int build_segs(int count, const void* const* packed, const int64_t* N, uint16_t* const* y,
+               SegTable* t, int64_t* n_total) {
+  if (count < 1 || count > kMaxSegs)
+    return fail(EGOPQ_ERR_INVALID_ARG, "count must be in [1, %d] (got %d)", kMaxSegs, count);
+  if (!packed || !N || !y) return fail(EGOPQ_ERR_INVALID_ARG, "packed, N and y_bf16 must be non-NULL");
+  *t = SegTable{};
+  t->count = count;
+  int64_t tiles = 0;
+  for (int j = 0; j < count; ++j) {
+    if (N[j] <= 0) return fail(EGOPQ_ERR_INVALID_ARG, "N[%d] = %lld", j, (long long)N[j]);
+    if (N[j] % 128)
+      return fail(EGOPQ_ERR_UNSUPPORTED_SHAPE, "N[%d] = %lld is not a multiple of 128", j,
+                  (long long)N[j]);
+    if (!packed[j] || !y[j]) return fail(EGOPQ_ERR_INVALID_ARG, "packed[%d] or y_bf16[%d] is NULL", j, j);
+    if (!aligned16(packed[j]) || !aligned16(y[j]))
+      return fail(EGOPQ_ERR_MISALIGNED, "packed[%d] or y_bf16[%d] is not 16-byte aligned", j, j);
+    t->tile0[j] = (int)tiles;
+    t->packed[j] = static_cast<const uint8_t*>(packed[j]);
+    t->y[j] = y[j];
+    t->N[j] = N[j];
+    tiles += N[j] / 128;
+    if (tiles * 128 >= kMaxDim)
+      return fail(EGOPQ_ERR_UNSUPPORTED_SHAPE, "the linears' outputs exceed 2^31 - 1 rows");
+  }
+  t->tile0[count] = (int)tiles;
+  *n_total = tiles * 128;
+  return EGOPQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int egopq_w4a8_gemm_grouped(const int8_t* a_q, const void* a_tc, const float* a_s,
+                            const int32_t* a_gsum, int count, const void* const* packed,
+                            const int64_t* N, int64_t M, int64_t K, int group,
+                            uint16_t* const* y_bf16, int path, egopq_stream_t stream) {
+  SegTable segs;
+  int64_t n_total = 0;
+  int rc = build_segs(count, packed, N, y_bf16, &segs, &n_total);
+  if (rc) return rc;
+  if ((rc = check_w4_shape(M, n_total, K, group))) return rc;
+  if (M == 0) return EGOPQ_OK;
+  rc = check_ptrs(3, "a_q", a_q, "a_s", a_s, "a_gsum", a_gsum);
+  if (rc) return rc;
+  if (a_tc && !aligned16(a_tc)) return fail(EGOPQ_ERR_MISALIGNED, "a_tc is not 16-byte aligned");
+  GemmArgs a{};
+  a.variant = kW4A8;
+  a.M = M;
+  a.N = n_total;
+  a.K = K;
+  a.a_q = a_q;
+  a.a_tc = a_tc;
+  a.a_s = a_s;
+  a.a_gsum = a_gsum;
+  a.packed = segs.packed[0];
+  a.y = segs.y[0];
+  a.segs = &segs;
+  a.timeout_ns = kDefaultTimeoutNs;
+  return run_gemm(a, path, (cudaStream_t)stream);
+}
+
 int egopq_w4a8_gemm(const int8_t* a_q, const void* a_tc, const float* a_s,
                     const int32_t* a_gsum, const void* packed, int64_t M, int64_t N, int64_t K,
                     int group, uint16_t* y_bf16, egopq_stream_t stream) {
@@ -218,10 +320,7 @@ int egopq_w4a8_gemm(const int8_t* a_q, const void* a_tc, const float* a_s,
 // scales fp32 [M], group sums int32 [M][G], and on the tensor-core path the
 // fp16 codes [M][K] its TMA loads read.
 static size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
-static int linear_path(int64_t M, int path) {
-  if (path == EGOPQ_PATH_AUTO) return M <= kGemvAutoMaxM ? EGOPQ_PATH_GEMV : EGOPQ_PATH_TC;
-  return path;
-}
+static int linear_path(int64_t M, int path) { return auto_path(M, kW4A8, path); }
 
 size_t egopq_w4a8_linear_workspace_bytes(int64_t M, int64_t K, int group, int path) {
   if (M <= 0 || K <= 0 || group != 128 || K % 128 || M >= kMaxDim || K >= kMaxDim) return 0;
@@ -239,9 +338,10 @@ namespace egopq {
 // egopq_last_error_string) and return `code`.
 int set_last_error(int code, const char* msg) { return fail(code, "%s", msg); }
 
-// Quantize x into `ws` (layout above) and run the W4A8 GEMM on `use`.
-int run_linear(const uint16_t* x_bf16, const void* packed, int64_t M, int64_t N, int64_t K,
-               uint16_t* y_bf16, uint8_t* ws, int use, cudaStream_t st) {
+// Quantize x into `ws` (layout above) and run the W4A8 GEMM of the linears in
+// `segs` (N output rows in all) on `use`.
+int run_linear_segs(const uint16_t* x_bf16, const SegTable& segs, int64_t M, int64_t N, int64_t K,
+                    uint8_t* ws, int use, cudaStream_t st) {
   int8_t* a_q = reinterpret_cast<int8_t*>(ws);
   float* a_s = reinterpret_cast<float*>(ws + align256((size_t)(M * K)));
   int32_t* asum = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(a_s) + align256((size_t)(4 * M)));
@@ -259,13 +359,27 @@ int run_linear(const uint16_t* x_bf16, const void* packed, int64_t M, int64_t N,
   a.a_tc = a_tc;
   a.a_s = a_s;
   a.a_gsum = asum;
-  a.packed = static_cast<const uint8_t*>(packed);
-  a.y = y_bf16;
+  a.packed = segs.packed[0];
+  a.y = segs.y[0];
+  a.segs = &segs;
   a.timeout_ns = kDefaultTimeoutNs;
   e = (use == EGOPQ_PATH_GEMV) ? launch_gemv(a, st) : launch_tc_gemm(a, st);
   if (e == cudaErrorNotSupported)
     return fail(EGOPQ_ERR_UNSUPPORTED_SHAPE, "shape not supported by the requested path");
   return e == cudaSuccess ? EGOPQ_OK : cuda_fail(e, "gemm launch");
+}
+
+// The one-call linear of a single weight.
+int run_linear(const uint16_t* x_bf16, const void* packed, int64_t M, int64_t N, int64_t K,
+               uint16_t* y_bf16, uint8_t* ws, int use, cudaStream_t st) {
+  SegTable segs{};
+  segs.count = 1;
+  segs.tile0[0] = 0;
+  segs.tile0[1] = (int)(N / 128);
+  segs.packed[0] = static_cast<const uint8_t*>(packed);
+  segs.y[0] = y_bf16;
+  segs.N[0] = N;
+  return run_linear_segs(x_bf16, segs, M, N, K, ws, use, st);
 }
 }  // namespace egopq
 
@@ -288,6 +402,29 @@ int egopq_w4a8_linear(const uint16_t* x_bf16, const void* packed, int64_t M, int
   if ((rc = check_arch())) return rc;
   return run_linear(x_bf16, packed, M, N, K, y_bf16, static_cast<uint8_t*>(workspace),
                     linear_path(M, path), (cudaStream_t)stream);
+}
+
+int egopq_w4a8_linear_grouped(const uint16_t* x_bf16, int count, const void* const* packed,
+                              const int64_t* N, int64_t M, int64_t K, int group,
+                              uint16_t* const* y_bf16, void* workspace, size_t workspace_bytes,
+                              int path, egopq_stream_t stream) {
+  SegTable segs;
+  int64_t n_total = 0;
+  int rc = build_segs(count, packed, N, y_bf16, &segs, &n_total);
+  if (rc) return rc;
+  if ((rc = check_w4_shape(M, n_total, K, group))) return rc;
+  if (path != EGOPQ_PATH_AUTO && path != EGOPQ_PATH_GEMV && path != EGOPQ_PATH_TC)
+    return fail(EGOPQ_ERR_INVALID_ARG, "unknown path %d", path);
+  if (M == 0) return EGOPQ_OK;
+  rc = check_ptrs(2, "x_bf16", x_bf16, "workspace", workspace);
+  if (rc) return rc;
+  const size_t need = egopq_w4a8_linear_workspace_bytes(M, K, group, path);
+  if (workspace_bytes < need)
+    return fail(EGOPQ_ERR_INVALID_ARG, "workspace of %zu bytes is smaller than %zu", workspace_bytes,
+                need);
+  if ((rc = check_arch())) return rc;
+  return run_linear_segs(x_bf16, segs, M, n_total, K, static_cast<uint8_t*>(workspace),
+                         linear_path(M, path), (cudaStream_t)stream);
 }
 
 int egopq_w4a8_group_partials(const int8_t* a_q, const void* a_tc, const int32_t* a_gsum,
@@ -402,6 +539,22 @@ int egopq_supported(int64_t M, int64_t N, int64_t K, int group, int variant) {
   if (group != 128 || K % 128 || N % 128) return 0;
   if (check_arch() != EGOPQ_OK) return 0;
   return 1;
+}
+
+int egopq_auto_path(int64_t M, int variant) {
+  if (variant < EGOPQ_VARIANT_W4A8 || variant > EGOPQ_VARIANT_W8A8 || M < 0)
+    return fail(EGOPQ_ERR_INVALID_ARG, "bad variant %d or M %lld", variant, (long long)M);
+  return auto_path(M, variant, EGOPQ_PATH_AUTO);
+}
+
+size_t egopq_tc_operand_bytes(int64_t M, int64_t K, int group) {
+  if (M <= 0 || K <= 0 || M >= kMaxDim || K >= kMaxDim || group != 128 || K % 128) return 0;
+  return (size_t)(2 * M * K);
+}
+
+int egopq_tc_operand_form(int64_t M) {
+  if (M <= 0 || M >= kMaxDim) return fail(EGOPQ_ERR_INVALID_ARG, "bad M %lld", (long long)M);
+  return M <= kTcFp8MaxM ? EGOPQ_TC_FORM_E4M3_PLANES : EGOPQ_TC_FORM_F16;
 }
 
 int egopq_device_status(egopq_stream_t stream) {

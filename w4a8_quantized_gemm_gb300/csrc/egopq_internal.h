@@ -1,15 +1,99 @@
 // egopq_internal.h -- launchers shared between the kernel files and the C ABI.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
+#include <mutex>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "../../include/egopq.h"
 #include "egopq_common.cuh"
 
 namespace egopq {
 
 enum Variant { kW4A8 = 0, kW4A16 = 1, kW8A16 = 2, kW8A8 = 3 };
+
+// Launch state that depends on the device (shared-memory opt-ins, SM counts)
+// is kept per device ordinal, up to this many devices.
+constexpr int kMaxDevices = 64;
+
+// Host-side checks shared by the entry points; each records its message as the
+// calling thread's last error and returns a negative egopq_status on failure.
+// Shape gate of the packed int4 weight (and the size limit of every call).
+int check_w4_shape(int64_t M, int64_t N, int64_t K, int group);
+// The current device is an sm_103 (cached per device).
+int check_arch();
+
+// Ordinal of the calling thread's current device, or -1 if cudaGetDevice
+// fails or the ordinal is kMaxDevices or more.
+int current_device();
+// SM count of the current device (cached per device; 0 if it cannot be read).
+int device_sm_count();
+
+// A kernel's dynamic shared-memory opt-in, kept per device: cudaFuncSetAttribute
+// applies to the current device only, so each device gets its own call. ensure()
+// raises the opt-in to at least `bytes` (never lowers it); thread-safe.
+class SmemOptIn {
+ public:
+  template <typename Kernel>
+  cudaError_t ensure(Kernel kern, size_t bytes) {
+    const int dev = current_device();
+    if (dev < 0) return cudaErrorInvalidDevice;
+    if (done_[dev].load(std::memory_order_acquire) >= bytes) return cudaSuccess;
+    std::lock_guard<std::mutex> lock(mu_);
+    if (done_[dev].load(std::memory_order_relaxed) >= bytes) return cudaSuccess;
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e != cudaSuccess) return e;
+    done_[dev].store(bytes, std::memory_order_release);
+    return cudaSuccess;
+  }
+
+ private:
+  std::mutex mu_;
+  std::atomic<size_t> done_[kMaxDevices] = {};
+};
+
+// Sibling linears that read the same activations, run as one launch: the
+// output tiles (128 weight rows each) of linear j are the global tiles
+// [tile0[j], tile0[j + 1]); a single linear is the table with count 1.
+constexpr int kMaxSegs = 8;
+struct SegTable {
+  int count;
+  int tile0[kMaxSegs + 1];
+  const uint8_t* packed[kMaxSegs];  // packed int4 weight of linear j
+  uint16_t* y[kMaxSegs];            // its bf16 output [M][N[j]]
+  int64_t N[kMaxSegs];
+};
+
+// Global tile `nt` resolved to its linear: the packed record (tile, group 0)
+// (records of one tile are consecutive, 8512 bytes apart), the output, its row
+// count and the tile's first output row. Compile-time indexes only, so the
+// table stays in the parameter space.
+struct TileRef {
+  const uint8_t* rec0;
+  uint16_t* y;
+  int64_t N;
+  int64_t n0;
+};
+__device__ __forceinline__ TileRef tile_ref(const SegTable& s, int nt, int G) {
+  const uint8_t* pk = s.packed[0];
+  uint16_t* y = s.y[0];
+  int64_t N = s.N[0];
+  int t0 = 0;
+#pragma unroll
+  for (int j = 1; j < kMaxSegs; ++j) {
+    if (j < s.count && nt >= s.tile0[j]) {
+      pk = s.packed[j];
+      y = s.y[j];
+      N = s.N[j];
+      t0 = s.tile0[j];
+    }
+  }
+  const int64_t lt = nt - t0;
+  return TileRef{pk + lt * G * 8512, y, N, lt * 128};
+}
 
 // Operands of one GEMM call, already validated by the ABI layer.
 struct GemmArgs {
@@ -31,7 +115,23 @@ struct GemmArgs {
   uint16_t* y;
   int32_t* partials;  // non-null: write group partials instead of y (W4A8 only)
   uint64_t timeout_ns;
+  // packed int4 variants: sibling linears sharing the activations (null: one
+  // linear, packed / y / N above)
+  const SegTable* segs;
 };
+
+// The segment table of a call: `a.segs`, or the one linear of packed / y / N.
+inline SegTable seg_table(const GemmArgs& a) {
+  if (a.segs) return *a.segs;
+  SegTable t{};
+  t.count = 1;
+  t.tile0[0] = 0;
+  t.tile0[1] = (int)(a.N / 128);
+  t.packed[0] = a.packed;
+  t.y[0] = a.y;
+  t.N[0] = a.N;
+  return t;
+}
 
 cudaError_t launch_quant_act(const uint16_t* x, int64_t M, int64_t K, int8_t* a_q, float* a_s,
                              int32_t* a_gsum, void* a_tc, cudaStream_t st);
@@ -67,5 +167,15 @@ constexpr int kTcFp8MaxM = 64;
 constexpr int kGemvMaxRows = 16;
 // AUTO path: W4A8 batches up to this many tokens take the GEMV.
 constexpr int kGemvAutoMaxM = 4;
+
+// The kernel path a call takes: `path` itself unless it is EGOPQ_PATH_AUTO,
+// which resolves by token count -- W4A8 on the CUDA-core GEMV up to
+// kGemvAutoMaxM tokens, W8A8 on its GEMV up to kTcFp8MaxM (its tensor-core
+// form exists only above), everything else on the tensor cores.
+inline int auto_path(int64_t M, int variant, int path) {
+  if (path != EGOPQ_PATH_AUTO) return path;
+  if (variant == kW8A8) return M <= kTcFp8MaxM ? EGOPQ_PATH_GEMV : EGOPQ_PATH_TC;
+  return (variant == kW4A8 && M <= kGemvAutoMaxM) ? EGOPQ_PATH_GEMV : EGOPQ_PATH_TC;
+}
 
 }  // namespace egopq

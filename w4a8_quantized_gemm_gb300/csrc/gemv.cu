@@ -38,16 +38,15 @@ constexpr int kGemvStageBytes = 8512;               // one packed record: codes,
 constexpr int kGemvMaxGroupsPerCta = 64;
 
 struct GemvParams {
-  int64_t M, N, K;
+  int64_t M, N, K;  // N: output rows of all linears together
   int G, ks, rows;
   const int8_t* a_q;
   const float* a_s;
   const int32_t* a_gsum;
   const uint16_t* x;
-  const uint8_t* packed;
-  uint16_t* y;
   int32_t* partials;
   uint64_t timeout_ns;
+  SegTable seg;  // packed weight and output of each linear (outputs offset to this row chunk)
 };
 
 // Decode kernel for the packed int4 weight (W4A8 and W4A16). CTA = one
@@ -59,14 +58,16 @@ struct GemvParams {
 // thread owns one weight row.
 template <int VARIANT, int MT, bool PARTIALS>
 __global__ void __launch_bounds__(kGemvThreads)
-gemv_w4_kernel(const GemvParams p) {
+gemv_w4_kernel(const __grid_constant__ GemvParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ks = blockIdx.x, t = blockIdx.y;
   const int G = p.G;
   const int g0 = (int)((int64_t)ks * G / p.ks), g1 = (int)((int64_t)(ks + 1) * G / p.ks);
   const int ng = g1 - g0;
-  const int64_t N = p.N, K = p.K;
+  const int64_t K = p.K;
+  const TileRef tile = tile_ref(p.seg, t, G);  // this tile's linear
+  const int64_t N = tile.N;
 
   // smem: ring | barriers | abort flag | reduction buffer | staged activations
   uint8_t* ring = smem;
@@ -99,7 +100,7 @@ gemv_w4_kernel(const GemvParams p) {
         const int s = i % kGemvStages, g = g0 + i;
         mbar_arrive_expect_tx(full_bar(s), kGemvStageBytes);
         bulk_load(smem_u32(ring + s * kGemvStageBytes),
-                  p.packed + ((int64_t)t * G + g) * kGemvStageBytes, kGemvStageBytes, full_bar(s));
+                  tile.rec0 + (int64_t)g * kGemvStageBytes, kGemvStageBytes, full_bar(s));
       };
       int issued = 0;
       for (int i = 0; i < ng; ++i) {
@@ -118,7 +119,7 @@ gemv_w4_kernel(const GemvParams p) {
   } else {
     // ---------------------------------------------------------------- consumers
     const int r = threadIdx.x;  // row in the tile
-    const int64_t n = (int64_t)t * 128 + r;
+    const int64_t n = tile.n0 + r;
     griddep_wait();             // activations come from the preceding kernel
     if (threadIdx.x == 0) griddep_launch_dependents();
     // the tokens' scales, needed only by the epilogue: loaded now so that
@@ -255,7 +256,7 @@ gemv_w4_kernel(const GemvParams p) {
           if (m < p.rows) {
             float v = acc[m];
             if constexpr (VARIANT == kW4A8) v = asc[m] * v;
-            p.y[m * N + n] = f32_to_bf16_bits(v);
+            tile.y[m * N + n] = f32_to_bf16_bits(v);
           }
         }
       }
@@ -271,7 +272,7 @@ gemv_w4_kernel(const GemvParams p) {
       cluster_sync_all();
       if (cluster_ctarank() == 0 && warp < 4) {
         const int r = threadIdx.x;
-        const int64_t n = (int64_t)t * 128 + r;
+        const int64_t n = tile.n0 + r;
         float acc[MT];
 #pragma unroll
         for (int m = 0; m < MT; ++m) acc[m] = red[m * 128 + r];
@@ -305,7 +306,7 @@ gemv_w4_kernel(const GemvParams p) {
           if (m < p.rows) {
             float v = acc[m];
             if constexpr (VARIANT == kW4A8) v = red_scale[m] * v;
-            p.y[m * N + n] = f32_to_bf16_bits(v);
+            tile.y[m * N + n] = f32_to_bf16_bits(v);
           }
         }
       }
@@ -479,14 +480,8 @@ gemv_w8a8_kernel(const int8_t* __restrict__ a_q, const float* __restrict__ a_s,
 
 // ---- launchers ----------------------------------------------------------------
 static int sm_count() {
-  static int count = 0;
-  if (!count) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&count, cudaDevAttrMultiProcessorCount, dev);
-    if (count <= 0) count = 148;
-  }
-  return count;
+  const int n = device_sm_count();
+  return n > 0 ? n : 148;
 }
 
 template <int VARIANT, int MT, bool PARTIALS>
@@ -496,13 +491,8 @@ static cudaError_t launch_w4_slice(const GemvParams& p, cudaStream_t st) {
                                               : (size_t)ng_max * MT * 128 * 4;
   const size_t smem = (size_t)kGemvStages * kGemvStageBytes + 256 + MT * 128 * 4 + act_bytes;
   auto kern = gemv_w4_kernel<VARIANT, MT, PARTIALS>;
-  static size_t attr_smem = 0;  // largest carve-out requested so far for this instantiation
-  if (smem > attr_smem) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
-    attr_smem = smem;
-  }
+  static SmemOptIn opt_in;  // largest carve-out requested so far, per device
+  if (cudaError_t e = opt_in.ensure(kern, smem); e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)p.ks, (unsigned)(p.N / 128), 1);
   cfg.blockDim = dim3(kGemvThreads, 1, 1);
@@ -578,6 +568,7 @@ cudaError_t launch_gemv(const GemmArgs& a, cudaStream_t st) {
   }
   const int G = (int)(a.K / 128);
   const int64_t tiles = a.N / 128;
+  const SegTable seg = seg_table(a);
   // split the groups of each tile over a cluster so that about two CTAs per
   // SM stream weights, keeping at most kGemvMaxGroupsPerCta groups per CTA
   const int64_t slots = 2LL * sm_count();
@@ -603,8 +594,8 @@ cudaError_t launch_gemv(const GemmArgs& a, cudaStream_t st) {
     p.G = G;
     p.ks = ks;
     p.rows = (int)((a.M - m0) < max_rows ? (a.M - m0) : max_rows);
-    p.packed = a.packed;
-    p.y = a.y + m0 * a.N;
+    p.seg = seg;
+    for (int j = 0; j < seg.count; ++j) p.seg.y[j] = seg.y[j] + m0 * seg.N[j];
     p.timeout_ns = a.timeout_ns;
     cudaError_t e;
     if (a.variant == kW4A8) {

@@ -16,9 +16,12 @@
 //  - a call whose staged activations exceed that size is refused;
 //  - all calls share the one array: calls that overlap on the GPU (different
 //    streams, or different host threads without ordering) race on it;
-//  - the first call on each device looks up the array's device address
-//    (cudaGetSymbolAddress, with that device current); make that first call
-//    before any stream capture.
+//  - the first call in each CUDA context looks up the array's device address
+//    (cudaGetSymbolAddress, with that context's device current); make that
+//    first call before any stream capture. The address is kept per device and
+//    tagged with the context it was read in, so a call after a device reset
+//    (a new primary context, where the array may have moved) looks it up
+//    again.
 #include <mutex>
 
 #include "../../include/egopq.h"
@@ -28,20 +31,53 @@ namespace egopq {
 int run_linear(const uint16_t* x_bf16, const void* packed, int64_t M, int64_t N, int64_t K,
                uint16_t* y_bf16, uint8_t* ws, int use, cudaStream_t st);
 int set_last_error(int code, const char* msg);
-}
+}  // namespace egopq
 
 namespace {
 
 constexpr size_t kStaticScratchBytes = size_t(16) << 20;
-constexpr int kMaxDevices = 64;
 
 // Staging buffer of egopq_w4a8_linear_noalloc. Host code must not use this
 // name as an address (it denotes a host-side stand-in); the device address
 // comes from cudaGetSymbolAddress, per device.
 static __device__ __align__(256) uint8_t g_linear_scratch[kStaticScratchBytes];
 
+// Identity of the calling thread's current context (cuCtxGetId through the
+// runtime's driver entry points); 0 when there is none or it cannot be read.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+unsigned long long current_context_id() {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  if (!get_current || !get_id) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+struct ScratchAddr {
+  void* ptr = nullptr;
+  unsigned long long ctx = 0;  // context the address was read in (0: unknown)
+};
 std::mutex g_addr_mu;
-void* g_addr[kMaxDevices] = {};
+ScratchAddr g_addr[egopq::kMaxDevices];
 
 bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
 
@@ -53,11 +89,8 @@ extern "C" int egopq_w4a8_linear_noalloc(const uint16_t* x_bf16, const void* pac
   using egopq::set_last_error;
   if (path != EGOPQ_PATH_AUTO && path != EGOPQ_PATH_GEMV && path != EGOPQ_PATH_TC)
     return set_last_error(EGOPQ_ERR_INVALID_ARG, "egopq_w4a8_linear_noalloc: unknown path");
-  if (M < 0 || N <= 0 || K <= 0)
-    return set_last_error(EGOPQ_ERR_INVALID_ARG, "egopq_w4a8_linear_noalloc: bad sizes");
-  if (group != 128 || K % 128 || N % 128)
-    return set_last_error(EGOPQ_ERR_UNSUPPORTED_SHAPE,
-                          "egopq_w4a8_linear_noalloc: group must be 128 and K, N multiples of 128");
+  // the same shape gate as egopq_w4a8_linear, before any size arithmetic
+  if (const int rc = egopq::check_w4_shape(M, N, K, group)) return rc;
   if (M == 0) return EGOPQ_OK;
   if (!x_bf16 || !packed || !y_bf16)
     return set_last_error(EGOPQ_ERR_INVALID_ARG, "egopq_w4a8_linear_noalloc: NULL pointer");
@@ -65,34 +98,34 @@ extern "C" int egopq_w4a8_linear_noalloc(const uint16_t* x_bf16, const void* pac
     return set_last_error(EGOPQ_ERR_MISALIGNED,
                           "egopq_w4a8_linear_noalloc: a pointer is not 16-byte aligned");
   const size_t need = egopq_w4a8_linear_workspace_bytes(M, K, group, path);
-  if (need == 0 || need > kStaticScratchBytes)
+  if (need > kStaticScratchBytes)
     return set_last_error(EGOPQ_ERR_UNSUPPORTED_SHAPE,
                           "egopq_w4a8_linear_noalloc: the staged activations (about 3*M*K bytes "
                           "on the tensor-core path, M*K on the GEMV path) exceed its 16 MiB "
                           "static scratch; use egopq_w4a8_linear with a workspace");
-  if (!egopq_supported(M, N, K, group, EGOPQ_VARIANT_W4A8))
-    return set_last_error(EGOPQ_ERR_ARCH, "egopq_w4a8_linear_noalloc: device is not sm_103");
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+  if (const int rc = egopq::check_arch()) return rc;
+  const int dev = egopq::current_device();
+  if (dev < 0)
     return set_last_error(EGOPQ_ERR_CUDA, "egopq_w4a8_linear_noalloc: cudaGetDevice failed");
   void* scratch = nullptr;
   {
     std::lock_guard<std::mutex> lock(g_addr_mu);
-    if (!g_addr[dev]) {
-      // set-up, once per device, with that device current
+    ScratchAddr& a = g_addr[dev];
+    const unsigned long long ctx = current_context_id();
+    if (!a.ptr || ctx == 0 || ctx != a.ctx) {
+      // set-up, once per device and context, with that device current
       void* ptr = nullptr;
       const cudaError_t e = cudaGetSymbolAddress(&ptr, g_linear_scratch);
       if (e != cudaSuccess || !ptr)
         return set_last_error(EGOPQ_ERR_CUDA,
                               "egopq_w4a8_linear_noalloc: cudaGetSymbolAddress failed");
-      g_addr[dev] = ptr;
+      a.ptr = ptr;
+      a.ctx = current_context_id();  // the lookup made the context current if it was not
     }
-    scratch = g_addr[dev];
+    scratch = a.ptr;
   }
   // the quantization kernel overwrites every staged byte the GEMM then reads,
   // so nothing in the shared array needs clearing between calls
-  const int use = (path == EGOPQ_PATH_AUTO) ? (M <= egopq::kGemvAutoMaxM ? EGOPQ_PATH_GEMV : EGOPQ_PATH_TC)
-                                            : path;
-  return egopq::run_linear(x_bf16, packed, M, N, K, y_bf16, static_cast<uint8_t*>(scratch), use,
-                           (cudaStream_t)stream);
+  return egopq::run_linear(x_bf16, packed, M, N, K, y_bf16, static_cast<uint8_t*>(scratch),
+                           egopq::auto_path(M, egopq::kW4A8, path), (cudaStream_t)stream);
 }

@@ -82,11 +82,10 @@ struct TcParams {
   int act3d;       // 1: activation map is 3-D, one copy per 128-wide group; 0: 2-D, two copies
   const float* a_s;
   const int32_t* a_gsum;  // per-token group sums (e4m3 W4A8 form: zero points in the drain)
-  const uint8_t* packed;
   const uint16_t* s8;
-  uint16_t* y;
   int32_t* partials;
   uint64_t timeout_ns;
+  SegTable seg;  // packed weight, output and N of each linear, by output tile
 };
 
 template <int VARIANT, int BT>
@@ -248,12 +247,13 @@ __device__ __forceinline__ void cvt_w4_unit(const uint4& v, uint32_t z, uint32_t
   }
 }
 
-// y[m0+t][n] = bf16(a_s[m0+t] * R[t]) (W4A8) or bf16(R[t]), t < HB, rows < M.
-// Eight rows at a time, with a compiler barrier between chunks so the a_s
-// loads are not all hoisted (they would cost a register each).
+// y[m0+t][n] = bf16(a_s[m0+t] * R[t]) (W4A8) or bf16(R[t]), t < HB, rows < M,
+// into the output `o` of this tile's linear. Eight rows at a time, with a
+// compiler barrier between chunks so the a_s loads are not all hoisted (they
+// would cost a register each).
 template <int VARIANT, int HB>
-__device__ __forceinline__ void store_row(const float (&R)[HB], const TcParams& p, int64_t m0,
-                                          int64_t n) {
+__device__ __forceinline__ void store_row(const float (&R)[HB], const TcParams& p,
+                                          const TileRef& o, int64_t m0, int64_t n) {
   constexpr int CH = HB < 8 ? HB : 8;
 #pragma unroll
   for (int c = 0; c < HB; c += CH) {
@@ -264,7 +264,7 @@ __device__ __forceinline__ void store_row(const float (&R)[HB], const TcParams& 
       if (m < p.M) {
         float v = R[t];
         if constexpr (VARIANT == kW4A8 || VARIANT == kW8A8) v = __ldg(p.a_s + m) * v;
-        p.y[m * p.N + n] = f32_to_bf16_bits(v);
+        o.y[m * o.N + n] = f32_to_bf16_bits(v);
       }
     }
   }
@@ -274,18 +274,19 @@ __device__ __forceinline__ void store_row(const float (&R)[HB], const TcParams& 
 // variant has none).
 template <int HB>
 __device__ __forceinline__ void store_row_scaled(const float (&R)[HB], const float (&asv)[HB],
-                                                 const TcParams& p, int64_t m0, int64_t n) {
+                                                 const TcParams& p, const TileRef& o, int64_t m0,
+                                                 int64_t n) {
 #pragma unroll
   for (int t = 0; t < HB; ++t) {
     const int64_t m = m0 + t;
-    if (m < p.M) p.y[m * p.N + n] = f32_to_bf16_bits(asv[t] * R[t]);
+    if (m < p.M) o.y[m * o.N + n] = f32_to_bf16_bits(asv[t] * R[t]);
   }
 }
 
 template <int VARIANT, int BT, bool PARTIALS>
 __global__ void __launch_bounds__(TcCfg<VARIANT, BT>::kThreads, TcCfg<VARIANT, BT>::kCtasPerSm)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
-               const __grid_constant__ CUtensorMap w8_map, const TcParams p) {
+               const __grid_constant__ CUtensorMap w8_map, const __grid_constant__ TcParams p) {
   using C = TcCfg<VARIANT, BT>;
   constexpr bool kCodes = (VARIANT == kW4A8 || VARIANT == kW8A8);  // per-token scales
   constexpr int S = C::kStages;
@@ -299,7 +300,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
   uint8_t* smem = smem_raw + (base - raw_addr);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t N = p.N;
   const int G = p.G;
 
   // ---- this CTA's work: a flat sequence of (tile, group) items ---------------
@@ -433,8 +433,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
         if constexpr (C::kW8) {
           tma_load_2d(stage_act(s) + C::kActBytes, &w8_map, full_bar(s), g * 128, nt * 128);
         } else {
-          bulk_load(stage_act(s) + C::kActBytes, p.packed + ((int64_t)nt * G + g) * 8512, 8512,
-                    full_bar(s));
+          bulk_load(stage_act(s) + C::kActBytes, tile_ref(p.seg, nt, G).rec0 + (int64_t)g * 8512,
+                    8512, full_bar(s));
         }
       };
       auto load_act = [&](int s) {
@@ -675,7 +675,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
     // scale of row r, group g: half-word 4096 + r of record (tile, g), records
     // 4256 half-words apart
     auto scale_ptr = [&](int tile, int g) {
-      return reinterpret_cast<const uint16_t*>(p.packed + ((int64_t)tile * G + g) * 8512 + 8192) + r;
+      return reinterpret_cast<const uint16_t*>(tile_ref(p.seg, tile, G).rec0 + (int64_t)g * 8512 +
+                                               8192) + r;
     };
     griddep_wait();  // a_s and y belong to the stream's order
     float R[HB];     // fp32 running sums for this thread's weight row
@@ -694,9 +695,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
       if constexpr (kScaleFromGlobal) s_next = __ldg(sp);
     }
     bool ok = true;
+    TileRef out{};  // the current tile's linear: output, its rows, first row
     for (int k = 0; k < n_units && ok; ++k) {
       if (k > 0) unit_tile(k, mt, nt);
-      const int64_t n = (int64_t)nt * 128 + r;
+      out = tile_ref(p.seg, nt, G);
+      const int64_t n = out.n0 + r;  // row of this thread in its linear's output
+      const int64_t N = out.N;
       const int64_t m0 = (int64_t)mt * BT;
       const uint16_t* sp_tile = scale_ptr(nt, g0);
       // the next tile's first scale, fetched now and used after this tile
@@ -840,7 +844,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
       }
       if constexpr (!PARTIALS) {
         if (!cluster_reduce) {
-          store_row<VARIANT, HB>(R, p, m0 + col0, n);
+          store_row<VARIANT, HB>(R, p, out, m0 + col0, n);
         }
       }
     }
@@ -849,7 +853,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
     if (cluster_reduce) {
       // one tile per CTA; every copy and MMA of this CTA has completed, so the
       // stages are free for the partial sums
-      const int64_t n = (int64_t)nt * 128 + r;
+      const int64_t n = out.n0 + r;
       const int64_t m0 = (int64_t)mt * BT;
       float* red = reinterpret_cast<float*>(smem);  // [BT][128]
 #pragma unroll
@@ -890,7 +894,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
         }
         cluster_sync_all();
         if (cluster_ctarank() == 0) {
-          store_row_scaled<HB>(R, asv, p, m0 + col0, n);
+          store_row_scaled<HB>(R, asv, p, out, m0 + col0, n);
         }
       } else {  // (wide tiles: their drain registers have no room for the batch)
         cluster_sync_all();
@@ -904,7 +908,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
         }
         cluster_sync_all();
         if (cluster_ctarank() == 0) {
-          store_row<VARIANT, HB>(R, p, m0 + col0, n);
+          store_row<VARIANT, HB>(R, p, out, m0 + col0, n);
         }
       }
     }
@@ -1022,14 +1026,8 @@ static bool make_act_map_planes(CUtensorMap* map, const void* ptr, int64_t rows,
 }
 
 static int tc_sm_count() {
-  static int count = 0;
-  if (!count) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&count, cudaDevAttrMultiProcessorCount, dev);
-    if (count <= 0) count = 148;
-  }
-  return count;
+  const int n = device_sm_count();
+  return n > 0 ? n : 148;
 }
 
 // Split of the work over the GPU. With enough tiles, a persistent grid (one
@@ -1114,28 +1112,30 @@ static cudaError_t launch_tc(const GemmArgs& a, cudaStream_t st) {
                       : 1;
   p.a_s = a.a_s;
   p.a_gsum = a.a_gsum;
-  p.packed = a.packed;
   p.s8 = a.s8;
-  p.y = a.y;
   p.partials = a.partials;
+  p.seg = seg_table(a);
   p.timeout_ns = a.timeout_ns;
   auto kern = tc_gemm_kernel<VARIANT, BT, PARTIALS>;
-  static bool attr_set = false;  // one-time opt-in to the large shared-memory carve-out
-  if (!attr_set) {
-    cudaError_t e =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    if constexpr (C::kRegSplit) {
-      // the warpgroups' register budgets must fit in what the block is
-      // launched with, or a setmaxnreg increase would wait for ever
+  // opt-in to the large shared-memory carve-out, once per device
+  static SmemOptIn opt_in;
+  if (cudaError_t e = opt_in.ensure(kern, C::kSmemBytes); e != cudaSuccess) return e;
+  if constexpr (C::kRegSplit) {
+    // the warpgroups' register budgets must fit in what the block is launched
+    // with, or a setmaxnreg increase would wait for ever (checked once: the
+    // register count is a property of the compiled kernel)
+    static std::atomic<int> regs_ok{0};  // 0 unchecked, 1 fits, 2 does not
+    if (regs_ok.load(std::memory_order_relaxed) == 0) {
       cudaFuncAttributes fa;
-      e = cudaFuncGetAttributes(&fa, kern);
+      cudaError_t e = cudaFuncGetAttributes(&fa, kern);
       if (e != cudaSuccess) return e;
-      if (C::kDrainWGs * C::kRegDrain + C::kConvSets * C::kRegConv + C::kRegOther >
-          (C::kWarps / 4) * fa.numRegs)
-        return cudaErrorInvalidConfiguration;
+      regs_ok.store(C::kDrainWGs * C::kRegDrain + C::kConvSets * C::kRegConv + C::kRegOther <=
+                            (C::kWarps / 4) * fa.numRegs
+                        ? 1
+                        : 2,
+                    std::memory_order_relaxed);
     }
-    attr_set = true;
+    if (regs_ok.load(std::memory_order_relaxed) != 1) return cudaErrorInvalidConfiguration;
   }
   cudaLaunchConfig_t cfg = {};
   if (persistent)
