@@ -76,12 +76,13 @@ struct TileRef {
   uint16_t* y;
   int64_t N;
   int64_t n0;
+  int seg;  // which linear
 };
 __device__ __forceinline__ TileRef tile_ref(const SegTable& s, int nt, int G) {
   const uint8_t* pk = s.packed[0];
   uint16_t* y = s.y[0];
   int64_t N = s.N[0];
-  int t0 = 0;
+  int t0 = 0, seg = 0;
 #pragma unroll
   for (int j = 1; j < kMaxSegs; ++j) {
     if (j < s.count && nt >= s.tile0[j]) {
@@ -89,10 +90,11 @@ __device__ __forceinline__ TileRef tile_ref(const SegTable& s, int nt, int G) {
       y = s.y[j];
       N = s.N[j];
       t0 = s.tile0[j];
+      seg = j;
     }
   }
   const int64_t lt = nt - t0;
-  return TileRef{pk + lt * G * 8512, y, N, lt * 128};
+  return TileRef{pk + lt * G * 8512, y, N, lt * 128, seg};
 }
 
 // Operands of one GEMM call, already validated by the ABI layer.

@@ -73,6 +73,19 @@ namespace egopq {
 constexpr int kMaxSmem = 232448;      // dynamic shared memory of a CTA alone on its SM
 constexpr int kMaxSmemHalf = 114688;  // each of two CTAs sharing an SM
 
+// Wide tiles: the token tile of the per-group (W4A8 fp16, W4A16) tensor-core
+// path above kTcFp8MaxM tokens, and its TMEM split -- kWideNumD accumulators
+// of kWideBT columns and kWideNumA A-operand buffers of 64 columns -- and MMA
+// issuer count.
+constexpr int kWideBT = 128;
+constexpr int kWideNumD = 3, kWideNumA = 2, kWideIssuers = 2;
+
+// Output tensor maps of the linears (wide tiles' bulk-store epilogue): bf16
+// y_j as 2-D {N_j, M}, box {128, drain columns}.
+struct YMaps {
+  CUtensorMap map[kMaxSegs];
+};
+
 struct TcParams {
   int64_t M, N, K;
   int G, ks;
@@ -122,17 +135,18 @@ struct TcCfg {
   static constexpr int kCtasPerSm = kLean ? 2 : 1;
   static constexpr int kDrainWGs = kLean ? 1 : 2;
   static constexpr int kConvWarp0 = 4 * kDrainWGs;  // drain warps first
+  static constexpr bool kWide = BT > 64 && kDrainPerGroup;
   static constexpr int kMmaWarps =
-      kLean ? 1 : ((kDrainPerGroup && (BT <= 32 || BT == 128)) ? 2 : 1);
+      kLean ? 1 : (kWide ? kWideIssuers : ((kDrainPerGroup && BT <= 32) ? 2 : 1));
   // TMEM: kNumD accumulators of kDCols columns + kNumA A-operand buffers of
   // kACols columns (deep for small tiles: the converters run ahead of the
   // MMAs and the MMAs ahead of the drain).
-  // (128-token per-group tiles: three 128-column accumulators and two A
-  // buffers -- with two the MMAs of a group wait for the drain two back)
-  static constexpr bool kWide = BT == 128 && kDrainPerGroup;
+  // (wide per-group tiles: kWideNumD accumulators and kWideNumA A buffers --
+  // with two 128-column accumulators the MMAs of a group wait for the drain
+  // two back)
   static constexpr int kNumD =
-      kLean ? 4 : (kWide ? 3 : (kFp8 ? (BT == 32 ? 4 : 2) : (BT <= 64 ? 4 : 2)));
-  static constexpr int kNumA = kLean ? 4 : (kWide ? 2 : (kFp8 ? 8 : 4));
+      kLean ? 4 : (kWide ? kWideNumD : (kFp8 ? (BT == 32 ? 4 : 2) : (BT <= 64 ? 4 : 2)));
+  static constexpr int kNumA = kLean ? 4 : (kWide ? kWideNumA : (kFp8 ? 8 : 4));
   static constexpr int kActBox = BT * 128;                        // one 64-wide K box, bytes
   static constexpr int kActBytes = 2 * kActBox;                   // a 128-wide group
   // weights of one group: the int8 tile, or one packed int4 record (8192 B of
@@ -143,12 +157,21 @@ struct TcCfg {
   static constexpr int kStageBytes = kActBytes + kWBytes;        // multiple of 1024
   static constexpr int kTxBytes = kActBytes + kWCopyBytes;
   static constexpr int kSmemLimit = kCtasPerSm == 1 ? kMaxSmem : kMaxSmemHalf;
-  static constexpr int kStagesRaw = (kSmemLimit - 3072) / kStageBytes;
+  // Wide tiles stage each finished tile in shared memory (bf16 [BT][128]) and
+  // write it with TMA bulk stores, one per drain warpgroup, so that the drain
+  // goes straight on to the next tile's groups; the tokens' scales of a tile
+  // are staged at its start (two tiles' worth: double-buffered).
+  static constexpr bool kTmaEpi = kWide;
+  static constexpr int kEpiBytes = kTmaEpi ? BT * 128 * 2 : 0;
+  static constexpr int kAsBytes = kTmaEpi ? 2 * BT * 4 : 0;
+  static constexpr int kStagesRaw = (kSmemLimit - 3072 - kEpiBytes - kAsBytes) / kStageBytes;
   // deep rings for small token tiles (decode streams weights: bytes in flight
   // hide HBM latency); larger tiles are bounded by shared memory
   static constexpr int kStageCap = BT <= 32 ? 16 : 8;
   static constexpr int kStages = kStagesRaw > kStageCap ? kStageCap : kStagesRaw;
-  static constexpr int kBarOffset = kStages * kStageBytes;
+  static constexpr int kEpiOffset = kStages * kStageBytes;  // 1024-byte aligned
+  static constexpr int kAsOffset = kEpiOffset + kEpiBytes;
+  static constexpr int kBarOffset = kAsOffset + kAsBytes;
   static constexpr int kSmemBytes = kBarOffset + 1024 + 1024;    // + barriers + alignment slack
   static constexpr int kTmemColsRaw = kNumD * kDCols + kNumA * kACols;
   static constexpr int kTmemCols = kTmemColsRaw <= 32    ? 32
@@ -159,8 +182,7 @@ struct TcCfg {
   // Converter warp sets: with small token tiles the MMA and drain per group are
   // short, so a second set of four converter warps takes every other group
   // (each set's store-to-arrive latency overlaps the other's conversion).
-  static constexpr int kConvSets =
-      kLean ? 1 : ((BT <= 32 || (BT == 128 && kDrainPerGroup)) ? 2 : 1);
+  static constexpr int kConvSets = kLean ? 1 : ((BT <= 32 || kWide) ? 2 : 1);
   static constexpr int kDrainCols = BT / kDrainWGs;  // token columns per drain thread
   static constexpr int kProducerWarp = kConvWarp0 + 4 * kConvSets;
   static constexpr int kMmaWarp = kProducerWarp + 1;  // first issuer; allocates TMEM
@@ -286,7 +308,8 @@ __device__ __forceinline__ void store_row_scaled(const float (&R)[HB], const flo
 template <int VARIANT, int BT, bool PARTIALS>
 __global__ void __launch_bounds__(TcCfg<VARIANT, BT>::kThreads, TcCfg<VARIANT, BT>::kCtasPerSm)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
-               const __grid_constant__ CUtensorMap w8_map, const __grid_constant__ TcParams p) {
+               const __grid_constant__ CUtensorMap w8_map, const __grid_constant__ TcParams p,
+               const __grid_constant__ YMaps ymaps) {
   using C = TcCfg<VARIANT, BT>;
   constexpr bool kCodes = (VARIANT == kW4A8 || VARIANT == kW8A8);  // per-token scales
   constexpr int S = C::kStages;
@@ -640,12 +663,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
       }
       // A buffer ab is free once the MMAs of item i - kNumA have completed
       if (!mbar_wait(aempty_bar(ab), ((i / kNumA) & 1) ^ 1, abort_flag, tmo)) break;
-      // the accumulator this item feeds must have been drained; one warp of
-      // the set waits (afull completes only with all four arrivals)
-      if (((warp - kConvWarp0) & 3) == 0) {
-        const int di = drain_of(i);
-        if (!mbar_wait(dempty_bar(di % kNumD), ((di / kNumD) & 1) ^ 1, abort_flag, tmo)) break;
-      }
       tc_fence_after();
       const uint32_t dst = a_tmem + lane_base + ab * C::kACols;
 #pragma unroll
@@ -656,6 +673,14 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
         tmem_st16(dst + c * 16, chunk);
       }
       tmem_wait_st();
+      // the accumulator this item feeds must have been drained before its
+      // MMAs are released (the A operand is stored first: only the MMAs, not
+      // the stores, wait for the drain); one warp of the set waits (afull
+      // completes only with all four arrivals)
+      if (((warp - kConvWarp0) & 3) == 0) {
+        const int di = drain_of(i);
+        if (!mbar_wait(dempty_bar(di % kNumD), ((di / kNumD) & 1) ^ 1, abort_flag, tmo)) break;
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(afull_bar(ab));
@@ -679,6 +704,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
                                                8192) + r;
     };
     griddep_wait();  // a_s and y belong to the stream's order
+    if constexpr (C::kTmaEpi && !PARTIALS) {
+      if ((warp & 3) == 0 && lane < p.seg.count) prefetch_tensormap(&ymaps.map[lane]);
+    }
     float R[HB];     // fp32 running sums for this thread's weight row
     // per-group scales of this thread's row, walked with a pointer and
     // prefetched one group ahead (the next tile's first one at a tile's end);
@@ -696,12 +724,57 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
     }
     bool ok = true;
     TileRef out{};  // the current tile's linear: output, its rows, first row
+    // bulk-store epilogue (wide tiles): the warpgroup's staging rows, its
+    // token scales, and the one thread that issues its stores
+    const int wg = warp >> 2;
+    const bool epi_thread = (warp & 3) == 0 && lane == 0;
+    uint16_t* ybuf = reinterpret_cast<uint16_t*>(smem + C::kEpiOffset) + col0 * 128;
+    float* as_stage = reinterpret_cast<float*>(smem + C::kAsOffset);
+    // y rows [m0 + col0, +HB) of tile k's linear `o`: scaled and rounded into
+    // the warpgroup's staging rows, then one bulk store
+    auto epilogue_tma = [&](const float (&Rv)[HB], int k, int64_t m0, const TileRef& o) {
+      // the warpgroup's previous bulk store must have read its rows
+      if (epi_thread) bulk_wait_group_read0();
+      asm volatile("bar.sync %0, 128;" ::"r"(2 + wg) : "memory");
+      // eight tokens at a time: their scales as two vector loads issued
+      // before the chunk's stores (so that no load waits behind a store)
+      const float* as_row = as_stage + (k & 1) * BT + col0;
+#pragma unroll
+      for (int c = 0; c < HB; c += 8) {
+        float av[8] = {1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f, 1.f};
+        if constexpr (kCodes) {
+          const float4 a0 = *reinterpret_cast<const float4*>(as_row + c);
+          const float4 a1 = *reinterpret_cast<const float4*>(as_row + c + 4);
+          av[0] = a0.x; av[1] = a0.y; av[2] = a0.z; av[3] = a0.w;
+          av[4] = a1.x; av[5] = a1.y; av[6] = a1.z; av[7] = a1.w;
+        }
+        uint16_t yv[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) yv[q] = f32_to_bf16_bits(Rv[c + q] * av[q]);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) ybuf[(c + q) * 128 + r] = yv[q];
+      }
+      fence_proxy_async_smem();
+      asm volatile("bar.sync %0, 128;" ::"r"(2 + wg) : "memory");
+      if (epi_thread && m0 + col0 < p.M) {
+        tma_store_2d(&ymaps.map[o.seg], smem_u32(ybuf), (int)o.n0, (int)(m0 + col0));
+        bulk_commit_group();
+      }
+    };
     for (int k = 0; k < n_units && ok; ++k) {
       if (k > 0) unit_tile(k, mt, nt);
       out = tile_ref(p.seg, nt, G);
       const int64_t n = out.n0 + r;  // row of this thread in its linear's output
       const int64_t N = out.N;
       const int64_t m0 = (int64_t)mt * BT;
+      // this tile's token scales for the bulk-store epilogue: loaded now,
+      // staged in shared memory once the first group has been waited for
+      // (the load's latency hides behind that wait)
+      float as_pending = 0.f;
+      if constexpr (C::kTmaEpi && kCodes && !PARTIALS) {
+        const int64_t m = m0 + col0 + r;
+        if (r < HB && m < p.M) as_pending = __ldg(p.a_s + m);
+      }
       const uint16_t* sp_tile = scale_ptr(nt, g0);
       // the next tile's first scale, fetched now and used after this tile
       uint16_t s_first_next = 0;
@@ -723,6 +796,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
         if (!mbar_wait(dfull_bar(db), (di / kNumD) & 1, abort_flag, tmo)) {
           ok = false;
           break;
+        }
+        if constexpr (C::kTmaEpi && kCodes && !PARTIALS) {
+          if (gi == 0 && r < HB) as_stage[(k & 1) * BT + col0 + r] = as_pending;
         }
         tc_fence_after();
         float nz = 0.f;
@@ -788,14 +864,19 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
         // columns per tcgen05.ld (8 at 64 columns per thread without the
         // register split: the 64 running sums leave room for no more at 96
         // registers; with it, 16)
-        constexpr int CW = HB < 16 ? HB : ((HB >= 64 && !C::kRegSplit) ? 8 : 16);
-        // loads in flight per wait (32 columns at most)
-        constexpr int PAIR = (HB / CW) >= 2 ? 2 : 1;
+        constexpr int CW =
+            HB < 16 ? HB : (((HB >= 64 && !C::kRegSplit) || HB % 16) ? 8 : 16);
+        static_assert(HB % CW == 0, "drain columns");
+        constexpr int NCH = HB / CW;  // loads per drain
+        // loads in flight per wait (32 columns at most with the register
+        // split, two loads without it)
+        constexpr int PAIR = C::kRegSplit ? (NCH < 32 / CW ? NCH : 32 / CW) : (NCH >= 2 ? 2 : 1);
 #pragma unroll
-        for (int cb = 0; cb < HB / CW; cb += PAIR) {
+        for (int cb = 0; cb < NCH; cb += PAIR) {
           uint32_t v[PAIR][16];
 #pragma unroll
           for (int q2 = 0; q2 < PAIR; ++q2) {
+            if (cb + q2 >= NCH) break;
             const uint32_t src = d_tmem + lane_base + db * C::kDCols + col0 + (cb + q2) * CW;
             if constexpr (CW == 16) tmem_ld16(src, v[q2]);
             else tmem_ld8(src, v[q2]);
@@ -803,6 +884,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
           tmem_wait_ld();
 #pragma unroll
           for (int q2 = 0; q2 < PAIR; ++q2) {
+            if (cb + q2 >= NCH) break;
             if constexpr (PARTIALS) {
               const int g = g0 + gi;
 #pragma unroll
@@ -844,9 +926,16 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
       }
       if constexpr (!PARTIALS) {
         if (!cluster_reduce) {
-          store_row<VARIANT, HB>(R, p, out, m0 + col0, n);
+          if constexpr (C::kTmaEpi) {
+            epilogue_tma(R, k, m0, out);
+          } else {
+            store_row<VARIANT, HB>(R, p, out, m0 + col0, n);
+          }
         }
       }
+    }
+    if constexpr (C::kTmaEpi && !PARTIALS) {
+      if (epi_thread) bulk_wait_group0();  // the last tile's stores have landed
     }
     __syncwarp();
     teardown_sync();
@@ -908,7 +997,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
         }
         cluster_sync_all();
         if (cluster_ctarank() == 0) {
-          store_row<VARIANT, HB>(R, p, out, m0 + col0, n);
+          if constexpr (C::kTmaEpi) {
+            epilogue_tma(R, 0, m0, out);
+            if (epi_thread) bulk_wait_group0();
+          } else {
+            store_row<VARIANT, HB>(R, p, out, m0 + col0, n);
+          }
         }
       }
     }
@@ -1033,7 +1127,8 @@ static int tc_sm_count() {
 // Split of the work over the GPU. With enough tiles, a persistent grid (one
 // CTA per SM) strides over them with all of K; otherwise each tile's K groups
 // are split over a cluster of ks CTAs. ks minimises rounds * groups-per-unit.
-static void choose_split(int64_t tiles, int G, int sms, int* ks_out, int* persistent_out) {
+static void choose_split(int64_t tiles, int G, int sms, double split_cost, int* ks_out,
+                         int* persistent_out) {
   // enough tiles to fill the GPU: persistent, all of K per tile
   if (tiles >= sms) {
     *ks_out = 1;
@@ -1041,13 +1136,13 @@ static void choose_split(int64_t tiles, int G, int sms, int* ks_out, int* persis
     return;
   }
   // otherwise split K over a cluster, one round, as many SMs busy as possible
-  // (a split costs about one group of prologue/reduction per CTA)
+  // (a split costs `split_cost` groups of prologue and reduction per CTA)
   double best = 1e30;
   int best_ks = 1;
   for (int ks = 1; ks <= 8 && ks <= G; ++ks) {
     const int64_t units = tiles * ks;
     const int64_t rounds = (units + sms - 1) / sms;
-    const double cost = (double)rounds * ((G + ks - 1) / ks + (ks > 1 ? 1.0 : 0.0));
+    const double cost = (double)rounds * ((G + ks - 1) / ks + (ks > 1 ? split_cost : 0.0));
     if (cost < best - 1e-9) {
       best = cost;
       best_ks = ks;
@@ -1095,7 +1190,8 @@ static cudaError_t launch_tc(const GemmArgs& a, cudaStream_t st) {
   if (m_tiles > 65535 || n_tiles > 65535 || tiles >= (1LL << 31)) return cudaErrorInvalidValue;
   const int sms = tc_sm_count() * C::kCtasPerSm;  // CTA slots of one wave
   int ks = 1, persistent = 0;
-  choose_split(tiles, G, sms, &ks, &persistent);
+  // (wide tiles reduce 128 x BT partial sums through DSMEM: two groups' worth)
+  choose_split(tiles, G, sms, C::kWide ? 2.0 : 1.0, &ks, &persistent);
   TcParams p{};
   p.M = a.M;
   p.N = a.N;
@@ -1116,6 +1212,22 @@ static cudaError_t launch_tc(const GemmArgs& a, cudaStream_t st) {
   p.partials = a.partials;
   p.seg = seg_table(a);
   p.timeout_ns = a.timeout_ns;
+  YMaps ymaps;
+  memset(&ymaps, 0, sizeof(ymaps));
+  if constexpr (C::kTmaEpi && !PARTIALS) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return cudaErrorInvalidValue;
+    for (int j = 0; j < p.seg.count; ++j) {
+      cuuint64_t dims[2] = {(cuuint64_t)p.seg.N[j], (cuuint64_t)a.M};
+      cuuint64_t strides[1] = {(cuuint64_t)(p.seg.N[j] * 2)};
+      cuuint32_t box[2] = {128, (cuuint32_t)C::kDrainCols};
+      cuuint32_t estr[2] = {1, 1};
+      if (fn(&ymaps.map[j], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.seg.y[j], dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    }
+  }
   auto kern = tc_gemm_kernel<VARIANT, BT, PARTIALS>;
   // opt-in to the large shared-memory carve-out, once per device
   static SmemOptIn opt_in;
@@ -1154,7 +1266,7 @@ static cudaError_t launch_tc(const GemmArgs& a, cudaStream_t st) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, kern, act_map, w8_map, p);
+  return cudaLaunchKernelEx(&cfg, kern, act_map, w8_map, p, ymaps);
 }
 
 template <int VARIANT, bool PARTIALS>
@@ -1162,7 +1274,9 @@ static cudaError_t launch_tc_bt(const GemmArgs& a, cudaStream_t st) {
   if (a.M <= 16) return launch_tc<VARIANT, 16, PARTIALS>(a, st);
   if (a.M <= 32) return launch_tc<VARIANT, 32, PARTIALS>(a, st);
   if (a.M <= 64) return launch_tc<VARIANT, 64, PARTIALS>(a, st);
-  return launch_tc<VARIANT, 128, PARTIALS>(a, st);
+  // per-group variants take the wide tile; W8A16 accumulates all of K
+  constexpr int kBig = (VARIANT == kW4A8 || VARIANT == kW4A16) ? kWideBT : 128;
+  return launch_tc<VARIANT, kBig, PARTIALS>(a, st);
 }
 
 cudaError_t launch_tc_gemm(const GemmArgs& a, cudaStream_t st) {
