@@ -633,6 +633,75 @@ def measure_int8_yardstick(torch, dev):
         return {"tops": None, "how": f"torch._int_mm unavailable: {str(e)[:120]}"}
 
 
+def measure_twin(parts, stream, steps, torch, eg):
+    """Dense comparisons on the step's tensor-core-sized W4A8 products (more
+    than 64 tokens), each weight dequantized once to bf16 by egopq_dequant_w4:
+    the same products as cuBLAS bf16 GEMMs (torch.matmul), as the structure
+    twin (egopq_bf16_gemm_twin: the W4A16 pipeline with a copy in place of the
+    int4 unpack), and as the W4A16 kernel on the packed weights -- all on the
+    same bf16 activations. Each leg is one CUDA graph, K replays."""
+    prods = []
+    for p in parts:
+        for i, c in enumerate(p.cells):
+            if c.kind != "w4a8" or c.M <= 64:
+                continue
+            Ns = [y.shape[1] for y in p.y[i]] if len(p.y[i]) > 1 else [c.N]
+            for nm, n in zip(c.names if len(Ns) > 1 else c.names[:1], Ns):
+                key = (c.layer, nm) if not (p.args.fused and len(c.names) > 1) else None
+                packed = p.packs[0][key] if key else p.packs[0][(c.layer, "+".join(c.names))]
+                prods.append((c.M, n, c.K, p.x[(c.M, c.inp)], packed))
+    if not prods:
+        return None
+    dense, t_dq = {}, 0.0
+    for (M, N, K, xd, packed) in prods:
+        if packed.data_ptr() not in dense:
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                a.record(stream)
+                dense[packed.data_ptr()] = eg.dequant_w4(packed, N, K, stream=stream)
+                b.record(stream)
+            stream.synchronize()
+            t_dq += a.elapsed_time(b)
+    outs = [torch.empty((M, N), dtype=torch.bfloat16, device=xd.device)
+            for (M, N, K, xd, _) in prods]
+    legs = {
+        "cublas_bf16": lambda: [torch.matmul(xd, dense[pk.data_ptr()].t(), out=o)
+                                for (M, N, K, xd, pk), o in zip(prods, outs)],
+        "structure_twin_bf16": lambda: [eg.bf16_gemm_twin(xd, dense[pk.data_ptr()], out=o)
+                                        for (M, N, K, xd, pk), o in zip(prods, outs)],
+        "w4a16_packed": lambda: [eg.w4a16_gemm(xd, pk, N, K, out=o, path=eg.PATH_TC)
+                                 for (M, N, K, xd, pk), o in zip(prods, outs)],
+    }
+    flops = sum(2 * M * N * K for (M, N, K, _, _) in prods)
+    res = {}
+    for name, fn in legs.items():
+        with torch.cuda.stream(stream):
+            fn()  # warm-up (library heuristics, kernel attributes)
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                g.replay()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(steps):
+                g.replay()
+            b.record(stream)
+        stream.synchronize()
+        ms = a.elapsed_time(b) / steps
+        res[name] = {"ms_per_step": round(ms, 4), "TFLOP/s": round(flops / (ms * 1e-3) / 1e12, 1)}
+        del g
+    res["products"] = len(prods)
+    res["dequant_once_ms"] = round(t_dq, 3)
+    res["how"] = ("the step's W4A8 products above 64 tokens on bf16 activations: cuBLAS and the "
+                  "structure twin on weights dequantized once, W4A16 on the packed weights")
+    del dense, outs
+    torch.cuda.empty_cache()
+    return res
+
+
 def _roofline(label, ms, nbytes, nops, launches, peaks, int8, traffic):
     # the bound that binds: tensor where the kernel's work has more ops per
     # byte than the ridge of the two measured peaks, HBM otherwise
@@ -897,6 +966,8 @@ def run_ours(args, rank, world):
         "clocks": clk.summary(),
         "device_status": status,
     }
+    if args.twin:
+        result["twin"] = measure_twin(parts, stream, args.steps, torch, eg)
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(args, unit_is_ops, budget_s=args.cpu_budget)
     return result
@@ -1009,6 +1080,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-cells", dest="cells", action="store_false",
                     help="skip timing each library call of the step alone")
+    ap.add_argument("--twin", action="store_true",
+                    help="also time the dense comparisons (cuBLAS bf16, the structure twin, "
+                         "W4A16) on the step's tensor-core-sized products")
     ap.add_argument("--path", choices=["auto", "gemv", "tc"], default="auto")
     ap.add_argument("--variant", choices=["w4a8", "w4a16", "w8a16", "w8a8"], default="w4a8",
                     help="variant for --workload linear")

@@ -297,6 +297,19 @@ int egopq_w8a8_gemm_ex(const int8_t* a_q, const void* a_tc, const float* a_s, co
                        const uint16_t* scale_f16, int64_t M, int64_t N, int64_t K,
                        uint16_t* y_bf16, int path, egopq_stream_t stream);
 
+/* ---- dense bf16 twin (comparison kernel) -------------------------------------------
+ * y[m,n] = bf16( sum_k x[m,k] * w[n,k] ), x bf16 [M][K], w dense bf16 [N][K]
+ * row-major, y bf16 [M][N]; K % 128 == 0, N % 128 == 0.
+ * The W4A16 tensor-core pipeline with the int4 unpack taken out: the same
+ * warp roles, shared-memory stages, TMEM buffers, per-128-K-group drains and
+ * epilogue, with the weight tile staged by TMA and copied into the MMA operand
+ * as it is. Timed beside the packed kernels it measures what the int4 unpack
+ * costs ("OSCAR PR #20", commit message: a bf16 twin kernel of identical
+ * structure as the fair speed baseline); egopq_dequant_w4 plus any dense
+ * library GEMM is the other comparison. Not a quantized path. */
+int egopq_bf16_gemm_twin(const uint16_t* x_bf16, const uint16_t* w_bf16, int64_t M, int64_t N,
+                         int64_t K, uint16_t* y_bf16, egopq_stream_t stream);
+
 /* ---- support, status --------------------------------------------------------------
  * 1 if (M, N, K, group, variant) is accepted by the parity-tested kernels on
  * the current device, 0 if not. It claims nothing the kernels do not run (a

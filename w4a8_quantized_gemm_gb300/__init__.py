@@ -82,6 +82,7 @@ def load() -> ctypes.CDLL:
                                               i32, vp]),
             "egopq_w4a8_linear_grouped": (i32, [vp, i32, vp, vp, i64, i64, i32, vp, vp, sz, i32,
                                                 vp]),
+            "egopq_bf16_gemm_twin": (i32, [vp, vp, i64, i64, i64, vp, vp]),
             "egopq_supported": (i32, [i64, i64, i64, i32, i32]),
             "egopq_auto_path": (i32, [i64, i32]),
             "egopq_tc_operand_bytes": (sz, [i64, i64, i32]),
@@ -380,6 +381,20 @@ def w8a8_gemm(a: QuantAct, w_q: torch.Tensor, scale_f16: torch.Tensor, path: int
     _check(load().egopq_w8a8_gemm_ex(_ptr(a.a_q), _ptr(a.a_tc), _ptr(a.a_s), _ptr(w_q),
                                      _ptr(scale_f16), M, N, K, _ptr(out), path,
                                      _stream(stream)))
+    return out
+
+
+def bf16_gemm_twin(x: torch.Tensor, w: torch.Tensor, out: Optional[torch.Tensor] = None,
+                   stream=None) -> torch.Tensor:
+    """Dense bf16 x [M, K] times w [N, K] through the W4A16 tensor-core
+    pipeline with a copy in place of the int4 unpack (comparison kernel)."""
+    _dtype(x, torch.bfloat16)
+    _dtype(w, torch.bfloat16)
+    M, K = x.shape
+    N = w.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _check(load().egopq_bf16_gemm_twin(_ptr(x), _ptr(w), M, N, K, _ptr(out), _stream(stream)))
     return out
 
 

@@ -532,6 +532,27 @@ int egopq_w8a8_gemm(const int8_t* a_q, const void* a_tc, const float* a_s, const
                             stream);
 }
 
+int egopq_bf16_gemm_twin(const uint16_t* x_bf16, const uint16_t* w_bf16, int64_t M, int64_t N,
+                         int64_t K, uint16_t* y_bf16, egopq_stream_t stream) {
+  int rc = check_w4_shape(M, N, K, 128);
+  if (rc) return rc;
+  if (M == 0) return EGOPQ_OK;
+  rc = check_ptrs(3, "x_bf16", x_bf16, "w_bf16", w_bf16, "y_bf16", y_bf16);
+  if (rc) return rc;
+  if ((rc = check_arch())) return rc;
+  GemmArgs a{};
+  a.variant = kW16A16;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.x = x_bf16;
+  a.w16 = w_bf16;
+  a.y = y_bf16;
+  a.timeout_ns = kDefaultTimeoutNs;
+  cudaError_t e = launch_tc_gemm(a, (cudaStream_t)stream);
+  return e == cudaSuccess ? EGOPQ_OK : cuda_fail(e, "bf16 twin launch");
+}
+
 int egopq_supported(int64_t M, int64_t N, int64_t K, int group, int variant) {
   if (variant < EGOPQ_VARIANT_W4A8 || variant > EGOPQ_VARIANT_W8A8) return 0;
   if (variant == EGOPQ_VARIANT_W8A16 || variant == EGOPQ_VARIANT_W8A8) group = 128;

@@ -12,7 +12,10 @@
 
 namespace egopq {
 
-enum Variant { kW4A8 = 0, kW4A16 = 1, kW8A16 = 2, kW8A8 = 3 };
+// kW16A16: dense bf16 weights through the W4A16 tensor-core pipeline (the
+// same roles, buffers and per-group drains; the converters copy instead of
+// unpacking) -- a yardstick, not a quantized path.
+enum Variant { kW4A8 = 0, kW4A16 = 1, kW8A16 = 2, kW8A8 = 3, kW16A16 = 4 };
 
 // Launch state that depends on the device (shared-memory opt-ins, SM counts)
 // is kept per device ordinal, up to this many devices.
@@ -113,6 +116,8 @@ struct GemmArgs {
   // int8 weight and per-channel scale (W8A16, W8A8)
   const int8_t* w8;
   const uint16_t* s8;
+  // dense bf16 weight [N][K] (W16A16)
+  const uint16_t* w16;
   // outputs
   uint16_t* y;
   int32_t* partials;  // non-null: write group partials instead of y (W4A8 only)

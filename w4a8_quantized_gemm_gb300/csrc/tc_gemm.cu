@@ -64,7 +64,6 @@
 // int8 weights to fp16 against the fp16 activation codes, drains every 8
 // groups (exact: 1024 * 127^2 < 2^24), adds the partials as int32 and scales
 // by a_s[m] * s[n] at the end.
-#include <cmath>
 
 #include "egopq_internal.h"
 
@@ -118,10 +117,15 @@ struct TcCfg {
   // so the fp32 accumulator holds it exactly) and adds the partials as int32
   // (a whole K row can exceed 2^24); its scales come only in the epilogue.
   static constexpr int kGroupsPerDrain = (VARIANT == kW8A16) ? 0 : (VARIANT == kW8A8 ? 8 : 1);
+  static constexpr bool kCodes = (VARIANT == kW4A8 || VARIANT == kW8A8);  // per-token scales
   static constexpr bool kDrainPerGroup = (kGroupsPerDrain == 1);
   static constexpr bool kIntAcc = (VARIANT == kW8A8);
   // int8 weight tiles (W8A16, W8A8): staged by a 2-D TMA copy, no pack step
   static constexpr bool kW8 = (VARIANT == kW8A16 || VARIANT == kW8A8);
+  // weights staged by a 2-D TMA copy (no pack step): int8 tiles, or the
+  // dense bf16 tiles of the twin (two 64-column boxes a group)
+  static constexpr bool kW16 = (VARIANT == kW16A16);
+  static constexpr bool kTmaW = kW8 || kW16;
   // MMA issuers. An MMA instruction up to N = 64 costs its issuing thread
   // about as much as the tensor core, and every barrier test costs it a
   // round trip, so small token tiles use two issuing warps that take
@@ -152,8 +156,8 @@ struct TcCfg {
   // weights of one group: the int8 tile, or one packed int4 record (8192 B of
   // codes, 256 B of scales, 64 B of zero nibbles), padded to keep stages
   // 1024-byte aligned
-  static constexpr int kWCopyBytes = kW8 ? 16384 : 8512;
-  static constexpr int kWBytes = kW8 ? 16384 : 9216;
+  static constexpr int kWCopyBytes = kW16 ? 32768 : (kW8 ? 16384 : 8512);
+  static constexpr int kWBytes = kW16 ? 32768 : (kW8 ? 16384 : 9216);
   static constexpr int kStageBytes = kActBytes + kWBytes;        // multiple of 1024
   static constexpr int kTxBytes = kActBytes + kWCopyBytes;
   static constexpr int kSmemLimit = kCtasPerSm == 1 ? kMaxSmem : kMaxSmemHalf;
@@ -163,7 +167,7 @@ struct TcCfg {
   // are staged at its start (two tiles' worth: double-buffered).
   static constexpr bool kTmaEpi = kWide;
   static constexpr int kEpiBytes = kTmaEpi ? BT * 128 * 2 : 0;
-  static constexpr int kAsBytes = kTmaEpi ? 2 * BT * 4 : 0;
+  static constexpr int kAsBytes = (kTmaEpi && kCodes) ? 2 * BT * 4 : 0;
   static constexpr int kStagesRaw = (kSmemLimit - 3072 - kEpiBytes - kAsBytes) / kStageBytes;
   // deep rings for small token tiles (decode streams weights: bytes in flight
   // hide HBM latency); larger tiles are bounded by shared memory
@@ -410,7 +414,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
   }
   if (warp == C::kProducerWarp && lane == 0) {
     prefetch_tensormap(&act_map);
-    if constexpr (C::kW8) prefetch_tensormap(&w8_map);
+    if constexpr (C::kTmaW) prefetch_tensormap(&w8_map);
   }
   if (warp == C::kMmaWarp) {
     tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
@@ -453,7 +457,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
       auto load_weights = [&](int s) {
         const int nt = w_nt, g = g0 + w_gi;
         advance(w_k, w_gi, w_mt, w_nt);
-        if constexpr (C::kW8) {
+        if constexpr (C::kW16) {
+          tma_load_2d(stage_act(s) + C::kActBytes, &w8_map, full_bar(s), g * 128, nt * 128);
+          tma_load_2d(stage_act(s) + C::kActBytes + 16384, &w8_map, full_bar(s), g * 128 + 64,
+                      nt * 128);
+        } else if constexpr (C::kW8) {
           tma_load_2d(stage_act(s) + C::kActBytes, &w8_map, full_bar(s), g * 128, nt * 128);
         } else {
           bulk_load(stage_act(s) + C::kActBytes, tile_ref(p.seg, nt, G).rec0 + (int64_t)g * 8512,
@@ -613,6 +621,23 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
             out[c * 8 + j * 2 + 1] = prmt(kT0, kT1, w >> 16) | prmt(kT2, kT3, wx >> 16);
           }
         }
+      } else if constexpr (C::kW16) {
+        // dense bf16 row r: two 128-byte-swizzled boxes of 64 K values, copied
+        // as they are (K pairs per 32-bit word, the A operand's layout)
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+          const uint8_t* wt = stage_w_ptr(s) + b * 16384 + r * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint4 v = *reinterpret_cast<const uint4*>(wt + ((c ^ (r & 7)) * 16));
+            out[b * 32 + c * 4 + 0] = v.x;
+            out[b * 32 + c * 4 + 1] = v.y;
+            out[b * 32 + c * 4 + 2] = v.z;
+            out[b * 32 + c * 4 + 3] = v.w;
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty_bar(s));
       } else if constexpr (C::kW8) {
         const uint8_t* wt = stage_w_ptr(s) + r * 128;
         uint4 v[8];
@@ -711,7 +736,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
     // per-group scales of this thread's row, walked with a pointer and
     // prefetched one group ahead (the next tile's first one at a tile's end);
     // the e4m3 form reads scale and zero point from the staged record instead
-    constexpr bool kScaleFromGlobal = C::kDrainPerGroup && !C::kFp8 && !C::kIntAcc;
+    constexpr bool kScaleFromGlobal = C::kDrainPerGroup && !C::kFp8 && !C::kIntAcc && !C::kW16;
     const uint16_t* sp = nullptr;
     // (kept as raw fp16 bits until used, so that the load's latency overlaps
     // a whole group; W8A16 has no per-group scale: 1.0)
@@ -1152,11 +1177,19 @@ static void choose_split(int64_t tiles, int G, int sms, double split_cost, int* 
   *persistent_out = 0;
 }
 
-// Band height (in m-tiles) for the persistent tile order: the tiles in flight
-// (about `concurrent`) cover `band` activation tiles and concurrent/band weight
-// tiles; minimise band*act + (concurrent/band)*w.
-static int choose_band(int64_t m_tiles, int64_t concurrent, double act_tile, double w_tile) {
-  int band = (int)(std::sqrt((double)concurrent * w_tile / act_tile) + 0.5);
+// Band height (in m-tiles) for the persistent tile order, which walks bands of
+// `band` m-tiles with m fastest inside a band: each weight tile is read from
+// DRAM once per band, each activation tile once if the band's activations stay
+// in L2. So DRAM traffic is lowest when one operand stays L2-resident while
+// the other streams once: all m-tiles in one band when the whole activation
+// matrix fits the L2 budget (weights stream once), one m-tile a band (n
+// fastest) when the whole weight matrix fits (activations stream once),
+// otherwise the tallest band whose activation tiles fit.
+static int choose_band(int64_t m_tiles, int64_t n_tiles, double act_tile, double w_tile) {
+  constexpr double kL2Budget = 48e6;  // bytes of one operand kept resident (129 MB L2)
+  if (m_tiles * act_tile <= kL2Budget) return (int)m_tiles;
+  if (n_tiles * w_tile <= kL2Budget) return 1;
+  int band = (int)(kL2Budget / act_tile);
   if (band < 1) band = 1;
   if (band > m_tiles) band = (int)m_tiles;
   return band;
@@ -1179,7 +1212,10 @@ static cudaError_t launch_tc(const GemmArgs& a, cudaStream_t st) {
     if (!act3d && !make_map(&act_map, adt, 2, act_ptr, a.M, a.K, 64, BT))
       return cudaErrorInvalidValue;
   }
-  if (C::kW8) {
+  if constexpr (C::kW16) {
+    if (!make_map(&w8_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.w16, a.N, a.K, 64, 128))
+      return cudaErrorInvalidValue;
+  } else if constexpr (C::kW8) {
     if (!make_map(&w8_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.w8, a.N, a.K, 128, 128))
       return cudaErrorInvalidValue;
   }
@@ -1202,9 +1238,8 @@ static cudaError_t launch_tc(const GemmArgs& a, cudaStream_t st) {
   p.n_tiles = (int)n_tiles;
   p.persistent = persistent;
   p.act3d = act3d;
-  p.band = persistent ? choose_band(m_tiles, tiles < sms ? tiles : sms,
-                                    (double)BT * a.K * 2.0,
-                                    (double)128 * a.K / (C::kW8 ? 1.0 : 2.0))
+  p.band = persistent ? choose_band(m_tiles, n_tiles, (double)BT * a.K * 2.0,
+                                    (double)128 * a.K * (C::kW16 ? 2.0 : (C::kW8 ? 1.0 : 0.5)))
                       : 1;
   p.a_s = a.a_s;
   p.a_gsum = a.a_gsum;
@@ -1275,7 +1310,8 @@ static cudaError_t launch_tc_bt(const GemmArgs& a, cudaStream_t st) {
   if (a.M <= 32) return launch_tc<VARIANT, 32, PARTIALS>(a, st);
   if (a.M <= 64) return launch_tc<VARIANT, 64, PARTIALS>(a, st);
   // per-group variants take the wide tile; W8A16 accumulates all of K
-  constexpr int kBig = (VARIANT == kW4A8 || VARIANT == kW4A16) ? kWideBT : 128;
+  constexpr int kBig =
+      (VARIANT == kW4A8 || VARIANT == kW4A16 || VARIANT == kW16A16) ? kWideBT : 128;
   return launch_tc<VARIANT, kBig, PARTIALS>(a, st);
 }
 
@@ -1288,6 +1324,8 @@ cudaError_t launch_tc_gemm(const GemmArgs& a, cudaStream_t st) {
       return launch_tc_bt<kW4A16, false>(a, st);
     case kW8A16:
       return launch_tc_bt<kW8A16, false>(a, st);
+    case kW16A16:
+      return launch_tc_bt<kW16A16, false>(a, st);
     case kW8A8:
       // the fp16 activation-code form exists for M > kTcFp8MaxM only (the
       // e4m3 planes below it are specific to 4-bit weights); smaller M run
