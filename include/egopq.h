@@ -52,7 +52,8 @@ typedef enum {
   EGOPQ_ERR_MISALIGNED = -3,        /* an operand pointer is not 16-byte aligned */
   EGOPQ_ERR_ARCH = -4,              /* current device is not sm_103 */
   EGOPQ_ERR_CUDA = -5,              /* a CUDA runtime call or launch failed */
-  EGOPQ_ERR_TIMEOUT = -6            /* a kernel's bounded wait expired */
+  EGOPQ_ERR_TIMEOUT = -6,           /* a kernel's bounded wait expired */
+  EGOPQ_ERR_DEVICE_INDEX = -7       /* a debug build's device-side index check failed */
 } egopq_status;
 
 /* Kernel path. AUTO picks by M (W4A8: CUDA-core GEMV for M <= 4, the tcgen05
@@ -320,6 +321,7 @@ int egopq_supported(int64_t M, int64_t N, int64_t K, int group, int variant);
 
 /* Synchronize `stream`, then read and clear the device error word: EGOPQ_OK,
  * EGOPQ_ERR_TIMEOUT if a kernel's bounded wait expired since the last call,
+ * EGOPQ_ERR_DEVICE_INDEX if a debug build's index check failed,
  * EGOPQ_ERR_INVALID_ARG if egopq_pack_w4_gptq met a zero point it cannot store, or
  * EGOPQ_ERR_CUDA if the synchronization itself failed. Every wait inside the
  * kernels is bounded (2 s); once one expires its kernel's results are invalid,
@@ -328,6 +330,22 @@ int egopq_device_status(egopq_stream_t stream);
 
 /* Human-readable text for the calling thread's most recent failure. */
 const char* egopq_last_error_string(void);
+
+/* ---- debug build -------------------------------------------------------------------
+ * The library also builds as libegopq_debug.so (EGOPQ_DEBUG): the same kernels
+ * with device-side read-index checks on the packed-weight record copies, the
+ * per-group scale reads and the activation, group-sum and token reads of the
+ * GEMV and tensor-core paths. A failed check records itself in the device
+ * error word (egopq_device_status then returns EGOPQ_ERR_DEVICE_INDEX) and the
+ * read goes to a known-valid address instead, so a bad index never becomes a
+ * memory fault; results of such a call are invalid.
+ * egopq_debug_build: 1 in the debug build, 0 otherwise.
+ * egopq_debug_set_record_limit: lower the byte size the packed-record checks
+ * allow (0 restores each buffer's own size), for tests that make the checks
+ * fire while every read stays inside the real buffer; EGOPQ_ERR_INVALID_ARG
+ * in a release build. Not thread-safe against kernels in flight. */
+int egopq_debug_build(void);
+int egopq_debug_set_record_limit(uint64_t bytes);
 
 /* Self-test of the bounded-wait machinery: launches one CTA that waits on an
  * mbarrier nothing will complete, with a deadline of `timeout_us`

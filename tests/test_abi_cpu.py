@@ -85,6 +85,12 @@ def test_sizes_beyond_the_limit_are_unsupported_shapes(lib):
     assert lib.egopq_quant_act_i8(A, big, 512, 128, A, A, A, None, s) == -2
 
 
+def test_release_build_has_no_debug_hooks(lib):
+    assert lib.egopq_debug_build() == 0
+    assert lib.egopq_debug_set_record_limit(4096) == -1
+    assert b"debug build" in lib.egopq_last_error_string()
+
+
 def test_binding_fails_loudly_without_library(monkeypatch):
     monkeypatch.setattr(eg, "LIB_PATH", os.path.join(os.path.dirname(eg.LIB_PATH), "nope.so"))
     monkeypatch.setattr(eg, "_lib", None)

@@ -28,7 +28,8 @@ HEADER_PATH = os.path.join(os.path.dirname(_HERE), "include", "egopq.h")
 PATH_AUTO, PATH_GEMV, PATH_TC = 0, 1, 2
 VARIANT_W4A8, VARIANT_W4A16, VARIANT_W8A16, VARIANT_W8A8 = 0, 1, 2, 3
 STATUS = {0: "OK", -1: "INVALID_ARG", -2: "UNSUPPORTED_SHAPE", -3: "MISALIGNED",
-          -4: "ARCH", -5: "CUDA", -6: "TIMEOUT"}
+          -4: "ARCH", -5: "CUDA", -6: "TIMEOUT", -7: "DEVICE_INDEX"}
+DEBUG_LIB_PATH = os.path.join(_HERE, "_build", "libegopq_debug.so")
 GROUP = 128
 
 _lock = threading.Lock()
@@ -89,6 +90,8 @@ def load() -> ctypes.CDLL:
             "egopq_tc_operand_form": (i32, [i64]),
             "egopq_device_status": (i32, [vp]),
             "egopq_selftest_timeout": (i32, [i32, vp]),
+            "egopq_debug_build": (i32, []),
+            "egopq_debug_set_record_limit": (i32, [ctypes.c_uint64]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)

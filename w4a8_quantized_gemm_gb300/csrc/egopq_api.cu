@@ -591,9 +591,32 @@ int egopq_device_status(egopq_stream_t stream) {
     word |= w;
   }
   if (word & kErrTimeout) return fail(EGOPQ_ERR_TIMEOUT, "a kernel's bounded wait expired");
+  if (word & kErrIndex)
+    return fail(EGOPQ_ERR_DEVICE_INDEX, "a device-side index check of the debug build failed");
   if (word & kErrRange)
     return fail(EGOPQ_ERR_INVALID_ARG, "an imported zero point is outside [0, 15]");
   return EGOPQ_OK;
+}
+
+int egopq_debug_build(void) {
+#ifdef EGOPQ_DEBUG
+  return 1;
+#else
+  return 0;
+#endif
+}
+
+int egopq_debug_set_record_limit(uint64_t bytes) {
+#ifdef EGOPQ_DEBUG
+  int rc = check_arch();
+  if (rc) return rc;
+  cudaError_t e = set_record_limit_gemv(bytes);
+  if (e == cudaSuccess) e = set_record_limit_tc_gemm(bytes);
+  return e == cudaSuccess ? EGOPQ_OK : cuda_fail(e, "set the record limit");
+#else
+  (void)bytes;
+  return fail(EGOPQ_ERR_INVALID_ARG, "egopq_debug_set_record_limit needs the debug build");
+#endif
 }
 
 int egopq_selftest_timeout(int timeout_us, egopq_stream_t stream) {

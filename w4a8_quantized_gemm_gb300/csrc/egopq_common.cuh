@@ -26,6 +26,8 @@ namespace egopq {
 // a take_error_word_* function; the host ORs and clears them all.
 constexpr unsigned kErrTimeout = 1u;
 constexpr unsigned kErrRange = 2u;
+// Bit 2: a debug build's device-side index check failed (EGOPQ_ERR_DEVICE_INDEX).
+constexpr unsigned kErrIndex = 4u;
 static __device__ unsigned int g_error_word = 0;
 
 // Host: read this unit's word and clear it if set.
@@ -37,6 +39,38 @@ static inline cudaError_t take_local_error_word(unsigned* out) {
 }
 
 __device__ __forceinline__ void raise_error(unsigned bits) { atomicOr(&g_error_word, bits); }
+
+// ---- debug builds (EGOPQ_DEBUG): device-side read-index checks ---------------
+// dbg_ok(off, len, size): the read [off, off + len) lies inside a buffer of
+// `size` elements or bytes. A failed check records kErrIndex and returns
+// false; the caller then reads a known-valid address instead, so the check
+// never becomes a fault. dbg_record_ok() checks reads of packed weight records
+// against the buffer's size or, when a test has set it lower, against
+// g_dbg_record_limit: the checks can then be made to fire while every read
+// stays inside the real buffer. Release builds compile the checks away.
+#ifdef EGOPQ_DEBUG
+static __device__ unsigned long long g_dbg_record_limit = 0;  // 0: the buffer's size
+__device__ __forceinline__ bool dbg_ok(uint64_t off, uint64_t len, uint64_t size) {
+  if (off + len <= size) return true;
+  raise_error(kErrIndex);
+  return false;
+}
+__device__ __forceinline__ bool dbg_record_ok(uint64_t off, uint64_t len, uint64_t size) {
+  const unsigned long long lim = *reinterpret_cast<volatile unsigned long long*>(&g_dbg_record_limit);
+  return dbg_ok(off, len, (lim != 0 && lim < size) ? lim : size);
+}
+static inline cudaError_t set_local_record_limit(unsigned long long bytes) {
+  return cudaMemcpyToSymbol(g_dbg_record_limit, &bytes, sizeof(bytes));
+}
+#else
+__device__ __forceinline__ constexpr bool dbg_ok(uint64_t, uint64_t, uint64_t) { return true; }
+__device__ __forceinline__ constexpr bool dbg_record_ok(uint64_t, uint64_t, uint64_t) {
+  return true;
+}
+static inline cudaError_t set_local_record_limit(unsigned long long) {
+  return cudaErrorNotSupported;
+}
+#endif
 
 __device__ __forceinline__ uint64_t globaltimer() {
   uint64_t t;

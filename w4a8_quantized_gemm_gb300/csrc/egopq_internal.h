@@ -156,6 +156,15 @@ cudaError_t launch_dequant_w4(const void* packed, int64_t N, int64_t K, uint16_t
 cudaError_t take_error_word_quant_pack(unsigned* out);
 cudaError_t take_error_word_gemv(unsigned* out);
 cudaError_t take_error_word_tc_gemm(unsigned* out);
+// Debug builds: the packed-record read limit of each unit that reads records
+// (cudaErrorNotSupported in release builds).
+cudaError_t set_record_limit_gemv(unsigned long long bytes);
+cudaError_t set_record_limit_tc_gemm(unsigned long long bytes);
+
+// Byte size of the packed records of one linear with N rows and G groups.
+__host__ __device__ inline uint64_t packed_record_bytes(int64_t N, int G) {
+  return (uint64_t)(N / 128) * (uint64_t)G * 8512u;
+}
 
 // CUDA-core GEMV (small M). Returns cudaErrorNotSupported for shapes it does
 // not take.

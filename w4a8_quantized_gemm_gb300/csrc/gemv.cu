@@ -99,8 +99,12 @@ gemv_w4_kernel(const __grid_constant__ GemvParams p) {
       auto issue = [&](int i) {
         const int s = i % kGemvStages, g = g0 + i;
         mbar_arrive_expect_tx(full_bar(s), kGemvStageBytes);
-        bulk_load(smem_u32(ring + s * kGemvStageBytes),
-                  tile.rec0 + (int64_t)g * kGemvStageBytes, kGemvStageBytes, full_bar(s));
+        const uint8_t* seg_base = p.seg.packed[tile.seg];
+        const uint8_t* src = tile.rec0 + (int64_t)g * kGemvStageBytes;
+        if (!dbg_record_ok((uint64_t)(src - seg_base), kGemvStageBytes,
+                           packed_record_bytes(tile.N, G)))
+          src = seg_base;
+        bulk_load(smem_u32(ring + s * kGemvStageBytes), src, kGemvStageBytes, full_bar(s));
       };
       int issued = 0;
       for (int i = 0; i < ng; ++i) {
@@ -135,7 +139,8 @@ gemv_w4_kernel(const __grid_constant__ GemvParams p) {
       for (int i = threadIdx.x; i < ng * MT * 16; i += kGemvConsumers) {
         const int gl = i / (MT * 16), m = (i / 16) % MT, cj = i % 16;
         uint2 v = make_uint2(0, 0);
-        if (m < p.rows) {
+        if (m < p.rows && dbg_ok((uint64_t)(m * K + (int64_t)(g0 + gl) * 128 + cj * 8), 8,
+                                 (uint64_t)p.rows * K)) {
           const int64_t k0 = (int64_t)(g0 + gl) * 128 + cj * 8;
           const uint2 X = *reinterpret_cast<const uint2*>(p.a_q + m * K + k0);
           v.x = prmt(X.x, X.y, 0x5140);  // K offsets {0,4,1,5}
@@ -145,7 +150,9 @@ gemv_w4_kernel(const __grid_constant__ GemvParams p) {
       }
       for (int i = threadIdx.x; i < ng * MT; i += kGemvConsumers) {
         const int gl = i / MT, m = i % MT;
-        as[i] = (m < p.rows) ? p.a_gsum[m * G + g0 + gl] : 0;
+        as[i] = (m < p.rows && dbg_ok((uint64_t)(m * G + g0 + gl), 1, (uint64_t)p.rows * G))
+                    ? p.a_gsum[m * G + g0 + gl]
+                    : 0;
       }
     } else {
       float* xs = reinterpret_cast<float*>(act);
@@ -155,7 +162,9 @@ gemv_w4_kernel(const __grid_constant__ GemvParams p) {
         const int nib = kk & 7;
         const int e = (nib < 4) ? 2 * nib : 2 * (nib - 4) + 1;
         float v = 0.f;
-        if (m < p.rows)
+        if (m < p.rows &&
+            dbg_ok((uint64_t)(m * K + (int64_t)(g0 + gl) * 128 + (kk & ~7) + e), 1,
+                   (uint64_t)p.rows * K))
           v = bf16_bits_to_f32(p.x[m * K + (int64_t)(g0 + gl) * 128 + (kk & ~7) + e]);
         xs[i] = v;
       }
@@ -618,5 +627,6 @@ cudaError_t launch_gemv(const GemmArgs& a, cudaStream_t st) {
 }
 
 cudaError_t take_error_word_gemv(unsigned* out) { return take_local_error_word(out); }
+cudaError_t set_record_limit_gemv(unsigned long long bytes) { return set_local_record_limit(bytes); }
 
 }  // namespace egopq

@@ -464,8 +464,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
         } else if constexpr (C::kW8) {
           tma_load_2d(stage_act(s) + C::kActBytes, &w8_map, full_bar(s), g * 128, nt * 128);
         } else {
-          bulk_load(stage_act(s) + C::kActBytes, tile_ref(p.seg, nt, G).rec0 + (int64_t)g * 8512,
-                    8512, full_bar(s));
+          const TileRef tr = tile_ref(p.seg, nt, G);
+          const uint8_t* src = tr.rec0 + (int64_t)g * 8512;
+          if (!dbg_record_ok((uint64_t)(src - p.seg.packed[tr.seg]), 8512,
+                             packed_record_bytes(tr.N, G)))
+            src = p.seg.packed[tr.seg];
+          bulk_load(stage_act(s) + C::kActBytes, src, 8512, full_bar(s));
         }
       };
       auto load_act = [&](int s) {
@@ -724,19 +728,28 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     // scale of row r, group g: half-word 4096 + r of record (tile, g), records
     // 4256 half-words apart
+    // per-group scales of this thread's row, walked with a pointer and
+    // prefetched one group ahead (the next tile's first one at a tile's end);
+    // the e4m3 form reads scale and zero point from the staged record instead
+    constexpr bool kScaleFromGlobal = C::kDrainPerGroup && !C::kFp8 && !C::kIntAcc && !C::kW16;
+    constexpr bool kScaleCheck = kScaleFromGlobal;
     auto scale_ptr = [&](int tile, int g) {
-      return reinterpret_cast<const uint16_t*>(tile_ref(p.seg, tile, G).rec0 + (int64_t)g * 8512 +
-                                               8192) + r;
+      const TileRef tr = tile_ref(p.seg, tile, G);
+      const uint8_t* base = p.seg.packed[tr.seg];
+      const uint8_t* q = tr.rec0 + (int64_t)g * 8512 + 8192 + 2 * r;
+      // (the release build reads every per-group scale through this pointer
+      // plus multiples of 4256 half-words, one record per group, all within
+      // the tile's G records)
+      if (kScaleCheck && !dbg_record_ok((uint64_t)(q - base), 2u + (uint64_t)(G - 1 - g) * 8512u,
+                                        packed_record_bytes(tr.N, G)))
+        q = base + 8192;
+      return reinterpret_cast<const uint16_t*>(q);
     };
     griddep_wait();  // a_s and y belong to the stream's order
     if constexpr (C::kTmaEpi && !PARTIALS) {
       if ((warp & 3) == 0 && lane < p.seg.count) prefetch_tensormap(&ymaps.map[lane]);
     }
     float R[HB];     // fp32 running sums for this thread's weight row
-    // per-group scales of this thread's row, walked with a pointer and
-    // prefetched one group ahead (the next tile's first one at a tile's end);
-    // the e4m3 form reads scale and zero point from the staged record instead
-    constexpr bool kScaleFromGlobal = C::kDrainPerGroup && !C::kFp8 && !C::kIntAcc && !C::kW16;
     const uint16_t* sp = nullptr;
     // (kept as raw fp16 bits until used, so that the load's latency overlaps
     // a whole group; W8A16 has no per-group scale: 1.0)
@@ -868,7 +881,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
               const int32_t* asum_g = p.a_gsum + (g0 + gi);
               const int mfirst = (int)(m0 + col0) + cb * CW, mlast = (int)(p.M - 1);
 #pragma unroll
-              for (int q = 0; q < CW; ++q) asf[q] = (float)__ldg(asum_g + min(mfirst + q, mlast) * G);
+              for (int q = 0; q < CW; ++q) {
+                const int64_t ai = (int64_t)min(mfirst + q, mlast) * G + g0 + gi;
+                asf[q] = dbg_ok((uint64_t)ai, 1, (uint64_t)p.M * G)
+                             ? (float)__ldg(asum_g + min(mfirst + q, mlast) * G)
+                             : 0.f;
+              }
             }
             tmem_wait_ld();
 #pragma unroll
@@ -1152,8 +1170,8 @@ static int tc_sm_count() {
 // Split of the work over the GPU. With enough tiles, a persistent grid (one
 // CTA per SM) strides over them with all of K; otherwise each tile's K groups
 // are split over a cluster of ks CTAs. ks minimises rounds * groups-per-unit.
-static void choose_split(int64_t tiles, int G, int sms, double split_cost, int* ks_out,
-                         int* persistent_out) {
+static void choose_split(int64_t tiles, int G, int sms, double split_cost, bool one_wave,
+                         int* ks_out, int* persistent_out) {
   // enough tiles to fill the GPU: persistent, all of K per tile
   if (tiles >= sms) {
     *ks_out = 1;
@@ -1166,6 +1184,7 @@ static void choose_split(int64_t tiles, int G, int sms, double split_cost, int* 
   int best_ks = 1;
   for (int ks = 1; ks <= 8 && ks <= G; ++ks) {
     const int64_t units = tiles * ks;
+    if (one_wave && ks > 1 && units > sms) break;
     const int64_t rounds = (units + sms - 1) / sms;
     const double cost = (double)rounds * ((G + ks - 1) / ks + (ks > 1 ? split_cost : 0.0));
     if (cost < best - 1e-9) {
@@ -1226,8 +1245,11 @@ static cudaError_t launch_tc(const GemmArgs& a, cudaStream_t st) {
   if (m_tiles > 65535 || n_tiles > 65535 || tiles >= (1LL << 31)) return cudaErrorInvalidValue;
   const int sms = tc_sm_count() * C::kCtasPerSm;  // CTA slots of one wave
   int ks = 1, persistent = 0;
-  // (wide tiles reduce 128 x BT partial sums through DSMEM: two groups' worth)
-  choose_split(tiles, G, sms, C::kWide ? 2.0 : 1.0, &ks, &persistent);
+  // (wide tiles reduce 128 x BT partial sums through DSMEM, about two groups'
+  // worth, and split only while every CTA of the split fits one wave: a
+  // second wave of split clusters measured slower than no split, e.g. the
+  // 3584 x 3584 linear at 512 tokens 53 us split four ways against 23 us)
+  choose_split(tiles, G, sms, C::kWide ? 2.0 : 1.0, C::kWide, &ks, &persistent);
   TcParams p{};
   p.M = a.M;
   p.N = a.N;
@@ -1337,5 +1359,8 @@ cudaError_t launch_tc_gemm(const GemmArgs& a, cudaStream_t st) {
 }
 
 cudaError_t take_error_word_tc_gemm(unsigned* out) { return take_local_error_word(out); }
+cudaError_t set_record_limit_tc_gemm(unsigned long long bytes) {
+  return set_local_record_limit(bytes);
+}
 
 }  // namespace egopq
