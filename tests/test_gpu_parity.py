@@ -685,3 +685,50 @@ def test_w4a8_linear_workspace_checks():
     assert lib.egopq_w4a8_linear(*args, ws.data_ptr(), need, eg.PATH_TC, s) == 0
     assert lib.egopq_w4a8_linear(*args, None, 0, eg.PATH_GEMV, s) == -1
     assert eg.device_status() == 0
+
+
+def _tie_rows(M, K, seed):
+    """bf16 rows whose quotients x / a_s sit on or within a few fp32 ulps of
+    half-integers (the cases the fused quantizer divides exactly), plus an
+    all-zero row and a plain random row."""
+    rng = np.random.default_rng(seed)
+    x = np.zeros((M, K), np.float32)
+    for m in range(M):
+        if m == 1:
+            continue                                   # an all-zero token
+        if m == 2:
+            x[m] = rng.standard_normal(K)
+            continue
+        # amax = 254 -> a_s = 2: integers k give k / 2, odd k exact ties
+        x[m] = rng.integers(-254, 255, size=K).astype(np.float32)
+        x[m, 0] = 254.0
+        # values one bf16 ulp off the ties (above 128 a bf16 ulp is 1.0, so
+        # take them below: 2*j + 1 +- 1/128 for small j)
+        j = rng.integers(0, 60, size=K // 8)
+        x[m, 1:K // 8 + 1] = 2.0 * j + 1.0 + rng.choice([-1.0, 1.0], size=K // 8) / 128.0
+    bits = x.view(np.uint32)
+    return ((bits + 0x7FFF + ((bits >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+@pytest.mark.parametrize("N", [384, 128 * 300])    # split-K clusters; one CTA per tile
+@pytest.mark.parametrize("M", [1, 4, 16])
+def test_fused_quant_gemv_ties_bit_identical(N, M):
+    """Rows full of exact and near half-integer quotients: the quantization
+    (round half to even of the fp32 quotient) matches the oracle bit for bit,
+    and the one-call linear on the GEMV path gives the bits of
+    egopq_quant_act_i8 followed by the GEMV, on split-K clusters and on grids
+    of one CTA per tile."""
+    K = 3584
+    x = _tie_rows(M, K, 30 + M)
+    w = synth.w4_weights(14, M, 0, N, K)
+    packed = eg.pack_w4(*dev_weights(w))
+    xd = to_dev(x, torch.bfloat16)
+    y1 = eg.w4a8_linear(xd, packed, N, path=eg.PATH_GEMV)
+    a = eg.quant_act(xd)
+    y2 = eg.w4a8_gemm(a, packed, N, K, path=eg.PATH_GEMV)
+    assert torch.equal(y1, y2)
+    a_q, a_s, _ = oracle.quant_act(x)
+    assert np.array_equal(a.a_q.cpu().numpy(), a_q)
+    cols = np.unique(np.concatenate([np.arange(128), np.arange(N - 128, N)]))
+    _, y_ref = oracle.w4a8(a_q, a_s, w.w_q[cols], w.scale_f16[cols], w.zero[cols])
+    check_bf16_output(to_host_bits(y1)[:, cols], y_ref, f"fused quant GEMV N={N} M={M}")
