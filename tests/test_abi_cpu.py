@@ -72,6 +72,19 @@ def test_auto_path_and_operand_queries(lib):
     assert lib.egopq_tc_operand_form(64) == eg.TC_FORM_E4M3_PLANES
     assert lib.egopq_tc_operand_form(65) == eg.TC_FORM_F16
     assert lib.egopq_tc_operand_form(0) == -1
+    # token tile of the tensor-core path: by M up to 64, then a wide tile
+    # (192 or 128 tokens, from the grid on the device's SMs) or 128
+    W4A8, W8A16, W8A8 = eg.VARIANT_W4A8, eg.VARIANT_W8A16, eg.VARIANT_W8A8
+    assert [lib.egopq_tc_token_tile(m, 3584, 3584, W4A8) for m in (1, 16, 17, 64)] == \
+        [16, 16, 32, 64]
+    assert lib.egopq_tc_token_tile(256, 256, 512, W4A8) == 128     # same tiles at either width
+    assert lib.egopq_tc_token_tile(4096, 152064, 3584, W4A8) == 192
+    assert lib.egopq_tc_token_tile(4096, 3584, 3584, W8A16) == 128
+    assert lib.egopq_tc_token_tile(64, 3584, 3584, W8A8) == -2      # GEMV only up to 64
+    assert lib.egopq_tc_token_tile(65, 3584, 3584, W8A8) == 128
+    assert lib.egopq_tc_token_tile(0, 3584, 3584, W4A8) == -1
+    assert lib.egopq_tc_token_tile(16, 3500, 3584, W4A8) == -2
+    assert lib.egopq_tc_token_tile(16, 3584, 3584, 9) == -1
 
 
 def test_sizes_beyond_the_limit_are_unsupported_shapes(lib):

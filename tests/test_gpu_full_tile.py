@@ -1,0 +1,125 @@
+"""GPU parity of the 192-token tensor-core tiles (the full-rate wide tile: two
+TMEM accumulators, one converter set, one issuer that waits for the drained
+accumulator itself) against the CPU oracle.
+
+The library picks 192 or 128 tokens per tile from the grid each makes on the
+device's SMs (egopq_tc_token_tile). The shapes below are built from the SM
+count so that the 192-token grid has fewer rounds and is chosen: a persistent
+grid of exactly one round with a ragged token tail, a persistent grid of two
+rounds (several tiles per CTA: the double-buffered epilogue staging), and a
+split-K grid (cluster reduction of 192 x 128 partial sums). Outputs are
+compared in full; group partials bit for bit, worst-case magnitudes included.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from helpers import check_bf16_output, to_dev, to_host_bits, w4_case
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover - collected on CPU, skipped there
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+import w4a8_quantized_gemm_gb300 as eg  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    eg.load()
+    torch.cuda.set_device(0)
+    yield
+    assert eg.device_status() == 0
+
+
+def _sms():
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
+def _shape(case):
+    """(M, N, K) whose 192-token grid needs fewer rounds than the 128-token one."""
+    sms = _sms()
+    if case == "one_round":      # 2 x sms/2 tiles of 192 (1 round) against 3 x sms/2 of 128
+        return 300, 128 * (sms // 2), 512
+    if case == "two_rounds":     # 6 m-tiles of 192 (last: 40 tokens) against 8 of 128
+        return 1000, 128 * (sms // 3), 1024
+    if case == "split_k":        # 2 m-tiles of 192 small enough to split K in two
+        return 384, 128 * (sms * 2 // 9), 1024
+    raise ValueError(case)
+
+
+def _dev_weights(w):
+    return (to_dev(w.w_q), to_dev(w.scale_f16, torch.float16), to_dev(w.zero))
+
+
+@pytest.mark.parametrize("case", ["one_round", "two_rounds", "split_k"])
+def test_w4a8_full_tile_output(case):
+    M, N, K = _shape(case)
+    assert eg.tc_token_tile(M, N, K) == 192, (case, M, N, K)
+    x, w = w4_case(11, M, N, K)
+    packed = eg.pack_w4(*_dev_weights(w))
+    a = eg.quant_act(to_dev(x, torch.bfloat16))
+    y = eg.w4a8_gemm(a, packed, N, K, path=eg.PATH_TC)
+    a_q, a_s, _ = oracle.quant_act(x)
+    _, y_ref = oracle.w4a8(a_q, a_s, w.w_q, w.scale_f16, w.zero)
+    check_bf16_output(to_host_bits(y), y_ref, f"192-token tiles {case} M={M} N={N} K={K}")
+
+
+@pytest.mark.parametrize("case", ["one_round", "split_k"])
+def test_w4a8_full_tile_group_partials(case):
+    M, N, K = _shape(case)
+    x, w = w4_case(12, M, N, K)
+    packed = eg.pack_w4(*_dev_weights(w))
+    a = eg.quant_act(to_dev(x, torch.bfloat16))
+    Q = eg.w4a8_group_partials(a, packed, N, K, path=eg.PATH_TC).cpu().numpy()
+    a_q, _, _ = oracle.quant_act(x)
+    rows = np.array([0, 1, 190, 191, 192, 193, M - 1])
+    assert np.array_equal(Q[rows], oracle.group_partials(a_q[rows], w.w_q, w.zero))
+
+
+@pytest.mark.parametrize("case", ["max_pos", "alternating"])
+def test_w4a8_full_tile_worst_case_magnitudes(case):
+    """|Q| = 128 * 127 * 15 = 243840 in 192-token tiles: still exact in fp32."""
+    M, N, K = _shape("one_round")
+    G = K // 128
+    x = np.full((M, K), 0x3F80, np.uint16)                     # 1.0 -> a_q = 127
+    w_q = np.full((N, K), 15, np.uint8)
+    z = np.zeros((N, G), np.uint8)
+    if case == "alternating":
+        x[:, 1::2] = 0xBF80                                    # -1.0 -> a_q = -127
+        w_q[:, 1::2] = 0
+        w_q[::2, :] = 15 - w_q[::2, :]
+        z[:, :] = np.arange(N)[:, None] % 16
+    s = np.full((N, G), 0x3C00, np.uint16)
+    w = synth.W4Weights(w_q, s, z, 128)
+    packed = eg.pack_w4(*_dev_weights(w))
+    a = eg.quant_act(to_dev(x, torch.bfloat16))
+    Q = eg.w4a8_group_partials(a, packed, N, K, path=eg.PATH_TC).cpu().numpy()
+    a_q, _, _ = oracle.quant_act(x)
+    rows = np.array([0, 191, 192, M - 1])
+    ref = oracle.group_partials(a_q[rows], w_q, z)
+    if case == "max_pos":
+        assert ref.max() == 243840
+    assert np.array_equal(Q[rows], ref)
+
+
+def test_w4a16_full_tile_output():
+    M, N, K = _shape("one_round")
+    assert eg.tc_token_tile(M, N, K, eg.VARIANT_W4A16) == 192
+    x = synth.activations(13, 0, 0, M, K, outliers=False)
+    w = synth.w4_weights(13, 0, 0, N, K)
+    y = eg.w4a16_gemm(to_dev(x, torch.bfloat16), eg.pack_w4(*_dev_weights(w)), N, K,
+                      path=eg.PATH_TC)
+    _, y_ref = oracle.w4a16(x, w.w_q, w.scale_f16, w.zero)
+    check_bf16_output(to_host_bits(y), y_ref, "W4A16 192-token tiles")
+
+
+def test_token_tile_choice():
+    """Decode-sized tiles by M; 128 where 192 gains no round; W8A16 always 128."""
+    assert [eg.tc_token_tile(m, 3584, 3584) for m in (5, 16, 17, 32, 33, 64)] == \
+        [16, 16, 32, 32, 64, 64]
+    assert eg.tc_token_tile(256, 256, 512) == 128        # 2 m-tiles at either width
+    assert eg.tc_token_tile(4096, 152064, 3584) == 192   # the untied head at 4096 tokens
+    assert eg.tc_token_tile(4096, 3584, 3584, eg.VARIANT_W8A16) == 128

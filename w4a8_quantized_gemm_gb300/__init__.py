@@ -88,6 +88,7 @@ def load() -> ctypes.CDLL:
             "egopq_auto_path": (i32, [i64, i32]),
             "egopq_tc_operand_bytes": (sz, [i64, i64, i32]),
             "egopq_tc_operand_form": (i32, [i64]),
+            "egopq_tc_token_tile": (i32, [i64, i64, i64, i32]),
             "egopq_device_status": (i32, [vp]),
             "egopq_selftest_timeout": (i32, [i32, vp]),
             "egopq_debug_build": (i32, []),
@@ -207,6 +208,15 @@ def auto_path(M: int, variant: int = VARIANT_W4A8) -> int:
     """The path (PATH_GEMV or PATH_TC) the library's AUTO choice takes for M
     tokens of `variant`."""
     rc = int(load().egopq_auto_path(M, variant))
+    if rc < 0:
+        _check(rc)
+    return rc
+
+
+def tc_token_tile(M: int, N: int, K: int, variant: int = VARIANT_W4A8) -> int:
+    """Tokens per output tile (the MMA's N) the tensor-core path runs an
+    M x N x K call of `variant` with on the current device."""
+    rc = int(load().egopq_tc_token_tile(M, N, K, variant))
     if rc < 0:
         _check(rc)
     return rc

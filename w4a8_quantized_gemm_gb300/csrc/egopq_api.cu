@@ -568,6 +568,18 @@ int egopq_auto_path(int64_t M, int variant) {
   return auto_path(M, variant, EGOPQ_PATH_AUTO);
 }
 
+int egopq_tc_token_tile(int64_t M, int64_t N, int64_t K, int variant) {
+  if (variant < EGOPQ_VARIANT_W4A8 || variant > EGOPQ_VARIANT_W8A8 || M <= 0)
+    return fail(EGOPQ_ERR_INVALID_ARG, "bad variant %d or M %lld", variant, (long long)M);
+  if (N <= 0 || K <= 0 || N % 128 || K % 128 || M >= kMaxDim || N >= kMaxDim || K >= kMaxDim)
+    return fail(EGOPQ_ERR_UNSUPPORTED_SHAPE, "shape %lld x %lld x %lld", (long long)M,
+                (long long)N, (long long)K);
+  if (variant == EGOPQ_VARIANT_W8A8 && M <= kTcFp8MaxM)
+    return fail(EGOPQ_ERR_UNSUPPORTED_SHAPE, "W8A8 has no tensor-core form for M <= %d",
+                kTcFp8MaxM);
+  return tc_token_tile(variant, M, N, K);
+}
+
 size_t egopq_tc_operand_bytes(int64_t M, int64_t K, int group) {
   if (M <= 0 || K <= 0 || M >= kMaxDim || K >= kMaxDim || group != 128 || K % 128) return 0;
   return (size_t)(2 * M * K);

@@ -171,6 +171,10 @@ __host__ __device__ inline uint64_t packed_record_bytes(int64_t N, int G) {
 cudaError_t launch_gemv(const GemmArgs& a, cudaStream_t st);
 // tcgen05 tensor-core GEMM (any M).
 cudaError_t launch_tc_gemm(const GemmArgs& a, cudaStream_t st);
+// Token tile (MMA N) the tensor-core GEMM runs an M x N x K call of `variant`
+// with: 16, 32 or 64 up to 64 tokens; above, 128 or 192 (per-group variants,
+// chosen from the grid each makes) or 128.
+int tc_token_tile(int variant, int64_t M, int64_t N, int64_t K);
 // Bounded-wait self test.
 cudaError_t launch_selftest_timeout(uint64_t timeout_ns, cudaStream_t st);
 

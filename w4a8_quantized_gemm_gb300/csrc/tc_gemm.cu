@@ -65,6 +65,8 @@
 // groups (exact: 1024 * 127^2 < 2^24), adds the partials as int32 and scales
 // by a_s[m] * s[n] at the end.
 
+#include <type_traits>
+
 #include "egopq_internal.h"
 
 namespace egopq {
@@ -72,12 +74,21 @@ namespace egopq {
 constexpr int kMaxSmem = 232448;      // dynamic shared memory of a CTA alone on its SM
 constexpr int kMaxSmemHalf = 114688;  // each of two CTAs sharing an SM
 
-// Wide tiles: the token tile of the per-group (W4A8 fp16, W4A16) tensor-core
-// path above kTcFp8MaxM tokens, and its TMEM split -- kWideNumD accumulators
-// of kWideBT columns and kWideNumA A-operand buffers of 64 columns -- and MMA
-// issuer count.
+// Wide tiles: the token tiles of the per-group (W4A8 fp16, W4A16) tensor-core
+// path above kTcFp8MaxM tokens. With A in TMEM an MMA of N tokens costs
+// max(~95, N/2) cycles per K = 16 step (measured on GB300: a 128-wide group
+// takes 757 cycles at N = 128..176 and 4*N from N = 192 up, also with a CTA
+// pair), so the tensor pipe reaches its full rate only from 192 tokens a tile.
+//  - kWideBT (128 tokens): three 128-column accumulators and two 64-column A
+//    buffers, two converter sets, two issuers;
+//  - kFullBT (192 tokens): two 192-column accumulators and two A buffers fill
+//    the 512 TMEM columns, so the drain of group i gates the MMAs of group
+//    i + 2; one converter set, one issuer, which waits for the drained
+//    accumulator itself (one hand-off fewer on that chain).
+// The launcher picks the width per linear from the grid it makes (192-token
+// tiles quantise some grids into a short last wave).
 constexpr int kWideBT = 128;
-constexpr int kWideNumD = 3, kWideNumA = 2, kWideIssuers = 2;
+constexpr int kFullBT = 192;
 
 // Output tensor maps of the linears (wide tiles' bulk-store epilogue): bf16
 // y_j as 2-D {N_j, M}, box {128, drain columns}.
@@ -140,17 +151,30 @@ struct TcCfg {
   static constexpr int kDrainWGs = kLean ? 1 : 2;
   static constexpr int kConvWarp0 = 4 * kDrainWGs;  // drain warps first
   static constexpr bool kWide = BT > 64 && kDrainPerGroup;
+  static constexpr bool kFull = kWide && BT == kFullBT;  // full-rate tile (see kFullBT)
   static constexpr int kMmaWarps =
-      kLean ? 1 : (kWide ? kWideIssuers : ((kDrainPerGroup && BT <= 32) ? 2 : 1));
+      kLean ? 1 : (kWide ? (kFull ? 1 : 2) : ((kDrainPerGroup && BT <= 32) ? 2 : 1));
+  // the issuer, not the converters, waits for the drained accumulator
+  static constexpr bool kIssuerWaitsD = false;
+  // 192-token tiles hand each group from the converters to the issuer on a
+  // hardware named barrier (one per A buffer), and the converters' first warp
+  // waits for the drained accumulator and the landed activations before its
+  // arrival. The issuer then performs no mbarrier operation at all: an
+  // mbarrier test queues behind the MMAs the issuing warp has just issued
+  // (they wait for the tensor pipe in the same memory-instruction queue), so
+  // a test between groups idled the pipe for ~400 cycles a group.
+  static constexpr bool kNamedHandoff = kFull;
+  static constexpr int kHandoffBar0 = 6;  // named barriers 6, 7 (A buffers 0, 1)
+  static constexpr int kHandoffCount = 32 * 4 + 32;  // converter set + issuer warp
   // TMEM: kNumD accumulators of kDCols columns + kNumA A-operand buffers of
   // kACols columns (deep for small tiles: the converters run ahead of the
   // MMAs and the MMAs ahead of the drain).
-  // (wide per-group tiles: kWideNumD accumulators and kWideNumA A buffers --
-  // with two 128-column accumulators the MMAs of a group wait for the drain
-  // two back)
+  // (wide per-group tiles: three accumulators at 128 tokens -- with two the
+  // MMAs of a group wait for the drain two back -- and two at 192, which is
+  // all TMEM holds; two A buffers)
   static constexpr int kNumD =
-      kLean ? 4 : (kWide ? kWideNumD : (kFp8 ? (BT == 32 ? 4 : 2) : (BT <= 64 ? 4 : 2)));
-  static constexpr int kNumA = kLean ? 4 : (kWide ? kWideNumA : (kFp8 ? 8 : 4));
+      kLean ? 4 : (kWide ? (kFull ? 2 : 3) : (kFp8 ? (BT == 32 ? 4 : 2) : (BT <= 64 ? 4 : 2)));
+  static constexpr int kNumA = kLean ? 4 : (kWide ? 2 : (kFp8 ? 8 : 4));
   static constexpr int kActBox = BT * 128;                        // one 64-wide K box, bytes
   static constexpr int kActBytes = 2 * kActBox;                   // a 128-wide group
   // weights of one group: the int8 tile, or one packed int4 record (8192 B of
@@ -158,8 +182,15 @@ struct TcCfg {
   // 1024-byte aligned
   static constexpr int kWCopyBytes = kW16 ? 32768 : (kW8 ? 16384 : 8512);
   static constexpr int kWBytes = kW16 ? 32768 : (kW8 ? 16384 : 9216);
-  static constexpr int kStageBytes = kActBytes + kWBytes;        // multiple of 1024
-  static constexpr int kTxBytes = kActBytes + kWCopyBytes;
+  // 192-token tiles keep the weight records in a ring of their own: a
+  // record's slot is free as soon as the converters have read it, while an
+  // activation stage is held until its MMAs complete. (With one ring, only
+  // three 57 KB stages fit, and each stage stayed held from its record's HBM
+  // load through conversion, hand-offs and MMAs: ~5000 cycles, one group per
+  // ~1700.) Each ring has its own producer thread.
+  static constexpr bool kSplitRings = kFull && !kTmaW;
+  static constexpr int kStageBytes = kSplitRings ? kActBytes : kActBytes + kWBytes;  // x 1024
+  static constexpr int kTxBytes = kSplitRings ? kActBytes : kActBytes + kWCopyBytes;
   static constexpr int kSmemLimit = kCtasPerSm == 1 ? kMaxSmem : kMaxSmemHalf;
   // Wide tiles stage each finished tile in shared memory (bf16 [BT][128]) and
   // write it with TMA bulk stores, one per drain warpgroup, so that the drain
@@ -168,12 +199,17 @@ struct TcCfg {
   static constexpr bool kTmaEpi = kWide;
   static constexpr int kEpiBytes = kTmaEpi ? BT * 128 * 2 : 0;
   static constexpr int kAsBytes = (kTmaEpi && kCodes) ? 2 * BT * 4 : 0;
-  static constexpr int kStagesRaw = (kSmemLimit - 3072 - kEpiBytes - kAsBytes) / kStageBytes;
+  // record ring (split rings): kRecStages slots of one 8512-byte record
+  static constexpr int kRecStages = kSplitRings ? 3 : 0;
+  static constexpr int kRecBytes = (kRecStages * 8512 + 1023) / 1024 * 1024;
+  static constexpr int kStagesRaw =
+      (kSmemLimit - 3072 - kEpiBytes - kAsBytes - kRecBytes) / kStageBytes;
   // deep rings for small token tiles (decode streams weights: bytes in flight
   // hide HBM latency); larger tiles are bounded by shared memory
   static constexpr int kStageCap = BT <= 32 ? 16 : 8;
   static constexpr int kStages = kStagesRaw > kStageCap ? kStageCap : kStagesRaw;
-  static constexpr int kEpiOffset = kStages * kStageBytes;  // 1024-byte aligned
+  static constexpr int kRecOffset = kStages * kStageBytes;  // 1024-byte aligned
+  static constexpr int kEpiOffset = kRecOffset + kRecBytes;
   static constexpr int kAsOffset = kEpiOffset + kEpiBytes;
   static constexpr int kBarOffset = kAsOffset + kAsBytes;
   static constexpr int kSmemBytes = kBarOffset + 1024 + 1024;    // + barriers + alignment slack
@@ -186,7 +222,7 @@ struct TcCfg {
   // Converter warp sets: with small token tiles the MMA and drain per group are
   // short, so a second set of four converter warps takes every other group
   // (each set's store-to-arrive latency overlaps the other's conversion).
-  static constexpr int kConvSets = kLean ? 1 : ((BT <= 32 || kWide) ? 2 : 1);
+  static constexpr int kConvSets = kLean ? 1 : ((BT <= 32 || (kWide && !kFull)) ? 2 : 1);
   static constexpr int kDrainCols = BT / kDrainWGs;  // token columns per drain thread
   static constexpr int kProducerWarp = kConvWarp0 + 4 * kConvSets;
   static constexpr int kMmaWarp = kProducerWarp + 1;  // first issuer; allocates TMEM
@@ -201,8 +237,15 @@ struct TcCfg {
   static constexpr bool kRegSplit = kWide;
   static constexpr int kWarpsUsed = kMmaWarp + kMmaWarps;
   static constexpr int kWarps = kRegSplit ? (kWarpsUsed + 3) / 4 * 4 : kWarpsUsed;
+  // split rings: the first padding warp loads the activations, the producer
+  // warp the weight records
+  static constexpr int kActWarp = kSplitRings ? kWarpsUsed : -1;
+  static_assert(!kSplitRings || kWarps > kWarpsUsed, "activation producer warp");
   static constexpr int kThreads = 32 * kWarps;
-  static constexpr int kRegDrain = 120, kRegConv = 96, kRegOther = 48;
+  // (192-token tiles: four warpgroups of 128 registers at launch; the drains
+  // hold 96 running sums and 48 TMEM columns in flight)
+  static constexpr int kRegDrain = kFull ? 168 : 120, kRegConv = kFull ? 120 : 96,
+                       kRegOther = kFull ? 56 : 48;
   // (converters keep a whole converted group, 64 registers, in flight)
   static_assert(!kRegSplit || kRegConv >= 96, "converter registers");
   // registers every thread has at launch (ptxas holds a kernel that uses
@@ -220,8 +263,9 @@ struct TcCfg {
   // i - kNumA - kNumD done, drains run in order) covers i - 2*kNumD.
   static_assert(kNumA % kConvSets == 0 && (kNumD % kConvSets == 0 || kNumA <= kNumD),
                 "buffer reuse waits");
-  static_assert(8 * (2 * kStages + 2 * kNumA + 2 * kNumD + kMmaWarps) + 8 <= 1024, "barrier region");
-  static_assert(BT % 16 == 0 && BT >= 16 && BT <= 128, "token tile");
+  static_assert(8 * (2 * kStages + 2 * kNumA + 2 * kNumD + kMmaWarps + 2 * kRecStages) + 8 <= 1024,
+                "barrier region");
+  static_assert(BT % 16 == 0 && BT >= 16 && (BT <= 128 || kFull), "token tile");
   // the split hands out exactly the registers the block was launched with
   static_assert(!kRegSplit || (kWarps / 4 == kDrainWGs + kConvSets + 1 &&
                                kDrainWGs * kRegDrain + kConvSets * kRegConv + kRegOther <=
@@ -386,11 +430,22 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
   auto dempty_bar = [&](int i) { return bar0 + 8u * (2 * S + 2 * kNumA + kNumD + i); };
   // one per issuer: its final commit, waited on before teardown
   auto fin_bar = [&](int i) { return bar0 + 8u * (2 * S + 2 * kNumA + 2 * kNumD + i); };
-  uint8_t* misc = smem + C::kBarOffset + 8 * (2 * S + 2 * kNumA + 2 * kNumD + C::kMmaWarps);
+  // split rings: record slot r landed / read by the converters
+  // (R is 1 without split rings, where nothing uses it: a divisor everywhere)
+  constexpr int R = C::kRecStages > 0 ? C::kRecStages : 1;
+  constexpr int kRecBar0 = 2 * S + 2 * kNumA + 2 * kNumD + C::kMmaWarps;
+  auto wfull_bar = [&](int r) { return bar0 + 8u * (kRecBar0 + r); };
+  auto wempty_bar = [&](int r) { return bar0 + 8u * (kRecBar0 + R + r); };
+  uint8_t* misc = smem + C::kBarOffset + 8 * (kRecBar0 + 2 * C::kRecStages);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 4);
   auto stage_act = [&](int s) { return base + (uint32_t)(s * C::kStageBytes); };
   auto stage_w_ptr = [&](int s) { return smem + s * C::kStageBytes + C::kActBytes; };
+  // the weight record of item i: its record-ring slot, or its stage
+  auto rec_ptr = [&](int i) {
+    if constexpr (C::kSplitRings) return smem + C::kRecOffset + (i % R) * 8512;
+    else return stage_w_ptr(i % S);
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -398,7 +453,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
       // released by the MMA commit and the 4 converter warps (and, in the
       // e4m3 form, the 8 drain warps, which read the record's scales and
       // zero points from the stage)
-      mbar_init(empty_bar(s), 1 + 4 + (C::kFp8 ? 4 * C::kDrainWGs : 0));
+      mbar_init(empty_bar(s), 1 + (C::kSplitRings ? 0 : 4) + (C::kFp8 ? 4 * C::kDrainWGs : 0));
+    }
+    for (int r = 0; r < C::kRecStages; ++r) {
+      mbar_init(wfull_bar(r), 1);
+      mbar_init(wempty_bar(r), 4);
     }
     for (int i = 0; i < kNumA; ++i) {
       mbar_init(afull_bar(i), 4);
@@ -412,7 +471,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == C::kProducerWarp && lane == 0) {
+  if ((warp == C::kProducerWarp || warp == C::kActWarp) && lane == 0) {
     prefetch_tensormap(&act_map);
     if constexpr (C::kTmaW) prefetch_tensormap(&w8_map);
   }
@@ -437,7 +496,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
     asm volatile("bar.sync 1, %0;" ::"n"(C::kThreads) : "memory");
   };
 
-  auto producer_role = [&]() {
+  // kRecords / kActs: which copies this producer thread issues (both with one
+  // ring; with split rings the producer warp the records, kActWarp the
+  // activations)
+  auto producer_role = [&](auto records_tag, auto acts_tag) {
+    constexpr bool kRecords = decltype(records_tag)::value;
+    constexpr bool kActs = decltype(acts_tag)::value;
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       // item i = (unit i / ng, group g0 + i % ng), walked with counters
@@ -454,22 +518,30 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
           if (++k < n_units) unit_tile(k, mt, nt);
         }
       };
-      auto load_weights = [&](int s) {
+      // weights of the next item into shared address dst, completing on bar
+      auto load_weights_to = [&](uint32_t dst, uint32_t bar) {
         const int nt = w_nt, g = g0 + w_gi;
         advance(w_k, w_gi, w_mt, w_nt);
+        const TileRef tr = tile_ref(p.seg, nt, G);
+        const uint8_t* src = tr.rec0 + (int64_t)g * 8512;
+        if (!dbg_record_ok((uint64_t)(src - p.seg.packed[tr.seg]), 8512,
+                           packed_record_bytes(tr.N, G)))
+          src = p.seg.packed[tr.seg];
+        bulk_load(dst, src, 8512, bar);
+      };
+      auto load_weights = [&](int s) {
         if constexpr (C::kW16) {
+          const int nt = w_nt, g = g0 + w_gi;
+          advance(w_k, w_gi, w_mt, w_nt);
           tma_load_2d(stage_act(s) + C::kActBytes, &w8_map, full_bar(s), g * 128, nt * 128);
           tma_load_2d(stage_act(s) + C::kActBytes + 16384, &w8_map, full_bar(s), g * 128 + 64,
                       nt * 128);
         } else if constexpr (C::kW8) {
+          const int nt = w_nt, g = g0 + w_gi;
+          advance(w_k, w_gi, w_mt, w_nt);
           tma_load_2d(stage_act(s) + C::kActBytes, &w8_map, full_bar(s), g * 128, nt * 128);
         } else {
-          const TileRef tr = tile_ref(p.seg, nt, G);
-          const uint8_t* src = tr.rec0 + (int64_t)g * 8512;
-          if (!dbg_record_ok((uint64_t)(src - p.seg.packed[tr.seg]), 8512,
-                             packed_record_bytes(tr.N, G)))
-            src = p.seg.packed[tr.seg];
-          bulk_load(stage_act(s) + C::kActBytes, src, 8512, full_bar(s));
+          load_weights_to(stage_act(s) + C::kActBytes, full_bar(s));
         }
       };
       auto load_act = [&](int s) {
@@ -485,29 +557,63 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
           tma_load_2d(stage_act(s) + C::kActBox, &act_map, full_bar(s), g * 128 + 64, mt * BT);
         }
       };
-      // weights do not depend on the preceding grid: start streaming them
-      // before waiting for it; activations only after
-      const int n_pre = n_items < S ? n_items : S;
-      for (int i = 0; i < n_pre; ++i) {
-        mbar_arrive_expect_tx(full_bar(i), C::kTxBytes);
-        load_weights(i);
-      }
-      griddep_wait();
-      griddep_launch_dependents();
-      for (int i = 0; i < n_pre; ++i) load_act(i);
-      int issued = n_pre;
-      for (int i = n_pre; i < n_items; ++i) {
-        const int s = i % S;
-        if (!mbar_wait(empty_bar(s), ((i / S) & 1) ^ 1, abort_flag, tmo)) break;
-        mbar_arrive_expect_tx(full_bar(s), C::kTxBytes);
-        load_weights(s);
-        load_act(s);
-        ++issued;
-      }
-      // wait (bounded) for every copy this thread issued to land before exit
-      for (int i = (issued > S ? issued - S : 0); i < issued; ++i) {
-        volatile int no_abort = 0;
-        mbar_wait(full_bar(i % S), (i / S) & 1, &no_abort, tmo);
+      if constexpr (kRecords && !kActs) {
+        // record ring: slot i % R is refilled once the converters of item
+        // i - R have read it (weights do not depend on the preceding grid)
+        int issued = 0;
+        for (int i = 0; i < n_items; ++i) {
+          const int r = i % R;
+          if (i >= R && !mbar_wait(wempty_bar(r), ((i / R) & 1) ^ 1, abort_flag, tmo)) break;
+          mbar_arrive_expect_tx(wfull_bar(r), 8512);
+          load_weights_to(base + C::kRecOffset + (uint32_t)(r * 8512), wfull_bar(r));
+          ++issued;
+        }
+        for (int i = (issued > R ? issued - R : 0); i < issued; ++i) {
+          volatile int no_abort = 0;
+          mbar_wait(wfull_bar(i % R), (i / R) & 1, &no_abort, tmo);
+        }
+      } else if constexpr (kActs && !kRecords) {
+        // activation ring: stage i % S is refilled once the MMAs of item
+        // i - S have completed
+        griddep_wait();
+        griddep_launch_dependents();
+        int issued = 0;
+        for (int i = 0; i < n_items; ++i) {
+          const int s = i % S;
+          if (i >= S && !mbar_wait(empty_bar(s), ((i / S) & 1) ^ 1, abort_flag, tmo)) break;
+          mbar_arrive_expect_tx(full_bar(s), C::kTxBytes);
+          load_act(s);
+          ++issued;
+        }
+        for (int i = (issued > S ? issued - S : 0); i < issued; ++i) {
+          volatile int no_abort = 0;
+          mbar_wait(full_bar(i % S), (i / S) & 1, &no_abort, tmo);
+        }
+      } else {
+        // weights do not depend on the preceding grid: start streaming them
+        // before waiting for it; activations only after
+        const int n_pre = n_items < S ? n_items : S;
+        for (int i = 0; i < n_pre; ++i) {
+          mbar_arrive_expect_tx(full_bar(i), C::kTxBytes);
+          load_weights(i);
+        }
+        griddep_wait();
+        griddep_launch_dependents();
+        for (int i = 0; i < n_pre; ++i) load_act(i);
+        int issued = n_pre;
+        for (int i = n_pre; i < n_items; ++i) {
+          const int s = i % S;
+          if (!mbar_wait(empty_bar(s), ((i / S) & 1) ^ 1, abort_flag, tmo)) break;
+          mbar_arrive_expect_tx(full_bar(s), C::kTxBytes);
+          load_weights(s);
+          load_act(s);
+          ++issued;
+        }
+        // wait (bounded) for every copy this thread issued to land before exit
+        for (int i = (issued > S ? issued - S : 0); i < issued; ++i) {
+          volatile int no_abort = 0;
+          mbar_wait(full_bar(i % S), (i / S) & 1, &no_abort, tmo);
+        }
       }
     }
     __syncwarp();
@@ -534,8 +640,15 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
     auto wait_group = [&](int i) -> bool {
       const int ab = i % kNumA;
       // one wait per group: the converters arrive on afull only once the
-      // stage has landed, the A buffer is free and the accumulator drained
-      return mbar_wait(afull_bar(ab), (i / kNumA) & 1, abort_flag, tmo);
+      // stage has landed, the A buffer is free and (unless the issuer waits
+      // for it itself) the accumulator drained
+      if (!mbar_wait(afull_bar(ab), (i / kNumA) & 1, abort_flag, tmo)) return false;
+      if constexpr (C::kIssuerWaitsD) {
+        // (per-group tiles: every group starts its accumulator)
+        const int di = drain_of(i);
+        return mbar_wait(dempty_bar(di % kNumD), ((di / kNumD) & 1) ^ 1, abort_flag, tmo);
+      }
+      return true;
     };
     // (lane 0) group i's MMAs and the commits that release its buffers
     auto issue_group = [&](int i) {
@@ -569,7 +682,21 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
       if (d_last) tc_commit(dfull_bar(db));
     };
     bool any = false;
-    if (lane == 0) {
+    if constexpr (C::kNamedHandoff) {
+      // the whole warp meets the converters on each group's named barrier
+      // (every group, also after an abort: see the converters); lane 0
+      // issues unless a wait somewhere in the CTA gave up
+      static_assert(kNumA == 2 && C::kMmaWarps == 1, "named hand-off layout");
+      for (int i = q; i < n_items; i += C::kMmaWarps) {
+        asm volatile("bar.sync %0, %1;" ::"r"(C::kHandoffBar0 + i % kNumA), "n"(C::kHandoffCount)
+                     : "memory");
+        if (!__shfl_sync(0xffffffffu, *abort_flag != 0 ? 1 : 0, 0)) {
+          if (lane == 0) issue_group(i);
+          any = true;
+        }
+        __syncwarp();
+      }
+    } else if (lane == 0) {
       for (int i = q; i < n_items; i += C::kMmaWarps) {
         if (!wait_group(i)) break;
         issue_group(i);
@@ -597,9 +724,14 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
     const int r = ((warp - kConvWarp0) & 3) * 32 + lane;  // weight row == TMEM lane
     const int set = (warp - kConvWarp0) >> 2;             // this set converts items set, +sets..
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    for (int i = set; i < n_items; i += C::kConvSets) {
+    // item i: stage its weights as the A operand (false once a wait gave up)
+    auto convert_item = [&](int i) -> bool {
       const int s = i % S, ab = i % kNumA;
-      if (!mbar_wait(full_bar(s), (i / S) & 1, abort_flag, tmo)) break;
+      if constexpr (C::kSplitRings) {
+        if (!mbar_wait(wfull_bar(i % R), (i / R) & 1, abort_flag, tmo)) return false;
+      } else {
+        if (!mbar_wait(full_bar(s), (i / S) & 1, abort_flag, tmo)) return false;
+      }
       uint32_t out[64];
       if constexpr (C::kFp8) {
         const uint8_t* wt = stage_w_ptr(s) + r * 16;
@@ -674,13 +806,14 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
           }
         }
       } else {
-        const uint8_t* wt = stage_w_ptr(s) + r * 16;
+        const uint8_t* rec = rec_ptr(i);
+        const uint8_t* wt = rec + r * 16;
         uint4 v[4];
 #pragma unroll
         for (int c = 0; c < 4; ++c) v[c] = *reinterpret_cast<const uint4*>(wt + c * 2048);
-        const uint8_t zb = stage_w_ptr(s)[8448 + (r >> 1)];
+        const uint8_t zb = rec[8448 + (r >> 1)];
         __syncwarp();
-        if (lane == 0) mbar_arrive(empty_bar(s));
+        if (lane == 0) mbar_arrive(C::kSplitRings ? wempty_bar(i % R) : empty_bar(s));
         const uint32_t z = (r & 1) ? (zb >> 4) : (zb & 0xF);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -691,7 +824,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
         }
       }
       // A buffer ab is free once the MMAs of item i - kNumA have completed
-      if (!mbar_wait(aempty_bar(ab), ((i / kNumA) & 1) ^ 1, abort_flag, tmo)) break;
+      if (!mbar_wait(aempty_bar(ab), ((i / kNumA) & 1) ^ 1, abort_flag, tmo)) return false;
       tc_fence_after();
       const uint32_t dst = a_tmem + lane_base + ab * C::kACols;
 #pragma unroll
@@ -706,13 +839,43 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
       // MMAs are released (the A operand is stored first: only the MMAs, not
       // the stores, wait for the drain); one warp of the set waits (afull
       // completes only with all four arrivals)
-      if (((warp - kConvWarp0) & 3) == 0) {
+      if (!C::kIssuerWaitsD && ((warp - kConvWarp0) & 3) == 0) {
         const int di = drain_of(i);
-        if (!mbar_wait(dempty_bar(di % kNumD), ((di / kNumD) & 1) ^ 1, abort_flag, tmo)) break;
+        if (!mbar_wait(dempty_bar(di % kNumD), ((di / kNumD) & 1) ^ 1, abort_flag, tmo)) return false;
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(afull_bar(ab));
+      // split rings: the activation stage the MMAs read has landed (one warp
+      // of the set waits; afull completes only with all four arrivals)
+      if (C::kSplitRings && ((warp - kConvWarp0) & 3) == 0) {
+        if (!mbar_wait(full_bar(s), (i / S) & 1, abort_flag, tmo)) return false;
+      }
+      return true;
+    };
+    if constexpr (C::kNamedHandoff) {
+      // rendezvous with the issuer on group i's named barrier, for every
+      // group, also after a failed wait (the work is skipped then): both
+      // sides always make exactly n_items rendezvous, so neither can wait
+      // for ever, and no barrier phase can collect a second arrival early
+      static_assert(C::kConvSets == 1, "named hand-off layout");
+      // (bar.sync is the .aligned form: each warp reaches it converged, and
+      // `ok` is kept warp-uniform)
+      bool ok = true;
+      for (int i = 0; i < n_items; ++i) {
+        if (ok) ok = convert_item(i);
+        ok = __all_sync(0xffffffffu, ok);
+        tc_fence_before();
+        __syncwarp();
+        asm volatile("bar.sync %0, %1;" ::"r"(C::kHandoffBar0 + i % kNumA), "n"(C::kHandoffCount)
+                     : "memory");
+      }
+    } else {
+      for (int i = set; i < n_items; i += C::kConvSets) {
+        if (!convert_item(i)) break;
+        // hand group i to its issuer (A stored, accumulator drained,
+        // activations landed)
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(afull_bar(i % kNumA));
+      }
     }
     __syncwarp();
     teardown_sync();
@@ -912,8 +1075,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
         static_assert(HB % CW == 0, "drain columns");
         constexpr int NCH = HB / CW;  // loads per drain
         // loads in flight per wait (32 columns at most with the register
-        // split, two loads without it)
-        constexpr int PAIR = C::kRegSplit ? (NCH < 32 / CW ? NCH : 32 / CW) : (NCH >= 2 ? 2 : 1);
+        // split -- 48 in the 192-token tiles -- two loads without it)
+        constexpr int kInFlight = C::kFull ? 48 : 32;
+        constexpr int PAIR =
+            C::kRegSplit ? (NCH < kInFlight / CW ? NCH : kInFlight / CW) : (NCH >= 2 ? 2 : 1);
+        static_assert(NCH % PAIR == 0, "drain batches");
 #pragma unroll
         for (int cb = 0; cb < NCH; cb += PAIR) {
           uint32_t v[PAIR][16];
@@ -925,6 +1091,13 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
             else tmem_ld8(src, v[q2]);
           }
           tmem_wait_ld();
+          if (cb + PAIR >= NCH) {
+            // the whole accumulator is in registers: release it before the
+            // last batch's arithmetic (the MMAs two groups on wait for it)
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(dempty_bar(db));
+          }
 #pragma unroll
           for (int q2 = 0; q2 < PAIR; ++q2) {
             if (cb + q2 >= NCH) break;
@@ -951,10 +1124,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
             }
           }
         }
-        }  // kind::f16 drain
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(dempty_bar(db));
+        }  // kind::f16 drain (released the accumulator after its last load)
+        if constexpr (C::kFp8) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(dempty_bar(db));
+        }
       }
       if (!ok) break;
       if constexpr (VARIANT == kW8A16) {
@@ -1057,9 +1232,16 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
     const int wg = warp >> 2;
     if (wg >= C::kDrainWGs + C::kConvSets) {
       setmaxnreg_dec<C::kRegOther>();
-      if (warp == C::kProducerWarp) producer_role();
-      else if (warp >= C::kWarpsUsed) pad_role();
-      else mma_role();
+      if (warp == C::kProducerWarp) {
+        if constexpr (C::kSplitRings) producer_role(std::true_type{}, std::false_type{});
+        else producer_role(std::true_type{}, std::true_type{});
+      } else if (warp == C::kActWarp) {
+        producer_role(std::false_type{}, std::true_type{});
+      } else if (warp >= C::kWarpsUsed) {
+        pad_role();
+      } else {
+        mma_role();
+      }
     } else if (wg >= C::kDrainWGs) {
       setmaxnreg_dec<C::kRegConv>();
       conv_role();
@@ -1068,7 +1250,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
       drain_role();
     }
   } else {
-    if (warp == C::kProducerWarp) producer_role();
+    if (warp == C::kProducerWarp) producer_role(std::true_type{}, std::true_type{});
     else if (warp >= C::kMmaWarp) mma_role();
     else if (warp >= kConvWarp0) conv_role();
     else drain_role();
@@ -1326,15 +1508,56 @@ static cudaError_t launch_tc(const GemmArgs& a, cudaStream_t st) {
   return cudaLaunchKernelEx(&cfg, kern, act_map, w8_map, p, ymaps);
 }
 
+// Time of a grid of `bt`-token wide tiles in units of one group of one
+// 128-token tile: the split choose_split makes, its rounds times the groups of
+// one unit, times the relative cost of a group at that width.
+static double wide_grid_cost(int64_t M, int64_t n_tiles, int G, int sms, int bt) {
+  // one 192-token group against one 128-token group, CTA time in a full grid
+  constexpr double kFullGroupCost = 1.0;
+  const int64_t tiles = ((M + bt - 1) / bt) * n_tiles;
+  int ks = 1, persistent = 0;
+  choose_split(tiles, G, sms, 2.0, true, &ks, &persistent);
+  const int64_t units = persistent ? tiles : tiles * ks;
+  const int64_t rounds = (units + sms - 1) / sms;
+  const double per_unit =
+      persistent ? (double)G : (double)((G + ks - 1) / ks) + (ks > 1 ? 2.0 : 0.0);
+  return (double)rounds * per_unit * (bt == kFullBT ? kFullGroupCost : 1.0);
+}
+
+int tc_token_tile(int variant, int64_t M, int64_t N, int64_t K) {
+  if (M <= 16) return 16;
+  if (M <= 32) return 32;
+  if (M <= 64) return 64;
+  // per-group variants take a wide tile, 192 tokens unless its grid costs
+  // more; W8A16 (all of K in TMEM) and W8A8 (drains every 8 groups) 128
+  if (variant == kW4A8 || variant == kW4A16 || variant == kW16A16) {
+    const int sms = tc_sm_count();
+    const int G = (int)(K / 128);
+    const int64_t n_tiles = N / 128;
+    return wide_grid_cost(M, n_tiles, G, sms, kFullBT) < wide_grid_cost(M, n_tiles, G, sms, kWideBT)
+               ? kFullBT
+               : kWideBT;
+  }
+  return 128;
+}
+
 template <int VARIANT, bool PARTIALS>
 static cudaError_t launch_tc_bt(const GemmArgs& a, cudaStream_t st) {
-  if (a.M <= 16) return launch_tc<VARIANT, 16, PARTIALS>(a, st);
-  if (a.M <= 32) return launch_tc<VARIANT, 32, PARTIALS>(a, st);
-  if (a.M <= 64) return launch_tc<VARIANT, 64, PARTIALS>(a, st);
-  // per-group variants take the wide tile; W8A16 accumulates all of K
-  constexpr int kBig =
-      (VARIANT == kW4A8 || VARIANT == kW4A16 || VARIANT == kW16A16) ? kWideBT : 128;
-  return launch_tc<VARIANT, kBig, PARTIALS>(a, st);
+  constexpr bool kPerGroup = (VARIANT == kW4A8 || VARIANT == kW4A16 || VARIANT == kW16A16);
+  switch (tc_token_tile(VARIANT, a.M, a.N, a.K)) {
+    case 16:
+      return launch_tc<VARIANT, 16, PARTIALS>(a, st);
+    case 32:
+      return launch_tc<VARIANT, 32, PARTIALS>(a, st);
+    case 64:
+      return launch_tc<VARIANT, 64, PARTIALS>(a, st);
+    case kFullBT:
+      if constexpr (kPerGroup) return launch_tc<VARIANT, kFullBT, PARTIALS>(a, st);
+      break;
+    default:
+      return launch_tc<VARIANT, 128, PARTIALS>(a, st);
+  }
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_tc_gemm(const GemmArgs& a, cudaStream_t st) {
