@@ -83,8 +83,10 @@ constexpr int kMaxSmemHalf = 114688;  // each of two CTAs sharing an SM
 //    buffers, two converter sets, two issuers;
 //  - kFullBT (192 tokens): two 192-column accumulators and two A buffers fill
 //    the 512 TMEM columns, so the drain of group i gates the MMAs of group
-//    i + 2; one converter set, one issuer, which waits for the drained
-//    accumulator itself (one hand-off fewer on that chain).
+//    i + 2; weight records in a ring of their own; one converter set, whose
+//    first warp also waits for the drained accumulator and the landed
+//    activations, meeting two alternating issuers on hardware named
+//    barriers (see kNamedHandoff).
 // The launcher picks the width per linear from the grid it makes (192-token
 // tiles quantise some grids into a short last wave).
 constexpr int kWideBT = 128;
@@ -153,13 +155,11 @@ struct TcCfg {
   static constexpr bool kWide = BT > 64 && kDrainPerGroup;
   static constexpr bool kFull = kWide && BT == kFullBT;  // full-rate tile (see kFullBT)
   static constexpr int kMmaWarps =
-      kLean ? 1 : (kWide ? (kFull ? 1 : 2) : ((kDrainPerGroup && BT <= 32) ? 2 : 1));
-  // the issuer, not the converters, waits for the drained accumulator
-  static constexpr bool kIssuerWaitsD = false;
-  // 192-token tiles hand each group from the converters to the issuer on a
-  // hardware named barrier (one per A buffer), and the converters' first warp
-  // waits for the drained accumulator and the landed activations before its
-  // arrival. The issuer then performs no mbarrier operation at all: an
+      kLean ? 1 : (kWide ? 2 : ((kDrainPerGroup && BT <= 32) ? 2 : 1));
+  // 192-token tiles hand each group from the converters to its issuer on a
+  // hardware named barrier (one per A buffer and issuer), the converters'
+  // first warp having waited for the drained accumulator and the landed
+  // activations. The issuers then perform no mbarrier operation at all: an
   // mbarrier test queues behind the MMAs the issuing warp has just issued
   // (they wait for the tensor pipe in the same memory-instruction queue), so
   // a test between groups idled the pipe for ~400 cycles a group.
@@ -640,15 +640,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
     auto wait_group = [&](int i) -> bool {
       const int ab = i % kNumA;
       // one wait per group: the converters arrive on afull only once the
-      // stage has landed, the A buffer is free and (unless the issuer waits
-      // for it itself) the accumulator drained
-      if (!mbar_wait(afull_bar(ab), (i / kNumA) & 1, abort_flag, tmo)) return false;
-      if constexpr (C::kIssuerWaitsD) {
-        // (per-group tiles: every group starts its accumulator)
-        const int di = drain_of(i);
-        return mbar_wait(dempty_bar(di % kNumD), ((di / kNumD) & 1) ^ 1, abort_flag, tmo);
-      }
-      return true;
+      // stage has landed, the A buffer is free and the accumulator drained
+      return mbar_wait(afull_bar(ab), (i / kNumA) & 1, abort_flag, tmo);
     };
     // (lane 0) group i's MMAs and the commits that release its buffers
     auto issue_group = [&](int i) {
@@ -686,7 +679,11 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
       // the whole warp meets the converters on each group's named barrier
       // (every group, also after an abort: see the converters); lane 0
       // issues unless a wait somewhere in the CTA gave up
-      static_assert(kNumA == 2 && C::kMmaWarps == 1, "named hand-off layout");
+      // (issuer q takes the groups i = q mod 2, whose A buffer and named
+      // barrier are q; the two issuers' MMAs queue in the tensor pipe back to
+      // back, so one issuer meets the converters while the other's MMAs are
+      // still being accepted and the pipe does not drain between groups)
+      static_assert(kNumA == 2 && C::kMmaWarps == 2, "named hand-off layout");
       for (int i = q; i < n_items; i += C::kMmaWarps) {
         asm volatile("bar.sync %0, %1;" ::"r"(C::kHandoffBar0 + i % kNumA), "n"(C::kHandoffCount)
                      : "memory");
@@ -839,7 +836,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
       // MMAs are released (the A operand is stored first: only the MMAs, not
       // the stores, wait for the drain); one warp of the set waits (afull
       // completes only with all four arrivals)
-      if (!C::kIssuerWaitsD && ((warp - kConvWarp0) & 3) == 0) {
+      if (((warp - kConvWarp0) & 3) == 0) {
         const int di = drain_of(i);
         if (!mbar_wait(dempty_bar(di % kNumD), ((di / kNumD) & 1) ^ 1, abort_flag, tmo)) return false;
       }
@@ -1513,7 +1510,8 @@ static cudaError_t launch_tc(const GemmArgs& a, cudaStream_t st) {
 // one unit, times the relative cost of a group at that width.
 static double wide_grid_cost(int64_t M, int64_t n_tiles, int G, int sms, int bt) {
   // one 192-token group against one 128-token group, CTA time in a full grid
-  constexpr double kFullGroupCost = 1.0;
+  // (measured on GB300 over the 7B prefill shapes: 1.20-1.25)
+  constexpr double kFullGroupCost = 1.23;
   const int64_t tiles = ((M + bt - 1) / bt) * n_tiles;
   int ks = 1, persistent = 0;
   choose_split(tiles, G, sms, 2.0, true, &ks, &persistent);
