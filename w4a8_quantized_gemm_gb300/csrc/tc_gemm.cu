@@ -80,7 +80,8 @@ constexpr int kMaxSmemHalf = 114688;  // each of two CTAs sharing an SM
 // takes 757 cycles at N = 128..176 and 4*N from N = 192 up, also with a CTA
 // pair), so the tensor pipe reaches its full rate only from 192 tokens a tile.
 //  - kWideBT (128 tokens): three 128-column accumulators and two 64-column A
-//    buffers, two converter sets, two issuers;
+//    buffers, two converter sets, two issuers (set q meets issuer q on a
+//    named barrier);
 //  - kFullBT (192 tokens): two 192-column accumulators and two A buffers fill
 //    the 512 TMEM columns, so the drain of group i gates the MMAs of group
 //    i + 2; weight records in a ring of their own; one converter set, whose
@@ -156,14 +157,14 @@ struct TcCfg {
   static constexpr bool kFull = kWide && BT == kFullBT;  // full-rate tile (see kFullBT)
   static constexpr int kMmaWarps =
       kLean ? 1 : (kWide ? 2 : ((kDrainPerGroup && BT <= 32) ? 2 : 1));
-  // 192-token tiles hand each group from the converters to its issuer on a
+  // Wide tiles hand each group from the converters to its issuer on a
   // hardware named barrier (one per A buffer and issuer), the converters'
   // first warp having waited for the drained accumulator and the landed
   // activations. The issuers then perform no mbarrier operation at all: an
   // mbarrier test queues behind the MMAs the issuing warp has just issued
   // (they wait for the tensor pipe in the same memory-instruction queue), so
   // a test between groups idled the pipe for ~400 cycles a group.
-  static constexpr bool kNamedHandoff = kFull;
+  static constexpr bool kNamedHandoff = kWide;
   static constexpr int kHandoffBar0 = 6;  // named barriers 6, 7 (A buffers 0, 1)
   static constexpr int kHandoffCount = 32 * 4 + 32;  // converter set + issuer warp
   // TMEM: kNumD accumulators of kDCols columns + kNumA A-operand buffers of
@@ -852,11 +853,14 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
       // group, also after a failed wait (the work is skipped then): both
       // sides always make exactly n_items rendezvous, so neither can wait
       // for ever, and no barrier phase can collect a second arrival early
-      static_assert(C::kConvSets == 1, "named hand-off layout");
-      // (bar.sync is the .aligned form: each warp reaches it converged, and
-      // `ok` is kept warp-uniform)
+      // (group i meets issuer i mod 2 on barrier i mod 2: one converter set
+      // takes every group, two sets take one barrier each; bar.sync is the
+      // .aligned form: each warp reaches it converged, and `ok` is kept
+      // warp-uniform)
+      static_assert(kNumA == 2 && (C::kConvSets == 1 || C::kConvSets == 2),
+                    "named hand-off layout");
       bool ok = true;
-      for (int i = 0; i < n_items; ++i) {
+      for (int i = set; i < n_items; i += C::kConvSets) {
         if (ok) ok = convert_item(i);
         ok = __all_sync(0xffffffffu, ok);
         tc_fence_before();
@@ -1510,8 +1514,8 @@ static cudaError_t launch_tc(const GemmArgs& a, cudaStream_t st) {
 // one unit, times the relative cost of a group at that width.
 static double wide_grid_cost(int64_t M, int64_t n_tiles, int G, int sms, int bt) {
   // one 192-token group against one 128-token group, CTA time in a full grid
-  // (measured on GB300 over the 7B prefill shapes: 1.20-1.25)
-  constexpr double kFullGroupCost = 1.23;
+  // (measured on GB300 over the 7B prefill shapes: 1.09-1.16)
+  constexpr double kFullGroupCost = 1.12;
   const int64_t tiles = ((M + bt - 1) / bt) * n_tiles;
   int ks = 1, persistent = 0;
   choose_split(tiles, G, sms, 2.0, true, &ks, &persistent);
