@@ -84,10 +84,10 @@ constexpr int kMaxSmemHalf = 114688;  // each of two CTAs sharing an SM
 //    named barrier);
 //  - kFullBT (192 tokens): two 192-column accumulators and two A buffers fill
 //    the 512 TMEM columns, so the drain of group i gates the MMAs of group
-//    i + 2; weight records in a ring of their own; one converter set, whose
-//    first warp also waits for the drained accumulator and the landed
-//    activations, meeting two alternating issuers on hardware named
-//    barriers (see kNamedHandoff).
+//    i + 2; weight records in a ring of their own; two converter sets that
+//    split each group's K between them (the first set's first warp also
+//    waits for the drained accumulator and the landed activations), meeting
+//    two alternating issuers on hardware named barriers (see kNamedHandoff).
 // The launcher picks the width per linear from the grid it makes (192-token
 // tiles quantise some grids into a short last wave).
 constexpr int kWideBT = 128;
@@ -166,7 +166,6 @@ struct TcCfg {
   // a test between groups idled the pipe for ~400 cycles a group.
   static constexpr bool kNamedHandoff = kWide;
   static constexpr int kHandoffBar0 = 6;  // named barriers 6, 7 (A buffers 0, 1)
-  static constexpr int kHandoffCount = 32 * 4 + 32;  // converter set + issuer warp
   // TMEM: kNumD accumulators of kDCols columns + kNumA A-operand buffers of
   // kACols columns (deep for small tiles: the converters run ahead of the
   // MMAs and the MMAs ahead of the drain).
@@ -223,7 +222,15 @@ struct TcCfg {
   // Converter warp sets: with small token tiles the MMA and drain per group are
   // short, so a second set of four converter warps takes every other group
   // (each set's store-to-arrive latency overlaps the other's conversion).
-  static constexpr int kConvSets = kLean ? 1 : ((BT <= 32 || (kWide && !kFull)) ? 2 : 1);
+  static constexpr int kConvSets = kLean ? 1 : ((BT <= 32 || kWide) ? 2 : 1);
+  // 192-token tiles: both converter sets work on every group, set q
+  // converting K offsets [64q, 64q + 64) (A columns [32q, 32q + 32)), which
+  // halves the conversion on each group's hand-off chain; elsewhere the sets
+  // take alternate groups
+  static constexpr bool kConvSplitK = kFull;
+  // named hand-off participants: the converter warps meeting an issuer on a
+  // group's barrier, and the issuer warp
+  static constexpr int kHandoffCount = 32 * 4 * (kConvSplitK ? kConvSets : 1) + 32;
   static constexpr int kDrainCols = BT / kDrainWGs;  // token columns per drain thread
   static constexpr int kProducerWarp = kConvWarp0 + 4 * kConvSets;
   static constexpr int kMmaWarp = kProducerWarp + 1;  // first issuer; allocates TMEM
@@ -243,12 +250,13 @@ struct TcCfg {
   static constexpr int kActWarp = kSplitRings ? kWarpsUsed : -1;
   static_assert(!kSplitRings || kWarps > kWarpsUsed, "activation producer warp");
   static constexpr int kThreads = 32 * kWarps;
-  // (192-token tiles: four warpgroups of 128 registers at launch; the drains
-  // hold 96 running sums and 48 TMEM columns in flight)
-  static constexpr int kRegDrain = kFull ? 168 : 120, kRegConv = kFull ? 120 : 96,
-                       kRegOther = kFull ? 56 : 48;
+  // (192-token tiles: five warpgroups of 96 registers at launch; the drains
+  // hold 96 running sums and 32 TMEM columns in flight, the two converter
+  // sets half a group's conversion each)
+  static constexpr int kRegDrain = kFull ? 136 : 120, kRegConv = kFull ? 80 : 96,
+                       kRegOther = 48;
   // (converters keep a whole converted group, 64 registers, in flight)
-  static_assert(!kRegSplit || kRegConv >= 96, "converter registers");
+  static_assert(!kRegSplit || kConvSplitK || kRegConv >= 96, "converter registers");
   // registers every thread has at launch (ptxas holds a kernel that uses
   // setmaxnreg at its launch-bounds maximum; the launcher checks it)
   static constexpr int kRegLaunch = (65536 / kThreads) / 8 * 8;
@@ -454,11 +462,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
       // released by the MMA commit and the 4 converter warps (and, in the
       // e4m3 form, the 8 drain warps, which read the record's scales and
       // zero points from the stage)
-      mbar_init(empty_bar(s), 1 + (C::kSplitRings ? 0 : 4) + (C::kFp8 ? 4 * C::kDrainWGs : 0));
+      mbar_init(empty_bar(s), 1 + (C::kSplitRings ? 0 : 4 * (C::kConvSplitK ? C::kConvSets : 1)) +
+                                  (C::kFp8 ? 4 * C::kDrainWGs : 0));
     }
     for (int r = 0; r < C::kRecStages; ++r) {
       mbar_init(wfull_bar(r), 1);
-      mbar_init(wempty_bar(r), 4);
+      mbar_init(wempty_bar(r), 4 * (C::kConvSplitK ? C::kConvSets : 1));
     }
     for (int i = 0; i < kNumA; ++i) {
       mbar_init(afull_bar(i), 4);
@@ -758,16 +767,18 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
       } else if constexpr (C::kW16) {
         // dense bf16 row r: two 128-byte-swizzled boxes of 64 K values, copied
         // as they are (K pairs per 32-bit word, the A operand's layout)
+        // (K split between the sets: set q copies box q into out[0, 32))
 #pragma unroll
-        for (int b = 0; b < 2; ++b) {
+        for (int bb = 0; bb < (C::kConvSplitK ? 1 : 2); ++bb) {
+          const int b = C::kConvSplitK ? set : bb;
           const uint8_t* wt = stage_w_ptr(s) + b * 16384 + r * 128;
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             const uint4 v = *reinterpret_cast<const uint4*>(wt + ((c ^ (r & 7)) * 16));
-            out[b * 32 + c * 4 + 0] = v.x;
-            out[b * 32 + c * 4 + 1] = v.y;
-            out[b * 32 + c * 4 + 2] = v.z;
-            out[b * 32 + c * 4 + 3] = v.w;
+            out[bb * 32 + c * 4 + 0] = v.x;
+            out[bb * 32 + c * 4 + 1] = v.y;
+            out[bb * 32 + c * 4 + 2] = v.z;
+            out[bb * 32 + c * 4 + 3] = v.w;
           }
         }
         __syncwarp();
@@ -804,17 +815,21 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
           }
         }
       } else {
+        // (K split between the sets: set q converts the record's 32-wide
+        // chunks 2q and 2q + 1 into out[0, 32))
+        constexpr int NC = C::kConvSplitK ? 2 : 4;
+        const int c0 = C::kConvSplitK ? 2 * set : 0;
         const uint8_t* rec = rec_ptr(i);
         const uint8_t* wt = rec + r * 16;
-        uint4 v[4];
+        uint4 v[NC];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) v[c] = *reinterpret_cast<const uint4*>(wt + c * 2048);
+        for (int c = 0; c < NC; ++c) v[c] = *reinterpret_cast<const uint4*>(wt + (c0 + c) * 2048);
         const uint8_t zb = rec[8448 + (r >> 1)];
         __syncwarp();
         if (lane == 0) mbar_arrive(C::kSplitRings ? wempty_bar(i % R) : empty_bar(s));
         const uint32_t z = (r & 1) ? (zb >> 4) : (zb & 0xF);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < NC; ++c) {
           uint32_t chunk[16];
           cvt_w4_unit<VARIANT>(v[c], z, chunk);
 #pragma unroll
@@ -825,25 +840,30 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
       if (!mbar_wait(aempty_bar(ab), ((i / kNumA) & 1) ^ 1, abort_flag, tmo)) return false;
       tc_fence_after();
       const uint32_t dst = a_tmem + lane_base + ab * C::kACols;
+      // (K split: this set's half of the columns)
+      constexpr int kStChunks = C::kConvSplitK ? C::kACols / 32 : C::kACols / 16;
+      const int st0 = C::kConvSplitK ? set * kStChunks : 0;
 #pragma unroll
-      for (int c = 0; c < C::kACols / 16; ++c) {
+      for (int c = 0; c < kStChunks; ++c) {
         uint32_t chunk[16];
 #pragma unroll
         for (int q = 0; q < 16; ++q) chunk[q] = out[c * 16 + q];
-        tmem_st16(dst + c * 16, chunk);
+        tmem_st16(dst + (st0 + c) * 16, chunk);
       }
       tmem_wait_st();
       // the accumulator this item feeds must have been drained before its
       // MMAs are released (the A operand is stored first: only the MMAs, not
       // the stores, wait for the drain); one warp of the set waits (afull
       // completes only with all four arrivals)
-      if (((warp - kConvWarp0) & 3) == 0) {
+      // (K split: the first set's first warp)
+      const bool gate_warp = C::kConvSplitK ? warp == kConvWarp0 : ((warp - kConvWarp0) & 3) == 0;
+      if (gate_warp) {
         const int di = drain_of(i);
         if (!mbar_wait(dempty_bar(di % kNumD), ((di / kNumD) & 1) ^ 1, abort_flag, tmo)) return false;
       }
       // split rings: the activation stage the MMAs read has landed (one warp
       // of the set waits; afull completes only with all four arrivals)
-      if (C::kSplitRings && ((warp - kConvWarp0) & 3) == 0) {
+      if (C::kSplitRings && gate_warp) {
         if (!mbar_wait(full_bar(s), (i / S) & 1, abort_flag, tmo)) return false;
       }
       return true;
@@ -859,8 +879,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
       // warp-uniform)
       static_assert(kNumA == 2 && (C::kConvSets == 1 || C::kConvSets == 2),
                     "named hand-off layout");
+      // (with the K split every set takes every group)
+      constexpr int kStep = C::kConvSplitK ? 1 : C::kConvSets;
       bool ok = true;
-      for (int i = set; i < n_items; i += C::kConvSets) {
+      for (int i = C::kConvSplitK ? 0 : set; i < n_items; i += kStep) {
         if (ok) ok = convert_item(i);
         ok = __all_sync(0xffffffffu, ok);
         tc_fence_before();
@@ -1077,7 +1099,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
         constexpr int NCH = HB / CW;  // loads per drain
         // loads in flight per wait (32 columns at most with the register
         // split -- 48 in the 192-token tiles -- two loads without it)
-        constexpr int kInFlight = C::kFull ? 48 : 32;
+        constexpr int kInFlight = 32;
         constexpr int PAIR =
             C::kRegSplit ? (NCH < kInFlight / CW ? NCH : kInFlight / CW) : (NCH >= 2 ? 2 : 1);
         static_assert(NCH % PAIR == 0, "drain batches");
