@@ -251,9 +251,9 @@ struct TcCfg {
   static_assert(!kSplitRings || kWarps > kWarpsUsed, "activation producer warp");
   static constexpr int kThreads = 32 * kWarps;
   // (192-token tiles: five warpgroups of 96 registers at launch; the drains
-  // hold 96 running sums and 32 TMEM columns in flight, the two converter
+  // hold 96 running sums and 48 TMEM columns in flight, the two converter
   // sets half a group's conversion each)
-  static constexpr int kRegDrain = kFull ? 136 : 120, kRegConv = kFull ? 80 : 96,
+  static constexpr int kRegDrain = kFull ? 144 : 120, kRegConv = kFull ? 72 : 96,
                        kRegOther = 48;
   // (converters keep a whole converted group, 64 registers, in flight)
   static_assert(!kRegSplit || kConvSplitK || kRegConv >= 96, "converter registers");
@@ -1099,7 +1099,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
         constexpr int NCH = HB / CW;  // loads per drain
         // loads in flight per wait (32 columns at most with the register
         // split -- 48 in the 192-token tiles -- two loads without it)
-        constexpr int kInFlight = 32;
+        constexpr int kInFlight = C::kFull ? 48 : 32;
         constexpr int PAIR =
             C::kRegSplit ? (NCH < kInFlight / CW ? NCH : kInFlight / CW) : (NCH >= 2 ? 2 : 1);
         static_assert(NCH % PAIR == 0, "drain batches");
@@ -1536,7 +1536,7 @@ static cudaError_t launch_tc(const GemmArgs& a, cudaStream_t st) {
 // one unit, times the relative cost of a group at that width.
 static double wide_grid_cost(int64_t M, int64_t n_tiles, int G, int sms, int bt) {
   // one 192-token group against one 128-token group, CTA time in a full grid
-  // (measured on GB300 over the 7B prefill shapes: 1.09-1.16)
+  // (measured on GB300 over the 7B prefill shapes: 1.06-1.14)
   constexpr double kFullGroupCost = 1.12;
   const int64_t tiles = ((M + bt - 1) / bt) * n_tiles;
   int ks = 1, persistent = 0;
