@@ -228,9 +228,16 @@ struct TcCfg {
   // halves the conversion on each group's hand-off chain; elsewhere the sets
   // take alternate groups
   static constexpr bool kConvSplitK = kFull;
+  // 192-token tiles (two accumulators): the drain warps join the rendezvous
+  // of group i + 2 as soon as group i's accumulator is in their registers,
+  // in place of an accumulator-free mbarrier the converters would test (with
+  // two accumulators the current phase of that barrier is then always group
+  // i + 2's: group i's completed before its MMAs were issued)
+  static constexpr bool kDrainRendezvous = kNamedHandoff && kFull;
   // named hand-off participants: the converter warps meeting an issuer on a
-  // group's barrier, and the issuer warp
-  static constexpr int kHandoffCount = 32 * 4 * (kConvSplitK ? kConvSets : 1) + 32;
+  // group's barrier, the issuer warp, and (see above) the drain warps
+  static constexpr int kHandoffCount = 32 * 4 * (kConvSplitK ? kConvSets : 1) + 32 +
+                                       (kDrainRendezvous ? 32 * 4 * kDrainWGs : 0);
   static constexpr int kDrainCols = BT / kDrainWGs;  // token columns per drain thread
   static constexpr int kProducerWarp = kConvWarp0 + 4 * kConvSets;
   static constexpr int kMmaWarp = kProducerWarp + 1;  // first issuer; allocates TMEM
@@ -857,7 +864,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
       // completes only with all four arrivals)
       // (K split: the first set's first warp)
       const bool gate_warp = C::kConvSplitK ? warp == kConvWarp0 : ((warp - kConvWarp0) & 3) == 0;
-      if (gate_warp) {
+      if (!C::kDrainRendezvous && gate_warp) {
         const int di = drain_of(i);
         if (!mbar_wait(dempty_bar(di % kNumD), ((di / kNumD) & 1) ^ 1, abort_flag, tmo)) return false;
       }
@@ -985,6 +992,20 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
         bulk_commit_group();
       }
     };
+    // (drain rendezvous: the drain warps join the named barrier of every group
+    // in order -- groups 0 and 1 at once, group i + 2 once group i's
+    // accumulator is loaded, and any left after a failed wait at the end -- so
+    // that they, too, make exactly n_items rendezvous)
+    int next_join = 0;
+    auto join = [&](int j) {
+      tc_fence_before();
+      __syncwarp();
+      asm volatile("bar.sync %0, %1;" ::"r"(C::kHandoffBar0 + j % kNumA), "n"(C::kHandoffCount)
+                   : "memory");
+    };
+    if constexpr (C::kDrainRendezvous) {
+      while (next_join < 2 && next_join < n_items) join(next_join++);
+    }
     for (int k = 0; k < n_units && ok; ++k) {
       if (k > 0) unit_tile(k, mt, nt);
       out = tile_ref(p.seg, nt, G);
@@ -1117,9 +1138,16 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
           if (cb + PAIR >= NCH) {
             // the whole accumulator is in registers: release it before the
             // last batch's arithmetic (the MMAs two groups on wait for it)
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(dempty_bar(db));
+            if constexpr (C::kDrainRendezvous) {
+              if (i + 2 < n_items) {
+                join(i + 2);
+                next_join = i + 3;
+              }
+            } else {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(dempty_bar(db));
+            }
           }
 #pragma unroll
           for (int q2 = 0; q2 < PAIR; ++q2) {
@@ -1174,6 +1202,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
           }
         }
       }
+    }
+    if constexpr (C::kDrainRendezvous) {
+      while (next_join < n_items) join(next_join++);
     }
     if constexpr (C::kTmaEpi && !PARTIALS) {
       if (epi_thread) bulk_wait_group0();  // the last tile's stores have landed
