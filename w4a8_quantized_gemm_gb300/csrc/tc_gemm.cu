@@ -987,7 +987,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
       }
       fence_proxy_async_smem();
       asm volatile("bar.sync %0, 128;" ::"r"(2 + wg) : "memory");
-      if (epi_thread && m0 + col0 < p.M) {
+      if (epi_thread && ok && m0 + col0 < p.M) {
         tma_store_2d(&ymaps.map[o.seg], smem_u32(ybuf), (int)o.n0, (int)(m0 + col0));
         bulk_commit_group();
       }
@@ -1006,7 +1006,14 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
     if constexpr (C::kDrainRendezvous) {
       while (next_join < 2 && next_join < n_items) join(next_join++);
     }
-    for (int k = 0; k < n_units && ok; ++k) {
+    // Wide tiles: after a failed wait a drain warp skips the work but keeps
+    // the warpgroup's barrier sequence (the epilogue's named barriers, the
+    // rendezvous joins) to the end, since its warpgroup's other warps may
+    // have seen the same phase complete (a wait that finds the phase
+    // complete on its first test returns at once, one that does not gives up
+    // on the CTA's abort flag) and would otherwise wait for it for ever.
+    constexpr bool kUniformDrain = C::kTmaEpi;
+    for (int k = 0; k < n_units && (ok || kUniformDrain); ++k) {
       if (k > 0) unit_tile(k, mt, nt);
       out = tile_ref(p.seg, nt, G);
       const int64_t n = out.n0 + r;  // row of this thread in its linear's output
@@ -1038,9 +1045,19 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
         float s = f16_bits_to_f32(s_next);
         if constexpr (kScaleFromGlobal)
           s_next = (gi + 1 < ng) ? __ldg(sp_tile + (int64_t)(gi + 1) * 4256) : s_first_next;
-        if (!mbar_wait(dfull_bar(db), (di / kNumD) & 1, abort_flag, tmo)) {
+        if (!(ok && mbar_wait(dfull_bar(db), (di / kNumD) & 1, abort_flag, tmo))) {
           ok = false;
-          break;
+          if constexpr (!kUniformDrain) {
+            break;
+          } else {
+            if constexpr (C::kDrainRendezvous) {
+              if (i + 2 < n_items) {
+                join(i + 2);
+                next_join = i + 3;
+              }
+            }
+            continue;
+          }
         }
         if constexpr (C::kTmaEpi && kCodes && !PARTIALS) {
           if (gi == 0 && r < HB) as_stage[(k & 1) * BT + col0 + r] = as_pending;
@@ -1182,7 +1199,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
           if (lane == 0) mbar_arrive(dempty_bar(db));
         }
       }
-      if (!ok) break;
+      if (!ok && !kUniformDrain) break;
       if constexpr (VARIANT == kW8A16) {
         const float sc = f16_bits_to_f32(__ldg(p.s8 + n));
 #pragma unroll
