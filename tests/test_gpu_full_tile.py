@@ -1,6 +1,7 @@
 """GPU parity of the 192-token tensor-core tiles (the full-rate wide tile: two
-TMEM accumulators, one converter set, one issuer that waits for the drained
-accumulator itself) against the CPU oracle.
+TMEM accumulators; two converter sets splitting each group's K, two
+alternating MMA issuers and the drain warps meeting on hardware named
+barriers) against the CPU oracle.
 
 The library picks 192 or 128 tokens per tile from the grid each makes on the
 device's SMs (egopq_tc_token_tile). The shapes below are built from the SM
@@ -123,3 +124,21 @@ def test_token_tile_choice():
     assert eg.tc_token_tile(256, 256, 512) == 128        # 2 m-tiles at either width
     assert eg.tc_token_tile(4096, 152064, 3584) == 192   # the untied head at 4096 tokens
     assert eg.tc_token_tile(4096, 3584, 3584, eg.VARIANT_W8A16) == 128
+
+
+def test_bf16_twin_full_tile():
+    """The structure twin (dense bf16 weights through the same pipeline) on a
+    192-token grid: each converter set copies its half of the group's K."""
+    from helpers import bf16_bits_to_f64
+    M, N, K = _shape("one_round")
+    assert eg.tc_token_tile(M, N, K, eg.VARIANT_W4A16) == 192   # the twin's rule
+    rng = np.random.default_rng(21)
+    x = synth.activations(14, 0, 0, M, K, outliers=False)
+    w = (rng.standard_normal((N, K)).astype(np.float32) * 0.05).view(np.uint32)
+    w = ((w + 0x7FFF + ((w >> 16) & 1)) >> 16).astype(np.uint16)   # bf16, round to even
+    y = eg.bf16_gemm_twin(to_dev(x, torch.bfloat16), to_dev(w, torch.bfloat16))
+    cols = np.unique(np.concatenate([np.arange(128), np.arange(N - 128, N),
+                                     rng.choice(N, 256, replace=False)]))
+    ref = bf16_bits_to_f64(x) @ bf16_bits_to_f64(w[cols]).T
+    ref_bits = np.vectorize(oracle.bf16_from_double, otypes=[np.uint16])(ref)
+    check_bf16_output(to_host_bits(y)[:, cols], ref_bits, "twin, 192-token tiles")
