@@ -271,8 +271,18 @@ def dtype_string(args) -> str:
 
 # --------------------------------------------------------- DRAM traffic table --
 
+def _code_only(text: str) -> str:
+    """The source with its comments and blank lines taken out (trailing
+    whitespace too): what a change to the counters can come from."""
+    import re
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def kernel_sources_hash() -> str:
-    """sha256 over the CUDA sources and the public header (names and bytes)."""
+    """sha256 over the CUDA sources and the public header (names and code,
+    comments left out: a comment edit does not invalidate measured traffic)."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "w4a8_quantized_gemm_gb300", "csrc")
@@ -281,8 +291,8 @@ def kernel_sources_hash() -> str:
     files.append(os.path.join(ROOT, "include", "egopq.h"))
     for f in files:
         h.update(os.path.basename(f).encode())
-        with open(f, "rb") as fh:
-            h.update(fh.read())
+        with open(f, encoding="utf-8") as fh:
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()
 
 

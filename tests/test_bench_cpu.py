@@ -103,3 +103,12 @@ def test_traffic_reported_only_for_the_captured_sources(tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "kernel_sources_hash", lambda: "0" * 64)
     assert bench.traffic_table() == {}
     assert os.path.exists(str(good / "profiles" / "dram_traffic.txt"))
+
+
+def test_sources_hash_ignores_comments_only():
+    """A comment or blank-line edit keeps the measured traffic valid; a code
+    edit does not."""
+    code = "int a = 1;  // the first\n/* a block\n   comment */\nint b = 2;\n"
+    assert bench._code_only(code) == bench._code_only(
+        "int a = 1;\n\n// another note\nint b = 2;  /* trailing */\n")
+    assert bench._code_only(code) != bench._code_only("int a = 1;\nint b = 3;\n")

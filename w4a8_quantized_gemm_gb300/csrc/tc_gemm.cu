@@ -25,7 +25,7 @@
 //
 // Operand roles ("swap AB"): the 128 weight rows of a tile are the MMA's M
 // dimension and live in TENSOR MEMORY as the A operand; the token tile (BT
-// tokens, 16..128) is the MMA's N dimension and comes from shared memory as
+// tokens, 16..192) is the MMA's N dimension and comes from shared memory as
 // the B operand, staged by TMA with 128-byte swizzle. The dequantized weights
 // therefore never touch shared memory: converter warps read the packed int4
 // record (one 8512-byte bulk copy per 128 rows x 128 K: codes, scales, zero
@@ -38,21 +38,25 @@
 //                    with all of them in the lean CTAs)
 //   converter warps  packed int4 (or int8) smem tile -> e4m3/fp16/bf16 in TMEM
 //                    (a second set of four takes every other group for token
-//                    tiles of 32 and for per-group 128-token tiles)
-//   producer warp    TMA: activations tile + weight record per group
+//                    tiles of 32 and 128-token per-group tiles, and half of
+//                    every group's K in 192-token tiles)
+//   producer warp    TMA: activations tile + weight record per group (192-token
+//                    tiles: the records only, on a ring of their own, and a
+//                    second producer warp for the activations)
 //   issuer warps     one MMA-issuing thread each (two for 32-token and
-//                    per-group 128-token tiles, taking alternate groups); the
+//                    per-group wide tiles, taking alternate groups); the
 //                    first allocates TMEM
-// (128-token per-group tiles add a padding warp and split the registers per
-// warpgroup with setmaxnreg: drains 120, converters 96, producer/issuers 48)
-// (a warp reaches TMEM lanes 32*(warp % 4) .. +31, so each role that touches
+// (wide per-group tiles split the registers per warpgroup with setmaxnreg;
+// a warp reaches TMEM lanes 32*(warp % 4) .. +31, so each role that touches
 // TMEM is a whole warpgroup)
-// Hand-offs, all on mbarriers with bounded waits: S shared-memory stages,
-// kNumA TMEM A buffers, kNumD TMEM accumulators. Every barrier test is a
-// round trip of about a hundred cycles on the waiting thread, so an MMA
-// issuer waits on one barrier per group: the converters arrive on it only
-// after the stage has landed, the A buffer is free and the accumulator has
-// been drained.
+// Hand-offs: S shared-memory stages, kNumA TMEM A buffers, kNumD TMEM
+// accumulators, on mbarriers with bounded waits; in the wide tiles the
+// converters hand each group to its issuer on a hardware named barrier
+// instead (see kNamedHandoff), which the drains of the 192-token tiles join
+// too (see kDrainRendezvous). Every mbarrier test is a round trip of about a
+// hundred cycles on the waiting thread, so an issuer waits on one barrier per
+// group at most: the converters release it only after the stage has landed,
+// the A buffer is free and the accumulator has been drained.
 //
 // Split-K for small grids: a cluster of up to 8 CTAs shares one output tile,
 // each taking a contiguous range of groups; partial sums are reduced through
