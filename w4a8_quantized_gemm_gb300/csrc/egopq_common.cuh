@@ -151,6 +151,24 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// ---- packed fp32 arithmetic (sm_100 and later) ------------------------------
+// {r0, r1} += s * {v0, v1} as one fma.rn.f32x2: two independent
+// round-to-nearest FMAs, bit for bit what fmaf gives each lane, in one issue.
+// s2 holds s in both halves (f32x2_splat).
+__device__ __forceinline__ uint64_t f32x2_splat(float s) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %1};" : "=l"(d) : "f"(s));
+  return d;
+}
+__device__ __forceinline__ void fma_f32x2(float& r0, float& r1, uint64_t s2, uint32_t v0,
+                                          uint32_t v1) {
+  uint64_t r, v;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(r0), "f"(r1));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "r"(v0), "r"(v1));
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(r) : "l"(s2), "l"(v));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r0), "=f"(r1) : "l"(r));
+}
+
 // ---- TMA --------------------------------------------------------------------
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                             int x, int y) {

@@ -1189,6 +1189,14 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
                 float& Rq = R[(cb + q2) * CW + q];
                 Rq = __int_as_float(__float_as_int(Rq) + __float2int_rn(__uint_as_float(v[q2][q])));
               }
+            } else if constexpr (C::kWide && CW % 2 == 0) {
+              // two columns a packed FMA (the same rounding as fmaf, half the
+              // issue slots of the drain's arithmetic)
+              const uint64_t s2 = f32x2_splat(s);
+#pragma unroll
+              for (int q = 0; q < CW; q += 2)
+                fma_f32x2(R[(cb + q2) * CW + q], R[(cb + q2) * CW + q + 1], s2, v[q2][q],
+                          v[q2][q + 1]);
             } else {
 #pragma unroll
               for (int q = 0; q < CW; ++q)
