@@ -81,10 +81,12 @@ def quant_bytes(M, K):
     return 2 * M * K + M * K + 4 * M + 4 * M * (K // G128)
 
 
-def quant_actual_bytes(M, K, with_tc=True):
-    """Also counts the tensor-core operand form (2 bytes a code) the quantizer
-    writes when the tensor-core path will read it."""
-    return quant_bytes(M, K) + (2 * M * K if with_tc else 0)
+def quant_actual_bytes(M, K, with_tc=True, with_codes=True):
+    """What the quantizer writes in place of the algorithmic int8 codes: the
+    int8 codes where a GEMV reads them, the tensor-core operand form (2 bytes
+    a code) where the tensor-core path reads it."""
+    codes = (M * K if with_codes else 0) + (2 * M * K if with_tc else 0)
+    return quant_bytes(M, K) - M * K + codes
 
 
 def w4a16_bytes(M, N, K):
@@ -431,9 +433,12 @@ def actual_bytes(eg, cell: Cell, path: int, tc_inputs=()) -> int:
     """Bytes the launch moves: the algorithmic bytes, plus the tensor-core
     operand form of the activations where that path writes or reads it."""
     if cell.kind == "quant":
-        return quant_actual_bytes(cell.M, cell.K, (cell.M, cell.inp) in tc_inputs)
+        key = (cell.M, cell.inp)
+        return quant_actual_bytes(cell.M, cell.K, key in tc_inputs, key not in tc_inputs)
     if cell.kind == "w4a8" and "tc_gemm" in kernel_label(eg, cell, path):
-        extra = 2 * cell.M * cell.K \
+        # the one-call linear on this path writes the 2-byte operand form and
+        # no int8 codes: one byte a code more than the algorithmic count
+        extra = cell.M * cell.K \
             if cell.with_quant and cell.bytes > w4a8_bytes(cell.M, cell.N, cell.K) else 0
         return cell.bytes + cell.M * cell.K + extra
     return cell.bytes
@@ -495,12 +500,15 @@ class Part:
                                     [packs[(layer, s)] for s in sib])
                 self.packs.append(packs)
         torch.cuda.synchronize()
-        # activations: one bf16 input per (M, input), one quantized set each
-        # (with the tensor-core operand form only where a tensor-core cell
-        # reads it)
+        # activations: one bf16 input per (M, input), one quantized set each:
+        # the tensor-core operand form where tensor-core cells read the input,
+        # the int8 codes otherwise (a path reads one or the other)
         self.x, self.q = {}, {}
         tc_inputs = {(c.M, c.inp) for c in self.cells
                      if c.kind in ("w4a8", "w8a8") and "tc_gemm" in kernel_label(eg, c, path)}
+        gemv_inputs = {(c.M, c.inp) for c in self.cells
+                       if c.kind in ("w4a8", "w8a8") and "tc_gemm" not in kernel_label(eg, c, path)}
+        assert not (tc_inputs & gemv_inputs), "an input read by both paths"
         for c in self.cells:
             key = (c.M, c.inp)
             if key in self.x:
@@ -511,7 +519,8 @@ class Part:
                 x = synth.activations(cfg, 0, INPUT_SEED.get(c.inp, 0), c.M, c.K)
             self.x[key] = t(x, torch.bfloat16)
             self.q[key] = eg.QuantAct(
-                torch.empty((c.M, c.K), dtype=torch.int8, device=dev),
+                torch.empty((c.M, c.K), dtype=torch.int8, device=dev)
+                if key not in tc_inputs else None,
                 torch.empty((c.M,), dtype=torch.float32, device=dev),
                 torch.empty((c.M, c.K // G128), dtype=torch.int32, device=dev),
                 eg.tc_operand(c.M, c.K, dev) if key in tc_inputs else None)

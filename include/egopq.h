@@ -160,7 +160,9 @@ int egopq_unpack_w4(const void* packed, int64_t N, int64_t K, int group, uint8_t
  *   a_q[m,k]    = clamp(round_half_even(x / a_s), -127, 127)  (fp32 quotient)
  *   a_gsum[m,g] = sum_{k in g} a_q[m,k]
  * A row of zeros gives a_s = 0 and a_q = 0. Outputs (device): a_q int8
- * [M][K], a_s fp32 [M], a_gsum int32 [M][G]. a_tc (optional, may be NULL;
+ * [M][K], a_s fp32 [M], a_gsum int32 [M][G]. a_q may be NULL when a_tc is
+ * given: the codes are then written only in the operand form, which is all
+ * the tensor-core path reads (the GEMV path reads a_q). a_tc (optional, may be NULL;
  * egopq_tc_operand_bytes(M, K, group) bytes) receives the same codes in the
  * operand form the tensor-core path loads with TMA. The library chooses that
  * form from M (egopq_tc_operand_form); a buffer written for one M is valid
@@ -192,8 +194,9 @@ int egopq_quant_act_i8(const uint16_t* x_bf16, int64_t M, int64_t K, int group, 
  * y[m,n] = bf16( a_s[m] * sum_g s[n,g] * (sum_{k in g} a_q[m,k] w_q[n,k]
  *                                         - z[n,g] * a_gsum[m,g]) )
  * Inputs from egopq_quant_act_i8 and egopq_pack_w4; y is bf16 [M][N]. The
- * GEMV path reads a_q and a_gsum; the tensor-core path reads a_tc (required
- * when it runs) and, for M > 64, folds z into its weight operand, for
+ * GEMV path reads a_q and a_gsum (a_q required when it runs: NULL gives
+ * EGOPQ_ERR_INVALID_ARG); the tensor-core path reads a_tc (required when it
+ * runs; a_q may then be NULL) and, for M > 64, folds z into its weight operand, for
  * M <= 64 subtracts z * a_gsum in its epilogue. Every path forms each group's
  * integer partial exactly before scaling. */
 int egopq_w4a8_gemm(const int8_t* a_q, const void* a_tc, const float* a_s,
@@ -249,7 +252,7 @@ int egopq_w4a8_linear_grouped(const uint16_t* x_bf16, int count, const void* con
  * deployment convenience. Same arguments and results as egopq_w4a8_linear
  * minus the workspace: the quantized activations are staged in a 16 MiB
  * file-scope device array that every GPU loading the library holds until the
- * process exits. Calls whose staging exceeds 16 MiB (about 3*M*K bytes on the
+ * process exits. Calls whose staging exceeds 16 MiB (about 2*M*K bytes on the
  * tensor-core path, M*K on the GEMV path) return EGOPQ_ERR_UNSUPPORTED_SHAPE.
  * All calls share the array: calls that overlap on the GPU race on it. The
  * first call in each CUDA context looks the array's address up with that
@@ -263,7 +266,8 @@ int egopq_w4a8_linear_noalloc(const uint16_t* x_bf16, const void* packed, int64_
 
 /* Test readout: the integer group partials Q[m][n][g] (int32 [M][N][G]) the
  * chosen path forms before scaling, from the same main loop:
- *   Q[m,n,g] = sum_{k in g} a_q[m,k] w_q[n,k] - z[n,g] * sum_{k in g} a_q[m,k]. */
+ *   Q[m,n,g] = sum_{k in g} a_q[m,k] w_q[n,k] - z[n,g] * sum_{k in g} a_q[m,k].
+ * a_q and a_tc as for egopq_w4a8_gemm_ex (each required by its own path). */
 int egopq_w4a8_group_partials(const int8_t* a_q, const void* a_tc, const int32_t* a_gsum,
                               const void* packed, int64_t M, int64_t N, int64_t K, int group,
                               int32_t* Q, int path, egopq_stream_t stream);
@@ -294,7 +298,8 @@ int egopq_w8a16_gemm_ex(const uint16_t* x_bf16, const int8_t* w_q, const uint16_
  * y[m,n] = bf16( a_s[m] * s[n] * sum_k a_q[m,k] * w_q[n,k] )
  * Activations as egopq_quant_act_i8 produces them (per-token int8 a_q [M][K],
  * a_s fp32 [M]; a_tc, the tensor-core operand form, is read only on the
- * tensor-core path and only exists there for M > 64); weights int8 [N][K]
+ * tensor-core path and only exists there for M > 64; a_q is read only on
+ * the GEMV path and may be NULL when the tensor cores run); weights int8 [N][K]
  * row-major in [-127, 127] with fp16 per-output-channel scales [N], as for
  * W8A16. The integer dot products are exact (int32). AUTO runs the GEMV for
  * M <= 64 and the tensor cores above; EGOPQ_PATH_TC with M <= 64 returns

@@ -44,6 +44,9 @@ def test_host_validation_rejects_before_launch(lib):
     # shape gate
     assert lib.egopq_pack_w4(A, A, A, 100, 128, 128, A, s) == -2
     assert lib.egopq_quant_act_i8(A, 4, 200, 128, A, A, A, None, s) == -2
+    # the codes may be left out only when the operand form is written
+    assert lib.egopq_quant_act_i8(A, 4, 256, 128, None, A, A, None, s) == -1
+    assert b"a_q and a_tc" in lib.egopq_last_error_string()
     assert lib.egopq_w4a8_gemm_ex(A, A, A, A, A, 4, 256, 512, 32, A, 0, s) == -2
     assert lib.egopq_w4a8_gemm_ex(A, A, A, A, A, -1, 256, 512, 128, A, 0, s) == -1
     # unknown path is refused on the host

@@ -33,6 +33,8 @@ def test_algorithmic_bytes_match_the_formats():
     assert bench.quant_bytes(M, K) == 2 * M * K + M * K + 4 * M + 4 * M * G
     assert bench.quant_actual_bytes(M, K) == bench.quant_bytes(M, K) + 2 * M * K
     assert bench.quant_actual_bytes(M, K, with_tc=False) == bench.quant_bytes(M, K)
+    # the operand form alone (the int8 codes left out where no GEMV reads them)
+    assert bench.quant_actual_bytes(M, K, with_codes=False) == 2 * M * K + 2 * M * K + 4 * M + 4 * M * G
 
 
 def test_sweep_covers_m_1_to_4096_with_every_linear():

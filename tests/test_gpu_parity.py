@@ -77,6 +77,84 @@ def test_quant_act_ties_from_golden_rows():
     assert got.tolist() == [[127, 0, 2, -2, 0, 4, 0, 50], [-127, 2, 2, -2, 0, 0, 4, 6]]
 
 
+def _misrounding_rows(M, K, seed):
+    """bf16 rows each holding values x whose product with the reciprocal of
+    the row's scale, x * fl(1 / a_s), rounds to another integer than the fp32
+    quotient x / a_s (found by search over every bf16 value below the row's
+    absmax, in numpy's IEEE fp32 arithmetic); random values elsewhere. The
+    quantizer computes codes from that product and divides exactly where the
+    product lies near a half-integer: these are the values that check it."""
+    rng = np.random.default_rng(seed)
+    pos = (np.arange(0x0080, 0x7F80, dtype=np.uint32) << 16).view(np.float32)
+    x = np.zeros((M, K), np.float32)
+    m = 0
+    while m < M:
+        amax = pos[rng.integers(0x2F00, 0x4780)]     # absmax 2^-33 .. 2^16
+        s = np.float32(amax) / np.float32(127)
+        inv = np.float32(1) / s
+        cand = pos[pos <= amax]
+        bad = cand[np.rint(cand * inv) != np.rint(cand / s)]
+        if len(bad) == 0:
+            continue
+        row = (rng.uniform(-1.0, 1.0, K) * 0.99 * float(amax)).astype(np.float32)
+        row[0] = amax
+        where = rng.choice(np.arange(1, K), size=min(K // 4, 64), replace=False)
+        row[where] = rng.choice(np.concatenate([bad, -bad]), size=len(where))
+        x[m] = row
+        m += 1
+    bits = x.view(np.uint32)
+    return ((bits + 0x7FFF + ((bits >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+@pytest.mark.parametrize("M,K", [(3, 3584),      # few tokens: 512 threads a row
+                                 (5, 18944),     # few tokens: a cluster splits the row
+                                 (2, 33024),     # few tokens, row too long for both: two passes
+                                 # many tokens: persistent CTAs streaming rows through
+                                 # shared memory -- one row each, then several rows each
+                                 # (more rows than resident CTAs: double-buffered staging)
+                                 (70, 8192), (2600, 1024), (1000, 16384), (400, 32768),
+                                 (66, 33024)])   # many tokens, rows too long to stage: two passes
+@pytest.mark.parametrize("with_codes", [True, False])
+def test_quant_act_misrounding_products_bit_exact(M, K, with_codes):
+    """Every quantization kernel, on rows built from the values where the
+    reciprocal product alone would round wrong: codes, scales, group sums and
+    the operand form bit for bit against the oracle, with the int8 codes
+    written or left out."""
+    x = _misrounding_rows(M, K, 40 + M + K % 97)
+    a = eg.quant_act(to_dev(x, torch.bfloat16), with_codes=with_codes)
+    a_q, a_s, asum = oracle.quant_act(x)
+    if with_codes:
+        assert np.array_equal(a.a_q.cpu().numpy(), a_q)
+    else:
+        assert a.a_q is None
+    assert np.array_equal(a.a_s.cpu().numpy().view(np.uint32), a_s.view(np.uint32))
+    assert np.array_equal(a.a_gsum.cpu().numpy(), asum)
+    got = decode_tc_operand(a.a_tc.cpu().numpy(), M, K, M <= 64)
+    assert np.array_equal(got, a_q.astype(np.float64))
+
+
+@pytest.mark.parametrize("M", [16, 130])
+def test_w4a8_gemm_without_int8_codes(M):
+    """Codes kept only in the operand form: the tensor-core path gives the
+    bits it gives with the int8 codes present; the GEMV path, which reads
+    them, refuses."""
+    N, K = 256, 1024
+    x, w = w4_case(16, M, N, K)
+    packed = eg.pack_w4(*dev_weights(w))
+    xd = to_dev(x, torch.bfloat16)
+    y1 = eg.w4a8_gemm(eg.quant_act(xd), packed, N, K, path=eg.PATH_TC)
+    lean = eg.quant_act(xd, with_codes=False)
+    y2 = eg.w4a8_gemm(lean, packed, N, K, path=eg.PATH_TC)
+    assert torch.equal(y1, y2)
+    ys1 = eg.w4a8_gemm_grouped(eg.quant_act(xd), [packed, packed], [N, N], K, path=eg.PATH_TC)
+    ys2 = eg.w4a8_gemm_grouped(lean, [packed, packed], [N, N], K, path=eg.PATH_TC)
+    assert all(torch.equal(u, v) for u, v in zip(ys1, ys2))
+    with pytest.raises(eg.EgopqError) as err:
+        eg.w4a8_gemm(lean, packed, N, K, path=eg.PATH_GEMV)
+    assert err.value.code == -1
+    assert eg.device_status() == 0
+
+
 # -------------------------------------------------------------------- packing
 
 @pytest.mark.parametrize("N,K", [(128, 128), (256, 512), (512, 3584)])

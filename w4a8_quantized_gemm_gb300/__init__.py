@@ -193,7 +193,9 @@ def dequant_w4(packed: torch.Tensor, N: int, K: int, out: Optional[torch.Tensor]
 
 
 class QuantAct(NamedTuple):
-    a_q: torch.Tensor      # int8 [M, K]
+    # int8 [M, K], or None when the codes were written only in the tensor-core
+    # operand form (all the tensor-core path reads)
+    a_q: Optional[torch.Tensor]
     a_s: torch.Tensor      # fp32 [M]
     a_gsum: torch.Tensor   # int32 [M, G]
     # uint8: the codes in the tensor-core operand form the library picks for
@@ -243,13 +245,15 @@ def tc_operand(M: int, K: int, device) -> torch.Tensor:
 
 
 def quant_act(x: torch.Tensor, with_tc: bool = True, out: Optional[QuantAct] = None,
-              stream=None) -> QuantAct:
-    """Per-token symmetric int8 quantization of bf16 x [M, K]."""
+              stream=None, with_codes: bool = True) -> QuantAct:
+    """Per-token symmetric int8 quantization of bf16 x [M, K]. with_codes=False
+    leaves the int8 codes out (a_q None): only the tensor-core path can read
+    the result."""
     _dtype(x, torch.bfloat16, torch.int16, torch.uint16)
     M, K = x.shape
     if out is None:
         dev = x.device
-        out = QuantAct(torch.empty((M, K), dtype=torch.int8, device=dev),
+        out = QuantAct(torch.empty((M, K), dtype=torch.int8, device=dev) if with_codes else None,
                        torch.empty((M,), dtype=torch.float32, device=dev),
                        torch.empty((M, max(K // GROUP, 1)), dtype=torch.int32, device=dev),
                        tc_operand(M, K, dev) if with_tc else None)
@@ -260,9 +264,9 @@ def quant_act(x: torch.Tensor, with_tc: bool = True, out: Optional[QuantAct] = N
 
 def w4a8_gemm(a: QuantAct, packed: torch.Tensor, N: int, K: int, path: int = PATH_AUTO,
               out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    M = a.a_q.shape[0]
+    M = a.a_s.shape[0]
     if out is None:
-        out = torch.empty((M, N), dtype=torch.bfloat16, device=a.a_q.device)
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=a.a_s.device)
     _check(load().egopq_w4a8_gemm_ex(_ptr(a.a_q), _ptr(a.a_tc), _ptr(a.a_s), _ptr(a.a_gsum),
                                      _ptr(packed), M, N, K, GROUP, _ptr(out), path,
                                      _stream(stream)))
@@ -319,8 +323,8 @@ def w4a8_gemm_grouped(a: QuantAct, packed: list, N: list, K: int, path: int = PA
                       out: Optional[list] = None, stream=None) -> list:
     """Sibling linears sharing the activations `a` (q|k|v, gate|up) in one
     launch: returns [y_j bf16 [M, N_j]]."""
-    M = a.a_q.shape[0]
-    out = _grouped_outputs(M, N, a.a_q.device, out)
+    M = a.a_s.shape[0]
+    out = _grouped_outputs(M, N, a.a_s.device, out)
     g = _Group(packed, N, out)
     _check(load().egopq_w4a8_gemm_grouped(_ptr(a.a_q), _ptr(a.a_tc), _ptr(a.a_s), _ptr(a.a_gsum),
                                           g.count, g.packed, g.N, M, K, GROUP, g.y, path,
@@ -348,8 +352,8 @@ def w4a8_linear_grouped(x: torch.Tensor, packed: list, N: list, path: int = PATH
 
 def w4a8_group_partials(a: QuantAct, packed: torch.Tensor, N: int, K: int,
                         path: int = PATH_TC, stream=None) -> torch.Tensor:
-    M = a.a_q.shape[0]
-    Q = torch.empty((M, N, K // GROUP), dtype=torch.int32, device=a.a_q.device)
+    M = a.a_s.shape[0]
+    Q = torch.empty((M, N, K // GROUP), dtype=torch.int32, device=a.a_s.device)
     _check(load().egopq_w4a8_group_partials(_ptr(a.a_q), _ptr(a.a_tc), _ptr(a.a_gsum),
                                             _ptr(packed), M, N, K, GROUP, _ptr(Q), path,
                                             _stream(stream)))
@@ -387,10 +391,10 @@ def w8a8_gemm(a: QuantAct, w_q: torch.Tensor, scale_f16: torch.Tensor, path: int
     is read on the tensor-core path only) times int8 weights [N, K] with fp16
     per-channel scales [N]."""
     _dtype(w_q, torch.int8)
-    M, K = a.a_q.shape
-    N = w_q.shape[0]
+    M = a.a_s.shape[0]
+    N, K = w_q.shape
     if out is None:
-        out = torch.empty((M, N), dtype=torch.bfloat16, device=a.a_q.device)
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=a.a_s.device)
     _check(load().egopq_w8a8_gemm_ex(_ptr(a.a_q), _ptr(a.a_tc), _ptr(a.a_s), _ptr(w_q),
                                      _ptr(scale_f16), M, N, K, _ptr(out), path,
                                      _stream(stream)))

@@ -127,6 +127,8 @@ int run_gemm(const GemmArgs& a, int path, cudaStream_t st) {
   const int use = auto_path(a.M, a.variant, path);
   if (use == EGOPQ_PATH_TC && (a.variant == kW4A8 || a.variant == kW8A8) && !a.a_tc)
     return fail(EGOPQ_ERR_INVALID_ARG, "a_tc is required by the tensor-core path");
+  if (use == EGOPQ_PATH_GEMV && (a.variant == kW4A8 || a.variant == kW8A8) && !a.a_q)
+    return fail(EGOPQ_ERR_INVALID_ARG, "a_q is required by the GEMV path");
   cudaError_t e = (use == EGOPQ_PATH_GEMV) ? launch_gemv(a, st) : launch_tc_gemm(a, st);
   if (e == cudaErrorNotSupported)
     return fail(EGOPQ_ERR_UNSUPPORTED_SHAPE, "shape not supported by the requested path");
@@ -208,9 +210,11 @@ int egopq_quant_act_i8(const uint16_t* x_bf16, int64_t M, int64_t K, int group, 
   if (group != 128) return fail(EGOPQ_ERR_UNSUPPORTED_SHAPE, "group must be 128 (got %d)", group);
   if (K % 128) return fail(EGOPQ_ERR_UNSUPPORTED_SHAPE, "K must be a multiple of 128");
   if (M == 0) return EGOPQ_OK;
-  int rc = check_ptrs(4, "x_bf16", x_bf16, "a_q", a_q, "a_s", a_s, "a_gsum", a_gsum);
+  int rc = check_ptrs(3, "x_bf16", x_bf16, "a_s", a_s, "a_gsum", a_gsum);
   if (rc) return rc;
+  if (!a_q && !a_tc) return fail(EGOPQ_ERR_INVALID_ARG, "a_q and a_tc are both NULL");
   if (a_tc && !aligned16(a_tc)) return fail(EGOPQ_ERR_MISALIGNED, "a_tc is not 16-byte aligned");
+  if (a_q && !aligned16(a_q)) return fail(EGOPQ_ERR_MISALIGNED, "a_q is not 16-byte aligned");
   if ((rc = check_arch())) return rc;
   cudaError_t e = launch_quant_act(x_bf16, M, K, a_q, a_s, a_gsum, a_tc, (cudaStream_t)stream);
   return e == cudaSuccess ? EGOPQ_OK : cuda_fail(e, "quant_act launch");
@@ -222,9 +226,10 @@ int egopq_w4a8_gemm_ex(const int8_t* a_q, const void* a_tc, const float* a_s,
   int rc = check_w4_shape(M, N, K, group);
   if (rc) return rc;
   if (M == 0) return EGOPQ_OK;
-  rc = check_ptrs(5, "a_q", a_q, "a_s", a_s, "a_gsum", a_gsum, "packed", packed, "y_bf16", y_bf16);
+  rc = check_ptrs(4, "a_s", a_s, "a_gsum", a_gsum, "packed", packed, "y_bf16", y_bf16);
   if (rc) return rc;
   if (a_tc && !aligned16(a_tc)) return fail(EGOPQ_ERR_MISALIGNED, "a_tc is not 16-byte aligned");
+  if (a_q && !aligned16(a_q)) return fail(EGOPQ_ERR_MISALIGNED, "a_q is not 16-byte aligned");
   GemmArgs a{};
   a.variant = kW4A8;
   a.M = M;
@@ -289,9 +294,10 @@ int egopq_w4a8_gemm_grouped(const int8_t* a_q, const void* a_tc, const float* a_
   if (rc) return rc;
   if ((rc = check_w4_shape(M, n_total, K, group))) return rc;
   if (M == 0) return EGOPQ_OK;
-  rc = check_ptrs(3, "a_q", a_q, "a_s", a_s, "a_gsum", a_gsum);
+  rc = check_ptrs(2, "a_s", a_s, "a_gsum", a_gsum);
   if (rc) return rc;
   if (a_tc && !aligned16(a_tc)) return fail(EGOPQ_ERR_MISALIGNED, "a_tc is not 16-byte aligned");
+  if (a_q && !aligned16(a_q)) return fail(EGOPQ_ERR_MISALIGNED, "a_q is not 16-byte aligned");
   GemmArgs a{};
   a.variant = kW4A8;
   a.M = M;
@@ -316,19 +322,18 @@ int egopq_w4a8_gemm(const int8_t* a_q, const void* a_tc, const float* a_s,
 }
 
 // Workspace of the one-call linear: the quantized activations it stages
-// between its two kernels, in 256-byte aligned regions -- codes int8 [M][K],
-// scales fp32 [M], group sums int32 [M][G], and on the tensor-core path the
-// fp16 codes [M][K] its TMA loads read.
+// between its two kernels, in 256-byte aligned regions -- scales fp32 [M],
+// group sums int32 [M][G], then the codes in the form the path reads: int8
+// [M][K] for the GEMV, the 2*M*K-byte operand form for the tensor cores.
 static size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 static int linear_path(int64_t M, int path) { return auto_path(M, kW4A8, path); }
 
 size_t egopq_w4a8_linear_workspace_bytes(int64_t M, int64_t K, int group, int path) {
   if (M <= 0 || K <= 0 || group != 128 || K % 128 || M >= kMaxDim || K >= kMaxDim) return 0;
   if (path != EGOPQ_PATH_AUTO && path != EGOPQ_PATH_GEMV && path != EGOPQ_PATH_TC) return 0;
-  size_t bytes = align256((size_t)(M * K)) + align256((size_t)(4 * M)) +
-                 align256((size_t)(4 * M * (K / 128)));
-  if (linear_path(M, path) == EGOPQ_PATH_TC) bytes += align256((size_t)(2 * M * K));
-  return bytes;
+  const bool tc = linear_path(M, path) == EGOPQ_PATH_TC;
+  return align256((size_t)(4 * M)) + align256((size_t)(4 * M * (K / 128))) +
+         align256((size_t)((tc ? 2 : 1) * M * K));
 }
 
 }  // extern "C"
@@ -342,12 +347,11 @@ int set_last_error(int code, const char* msg) { return fail(code, "%s", msg); }
 // `segs` (N output rows in all) on `use`.
 int run_linear_segs(const uint16_t* x_bf16, const SegTable& segs, int64_t M, int64_t N, int64_t K,
                     uint8_t* ws, int use, cudaStream_t st) {
-  int8_t* a_q = reinterpret_cast<int8_t*>(ws);
-  float* a_s = reinterpret_cast<float*>(ws + align256((size_t)(M * K)));
-  int32_t* asum = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(a_s) + align256((size_t)(4 * M)));
-  void* a_tc = nullptr;
-  if (use == EGOPQ_PATH_TC)
-    a_tc = reinterpret_cast<uint8_t*>(asum) + align256((size_t)(4 * M * (K / 128)));
+  float* a_s = reinterpret_cast<float*>(ws);
+  int32_t* asum = reinterpret_cast<int32_t*>(ws + align256((size_t)(4 * M)));
+  uint8_t* codes = reinterpret_cast<uint8_t*>(asum) + align256((size_t)(4 * M * (K / 128)));
+  int8_t* a_q = use == EGOPQ_PATH_TC ? nullptr : reinterpret_cast<int8_t*>(codes);
+  void* a_tc = use == EGOPQ_PATH_TC ? codes : nullptr;
   cudaError_t e = launch_quant_act(x_bf16, M, K, a_q, a_s, asum, a_tc, st);
   if (e != cudaSuccess) return cuda_fail(e, "quant_act launch");
   GemmArgs a{};
@@ -433,9 +437,10 @@ int egopq_w4a8_group_partials(const int8_t* a_q, const void* a_tc, const int32_t
   int rc = check_w4_shape(M, N, K, group);
   if (rc) return rc;
   if (M == 0) return EGOPQ_OK;
-  rc = check_ptrs(4, "a_q", a_q, "a_gsum", a_gsum, "packed", packed, "Q", Q);
+  rc = check_ptrs(3, "a_gsum", a_gsum, "packed", packed, "Q", Q);
   if (rc) return rc;
   if (a_tc && !aligned16(a_tc)) return fail(EGOPQ_ERR_MISALIGNED, "a_tc is not 16-byte aligned");
+  if (a_q && !aligned16(a_q)) return fail(EGOPQ_ERR_MISALIGNED, "a_q is not 16-byte aligned");
   GemmArgs a{};
   a.variant = kW4A8;
   a.M = M;
@@ -507,9 +512,10 @@ int egopq_w8a8_gemm_ex(const int8_t* a_q, const void* a_tc, const float* a_s, co
   int rc = check_w4_shape(M, N, K, 128);
   if (rc) return rc;
   if (M == 0) return EGOPQ_OK;
-  rc = check_ptrs(5, "a_q", a_q, "a_s", a_s, "w_q", w_q, "scale_f16", scale_f16, "y_bf16", y_bf16);
+  rc = check_ptrs(4, "a_s", a_s, "w_q", w_q, "scale_f16", scale_f16, "y_bf16", y_bf16);
   if (rc) return rc;
   if (a_tc && !aligned16(a_tc)) return fail(EGOPQ_ERR_MISALIGNED, "a_tc is not 16-byte aligned");
+  if (a_q && !aligned16(a_q)) return fail(EGOPQ_ERR_MISALIGNED, "a_q is not 16-byte aligned");
   GemmArgs a{};
   a.variant = kW8A8;
   a.M = M;

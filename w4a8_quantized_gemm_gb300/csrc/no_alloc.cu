@@ -100,7 +100,7 @@ extern "C" int egopq_w4a8_linear_noalloc(const uint16_t* x_bf16, const void* pac
   const size_t need = egopq_w4a8_linear_workspace_bytes(M, K, group, path);
   if (need > kStaticScratchBytes)
     return set_last_error(EGOPQ_ERR_UNSUPPORTED_SHAPE,
-                          "egopq_w4a8_linear_noalloc: the staged activations (about 3*M*K bytes "
+                          "egopq_w4a8_linear_noalloc: the staged activations (about 2*M*K bytes "
                           "on the tensor-core path, M*K on the GEMV path) exceed its 16 MiB "
                           "static scratch; use egopq_w4a8_linear with a workspace");
   if (const int rc = egopq::check_arch()) return rc;

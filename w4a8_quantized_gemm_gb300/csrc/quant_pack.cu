@@ -36,10 +36,12 @@ __device__ __forceinline__ uint32_t e4m3_exact(int v) {
 // Writes the tensor-core operand form of the 8 codes q[0..7] (K = 8*vec ..
 // 8*vec+7) of token m, as documented for a_tc in include/egopq.h: with
 // fp8 = true two e4m3 planes [2][M][K] (high part a >> 4 in [-8, 7], low
-// part a & 15, a = 16 * high + low) with each 8-run in the packed weights' nibble order (even offsets,
-// then odd); otherwise fp16 [M][K].
+// part a & 15, a = 16 * high + low) with each 8-run in the packed weights'
+// nibble order (even offsets, then odd); otherwise fp16 [M][K] (the codes
+// qf as fp32 integers, exact in fp16).
 __device__ __forceinline__ void store_tc_operand(void* a_tc, bool fp8, int64_t M, int64_t K,
-                                                 int64_t m, int64_t vec, const int (&q)[8]) {
+                                                 int64_t m, int64_t vec, const int (&q)[8],
+                                                 const float (&qf)[8]) {
   if (fp8) {
     constexpr int kOrder[8] = {0, 2, 4, 6, 1, 3, 5, 7};
     uint32_t hi[2] = {0, 0}, lo[2] = {0, 0};
@@ -56,14 +58,104 @@ __device__ __forceinline__ void store_tc_operand(void* a_tc, bool fp8, int64_t M
     uint32_t h[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      __half2 hv = __halves2half2(__int2half_rn(q[2 * i]), __int2half_rn(q[2 * i + 1]));
-      h[i] = *reinterpret_cast<uint32_t*>(&hv);
+      const __half2 hv = __floats2half2_rn(qf[2 * i], qf[2 * i + 1]);
+      h[i] = *reinterpret_cast<const uint32_t*>(&hv);
     }
     reinterpret_cast<uint4*>(static_cast<uint16_t*>(a_tc) + m * K)[vec] =
         make_uint4(h[0], h[1], h[2], h[3]);
   }
 }
 
+// Reciprocal of the row scale s for quant_code's product form, or NaN where
+// that form is not used (s zero, below 2^-100, above 2^126 or not finite): a
+// NaN product sends every element of the row to the IEEE quotient.
+__device__ __forceinline__ float quant_recip(float s) {
+  return (s >= 0x1p-100f && s <= 0x1p+126f) ? __frcp_rn(s) : __int_as_float(0x7fc00000);
+}
+
+// clamp(round_half_even(fp32 quotient x / s), -127, 127) as an fp32 integer,
+// equal to __float2int_rn(__fdiv_rn(x, s)) clamped. With inv the correctly
+// rounded 1/s, r = fl(x * inv) is within |x / s| * 2^-23 of the exact quotient
+// q (two roundings of at most 2^-24 relative), and fl(q) within |q| * 2^-24 of
+// q; as |q| <= 127 * (1 + 2^-23), r and fl(q) lie within 2.3e-5 of each other.
+// So they round to the same integer unless r lies within that distance of a
+// half-integer; where r lies within 1e-4 of one (|r - rint(r)| >= 0.4999, or r
+// NaN) the IEEE quotient decides. On the product's side |r| < 127.5, so its
+// integer needs no clamp.
+__device__ __forceinline__ float quant_code(float x, float s, float inv) {
+  const float r = x * inv;
+  const float rf = rintf(r);
+  if (fabsf(r - rf) < 0.4999f) return rf;
+  return (float)max(-127, min(127, __float2int_rn(__fdiv_rn(x, s))));
+}
+
+// Quantizes the 8 bf16 values of one 16-byte vector v (K = 8*idx .. 8*idx+7
+// of token m, scale s, inv = quant_recip(s)) and writes their codes: to a_q
+// when given, to the tensor-core operand form when a_tc is given, and, summed
+// over the 16 vectors of a 128-wide group that one half-warp holds, to a_gsum.
+// All 16 lanes of the calling half-warp take part.
+__device__ __forceinline__ void quant_store_vec(const uint4& v, float s, float inv, bool zero_row,
+                                                int8_t* a_q, int32_t* a_gsum, void* a_tc,
+                                                bool tc_fp8, int64_t M, int64_t K, int64_t m,
+                                                int64_t idx) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  float qf[8];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    qf[2 * j] = zero_row ? 0.f : quant_code(__uint_as_float(w[j] << 16), s, inv);
+    qf[2 * j + 1] = zero_row ? 0.f : quant_code(__uint_as_float(w[j] & 0xFFFF0000u), s, inv);
+  }
+  int q[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) q[j] = (int)qf[j];  // exact: integers in [-127, 127]
+  if (a_q) {
+    uint2 packed;
+    packed.x = (uint32_t)(q[0] & 0xFF) | ((uint32_t)(q[1] & 0xFF) << 8) |
+               ((uint32_t)(q[2] & 0xFF) << 16) | ((uint32_t)(q[3] & 0xFF) << 24);
+    packed.y = (uint32_t)(q[4] & 0xFF) | ((uint32_t)(q[5] & 0xFF) << 8) |
+               ((uint32_t)(q[6] & 0xFF) << 16) | ((uint32_t)(q[7] & 0xFF) << 24);
+    reinterpret_cast<uint2*>(a_q + m * K)[idx] = packed;
+  }
+  if (a_tc) store_tc_operand(a_tc, tc_fp8, M, K, m, idx, q, qf);
+  // the group sum in fp32: |sum| <= 128 * 127, exact
+  float sum = ((qf[0] + qf[1]) + (qf[2] + qf[3])) + ((qf[4] + qf[5]) + (qf[6] + qf[7]));
+  const unsigned half_mask = 0xFFFFu << (threadIdx.x & 16);
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) sum += __shfl_xor_sync(half_mask, sum, o);
+  if ((threadIdx.x & 15) == 0) a_gsum[m * (K / 128) + idx / 16] = (int32_t)sum;
+}
+
+// max |x| over the 8 bf16 values of v folded into acc, a bf16 pair of running
+// maxima (max is exact in bf16; a NaN operand gives the other, as fmaxf)
+__device__ __forceinline__ __nv_bfloat162 vec_absmax(const uint4& v, __nv_bfloat162 acc) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t a = w[j] & 0x7FFF7FFFu;  // |x| of both halves
+    acc = __hmax2(acc, *reinterpret_cast<const __nv_bfloat162*>(&a));
+  }
+  return acc;
+}
+
+__device__ __forceinline__ float absmax_f32(__nv_bfloat162 acc) {
+  return fmaxf(__low2float(acc), __high2float(acc));
+}
+
+// Maximum of v over the block's threads (T of them); every thread gets it.
+template <int T>
+__device__ __forceinline__ float block_max(float v, float* warp_max) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = v;
+  __syncthreads();
+  v = warp_max[0];
+#pragma unroll
+  for (int i = 1; i < T / 32; ++i) v = fmaxf(v, warp_max[i]);
+  return v;
+}
+
+// Rows of any length: one CTA per token row, two passes over x (the row's
+// absmax, then the codes; the second pass reads the row from L2).
 __global__ void __launch_bounds__(kQuantThreads)
 quant_act_kernel(const uint16_t* __restrict__ x, int64_t K, int8_t* __restrict__ a_q,
                  float* __restrict__ a_s, int32_t* __restrict__ a_gsum,
@@ -74,69 +166,30 @@ quant_act_kernel(const uint16_t* __restrict__ x, int64_t K, int8_t* __restrict__
   const uint4* xr = reinterpret_cast<const uint4*>(x + m * K);
   const int64_t nvec = K / 8;  // 8 bf16 per 16-byte vector; K % 128 == 0
   __shared__ float warp_max[kQuantThreads / 32];
-
-  float amax = 0.f;
-  for (int64_t v = threadIdx.x; v < nvec; v += kQuantThreads) {
-    uint4 p = __ldg(xr + v);
-    uint32_t w[4] = {p.x, p.y, p.z, p.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      amax = fmaxf(amax, fabsf(__uint_as_float(w[i] << 16)));
-      amax = fmaxf(amax, fabsf(__uint_as_float(w[i] & 0xFFFF0000u)));
-    }
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-  if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = amax;
-  __syncthreads();
-  amax = warp_max[0];
-#pragma unroll
-  for (int i = 1; i < kQuantThreads / 32; ++i) amax = fmaxf(amax, warp_max[i]);
-
+  __nv_bfloat162 acc = __float2bfloat162_rn(0.f);
+  for (int64_t v = threadIdx.x; v < nvec; v += kQuantThreads) acc = vec_absmax(__ldg(xr + v), acc);
+  const float amax = block_max<kQuantThreads>(absmax_f32(acc), warp_max);
   const float s = __fdiv_rn(amax, 127.0f);
   if (threadIdx.x == 0) a_s[m] = s;
-  const bool zero_row = (amax == 0.f);
-
-  for (int64_t v = threadIdx.x; v < nvec; v += kQuantThreads) {
-    uint4 p = __ldg(xr + v);
-    uint32_t w[4] = {p.x, p.y, p.z, p.w};
-    int q[8];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      float lo = __uint_as_float(w[i] << 16);
-      float hi = __uint_as_float(w[i] & 0xFFFF0000u);
-      int ql = zero_row ? 0 : __float2int_rn(__fdiv_rn(lo, s));
-      int qh = zero_row ? 0 : __float2int_rn(__fdiv_rn(hi, s));
-      q[2 * i] = max(-127, min(127, ql));
-      q[2 * i + 1] = max(-127, min(127, qh));
-    }
-    uint2 packed;
-    packed.x = (uint32_t)(q[0] & 0xFF) | ((uint32_t)(q[1] & 0xFF) << 8) |
-               ((uint32_t)(q[2] & 0xFF) << 16) | ((uint32_t)(q[3] & 0xFF) << 24);
-    packed.y = (uint32_t)(q[4] & 0xFF) | ((uint32_t)(q[5] & 0xFF) << 8) |
-               ((uint32_t)(q[6] & 0xFF) << 16) | ((uint32_t)(q[7] & 0xFF) << 24);
-    reinterpret_cast<uint2*>(a_q + m * K)[v] = packed;
-    if (a_tc) store_tc_operand(a_tc, tc_fp8, gridDim.x, K, m, v, q);
-    // 16 consecutive vectors make one 128-wide group; kQuantThreads % 16 == 0
-    // K % 128 == 0, so the 16 lanes of a half-warp are all inside the loop or
-    // all outside it; reduce within the half-warp only.
-    int sum = q[0] + q[1] + q[2] + q[3] + q[4] + q[5] + q[6] + q[7];
-    const unsigned half_mask = 0xFFFFu << (threadIdx.x & 16);
-#pragma unroll
-    for (int o = 8; o > 0; o >>= 1) sum += __shfl_xor_sync(half_mask, sum, o);
-    if ((threadIdx.x & 15) == 0) a_gsum[m * (K / 128) + v / 16] = sum;
-  }
+  const float inv = quant_recip(s);
+  // 16 consecutive vectors make one 128-wide group; kQuantThreads % 16 == 0
+  // and nvec % 16 == 0, so the 16 lanes of a half-warp are all inside the
+  // loop or all outside it
+  for (int64_t v = threadIdx.x; v < nvec; v += kQuantThreads)
+    quant_store_vec(__ldg(xr + v), s, inv, amax == 0.f, a_q, a_gsum, a_tc, tc_fp8, gridDim.x, K,
+                    m, v);
 }
 
-// Single-pass variant: the whole row stays in registers (up to kRegVec 16-byte
-// vectors per thread, K <= kQuantRegThreads * kRegVec * 8), so x is read from
-// memory once. It waits for the preceding kernel only when the launch carried a
-// programmatic dependency.
-constexpr int kQuantRegThreads = 512;
-constexpr int kRegVec = 8;
+// Few tokens, rows up to kRowThreads * kRowVec * 8 values: one 512-thread CTA
+// a row holding the whole row in registers (up to kRowVec 16-byte vectors a
+// thread, every load issued before the first is used), so x is read once and
+// the row's latency is short. It waits for the preceding kernel only when the
+// launch carried a programmatic dependency.
+constexpr int kRowThreads = 512;
+constexpr int kRowVec = 8;
 
-__global__ void __launch_bounds__(kQuantRegThreads)
-quant_act_reg_kernel(const uint16_t* __restrict__ x, int64_t K, int8_t* __restrict__ a_q,
+__global__ void __launch_bounds__(kRowThreads, 1)
+quant_act_row_kernel(const uint16_t* __restrict__ x, int64_t K, int8_t* __restrict__ a_q,
                      float* __restrict__ a_s, int32_t* __restrict__ a_gsum,
                      void* __restrict__ a_tc, bool tc_fp8) {
   griddep_wait();
@@ -144,61 +197,91 @@ quant_act_reg_kernel(const uint16_t* __restrict__ x, int64_t K, int8_t* __restri
   const int64_t m = blockIdx.x;
   const uint4* xr = reinterpret_cast<const uint4*>(x + m * K);
   const int nvec = (int)(K / 8);
-  __shared__ float warp_max[kQuantRegThreads / 32];
-  uint4 v[kRegVec];
-  float amax = 0.f;
+  __shared__ float warp_max[kRowThreads / 32];
+  uint4 v[kRowVec];
 #pragma unroll
-  for (int i = 0; i < kRegVec; ++i) {
-    const int idx = threadIdx.x + i * kQuantRegThreads;
+  for (int i = 0; i < kRowVec; ++i) {
+    const int idx = threadIdx.x + i * kRowThreads;
     v[i] = idx < nvec ? __ldg(xr + idx) : make_uint4(0, 0, 0, 0);
-    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      amax = fmaxf(amax, fabsf(__uint_as_float(w[j] << 16)));
-      amax = fmaxf(amax, fabsf(__uint_as_float(w[j] & 0xFFFF0000u)));
-    }
   }
+  __nv_bfloat162 acc = __float2bfloat162_rn(0.f);
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-  if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = amax;
-  __syncthreads();
-  amax = warp_max[0];
-#pragma unroll
-  for (int i = 1; i < kQuantRegThreads / 32; ++i) amax = fmaxf(amax, warp_max[i]);
+  for (int i = 0; i < kRowVec; ++i) acc = vec_absmax(v[i], acc);
+  const float amax = block_max<kRowThreads>(absmax_f32(acc), warp_max);
   const float s = __fdiv_rn(amax, 127.0f);
   if (threadIdx.x == 0) a_s[m] = s;
-  const bool zero_row = (amax == 0.f);
+  const float inv = quant_recip(s);
 #pragma unroll
-  for (int i = 0; i < kRegVec; ++i) {
-    const int idx = threadIdx.x + i * kQuantRegThreads;
+  for (int i = 0; i < kRowVec; ++i) {
+    const int idx = threadIdx.x + i * kRowThreads;
     if (idx >= nvec) break;  // whole half-warps leave together (nvec % 16 == 0)
-    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-    int q[8];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float lo = __uint_as_float(w[j] << 16);
-      const float hi = __uint_as_float(w[j] & 0xFFFF0000u);
-      q[2 * j] = zero_row ? 0 : max(-127, min(127, __float2int_rn(__fdiv_rn(lo, s))));
-      q[2 * j + 1] = zero_row ? 0 : max(-127, min(127, __float2int_rn(__fdiv_rn(hi, s))));
+    quant_store_vec(v[i], s, inv, amax == 0.f, a_q, a_gsum, a_tc, tc_fp8, gridDim.x, K, m, idx);
+  }
+}
+
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Many tokens, rows up to kStreamMaxK values: persistent CTAs walk the rows
+// m = blockIdx.x, blockIdx.x + gridDim.x, ...; each row is staged whole in
+// shared memory by asynchronous copies while the previous one is quantized
+// (two buffers), so x streams from HBM once with a row always in flight, and
+// the row's absmax and codes are read from shared memory. T = 256 threads,
+// 512 for rows longer than 8192 (fewer CTAs fit beside their buffers).
+constexpr int64_t kStreamMaxK = 32768;
+
+template <int T>
+__global__ void __launch_bounds__(T)
+quant_act_stream_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K,
+                        int8_t* __restrict__ a_q, float* __restrict__ a_s,
+                        int32_t* __restrict__ a_gsum, void* __restrict__ a_tc, bool tc_fp8) {
+  extern __shared__ __align__(16) uint4 rows[];  // [2][K / 8]
+  __shared__ float warp_max[T / 32];
+  griddep_wait();
+  if (threadIdx.x == 0) griddep_launch_dependents();
+  const int nvec = (int)(K / 8);
+  auto stage = [&](int64_t m, int buf) {
+    const uint4* src = reinterpret_cast<const uint4*>(x + m * K);
+    uint4* dst = rows + buf * nvec;
+    for (int i = threadIdx.x; i < nvec; i += T) cp_async16(dst + i, src + i);
+    cp_async_commit();
+  };
+  int64_t m = blockIdx.x;
+  if (m < M) stage(m, 0);
+  for (int j = 0; m < M; ++j, m += gridDim.x) {
+    if (m + gridDim.x < M) {
+      stage(m + gridDim.x, (j + 1) & 1);
+      cp_async_wait<1>();  // this thread's copies of row m have landed
+    } else {
+      cp_async_wait<0>();
     }
-    uint2 packed;
-    packed.x = (uint32_t)(q[0] & 0xFF) | ((uint32_t)(q[1] & 0xFF) << 8) |
-               ((uint32_t)(q[2] & 0xFF) << 16) | ((uint32_t)(q[3] & 0xFF) << 24);
-    packed.y = (uint32_t)(q[4] & 0xFF) | ((uint32_t)(q[5] & 0xFF) << 8) |
-               ((uint32_t)(q[6] & 0xFF) << 16) | ((uint32_t)(q[7] & 0xFF) << 24);
-    reinterpret_cast<uint2*>(a_q + m * K)[idx] = packed;
-    if (a_tc) store_tc_operand(a_tc, tc_fp8, gridDim.x, K, m, idx, q);
-    int sum = q[0] + q[1] + q[2] + q[3] + q[4] + q[5] + q[6] + q[7];
-    const unsigned half_mask = 0xFFFFu << (threadIdx.x & 16);
-#pragma unroll
-    for (int o = 8; o > 0; o >>= 1) sum += __shfl_xor_sync(half_mask, sum, o);
-    if ((threadIdx.x & 15) == 0) a_gsum[m * (K / 128) + idx / 16] = sum;
+    __syncthreads();  // ... and every thread's
+    const uint4* row = rows + (j & 1) * nvec;
+    __nv_bfloat162 acc = __float2bfloat162_rn(0.f);
+    for (int i = threadIdx.x; i < nvec; i += T) acc = vec_absmax(row[i], acc);
+    const float amax = block_max<T>(absmax_f32(acc), warp_max);
+    const float s = __fdiv_rn(amax, 127.0f);
+    if (threadIdx.x == 0) a_s[m] = s;
+    const float inv = quant_recip(s);
+    // nvec % 16 == 0 and T % 16 == 0: whole half-warps iterate
+    for (int i = threadIdx.x; i < nvec; i += T)
+      quant_store_vec(row[i], s, inv, amax == 0.f, a_q, a_gsum, a_tc, tc_fp8, M, K, m, i);
+    __syncthreads();  // row buffer and warp_max are reused by the next row
   }
 }
 
 // Long rows for few tokens: one token's row is split over a cluster of CTAs
 // (whole 128-wide groups each, at most kSplitVec 16-byte vectors per thread),
-// so that the per-element divisions spread over several SMs; the CTAs combine
+// so that the per-element work spreads over several SMs; the CTAs combine
 // their partial absmax through distributed shared memory. Same arithmetic as
 // the kernels above, element for element.
 constexpr int kSplitThreads = 256;
@@ -220,60 +303,28 @@ quant_act_split_kernel(const uint16_t* __restrict__ x, int64_t M, int64_t K,
   __shared__ float warp_max[kSplitThreads / 32];
   __shared__ float cta_max;
   uint4 v[kSplitVec];
-  float amax = 0.f;
 #pragma unroll
   for (int i = 0; i < kSplitVec; ++i) {
     const int idx = v0 + threadIdx.x + i * kSplitThreads;
     v[i] = idx < v1 ? __ldg(xr + idx) : make_uint4(0, 0, 0, 0);
-    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      amax = fmaxf(amax, fabsf(__uint_as_float(w[j] << 16)));
-      amax = fmaxf(amax, fabsf(__uint_as_float(w[j] & 0xFFFF0000u)));
-    }
   }
+  __nv_bfloat162 acc = __float2bfloat162_rn(0.f);
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-  if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = amax;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float a = warp_max[0];
-#pragma unroll
-    for (int i = 1; i < kSplitThreads / 32; ++i) a = fmaxf(a, warp_max[i]);
-    cta_max = a;
-  }
+  for (int i = 0; i < kSplitVec; ++i) acc = vec_absmax(v[i], acc);
+  if (const float part = block_max<kSplitThreads>(absmax_f32(acc), warp_max); threadIdx.x == 0)
+    cta_max = part;
   cluster_sync_all();  // every CTA's partial maximum is in its shared memory
-  amax = 0.f;
+  float amax = 0.f;
   for (int r = 0; r < C; ++r) amax = fmaxf(amax, ld_dsmem_f32(map_to_rank(smem_u32(&cta_max), r)));
   cluster_sync_all();  // no CTA leaves while another still reads its partial
   const float s = __fdiv_rn(amax, 127.0f);
   if (rank == 0 && threadIdx.x == 0) a_s[m] = s;
-  const bool zero_row = (amax == 0.f);
+  const float inv = quant_recip(s);
 #pragma unroll
   for (int i = 0; i < kSplitVec; ++i) {
     const int idx = v0 + threadIdx.x + i * kSplitThreads;
     if (idx >= v1) break;  // whole half-warps leave together (v0, v1 multiples of 16)
-    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-    int q[8];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float lo = __uint_as_float(w[j] << 16);
-      const float hi = __uint_as_float(w[j] & 0xFFFF0000u);
-      q[2 * j] = zero_row ? 0 : max(-127, min(127, __float2int_rn(__fdiv_rn(lo, s))));
-      q[2 * j + 1] = zero_row ? 0 : max(-127, min(127, __float2int_rn(__fdiv_rn(hi, s))));
-    }
-    uint2 packed;
-    packed.x = (uint32_t)(q[0] & 0xFF) | ((uint32_t)(q[1] & 0xFF) << 8) |
-               ((uint32_t)(q[2] & 0xFF) << 16) | ((uint32_t)(q[3] & 0xFF) << 24);
-    packed.y = (uint32_t)(q[4] & 0xFF) | ((uint32_t)(q[5] & 0xFF) << 8) |
-               ((uint32_t)(q[6] & 0xFF) << 16) | ((uint32_t)(q[7] & 0xFF) << 24);
-    reinterpret_cast<uint2*>(a_q + m * K)[idx] = packed;
-    if (a_tc) store_tc_operand(a_tc, tc_fp8, M, K, m, idx, q);
-    int sum = q[0] + q[1] + q[2] + q[3] + q[4] + q[5] + q[6] + q[7];
-    const unsigned half_mask = 0xFFFFu << (threadIdx.x & 16);
-#pragma unroll
-    for (int o = 8; o > 0; o >>= 1) sum += __shfl_xor_sync(half_mask, sum, o);
-    if ((threadIdx.x & 15) == 0) a_gsum[m * G + idx / 16] = sum;
+    quant_store_vec(v[i], s, inv, amax == 0.f, a_q, a_gsum, a_tc, tc_fp8, M, K, m, idx);
   }
 }
 
@@ -441,35 +492,53 @@ static unsigned grid_for(int64_t work, int threads) {
 
 cudaError_t launch_quant_act(const uint16_t* x, int64_t M, int64_t K, int8_t* a_q, float* a_s,
                              int32_t* a_gsum, void* a_tc, cudaStream_t st) {
-  // few tokens: one wide CTA per row, one read of x (latency); many tokens:
-  // narrower CTAs, several resident per SM (throughput)
-  const bool reg = (M <= 64 && K <= (int64_t)kQuantRegThreads * kRegVec * 8);
+  const int64_t nvec = K / 8;
+  const bool tc_fp8 = M <= kTcFp8MaxM;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)M, 1, 1);
-  cfg.blockDim = dim3(reg ? kQuantRegThreads : kQuantThreads, 1, 1);
+  cfg.blockDim = dim3(kQuantThreads, 1, 1);
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const bool tc_fp8 = M <= kTcFp8MaxM;
-  // rows longer than 1024 vectors for few tokens: split over a cluster of up
-  // to 8 CTAs, each holding whole groups and at most kSplitMaxVec vectors
-  const int64_t nvec = K / 8;
-  if (M <= 64 && nvec > 1024) {
+  if (M > 64) {
+    // many tokens: persistent CTAs streaming rows through shared memory, as
+    // many as are resident at once with two row buffers each
+    if (K <= kStreamMaxK) {
+      const bool wide = K > 8192;
+      auto kern = wide ? quant_act_stream_kernel<512> : quant_act_stream_kernel<256>;
+      const int threads = wide ? 512 : 256;
+      const size_t smem = (size_t)(2 * K * 2);
+      static SmemOptIn opt_in[2];
+      if (cudaError_t e = opt_in[wide].ensure(kern, smem); e != cudaSuccess) return e;
+      int per_sm = 0;
+      if (cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
+          e != cudaSuccess)
+        return e;
+      const int sms = device_sm_count();
+      if (per_sm < 1 || sms < 1) return cudaErrorInvalidConfiguration;
+      const int64_t ctas = (int64_t)sms * per_sm;
+      cfg.gridDim = dim3((unsigned)(M < ctas ? M : ctas), 1, 1);
+      cfg.blockDim = dim3(threads, 1, 1);
+      cfg.dynamicSmemBytes = smem;
+      return cudaLaunchKernelEx(&cfg, kern, x, M, K, a_q, a_s, a_gsum, a_tc, tc_fp8);
+    }
+    return cudaLaunchKernelEx(&cfg, quant_act_kernel, x, K, a_q, a_s, a_gsum, a_tc, tc_fp8);
+  }
+  // few tokens: rows longer than 1024 vectors split over a cluster of up to 8
+  // CTAs, each holding whole groups and at most kSplitMaxVec vectors
+  if (nvec > 1024) {
     const int64_t G = K / 128;
     int split = (int)((nvec + kSplitMaxVec - 1) / kSplitMaxVec);
     if (split < 2) split = 2;
     // each CTA's share, ceil(G / split) groups, must fit its registers
     if (split <= 8 && (G + split - 1) / split * 16 <= kSplitMaxVec) {
-      cudaLaunchAttribute cattr[2];
-      cattr[0] = attr[0];
-      cattr[1].id = cudaLaunchAttributeClusterDimension;
-      cattr[1].val.clusterDim.x = (unsigned)split;
-      cattr[1].val.clusterDim.y = 1;
-      cattr[1].val.clusterDim.z = 1;
-      cfg.attrs = cattr;
+      attr[1].id = cudaLaunchAttributeClusterDimension;
+      attr[1].val.clusterDim.x = (unsigned)split;
+      attr[1].val.clusterDim.y = 1;
+      attr[1].val.clusterDim.z = 1;
       cfg.numAttrs = 2;
       cfg.gridDim = dim3((unsigned)(M * split), 1, 1);
       cfg.blockDim = dim3(kSplitThreads, 1, 1);
@@ -477,8 +546,10 @@ cudaError_t launch_quant_act(const uint16_t* x, int64_t M, int64_t K, int8_t* a_
                                 tc_fp8);
     }
   }
-  if (reg)
-    return cudaLaunchKernelEx(&cfg, quant_act_reg_kernel, x, K, a_q, a_s, a_gsum, a_tc, tc_fp8);
+  if (nvec <= (int64_t)kRowThreads * kRowVec) {
+    cfg.blockDim = dim3(kRowThreads, 1, 1);
+    return cudaLaunchKernelEx(&cfg, quant_act_row_kernel, x, K, a_q, a_s, a_gsum, a_tc, tc_fp8);
+  }
   return cudaLaunchKernelEx(&cfg, quant_act_kernel, x, K, a_q, a_s, a_gsum, a_tc, tc_fp8);
 }
 
