@@ -82,6 +82,9 @@ def test_auto_path_and_operand_queries(lib):
         [16, 16, 32, 64]
     assert lib.egopq_tc_token_tile(256, 256, 512, W4A8) == 128     # same tiles at either width
     assert lib.egopq_tc_token_tile(4096, 152064, 3584, W4A8) == 192
+    # the down projection at 2048 tokens: 192-token tiles leave a short last
+    # round, which a split second launch takes (cheaper than 128-token tiles)
+    assert lib.egopq_tc_token_tile(2048, 3584, 18944, W4A8) == 192
     assert lib.egopq_tc_token_tile(4096, 3584, 3584, W8A16) == 128
     assert lib.egopq_tc_token_tile(64, 3584, 3584, W8A8) == -2      # GEMV only up to 64
     assert lib.egopq_tc_token_tile(65, 3584, 3584, W8A8) == 128

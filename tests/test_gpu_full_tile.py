@@ -68,6 +68,28 @@ def test_w4a8_full_tile_output(case):
     check_bf16_output(to_host_bits(y), y_ref, f"192-token tiles {case} M={M} N={N} K={K}")
 
 
+@pytest.mark.parametrize("M", [384, 256])    # 192-token tiles; 128-token tiles
+def test_w4a8_split_tail_output(M):
+    """Persistent grids whose last round would hold a few tiles of a long K:
+    those tiles run as a second launch with K split over clusters (each rank
+    reducing a slice of the tile's columns). 2 m-tiles x (SMs + 2 or + 3)
+    n-tiles, 64 groups each: two full rounds, then the last n-tiles (every
+    m-tile) of the banded order split 8 ways; compared on the first, some
+    middle and the last 384 output columns (the split tiles)."""
+    sms = _sms()
+    N, K = 128 * (sms + (2 if M == 384 else 3)), 8192
+    assert eg.tc_token_tile(M, N, K) == (192 if M == 384 else 128)
+    x, w = w4_case(17, M, N, K)
+    packed = eg.pack_w4(*_dev_weights(w))
+    y = eg.w4a8_linear(to_dev(x, torch.bfloat16), packed, N, path=eg.PATH_TC)
+    rng = np.random.default_rng(M)
+    cols = np.unique(np.concatenate([np.arange(128), rng.choice(N, 256, replace=False),
+                                     np.arange(N - 384, N)]))
+    a_q, a_s, _ = oracle.quant_act(x)
+    _, y_ref = oracle.w4a8(a_q, a_s, w.w_q[cols], w.scale_f16[cols], w.zero[cols])
+    check_bf16_output(to_host_bits(y)[:, cols], y_ref, f"split tail M={M} N={N} K={K}")
+
+
 @pytest.mark.parametrize("case", ["one_round", "split_k"])
 def test_w4a8_full_tile_group_partials(case):
     M, N, K = _shape(case)

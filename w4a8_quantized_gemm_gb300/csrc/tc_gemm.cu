@@ -107,8 +107,14 @@ struct TcParams {
   int64_t M, N, K;
   int G, ks;
   int m_tiles, n_tiles;
-  int persistent;  // 1: CTAs stride over tiles with all of K; 0: one tile per CTA, split-K cluster
-  int band;        // persistent tile order: bands of `band` m-tiles, m fastest inside a band
+  // 1: CTAs stride over tiles [0, units) of the banded order with all of K;
+  // 0: one tile (blockIdx.y, blockIdx.z) per cluster of ks CTAs splitting K;
+  // 2: one tile tail_base + blockIdx.y of the banded order per cluster of ks
+  //    CTAs (the short last round of a persistent grid, split so that it
+  //    takes all SMs: run as a second launch after mode 1 over the rest)
+  int persistent;
+  int units, tail_base;
+  int band;        // banded tile order: bands of `band` m-tiles, m fastest inside a band
   int act3d;       // 1: activation map is 3-D, one copy per 128-wide group; 0: 2-D, two copies
   const float* a_s;
   const int32_t* a_gsum;  // per-token group sums (e4m3 W4A8 form: zero points in the drain)
@@ -395,17 +401,19 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
 
   // ---- this CTA's work: a flat sequence of (tile, group) items ---------------
   // persistent: tiles blockIdx.x, +gridDim.x, ... each with all G groups;
-  // split-K:    tile (blockIdx.y, blockIdx.z), groups of cluster rank blockIdx.x.
+  // split-K:    tile (blockIdx.y, blockIdx.z), or tail tile tail_base +
+  //             blockIdx.y, groups of cluster rank blockIdx.x.
   int u_begin, u_step, n_units, g0, g1;
-  if (p.persistent) {
-    const int total = p.m_tiles * p.n_tiles;
+  if (p.persistent == 1) {
+    const int total = p.units;
     u_begin = blockIdx.x;
     u_step = gridDim.x;
     n_units = u_begin < total ? (total - u_begin + u_step - 1) / u_step : 0;
     g0 = 0;
     g1 = G;
   } else {
-    u_begin = blockIdx.y + blockIdx.z * p.m_tiles;
+    u_begin = p.persistent == 2 ? p.tail_base + (int)blockIdx.y
+                                : (int)blockIdx.y + (int)blockIdx.z * p.m_tiles;
     u_step = 1;
     n_units = 1;
     g0 = (int)((int64_t)blockIdx.x * G / p.ks);
@@ -421,12 +429,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
     else if constexpr (GPD == 0) return i / ng;
     else return (i / ng) * nc + (i % ng) / (GPD > 1 ? GPD : 1);
   };
-  // tile u -> (mt, nt). Persistent grids walk bands of p.band m-tiles, m
-  // fastest inside a band, so the tiles in flight at once share a few
-  // activation tiles and a few weight tiles (both stay in L2).
+  // tile u -> (mt, nt). Persistent grids (and their split tails) walk bands
+  // of p.band m-tiles, m fastest inside a band, so the tiles in flight at
+  // once share a few activation tiles and a few weight tiles (both stay in L2).
   auto unit_tile = [&](int k, int& mt, int& nt) {
     const int u = u_begin + k * u_step;
-    if (p.persistent) {
+    if (p.persistent != 0) {
       const int band_tiles = p.band * p.n_tiles;
       const int b = u / band_tiles;
       const int idx = u - b * band_tiles;
@@ -507,7 +515,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
   const uint32_t d_tmem = tmem;                  // accumulators: columns [0, kNumD*BT)
   const uint32_t a_tmem = tmem + kNumD * C::kDCols;  // A operand: kNumA buffers of kACols
   const uint64_t tmo = p.timeout_ns;
-  const bool cluster_reduce = !PARTIALS && !p.persistent && p.ks > 1;
+  const bool cluster_reduce = !PARTIALS && p.persistent != 1 && p.ks > 1;
 
   // Each role ends with the same named CTA barrier (every thread) and, for
   // split-K clusters, the same two cluster barriers, so the drain warps can
@@ -1286,25 +1294,35 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap act_map,
         if (cluster_ctarank() == 0) {
           store_row_scaled<HB>(R, asv, p, out, m0 + col0, n);
         }
-      } else {  // (wide tiles: their drain registers have no room for the batch)
+      } else {
+        // wide tiles: reduce-scatter. Rank k sums the tile's columns
+        // [k * sw, (k + 1) * sw) over every rank's partials, in rank order
+        // (the order of a reduction by one rank), and stores them, so that
+        // each SM takes in 1/ks of the partial sums through DSMEM.
         cluster_sync_all();
-        if (cluster_ctarank() == 0) {
-          const uint32_t local = smem_u32(red);
-          for (int rk = 1; rk < p.ks; ++rk) {
-            const uint32_t remote = map_to_rank(local, rk);
+        const int ks = p.ks;
+        const int sw = (BT + ks - 1) / ks;
+        const int rank = (int)cluster_ctarank();
+        const int c_lo = max(rank * sw, col0), c_hi = min(rank * sw + sw, col0 + HB);
+        uint32_t rb[8];
 #pragma unroll
-            for (int t = 0; t < HB; ++t) R[t] += ld_dsmem_f32(remote + ((col0 + t) * 128 + r) * 4);
+        for (int j = 0; j < 8; ++j) rb[j] = j < ks ? map_to_rank(smem_u32(red), j) : 0u;
+        for (int c = c_lo; c < c_hi; ++c) {
+          const uint32_t off = (uint32_t)((c * 128 + r) * 4);
+          float v[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) v[j] = j < ks ? ld_dsmem_f32(rb[j] + off) : 0.f;
+          float acc = v[0];
+#pragma unroll
+          for (int j = 1; j < 8; ++j)
+            if (j < ks) acc += v[j];
+          const int64_t m = m0 + c;
+          if (m < p.M) {
+            if constexpr (kCodes) acc *= __ldg(p.a_s + m);
+            out.y[m * out.N + n] = f32_to_bf16_bits(acc);
           }
         }
-        cluster_sync_all();
-        if (cluster_ctarank() == 0) {
-          if constexpr (C::kTmaEpi) {
-            epilogue_tma(R, 0, m0, out);
-            if (epi_thread) bulk_wait_group0();
-          } else {
-            store_row<VARIANT, HB>(R, p, out, m0 + col0, n);
-          }
-        }
+        cluster_sync_all();  // no rank leaves while another reads its partials
       }
     }
   };
@@ -1461,6 +1479,54 @@ static void choose_split(int64_t tiles, int G, int sms, double split_cost, bool 
   *persistent_out = 0;
 }
 
+// Grid plan of one GEMM: a persistent grid over the first `units` tiles of the
+// banded order and, for wide tiles whose last round would leave most SMs idle,
+// a second launch splitting the remaining `tail` tiles' K over clusters of
+// `tail_ks` CTAs; or, with too few tiles to fill the GPU, one split-K grid
+// over all tiles (persistent = 0, split ks).
+struct GridPlan {
+  int persistent = 0;
+  int ks = 1;
+  int64_t units = 0, tail = 0;
+  int tail_ks = 1;
+  double cost = 0.0;  // CTA time in groups of one unit of this width
+};
+
+// the second launch of a split tail, in groups of a full-grid CTA: its launch
+// behind the first, pipeline fill, cluster reduction and stores (measured on
+// GB300: ~14 us beside the split groups' own time, ~26 groups of 192 tokens;
+// so the 3584 x 18944 linear at 4096 tokens takes a tail, 386 -> 334 us,
+// and the 3584 x 3584 one, 28 groups a tile, does not)
+constexpr double kTailLaunchCost = 24.0;
+
+static GridPlan plan_grid(int64_t tiles, int G, int sms, bool wide) {
+  GridPlan g;
+  const double split_cost = wide ? 2.0 : 1.0;
+  choose_split(tiles, G, sms, split_cost, wide, &g.ks, &g.persistent);
+  if (!g.persistent) {
+    const int64_t units = tiles * g.ks;
+    g.cost = (double)((units + sms - 1) / sms) *
+             ((G + g.ks - 1) / g.ks + (g.ks > 1 ? split_cost : 0.0));
+    return g;
+  }
+  const int64_t rounds = (tiles + sms - 1) / sms;
+  g.units = tiles;
+  g.cost = (double)rounds * G;
+  if (!wide || rounds < 2) return g;
+  const int64_t tail = tiles - (rounds - 1) * sms;
+  int ks = 1;
+  for (int k = 2; k <= 8 && k <= G && tail * k <= sms; ++k) ks = k;
+  if (ks < 2) return g;
+  const double split = (double)(rounds - 1) * G + (G + ks - 1) / ks + split_cost + kTailLaunchCost;
+  if (split < g.cost) {
+    g.units = (rounds - 1) * sms;
+    g.tail = tail;
+    g.tail_ks = ks;
+    g.cost = split;
+  }
+  return g;
+}
+
 // Band height (in m-tiles) for the persistent tile order, which walks bands of
 // `band` m-tiles with m fastest inside a band: each weight tile is read from
 // DRAM once per band, each activation tile once if the band's activations stay
@@ -1509,12 +1575,12 @@ static cudaError_t launch_tc(const GemmArgs& a, cudaStream_t st) {
   const int64_t tiles = m_tiles * n_tiles;
   if (m_tiles > 65535 || n_tiles > 65535 || tiles >= (1LL << 31)) return cudaErrorInvalidValue;
   const int sms = tc_sm_count() * C::kCtasPerSm;  // CTA slots of one wave
-  int ks = 1, persistent = 0;
   // (wide tiles reduce 128 x BT partial sums through DSMEM, about two groups'
   // worth, and split only while every CTA of the split fits one wave: a
   // second wave of split clusters measured slower than no split, e.g. the
   // 3584 x 3584 linear at 512 tokens 53 us split four ways against 23 us)
-  choose_split(tiles, G, sms, C::kWide ? 2.0 : 1.0, C::kWide, &ks, &persistent);
+  const GridPlan plan = plan_grid(tiles, G, sms, C::kWide);
+  const int ks = plan.ks, persistent = plan.persistent;
   TcParams p{};
   p.M = a.M;
   p.N = a.N;
@@ -1524,6 +1590,8 @@ static cudaError_t launch_tc(const GemmArgs& a, cudaStream_t st) {
   p.m_tiles = (int)m_tiles;
   p.n_tiles = (int)n_tiles;
   p.persistent = persistent;
+  p.units = (int)plan.units;
+  p.tail_base = (int)plan.units;
   p.act3d = act3d;
   p.band = persistent ? choose_band(m_tiles, n_tiles, (double)BT * a.K * 2.0,
                                     (double)128 * a.K * (C::kW16 ? 2.0 : (C::kW8 ? 1.0 : 0.5)))
@@ -1573,7 +1641,7 @@ static cudaError_t launch_tc(const GemmArgs& a, cudaStream_t st) {
   }
   cudaLaunchConfig_t cfg = {};
   if (persistent)
-    cfg.gridDim = dim3((unsigned)(tiles < sms ? tiles : sms), 1, 1);
+    cfg.gridDim = dim3((unsigned)(plan.units < sms ? plan.units : sms), 1, 1);
   else
     cfg.gridDim = dim3((unsigned)ks, (unsigned)m_tiles, (unsigned)n_tiles);
   cfg.blockDim = dim3(C::kThreads, 1, 1);
@@ -1588,25 +1656,26 @@ static cudaError_t launch_tc(const GemmArgs& a, cudaStream_t st) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, act_map, w8_map, p, ymaps);
+  if (e != cudaSuccess || plan.tail == 0) return e;
+  // the split tail: the last tiles of the banded order, K over clusters
+  p.persistent = 2;
+  p.ks = plan.tail_ks;
+  cfg.gridDim = dim3((unsigned)plan.tail_ks, (unsigned)plan.tail, 1);
+  attr[0].val.clusterDim.x = (unsigned)plan.tail_ks;
   return cudaLaunchKernelEx(&cfg, kern, act_map, w8_map, p, ymaps);
 }
 
 // Time of a grid of `bt`-token wide tiles in units of one group of one
-// 128-token tile: the split choose_split makes, its rounds times the groups of
-// one unit, times the relative cost of a group at that width.
+// 128-token tile: the cost of the grid plan_grid makes, times the relative
+// cost of a group at that width.
 static double wide_grid_cost(int64_t M, int64_t n_tiles, int G, int sms, int bt) {
   // one 192-token group against one 128-token group, CTA time in a full grid
   // (measured on GB300 over the 7B prefill shapes: 1.0-1.14 as the 192-token
   // kernel improved; every value in that range makes the same choices there)
   constexpr double kFullGroupCost = 1.12;
   const int64_t tiles = ((M + bt - 1) / bt) * n_tiles;
-  int ks = 1, persistent = 0;
-  choose_split(tiles, G, sms, 2.0, true, &ks, &persistent);
-  const int64_t units = persistent ? tiles : tiles * ks;
-  const int64_t rounds = (units + sms - 1) / sms;
-  const double per_unit =
-      persistent ? (double)G : (double)((G + ks - 1) / ks) + (ks > 1 ? 2.0 : 0.0);
-  return (double)rounds * per_unit * (bt == kFullBT ? kFullGroupCost : 1.0);
+  return plan_grid(tiles, G, sms, true).cost * (bt == kFullBT ? kFullGroupCost : 1.0);
 }
 
 int tc_token_tile(int variant, int64_t M, int64_t N, int64_t K) {
