@@ -299,7 +299,8 @@ def kernel_sources_hash() -> str:
 
 
 def traffic_table():
-    """{(kernel label, M, N, K): DRAM bytes of one launch} from the ncu
+    """{(kernel label, M, N, K): DRAM bytes of one call (all its launches of
+    that kernel)} from the ncu
     captures summarised in profiles/dram_traffic.txt, or {} when there is none
     or the kernels changed since they were taken (source hash mismatch)."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
@@ -320,16 +321,17 @@ def traffic_table():
     return table
 
 
-def measured_traffic(table, label, cells):
-    """Average DRAM bytes per launch of kernel `label` over the step's cells,
-    or None unless every cell's shape was captured."""
-    vals = []
+def measured_traffic(table, label, cells, launches):
+    """Average DRAM bytes per launch of kernel `label` over the step's cells
+    (launches[i]: launches of cells[i]), or None unless every cell's shape was
+    captured."""
+    total = 0.0
     for c in cells:
         key = (label, c.M, c.N, c.K)
         if key not in table:
             return None
-        vals.append(table[key])
-    return float(np.mean(vals)) if vals else None
+        total += table[key]
+    return total / sum(launches) if cells else None
 
 
 # ------------------------------------------------------------------ clocks ----
@@ -427,6 +429,23 @@ def kernel_label(eg, cell: Cell, path: int) -> str:
                 if eg.tc_operand_form(M) == eg.TC_FORM_E4M3_PLANES
                 else "tc_gemm_kernel (W4A8, fp16 tiles)")
     return f"tc_gemm_kernel ({kind.upper()})"
+
+
+def kernel_launches(eg, cell: Cell, path: int) -> int:
+    """Launches of the cell's kernel (the library's own count on the
+    tensor-core path: a long-K persistent grid whose last round would be
+    short runs that round as a second, split-K launch)."""
+    if cell.kind == "quant" or "tc_gemm" not in kernel_label(eg, cell, path):
+        return 1
+    variant = {"w4a8": eg.VARIANT_W4A8, "w4a16": eg.VARIANT_W4A16, "w8a16": eg.VARIANT_W8A16,
+               "w8a8": eg.VARIANT_W8A8}[cell.kind]
+    return eg.tc_launches(cell.M, cell.N, cell.K, variant)
+
+
+def call_launches(eg, cell: Cell, path: int) -> int:
+    """All launches of the cell's library call (the one-call linear also
+    launches its quantization)."""
+    return kernel_launches(eg, cell, path) + (1 if cell.with_quant else 0)
 
 
 def actual_bytes(eg, cell: Cell, path: int, tc_inputs=()) -> int:
@@ -870,7 +889,7 @@ def run_ours(args, rank, world):
             d["bytes"] += sum(c.bytes for c in cs) * args.steps
             d["actual"] += sum(actual_bytes(eg, c, path, p.tc_inputs) for c in cs) * args.steps
             d["ops"] += sum(c.ops for c in cs) * args.steps
-            d["launches"] += len(cs) * args.steps
+            d["launches"] += sum(kernel_launches(eg, c, path) for c in cs) * args.steps
             kernel_cells.setdefault(lab, []).extend(cs)
             del sub
 
@@ -915,7 +934,9 @@ def run_ours(args, rank, world):
     def roof(lab):
         d = per_kernel[lab]
         return _roofline(lab, d["ms"], d["bytes"], d["ops"], d["launches"], peaks, int8,
-                         measured_traffic(table, lab, kernel_cells[lab]))
+                         measured_traffic(table, lab, kernel_cells[lab],
+                                          [kernel_launches(eg, c, path)
+                                           for c in kernel_cells[lab]]))
 
     gemm_labels = [k for k in per_kernel if not k.startswith("quant")]
     dom = max(per_kernel, key=lambda k: per_kernel[k]["ms"])
@@ -1005,7 +1026,7 @@ def run_ours(args, rank, world):
         d = {"ms_per_step": round(ms / args.steps, 5), "GB/s": round(pb / sec / 1e9, 1),
              "TOPS": round(po / sec / 1e12, 2), "frac_hbm": round(pb / sec / 1e9 / peaks["hbm_gbs"], 4),
              "frac_bf16_sustained": round(po / sec / 1e12 / peaks["bf16_tflops_sustained"], 4),
-             "launches_per_step": len(p.cells)}
+             "launches_per_step": sum(call_launches(eg, c, path) for c in p.cells)}
         if int8 and int8.get("tops"):
             d["x_int8_peak"] = round(po / sec / 1e12 / int8["tops"], 3)
         parts_out[p.name] = d
@@ -1048,7 +1069,8 @@ def run_ours(args, rank, world):
                 "how": "pinned host buffers; each step's inputs in and outputs out on "
                        "copy streams of their own, overlapping the neighbouring steps' "
                        "compute (two device input/output sets, used by alternate steps)"},
-        "gpu_launches": sum(len(p.cells) for p in parts) * args.steps,
+        "gpu_launches": sum(call_launches(eg, c, path) for p in parts for c in p.cells)
+        * args.steps,
         "clocks": clk.summary(),
         "device_status": status,
     }

@@ -86,6 +86,14 @@ int egopq_auto_path(int64_t M, int variant);
  * M <= 64 (no tensor-core form). Reads the current device's SM count. */
 int egopq_tc_token_tile(int64_t M, int64_t N, int64_t K, int variant);
 
+/* Kernel launches the tensor-core path makes for an M x N x K call of
+ * `variant` (and for a grouped call whose outputs total N rows), for
+ * inspection, tests and launch accounting: 1, or 2 where a persistent grid of
+ * wide tiles would end in a short last round -- its full rounds run first,
+ * then the remaining tiles as a second launch with K split over clusters. The
+ * errors of egopq_tc_token_tile. Reads the current device's SM count. */
+int egopq_tc_launches(int64_t M, int64_t N, int64_t K, int variant);
+
 typedef void* egopq_stream_t; /* cudaStream_t */
 
 /* Library version, major*10000 + minor*100 + patch. */

@@ -91,6 +91,14 @@ def test_auto_path_and_operand_queries(lib):
     assert lib.egopq_tc_token_tile(0, 3584, 3584, W4A8) == -1
     assert lib.egopq_tc_token_tile(16, 3500, 3584, W4A8) == -2
     assert lib.egopq_tc_token_tile(16, 3584, 3584, 9) == -1
+    # launches of the tensor-core GEMM: a split second launch for the short
+    # last round of a long-K persistent grid, one launch otherwise
+    assert lib.egopq_tc_launches(2048, 3584, 18944, W4A8) == 2
+    assert lib.egopq_tc_launches(4096, 152064, 3584, W4A8) == 1
+    assert lib.egopq_tc_launches(16, 3584, 18944, W4A8) == 1
+    assert lib.egopq_tc_launches(4096, 3584, 18944, W8A16) == 1
+    assert lib.egopq_tc_launches(0, 3584, 3584, W4A8) == -1
+    assert lib.egopq_tc_launches(64, 3584, 3584, W8A8) == -2
 
 
 def test_sizes_beyond_the_limit_are_unsupported_shapes(lib):

@@ -86,8 +86,9 @@ def test_both_arms_print_the_same_config():
 
 
 def test_traffic_reported_only_for_the_captured_sources(tmp_path, monkeypatch):
-    """A capture keyed to the current kernel sources is read back per launch
-    shape; the same capture under any other sources hash is not (null)."""
+    """A capture keyed to the current kernel sources is read back per call
+    shape and averaged per launch; the same capture under any other sources
+    hash is not (null)."""
     good = tmp_path / "good"
     (good / "profiles").mkdir(parents=True)
     lab = "tc_gemm_kernel (W4A8, fp16 tiles)"
@@ -99,9 +100,11 @@ def test_traffic_reported_only_for_the_captured_sources(tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "kernel_sources_hash", lambda: "abc")
     table = bench.traffic_table()
     mk = lambda M: bench.Cell("x", "w4a8", M, 3584, 3584, "o", ("o",), 0, 0)
-    assert bench.measured_traffic(table, lab, [mk(512), mk(2048)]) == 2000.0
-    assert bench.measured_traffic(table, lab, [mk(512), mk(4096)]) is None
-    assert bench.measured_traffic(table, "gemv_w4_kernel (W4A8)", [mk(512)]) is None
+    assert bench.measured_traffic(table, lab, [mk(512), mk(2048)], [1, 1]) == 2000.0
+    # a call of two launches (a split second launch): bytes per launch
+    assert bench.measured_traffic(table, lab, [mk(512), mk(2048)], [1, 2]) == 4000.0 / 3
+    assert bench.measured_traffic(table, lab, [mk(512), mk(4096)], [1, 1]) is None
+    assert bench.measured_traffic(table, "gemv_w4_kernel (W4A8)", [mk(512)], [1]) is None
     monkeypatch.setattr(bench, "kernel_sources_hash", lambda: "0" * 64)
     assert bench.traffic_table() == {}
     assert os.path.exists(str(good / "profiles" / "dram_traffic.txt"))

@@ -79,6 +79,7 @@ def test_w4a8_split_tail_output(M):
     sms = _sms()
     N, K = 128 * (sms + (2 if M == 384 else 3)), 8192
     assert eg.tc_token_tile(M, N, K) == (192 if M == 384 else 128)
+    assert eg.tc_launches(M, N, K) == 2
     x, w = w4_case(17, M, N, K)
     packed = eg.pack_w4(*_dev_weights(w))
     y = eg.w4a8_linear(to_dev(x, torch.bfloat16), packed, N, path=eg.PATH_TC)

@@ -89,6 +89,7 @@ def load() -> ctypes.CDLL:
             "egopq_tc_operand_bytes": (sz, [i64, i64, i32]),
             "egopq_tc_operand_form": (i32, [i64]),
             "egopq_tc_token_tile": (i32, [i64, i64, i64, i32]),
+            "egopq_tc_launches": (i32, [i64, i64, i64, i32]),
             "egopq_device_status": (i32, [vp]),
             "egopq_selftest_timeout": (i32, [i32, vp]),
             "egopq_debug_build": (i32, []),
@@ -219,6 +220,15 @@ def tc_token_tile(M: int, N: int, K: int, variant: int = VARIANT_W4A8) -> int:
     """Tokens per output tile (the MMA's N) the tensor-core path runs an
     M x N x K call of `variant` with on the current device."""
     rc = int(load().egopq_tc_token_tile(M, N, K, variant))
+    if rc < 0:
+        _check(rc)
+    return rc
+
+
+def tc_launches(M: int, N: int, K: int, variant: int = VARIANT_W4A8) -> int:
+    """Kernel launches (1 or 2) the tensor-core path makes for an M x N x K
+    call of `variant` on the current device."""
+    rc = int(load().egopq_tc_launches(M, N, K, variant))
     if rc < 0:
         _check(rc)
     return rc

@@ -586,6 +586,11 @@ int egopq_tc_token_tile(int64_t M, int64_t N, int64_t K, int variant) {
   return tc_token_tile(variant, M, N, K);
 }
 
+int egopq_tc_launches(int64_t M, int64_t N, int64_t K, int variant) {
+  const int bt = egopq_tc_token_tile(M, N, K, variant);
+  return bt < 0 ? bt : tc_launches(variant, M, N, K);
+}
+
 size_t egopq_tc_operand_bytes(int64_t M, int64_t K, int group) {
   if (M <= 0 || K <= 0 || M >= kMaxDim || K >= kMaxDim || group != 128 || K % 128) return 0;
   return (size_t)(2 * M * K);

@@ -175,6 +175,9 @@ cudaError_t launch_tc_gemm(const GemmArgs& a, cudaStream_t st);
 // with: 16, 32 or 64 up to 64 tokens; above, 128 or 192 (per-group variants,
 // chosen from the grid each makes) or 128.
 int tc_token_tile(int variant, int64_t M, int64_t N, int64_t K);
+// Kernel launches of the tensor-core GEMM of that shape: 1, or 2 when the
+// persistent grid's short last round runs as a split-K second launch.
+int tc_launches(int variant, int64_t M, int64_t N, int64_t K);
 // Bounded-wait self test.
 cudaError_t launch_selftest_timeout(uint64_t timeout_ns, cudaStream_t st);
 

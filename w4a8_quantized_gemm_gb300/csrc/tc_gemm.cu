@@ -1701,6 +1701,14 @@ int tc_token_tile(int variant, int64_t M, int64_t N, int64_t K) {
   return 128;
 }
 
+int tc_launches(int variant, int64_t M, int64_t N, int64_t K) {
+  const int bt = tc_token_tile(variant, M, N, K);
+  const bool per_group = (variant == kW4A8 || variant == kW4A16 || variant == kW16A16);
+  if (bt <= 64 || !per_group) return 1;  // (only wide per-group tiles split a tail)
+  const int64_t tiles = ((M + bt - 1) / bt) * (N / 128);
+  return plan_grid(tiles, (int)(K / 128), tc_sm_count(), true).tail > 0 ? 2 : 1;
+}
+
 template <int VARIANT, bool PARTIALS>
 static cudaError_t launch_tc_bt(const GemmArgs& a, cudaStream_t st) {
   constexpr bool kPerGroup = (VARIANT == kW4A8 || VARIANT == kW4A16 || VARIANT == kW16A16);
