@@ -85,9 +85,10 @@ def test_auto_path_and_operand_queries(lib):
     # the down projection at 2048 tokens: 192-token tiles leave a short last
     # round, which a split second launch takes (cheaper than 128-token tiles)
     assert lib.egopq_tc_token_tile(2048, 3584, 18944, W4A8) == 192
-    assert lib.egopq_tc_token_tile(4096, 3584, 3584, W8A16) == 128
+    assert lib.egopq_tc_token_tile(4096, 12288, 3072, W8A16) == 192
     assert lib.egopq_tc_token_tile(64, 3584, 3584, W8A8) == -2      # GEMV only up to 64
-    assert lib.egopq_tc_token_tile(65, 3584, 3584, W8A8) == 128
+    assert lib.egopq_tc_token_tile(65, 3584, 3584, W8A8) == 128      # one m-tile at either width
+    assert lib.egopq_tc_token_tile(4096, 12288, 3072, W8A8) == 192
     assert lib.egopq_tc_token_tile(0, 3584, 3584, W4A8) == -1
     assert lib.egopq_tc_token_tile(16, 3500, 3584, W4A8) == -2
     assert lib.egopq_tc_token_tile(16, 3584, 3584, 9) == -1

@@ -140,13 +140,65 @@ def test_w4a16_full_tile_output():
     check_bf16_output(to_host_bits(y), y_ref, "W4A16 192-token tiles")
 
 
+@pytest.mark.parametrize("case", ["one_round", "two_rounds", "split_k"])
+def test_w8a16_full_tile_output(case):
+    """W8A16 on 192-token tiles (all of K accumulated in a 192-column TMEM
+    accumulator, two accumulators and two A buffers): one persistent round with
+    a ragged token tail, two rounds, and a split-K grid (cluster reduction)."""
+    M, N, K = _shape(case)
+    assert eg.tc_token_tile(M, N, K, eg.VARIANT_W8A16) == 192, (case, M, N, K)
+    x = synth.activations(18, 0, 0, M, K, outliers=False)
+    w8, s8 = synth.w8_weights(18, 0, 0, N, K)
+    y = eg.w8a16_gemm(to_dev(x, torch.bfloat16), to_dev(w8), to_dev(s8, torch.float16),
+                      path=eg.PATH_TC)
+    _, y_ref = oracle.w8a16(x, w8, s8)
+    check_bf16_output(to_host_bits(y), y_ref, f"W8A16 192-token tiles {case}")
+
+
+@pytest.mark.parametrize("case", ["one_round", "two_rounds", "split_k"])
+def test_w8a8_full_tile_output(case):
+    """W8A8 on 192-token tiles (partials of 8 groups exact in fp32, added as
+    int32): the same three grid forms."""
+    M, N, K = _shape(case)
+    assert eg.tc_token_tile(M, N, K, eg.VARIANT_W8A8) == 192, (case, M, N, K)
+    x = synth.activations(19, 0, 0, M, K)
+    w8, s8 = synth.w8_weights(19, 0, 0, N, K)
+    a = eg.quant_act(to_dev(x, torch.bfloat16))
+    y = eg.w8a8_gemm(a, to_dev(w8), to_dev(s8, torch.float16), path=eg.PATH_TC)
+    a_q, a_s, _ = oracle.quant_act(x)
+    _, _, y_ref = oracle.w8a8(a_q, a_s, w8, s8)
+    check_bf16_output(to_host_bits(y), y_ref, f"W8A8 192-token tiles {case}")
+
+
+def test_w8a8_full_tile_integer_case_bit_exact():
+    """Codes that quantize to themselves and unit scales: each output is an
+    integer dot product below 2^24, rounded once to bf16 on both sides."""
+    M, N, K = _shape("one_round")
+    assert eg.tc_token_tile(M, N, K, eg.VARIANT_W8A8) == 192
+    rng = np.random.default_rng(20)
+    xi = rng.integers(-127, 128, size=(M, K))
+    xi[:, 0] = 127
+    x = torch.tensor(xi, dtype=torch.float32).to(torch.bfloat16).view(torch.int16).numpy()
+    x = x.view(np.uint16)
+    w8 = rng.integers(-127, 128, size=(N, K)).astype(np.int8)
+    s8 = np.full(N, 0x3C00, dtype=np.uint16)  # fp16 1.0
+    a = eg.quant_act(to_dev(x, torch.bfloat16))
+    y = to_host_bits(eg.w8a8_gemm(a, to_dev(w8), to_dev(s8, torch.float16), path=eg.PATH_TC))
+    a_q, a_s, _ = oracle.quant_act(x)
+    dot, _, y_ref = oracle.w8a8(a_q, a_s, w8, s8)
+    assert np.abs(dot).max() < 2 ** 24
+    assert np.array_equal(y, y_ref)
+
+
 def test_token_tile_choice():
-    """Decode-sized tiles by M; 128 where 192 gains no round; W8A16 always 128."""
+    """Decode-sized tiles by M; 128 where 192 gains no round; the int8-weight
+    variants take 192 too."""
     assert [eg.tc_token_tile(m, 3584, 3584) for m in (5, 16, 17, 32, 33, 64)] == \
         [16, 16, 32, 32, 64, 64]
     assert eg.tc_token_tile(256, 256, 512) == 128        # 2 m-tiles at either width
     assert eg.tc_token_tile(4096, 152064, 3584) == 192   # the untied head at 4096 tokens
-    assert eg.tc_token_tile(4096, 3584, 3584, eg.VARIANT_W8A16) == 128
+    assert eg.tc_token_tile(4096, 12288, 3072, eg.VARIANT_W8A16) == 192
+    assert eg.tc_token_tile(4096, 12288, 3072, eg.VARIANT_W8A8) == 192
 
 
 def test_bf16_twin_full_tile():

@@ -184,7 +184,7 @@ struct TcCfg {
   // all TMEM holds; two A buffers)
   static constexpr int kNumD =
       kLean ? 4 : (kWide ? (kFull ? 2 : 3) : (kFp8 ? (BT == 32 ? 4 : 2) : (BT <= 64 ? 4 : 2)));
-  static constexpr int kNumA = kLean ? 4 : (kWide ? 2 : (kFp8 ? 8 : 4));
+  static constexpr int kNumA = kLean ? 4 : (kWide ? 2 : (kFp8 ? 8 : (BT > 128 ? 2 : 4)));
   static constexpr int kActBox = BT * 128;                        // one 64-wide K box, bytes
   static constexpr int kActBytes = 2 * kActBox;                   // a 128-wide group
   // weights of one group: the int8 tile, or one packed int4 record (8192 B of
@@ -296,7 +296,8 @@ struct TcCfg {
                 "buffer reuse waits");
   static_assert(8 * (2 * kStages + 2 * kNumA + 2 * kNumD + kMmaWarps + 2 * kRecStages) + 8 <= 1024,
                 "barrier region");
-  static_assert(BT % 16 == 0 && BT >= 16 && (BT <= 128 || kFull), "token tile");
+  static_assert(BT % 16 == 0 && BT >= 16 && (BT <= 128 || kFull || (kW8 && BT == kFullBT)),
+                "token tile");
   // the split hands out exactly the registers the block was launched with
   static_assert(!kRegSplit || (kWarps / 4 == kDrainWGs + kConvSets + 1 &&
                                kDrainWGs * kRegDrain + kConvSets * kRegConv + kRegOther <=
@@ -1675,26 +1676,30 @@ static cudaError_t launch_tc(const GemmArgs& a, cudaStream_t st) {
 // Time of a grid of `bt`-token wide tiles in units of one group of one
 // 128-token tile: the cost of the grid plan_grid makes, times the relative
 // cost of a group at that width.
-static double wide_grid_cost(int64_t M, int64_t n_tiles, int G, int sms, int bt) {
+static double wide_grid_cost(int64_t M, int64_t n_tiles, int G, int sms, int bt,
+                             bool wide = true) {
   // one 192-token group against one 128-token group, CTA time in a full grid
   // (measured on GB300 over the 7B prefill shapes: 1.0-1.14 as the 192-token
   // kernel improved; every value in that range makes the same choices there)
   constexpr double kFullGroupCost = 1.12;
   const int64_t tiles = ((M + bt - 1) / bt) * n_tiles;
-  return plan_grid(tiles, G, sms, true).cost * (bt == kFullBT ? kFullGroupCost : 1.0);
+  return plan_grid(tiles, G, sms, wide).cost * (bt == kFullBT ? kFullGroupCost : 1.0);
 }
 
 int tc_token_tile(int variant, int64_t M, int64_t N, int64_t K) {
   if (M <= 16) return 16;
   if (M <= 32) return 32;
   if (M <= 64) return 64;
-  // per-group variants take a wide tile, 192 tokens unless its grid costs
-  // more; W8A16 (all of K in TMEM) and W8A8 (drains every 8 groups) 128
-  if (variant == kW4A8 || variant == kW4A16 || variant == kW16A16) {
+  // per-group variants and W8A16 (all of K in TMEM) take 192 tokens unless
+  // that grid costs more; W8A8 (drains every 8 groups) 128
+  if (variant == kW4A8 || variant == kW4A16 || variant == kW16A16 || variant == kW8A16 ||
+      variant == kW8A8) {
     const int sms = tc_sm_count();
     const int G = (int)(K / 128);
     const int64_t n_tiles = N / 128;
-    return wide_grid_cost(M, n_tiles, G, sms, kFullBT) < wide_grid_cost(M, n_tiles, G, sms, kWideBT)
+    const bool wide = variant != kW8A16 && variant != kW8A8;  // (split tails, one-wave splits)
+    return wide_grid_cost(M, n_tiles, G, sms, kFullBT, wide) <
+                   wide_grid_cost(M, n_tiles, G, sms, kWideBT, wide)
                ? kFullBT
                : kWideBT;
   }
@@ -1720,7 +1725,8 @@ static cudaError_t launch_tc_bt(const GemmArgs& a, cudaStream_t st) {
     case 64:
       return launch_tc<VARIANT, 64, PARTIALS>(a, st);
     case kFullBT:
-      if constexpr (kPerGroup) return launch_tc<VARIANT, kFullBT, PARTIALS>(a, st);
+      if constexpr (kPerGroup || VARIANT == kW8A16 || VARIANT == kW8A8)
+        return launch_tc<VARIANT, kFullBT, PARTIALS>(a, st);
       break;
     default:
       return launch_tc<VARIANT, 128, PARTIALS>(a, st);
@@ -1744,6 +1750,8 @@ cudaError_t launch_tc_gemm(const GemmArgs& a, cudaStream_t st) {
       // e4m3 planes below it are specific to 4-bit weights); smaller M run
       // on the GEMV
       if (a.M <= kTcFp8MaxM) return cudaErrorNotSupported;
+      if (tc_token_tile(kW8A8, a.M, a.N, a.K) == kFullBT)
+        return launch_tc<kW8A8, kFullBT, false>(a, st);
       return launch_tc<kW8A8, 128, false>(a, st);
   }
   return cudaErrorInvalidValue;
