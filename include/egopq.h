@@ -56,9 +56,9 @@ typedef enum {
   EGOPQ_ERR_DEVICE_INDEX = -7       /* a debug build's device-side index check failed */
 } egopq_status;
 
-/* Kernel path. AUTO picks by M (W4A8: CUDA-core GEMV for M <= 4, the tcgen05
- * tensor-core GEMM otherwise; W8A8: GEMV for M <= 64; W4A16 and W8A16:
- * tensor-core GEMM); egopq_auto_path reports the choice. The others force one
+/* Kernel path. AUTO picks by M (W4A8, W4A16 and W8A16: CUDA-core GEMV for
+ * M <= 4, the tcgen05 tensor-core GEMM otherwise; W8A8: GEMV for M <= 64);
+ * egopq_auto_path reports the choice. The others force one
  * path for tests and benchmarks. The choice is always this explicit argument,
  * never global or environment state ("The 4-bit CPU path", section "Why the
  * path choice is a config field"). */

@@ -65,8 +65,8 @@ def test_auto_path_and_operand_queries(lib):
     assert [lib.egopq_auto_path(m, eg.VARIANT_W4A8) for m in (1, 4, 5, 16, 4096)] == \
         [GEMV, GEMV, TC, TC, TC]
     assert [lib.egopq_auto_path(m, eg.VARIANT_W8A8) for m in (1, 64, 65)] == [GEMV, GEMV, TC]
-    assert lib.egopq_auto_path(1, eg.VARIANT_W4A16) == TC
-    assert lib.egopq_auto_path(1, eg.VARIANT_W8A16) == TC
+    assert [lib.egopq_auto_path(m, eg.VARIANT_W4A16) for m in (1, 4, 5)] == [GEMV, GEMV, TC]
+    assert [lib.egopq_auto_path(m, eg.VARIANT_W8A16) for m in (1, 4, 5)] == [GEMV, GEMV, TC]
     assert lib.egopq_auto_path(1, 9) == -1
     assert lib.egopq_auto_path(-1, eg.VARIANT_W4A8) == -1
     assert lib.egopq_tc_operand_bytes(16, 3584, 128) == 2 * 16 * 3584

@@ -188,17 +188,21 @@ cudaError_t launch_selftest_timeout(uint64_t timeout_ns, cudaStream_t st);
 constexpr int kTcFp8MaxM = 64;
 // Largest M per W4A8 GEMV launch (larger M run as several launches).
 constexpr int kGemvMaxRows = 16;
-// AUTO path: W4A8 batches up to this many tokens take the GEMV.
+// AUTO path: W4A8, W4A16 and W8A16 batches up to this many tokens take the GEMV.
 constexpr int kGemvAutoMaxM = 4;
 
 // The kernel path a call takes: `path` itself unless it is EGOPQ_PATH_AUTO,
-// which resolves by token count -- W4A8 on the CUDA-core GEMV up to
-// kGemvAutoMaxM tokens, W8A8 on its GEMV up to kTcFp8MaxM (its tensor-core
-// form exists only above), everything else on the tensor cores.
+// which resolves by token count -- W4A8, W4A16 and W8A16 on the CUDA-core
+// GEMVs up to kGemvAutoMaxM tokens, W8A8 on its GEMV up to kTcFp8MaxM (its
+// tensor-core form exists only above), everything else on the tensor cores.
 inline int auto_path(int64_t M, int variant, int path) {
   if (path != EGOPQ_PATH_AUTO) return path;
   if (variant == kW8A8) return M <= kTcFp8MaxM ? EGOPQ_PATH_GEMV : EGOPQ_PATH_TC;
-  return (variant == kW4A8 && M <= kGemvAutoMaxM) ? EGOPQ_PATH_GEMV : EGOPQ_PATH_TC;
+  if (variant == kW16A16) return EGOPQ_PATH_TC;  // (no GEMV form)
+  // W4A8, W4A16, W8A16: the GEMV up to kGemvAutoMaxM tokens (measured on
+  // GB300: W4A16 3072 x 3072 at one token 5.5 us on the GEMV, 12.3 us on
+  // 16-token tensor-core tiles; from 8 tokens the tiles win on every shape)
+  return M <= kGemvAutoMaxM ? EGOPQ_PATH_GEMV : EGOPQ_PATH_TC;
 }
 
 }  // namespace egopq
