@@ -112,7 +112,8 @@ def _misrounding_rows(M, K, seed):
                                  # many tokens: persistent CTAs streaming rows through
                                  # shared memory -- one row each, then several rows each
                                  # (more rows than resident CTAs: double-buffered staging)
-                                 (70, 8192), (2600, 1024), (1000, 16384), (400, 32768),
+                                 (70, 8192), (2600, 1024), (101, 4096), (1000, 16384),
+                                 (400, 32768),
                                  (66, 33024)])   # many tokens, rows too long to stage: two passes
 @pytest.mark.parametrize("with_codes", [True, False])
 def test_quant_act_misrounding_products_bit_exact(M, K, with_codes):
