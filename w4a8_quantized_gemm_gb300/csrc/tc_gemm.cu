@@ -40,9 +40,10 @@
 //                    (a second set of four takes every other group for token
 //                    tiles of 32 and 128-token per-group tiles, and half of
 //                    every group's K in 192-token tiles)
-//   producer warp    TMA: activations tile + weight record per group (192-token
-//                    tiles: the records only, on a ring of their own, and a
-//                    second producer warp for the activations)
+//   producer warp    TMA: activations tile + weight record per group (per-group
+//                    tiles of 128 and 192 tokens: the records only, on a ring
+//                    of their own, and a second producer warp for the
+//                    activations; int8-weight tiles: both in one stage)
 //   issuer warps     one MMA-issuing thread each (two for 32-token and
 //                    per-group wide tiles, taking alternate groups); the
 //                    first allocates TMEM
@@ -84,14 +85,16 @@ constexpr int kMaxSmemHalf = 114688;  // each of two CTAs sharing an SM
 // takes 757 cycles at N = 128..176 and 4*N from N = 192 up, also with a CTA
 // pair), so the tensor pipe reaches its full rate only from 192 tokens a tile.
 //  - kWideBT (128 tokens): three 128-column accumulators and two 64-column A
-//    buffers, two converter sets, two issuers (set q meets issuer q on a
-//    named barrier);
+//    buffers, weight records in a ring of their own, two converter sets, two
+//    issuers (set q meets issuer q on a named barrier);
 //  - kFullBT (192 tokens): two 192-column accumulators and two A buffers fill
 //    the 512 TMEM columns, so the drain of group i gates the MMAs of group
 //    i + 2; weight records in a ring of their own; two converter sets that
 //    split each group's K between them (the first set's first warp also
 //    waits for the drained accumulator and the landed activations), meeting
 //    two alternating issuers on hardware named barriers (see kNamedHandoff).
+// The int8-weight tiles (W8A16, W8A8) come in the same two widths, each
+// accumulator holding several groups (two at 192 tokens, two A buffers).
 // The launcher picks the width per linear from the grid it makes (192-token
 // tiles quantise some grids into a short last wave).
 constexpr int kWideBT = 128;
@@ -1690,8 +1693,9 @@ int tc_token_tile(int variant, int64_t M, int64_t N, int64_t K) {
   if (M <= 16) return 16;
   if (M <= 32) return 32;
   if (M <= 64) return 64;
-  // per-group variants and W8A16 (all of K in TMEM) take 192 tokens unless
-  // that grid costs more; W8A8 (drains every 8 groups) 128
+  // above 64 tokens every variant takes 192 tokens unless that grid costs
+  // more (the int8-weight variants without the per-group tiles' split tails
+  // and one-wave splits)
   if (variant == kW4A8 || variant == kW4A16 || variant == kW16A16 || variant == kW8A16 ||
       variant == kW8A8) {
     const int sms = tc_sm_count();
