@@ -78,10 +78,9 @@ int egopq_auto_path(int64_t M, int variant);
 
 /* The token tile (the MMA's N: tokens per output tile) the tensor-core path
  * runs an M x N x K call of `variant` with, for inspection and tests: 16, 32
- * or 64 for M <= 64; above that 192 or 128 for W4A8 and W4A16 -- 192-token
- * tiles run the tensor pipe at its full rate, and the library takes them
- * unless the grid they make over the current device's SMs takes longer --
- * and 128 for W8A16 and W8A8. EGOPQ_ERR_INVALID_ARG for an unknown variant or
+ * or 64 for M <= 64; above that 192 or 128 -- 192-token tiles run the tensor
+ * pipe at its full rate, and the library takes them unless the grid they
+ * make over the current device's SMs takes longer. EGOPQ_ERR_INVALID_ARG for an unknown variant or
  * M <= 0; EGOPQ_ERR_UNSUPPORTED_SHAPE for a refused shape or W8A8 with
  * M <= 64 (no tensor-core form). Reads the current device's SM count. */
 int egopq_tc_token_tile(int64_t M, int64_t N, int64_t K, int variant);
