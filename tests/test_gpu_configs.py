@@ -152,6 +152,42 @@ def test_reduced_model_pass(two_layers, head, M):
     _check(x, w, to_host_bits(y), rows, _cols(HEAD_N, 7 + M, n_random=128), f"head M={M}")
 
 
+@pytest.mark.parametrize("M", [2048, 4096])
+def test_down_projection_split_tail_sampled(M):
+    """The down projection (K = 18944) at 2048 and 4096 tokens: 192-token tiles
+    whose short last round runs as a split-K second launch. Rows from every
+    region (first, last -- the last m-tile holds the split tiles on this
+    grid -- and random) against sampled columns including the last 384."""
+    K, N = 18944, 3584
+    assert eg.tc_token_tile(M, N, K) == 192 and eg.tc_launches(M, N, K) == 2
+    w = synth.w4_weights(3, 9, synth.LINEARS["down"], N, K)
+    packed = _pack(w)
+    x = synth.activations(3, 9, INPUT_OF["down"], M, K)
+    y = to_host_bits(eg.w4a8_gemm(eg.quant_act(to_dev(x, torch.bfloat16)), packed, N, K))
+    rng = np.random.default_rng(M + 7)
+    rows = np.unique(np.concatenate([np.arange(2), np.arange(M - 64, M, 9),
+                                     rng.choice(M, 6, replace=False)]))
+    cols = np.unique(np.concatenate([_cols(N, M + 8, n_random=128), np.arange(N - 384, N)]))
+    _check(x, w, y, rows, cols, f"down M={M} (split tail)")
+
+
+def test_w8a8_bench_shape_sampled():
+    """W8A8 at the bench's shape (4096 x 12288 x 3072, 192-token tiles) on
+    sampled rows and columns against the int8-dynamic oracle."""
+    M, N, K = 4096, 12288, 3072
+    assert eg.tc_token_tile(M, N, K, eg.VARIANT_W8A8) == 192
+    x = synth.activations(5, 2, 0, M, K)
+    w8, s8 = synth.w8_weights(5, 2, 0, N, K)
+    a = eg.quant_act(to_dev(x, torch.bfloat16))
+    y = to_host_bits(eg.w8a8_gemm(a, to_dev(w8), to_dev(s8, torch.float16)))
+    rng = np.random.default_rng(12)
+    rows = np.unique(np.concatenate([[0, 1, M - 1], rng.choice(M, 6, replace=False)]))
+    cols = _cols(N, 13)
+    a_q, a_s, _ = oracle.quant_act(x[rows])
+    _, _, y_ref = oracle.w8a8(a_q, a_s, w8[cols], s8[cols])
+    check_bf16_output(y[np.ix_(rows, cols)], y_ref, "W8A8 4096 x 12288 x 3072")
+
+
 # --------------------------------------------------- sibling linears, one launch
 
 @pytest.mark.parametrize("path", [eg.PATH_GEMV, eg.PATH_TC])
