@@ -381,18 +381,6 @@ __device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
   asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
   return v;
 }
-// four loads from another CTA's shared memory at addr + k * stride (bytes),
-// issued together so that their round trips overlap
-__device__ __forceinline__ void ld_dsmem_f32x4(uint32_t addr, uint32_t stride, float (&v)[4]) {
-  asm volatile(
-      "ld.shared::cluster.f32 %0, [%4];\n\t"
-      "ld.shared::cluster.f32 %1, [%5];\n\t"
-      "ld.shared::cluster.f32 %2, [%6];\n\t"
-      "ld.shared::cluster.f32 %3, [%7];"
-      : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3])
-      : "r"(addr), "r"(addr + stride), "r"(addr + 2 * stride), "r"(addr + 3 * stride)
-      : "memory");
-}
 
 // ---- small numeric helpers -------------------------------------------------------
 __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t mask, uint32_t magic) {
