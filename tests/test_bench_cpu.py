@@ -117,3 +117,21 @@ def test_sources_hash_ignores_comments_only():
     assert bench._code_only(code) == bench._code_only(
         "int a = 1;\n\n// another note\nint b = 2;  /* trailing */\n")
     assert bench._code_only(code) != bench._code_only("int a = 1;\nint b = 3;\n")
+
+
+def test_launch_accounting_counts_split_tails():
+    """gpu_launches counts every kernel launch of the step's calls: the
+    quantizations, one GEMM launch a call, and the second launch the library
+    reports for a long-K grid's split tail (the down projection at 2048 and
+    4096 tokens). Host-only queries of the library (its SM count falls back
+    to 148 without a device; these shapes split on 148 and 152 alike)."""
+    import w4a8_quantized_gemm_gb300 as eg
+    from w4a8_quantized_gemm_gb300 import builder
+    builder.build()
+    eg.load()
+    cells = bench.plan_part(_args(workload="prefill"), "prefill")
+    launches = [bench.call_launches(eg, c, eg.PATH_AUTO) for c in cells]
+    tails = [c for c in cells if c.kind == "w4a8" and
+             bench.kernel_launches(eg, c, eg.PATH_AUTO) == 2]
+    assert sorted((c.M, c.N, c.K) for c in tails) == [(2048, 3584, 18944), (4096, 3584, 18944)]
+    assert sum(launches) == len(cells) + 2 == 32
